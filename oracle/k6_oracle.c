@@ -1,0 +1,324 @@
+/*
+ * k6_oracle.c -- plain, slow fp64 CPU oracle for the joint-sequence attention
+ * hot path of long-context video DiTs.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or
+ * calls this file; only the tests, the smoke check and the CPU-baseline leg of
+ * the benchmark do.  It shares no code, header, table or constant with the
+ * CUDA library.
+ *
+ * What it computes, and where the pages say so:
+ *   - Full non-causal multi-head attention softmax(Q K^T * scale) V over the
+ *     joint sequence (video tokens followed by the text/audio "joint tensors"):
+ *     xDiT PR #586 "KV-cache and joint tensors for USP", section "How?" and the
+ *     USP dispatch listing (`_attention(query, key, value, is_causal=...)`);
+ *     "Context Parallelism in vLLM Omni Neuron", section "Self-Attention with
+ *     Context Parallelism" ("local Q x full K/V", `_nf_attend(q, k, v, scale)`).
+ *     Scale = 1/sqrt(d) [reading: the page shows `self.scale` but not its value].
+ *   - Rotary embeddings on Q and K only, from per-token cos/sin tables that can
+ *     be sliced by sequence range: "Context Parallelism in vLLM Omni Neuron",
+ *     sections "Self-Attention with Context Parallelism"
+ *     (`apply_rotary_emb_wan`) and "Positional Embedding Handling"; vLLM-Omni
+ *     recipe "Kandinsky 6 TI2VA -- H100", parallel features list ("visual
+ *     tokens (and their RoPE) are sharded").  The exact rotation is a reading
+ *     (the pages print no formula): each axis (t, h, w) owns a contiguous run of
+ *     d_a head dims in that order; pair i of that run, i.e. dims (2i, 2i+1),
+ *     turns by pos_a * theta^(-2i/d_a) as the complex product
+ *     (x + i y) * exp(i angle); positions are 0-based grid indices; joint
+ *     tokens are not rotated, or (joint_rope = 1) turn over the full head dim
+ *     by their 0-based joint index.
+ *   - Per-chunk partials (O_c, LSE_c) over a contiguous K/V range and their
+ *     log-sum-exp merge, the arithmetic ring attention splits across ranks:
+ *     "Context Parallelism in vLLM Omni Neuron", sections "Ring attention
+ *     (current implementation)" and "Scaling Properties".  The merge formula
+ *     is a reading: LSE = log sum_c exp(LSE_c), out = sum_c exp(LSE_c - LSE) O_c.
+ *   - The sequence-partitioned <-> head-partitioned relayout that Ulysses does
+ *     with all-to-all: xDiT PR #586 USP listing (`_ft_c_input_all_to_all`,
+ *     `_ft_c_output_all_to_all`); "Context Parallelism in vLLM Omni Neuron",
+ *     section "Comparison with Other CP Strategies".  Index map (reading), with
+ *     Sl = S/P and Hl = H/P:
+ *       head[p][b][r*Sl + s][hh][e] = seq[r][b][s][p*Hl + hh][e].
+ *
+ * Layouts: q [B][Sq][H][d] with Sq = Nv + Nj (video rows first, joint rows at
+ * the rear); k, v [B][Nv][H][d]; joint_k, joint_v [B][Nj][H][d].  The K/V
+ * sequence is concat(k, joint_k) along the token axis.  Outputs are double.
+ *
+ * Everything is fp64.  bf16 and f32 inputs are widened exactly.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { K6O_F32 = 0, K6O_BF16 = 1, K6O_F64 = 2 };
+
+typedef struct {
+    int B, H, d;
+    long Nv, Nj;              /* video tokens, joint tokens */
+    int grid_t, grid_h, grid_w; /* Nv = grid_t * grid_h * grid_w */
+    int axis_dim[3];          /* head dims owned by the t, h, w axes; sum = d */
+    double theta;             /* rotary base */
+    int joint_rope;           /* 0: joint tokens unrotated; 1: 1-D over full d */
+} k6o_geom;
+
+/* Exact widening of one element of a typed buffer to double. */
+static double load_elem(const void *p, int type, size_t i) {
+    if (type == K6O_F64) return ((const double *)p)[i];
+    if (type == K6O_F32) return (double)((const float *)p)[i];
+    /* bf16: the upper 16 bits of an IEEE binary32 */
+    uint32_t bits = (uint32_t)((const uint16_t *)p)[i] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+int k6o_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void k6o_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+static int geom_ok(const k6o_geom *g) {
+    if (g->B < 1 || g->H < 1 || g->d < 2 || (g->d & 1)) return 0;
+    if (g->Nv < 0 || g->Nj < 0) return 0;
+    if ((long)g->grid_t * g->grid_h * g->grid_w != g->Nv) return 0;
+    int sum = 0;
+    for (int a = 0; a < 3; a++) {
+        if (g->axis_dim[a] < 0 || (g->axis_dim[a] & 1)) return 0;
+        sum += g->axis_dim[a];
+    }
+    return sum == g->d;
+}
+
+/* Rotate pair (x[2i], x[2i+1]) by `angle`: complex product (x + iy) e^{i angle}. */
+static void rotate_pair(double *x, int i, double angle) {
+    double c = cos(angle), s = sin(angle);
+    double a = x[2 * i], b = x[2 * i + 1];
+    x[2 * i] = a * c - b * s;
+    x[2 * i + 1] = a * s + b * c;
+}
+
+/* Rotary embedding of one head vector x[0..d) of token n (in place). */
+void k6o_rope_vec(const k6o_geom *g, long n, double *x) {
+    if (n < g->Nv) {
+        long hw = (long)g->grid_h * g->grid_w;
+        long pos[3];
+        pos[0] = n / hw;               /* t */
+        pos[1] = (n / g->grid_w) % g->grid_h; /* h */
+        pos[2] = n % g->grid_w;        /* w */
+        int off = 0;                   /* first dim owned by the axis */
+        for (int a = 0; a < 3; a++) {
+            int da = g->axis_dim[a];
+            for (int i = 0; i < da / 2; i++) {
+                double omega = pow(g->theta, -2.0 * i / da);
+                rotate_pair(x + off, i, (double)pos[a] * omega);
+            }
+            off += da;
+        }
+    } else if (g->joint_rope == 1) {
+        long j = n - g->Nv;
+        for (int i = 0; i < g->d / 2; i++) {
+            double omega = pow(g->theta, -2.0 * i / g->d);
+            rotate_pair(x, i, (double)j * omega);
+        }
+    }
+    /* joint_rope == 0: joint tokens keep their values */
+}
+
+/* Rotary embedding of a whole [B][S][H][d] tensor (S = Nv + Nj) into y. */
+int k6o_rope(const k6o_geom *g, const void *x, int type, double *y) {
+    if (!geom_ok(g)) return -1;
+    long S = g->Nv + g->Nj;
+    long rows = (long)g->B * S * g->H;
+    int d = g->d;
+#pragma omp parallel for schedule(static)
+    for (long r = 0; r < rows; r++) {
+        long n = (r / g->H) % S;
+        double *out = y + (size_t)r * d;
+        for (int e = 0; e < d; e++) out[e] = load_elem(x, type, (size_t)r * d + e);
+        k6o_rope_vec(g, n, out);
+    }
+    return 0;
+}
+
+/* Element offset of token n (of the concatenated K/V sequence), batch b,
+ * head h, dim 0, and which buffer holds it. */
+static const void *kv_ptr(const k6o_geom *g, long n, int b, int h, const void *video,
+                          const void *joint, size_t *off) {
+    if (n < g->Nv) {
+        *off = (((size_t)b * g->Nv + n) * g->H + h) * g->d;
+        return video;
+    }
+    *off = (((size_t)b * g->Nj + (n - g->Nv)) * g->H + h) * g->d;
+    return joint;
+}
+
+/*
+ * Attention of the given query rows over keys [kv_begin, kv_end) of the
+ * concatenated K/V sequence.
+ *   rope: 1 = rotate Q and K here (inputs are raw); 0 = inputs pre-rotated.
+ *   rows[r] in [0, Sq); out [B][nrows][H][d]; lse [B][H][nrows] (natural log
+ *   of the sum of exp of the scaled logits).
+ * Per (b, h): rotate the K range once, then for each row
+ *   s_j = q~ . k~_j / sqrt(d),  m = max_j s_j,
+ *   LSE = m + log sum_j exp(s_j - m),  out = sum_j exp(s_j - LSE) v_j.
+ */
+int k6o_attention(const k6o_geom *g, int rope, const void *q, const void *k, const void *v,
+                  const void *jk, const void *jv, int type, long kv_begin, long kv_end,
+                  const long *rows, long nrows, double *out, double *lse) {
+    if (!geom_ok(g)) return -1;
+    long S = g->Nv + g->Nj;
+    if (kv_begin < 0 || kv_end > S || kv_begin >= kv_end) return -2;
+    for (long r = 0; r < nrows; r++)
+        if (rows[r] < 0 || rows[r] >= S) return -3;
+    int d = g->d, H = g->H;
+    long L = kv_end - kv_begin;
+    double scale = 1.0 / sqrt((double)d);
+    double *kr = (double *)malloc(sizeof(double) * (size_t)L * d);
+    double *vr = (double *)malloc(sizeof(double) * (size_t)L * d);
+    if (!kr || !vr) { free(kr); free(vr); return -4; }
+
+    for (int b = 0; b < g->B; b++) {
+        for (int h = 0; h < H; h++) {
+            /* the key/value rows of this head, keys rotated at their own positions */
+#pragma omp parallel for schedule(static)
+            for (long j = 0; j < L; j++) {
+                long n = kv_begin + j;
+                size_t off;
+                const void *kb = kv_ptr(g, n, b, h, k, jk, &off);
+                const void *vb = kv_ptr(g, n, b, h, v, jv, &off);
+                for (int e = 0; e < d; e++) {
+                    kr[(size_t)j * d + e] = load_elem(kb, type, off + e);
+                    vr[(size_t)j * d + e] = load_elem(vb, type, off + e);
+                }
+                if (rope) k6o_rope_vec(g, n, kr + (size_t)j * d);
+            }
+#pragma omp parallel
+            {
+                double *qv = (double *)malloc(sizeof(double) * d);
+                double *s = (double *)malloc(sizeof(double) * (size_t)L);
+#pragma omp for schedule(dynamic, 1)
+                for (long r = 0; r < nrows; r++) {
+                    long i = rows[r];
+                    size_t qoff = (((size_t)b * S + i) * H + h) * d;
+                    for (int e = 0; e < d; e++) qv[e] = load_elem(q, type, qoff + e);
+                    if (rope) k6o_rope_vec(g, i, qv);
+                    double m = -INFINITY;
+                    for (long j = 0; j < L; j++) {
+                        double acc = 0.0;
+                        const double *kj = kr + (size_t)j * d;
+                        for (int e = 0; e < d; e++) acc += qv[e] * kj[e];
+                        s[j] = acc * scale;
+                        if (s[j] > m) m = s[j];
+                    }
+                    double sum = 0.0;
+                    for (long j = 0; j < L; j++) sum += exp(s[j] - m);
+                    double lse_i = m + log(sum);
+                    double *o = out + (((size_t)b * nrows + r) * H + h) * d;
+                    for (int e = 0; e < d; e++) o[e] = 0.0;
+                    for (long j = 0; j < L; j++) {
+                        double p = exp(s[j] - lse_i);
+                        const double *vj = vr + (size_t)j * d;
+                        for (int e = 0; e < d; e++) o[e] += p * vj[e];
+                    }
+                    lse[((size_t)b * H + h) * nrows + r] = lse_i;
+                }
+                free(qv);
+                free(s);
+            }
+        }
+    }
+    free(kr);
+    free(vr);
+    return 0;
+}
+
+/*
+ * Log-sum-exp merge of n per-chunk partials.
+ *   part_o [n][B][Sq][H][d], part_lse [n][B][H][Sq] (typed: f32 or f64)
+ *   out [B][Sq][H][d], lse [B][H][Sq] (double)
+ *   LSE = M + log sum_c exp(LSE_c - M) with M = max_c LSE_c,
+ *   out = sum_c exp(LSE_c - LSE) O_c.
+ */
+int k6o_lse_merge(int n, int B, long Sq, int H, int d, const void *part_o, const void *part_lse,
+                  int type, double *out, double *lse) {
+    if (n < 1 || B < 1 || Sq < 0 || H < 1 || d < 1) return -1;
+    size_t o_stride = (size_t)B * Sq * H * d;   /* elements per chunk */
+    size_t l_stride = (size_t)B * H * Sq;
+    long rows = (long)B * Sq * H;
+#pragma omp parallel for schedule(static)
+    for (long r = 0; r < rows; r++) {
+        int h = (int)(r % H);
+        long s = (r / H) % Sq;
+        int b = (int)(r / ((long)H * Sq));
+        size_t li = ((size_t)b * H + h) * Sq + s;
+        double M = -INFINITY;
+        for (int c = 0; c < n; c++) {
+            double x = load_elem(part_lse, type, c * l_stride + li);
+            if (x > M) M = x;
+        }
+        double sum = 0.0;
+        for (int c = 0; c < n; c++) sum += exp(load_elem(part_lse, type, c * l_stride + li) - M);
+        double L = M + log(sum);
+        double *o = out + (size_t)r * d;
+        for (int e = 0; e < d; e++) o[e] = 0.0;
+        for (int c = 0; c < n; c++) {
+            double w = exp(load_elem(part_lse, type, c * l_stride + li) - L);
+            for (int e = 0; e < d; e++)
+                o[e] += w * load_elem(part_o, type, c * o_stride + (size_t)r * d + e);
+        }
+        lse[li] = L;
+    }
+    return 0;
+}
+
+/*
+ * Sequence-partitioned <-> head-partitioned relayout, byte copy.
+ *   seq  buffer: [P][B][S/P][H][d]   (rank r holds tokens [r*Sl, (r+1)*Sl))
+ *   head buffer: [P][B][S][H/P][d]   (rank p holds heads  [p*Hl, (p+1)*Hl))
+ *   direction 0: seq -> head, 1: head -> seq.
+ */
+int k6o_relayout(const void *src, void *dst, int B, long S, int H, int d, int elem_bytes, int P,
+                 int direction) {
+    if (P < 1 || S % P || H % P || elem_bytes < 1) return -1;
+    long Sl = S / P;
+    int Hl = H / P;
+    const unsigned char *sp = (const unsigned char *)src;
+    unsigned char *dp = (unsigned char *)dst;
+    for (int r = 0; r < P; r++)
+        for (int p = 0; p < P; p++)
+            for (int b = 0; b < B; b++)
+                for (long s = 0; s < Sl; s++)
+                    for (int hh = 0; hh < Hl; hh++)
+                        for (int e = 0; e < d; e++) {
+                            size_t seq_i = ((((size_t)r * B + b) * Sl + s) * H + (size_t)p * Hl + hh) * d + e;
+                            size_t head_i = ((((size_t)p * B + b) * S + (size_t)r * Sl + s) * Hl + hh) * d + e;
+                            if (direction == 0)
+                                memcpy(dp + head_i * elem_bytes, sp + seq_i * elem_bytes, elem_bytes);
+                            else
+                                memcpy(dp + seq_i * elem_bytes, sp + head_i * elem_bytes, elem_bytes);
+                        }
+    return 0;
+}
+
+/* Latent grid of a video: frames (F-1)//4 + 1, spatial (px//8)//2.
+ * "Context Parallelism in vLLM Omni Neuron", section "Sequence Length
+ * Constraints", worked example. */
+void k6o_latent_grid(int height, int width, int frames, int *t, int *h, int *w) {
+    *t = (frames - 1) / 4 + 1;
+    *h = (height / 8) / 2;
+    *w = (width / 8) / 2;
+}
