@@ -1,0 +1,219 @@
+/*
+ * k6attn.h -- C ABI of libk6attn: joint-sequence attention for long-context
+ * video diffusion transformers on one NVIDIA GB300 (sm_103a).
+ *
+ * The path: rotary embeddings on Q and K, full non-causal multi-head attention
+ * over the joint sequence (video tokens followed by text/audio tokens),
+ * computed per K/V chunk with online softmax into partial outputs and their
+ * log-sum-exp, the log-sum-exp merge of those partials, and the
+ * sequence-partitioned <-> head-partitioned relayout.
+ *
+ * Sources (web pages; section names in quotes):
+ *  [USP]  xDiT PR #586 "KV-cache and joint tensors for USP": "How?" (joint
+ *         tensors), the USP dispatch listing (`_attention`, `ring_attn`,
+ *         `_ft_c_input_all_to_all`, `_ft_c_output_all_to_all`).
+ *  [CP]   "Context Parallelism in vLLM Omni Neuron": "Ring attention (current
+ *         implementation)", "Self-Attention with Context Parallelism",
+ *         "Comparison with Other CP Strategies", "Positional Embedding
+ *         Handling", "Scaling Properties", "Sequence Length Constraints".
+ *  [K6]   vLLM-Omni recipe "Kandinsky 6 TI2VA -- H100": parallel features
+ *         ("visual tokens (and their RoPE) are sharded", "Audio queries gather
+ *         the full visual sequence").
+ *
+ * Conventions shared by every call:
+ *  - Tensors are caller-owned DEVICE pointers, 16-byte aligned, densely packed
+ *    in the stated layout.  The library never allocates or frees them.
+ *  - Layout BSHD: q [B][Sq][H][d] with Sq = Nv + Nj, video rows first and the
+ *    Nj joint rows at the rear; k, v [B][Nv][H][d]; joint_k, joint_v
+ *    [B][Nj][H][d].  The key/value sequence is concat(k, joint_k) along the
+ *    token axis (length Sk = Nv + Nj = Sq).
+ *  - Element type: K6ATTN_BF16 (storage bf16, products fp32-accumulated,
+ *    softmax fp32) or K6ATTN_F32 (everything fp32, no tf32).
+ *  - lse arrays are fp32 [B][H][Sq], natural log of sum_j exp(s_ij) with
+ *    s_ij = q~_i . k~_j / sqrt(d).
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
+ *    asynchronous on that stream and returns after enqueueing.
+ *  - Calls never abort or trap.  Argument errors are found on the host before
+ *    any launch and return K6ATTN_ERR_INVALID_ARG / _UNSUPPORTED /
+ *    _WORKSPACE; k6attn_last_error() then holds a message (thread-local).
+ *    Device-side waits are bounded; a wait that runs out sets the handle's
+ *    device error word, which k6attn_sync() reports as K6ATTN_ERR_TIMEOUT.
+ */
+#ifndef K6ATTN_H
+#define K6ATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    K6ATTN_OK = 0,
+    K6ATTN_ERR_INVALID_ARG = 1, /* null pointer, bad size, indivisible split, aliasing, misalignment */
+    K6ATTN_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (e.g. bf16 with d != 128) */
+    K6ATTN_ERR_CUDA = 3,        /* a CUDA runtime call failed; message in k6attn_last_error() */
+    K6ATTN_ERR_TIMEOUT = 4,     /* a device-side wait ran out (reported by k6attn_sync) */
+    K6ATTN_ERR_WORKSPACE = 5    /* workspace pointer null or smaller than k6attn_workspace_bytes() */
+} k6attn_status;
+
+typedef enum { K6ATTN_BF16 = 0, K6ATTN_F32 = 1 } k6attn_dtype;
+
+/*
+ * Problem descriptor, fixed at handle creation.
+ *  B, H, d       batch, heads, head dim.  d in {64, 128} for F32; d == 128 for BF16.
+ *  grid_t/h/w    video latent grid; Nv = grid_t * grid_h * grid_w video tokens,
+ *                flattened row-major (t slowest, w fastest).
+ *  axis_dim[3]   head dims owned by the t, h, w rotary axes, in that order,
+ *                each even, summing to d (e.g. 32,48,48 for d = 128; 0,64,64
+ *                for 2-D image grids).
+ *  theta         rotary base (10000).
+ *  n_joint       Nj joint (text/audio) tokens, appended after the video tokens
+ *                on both the query and the key/value side ([USP] "How?").
+ *  joint_rope    0: joint tokens are not rotated; 1: joint token j turns by a
+ *                1-D rotary over the full head dim at position j.
+ * Rotary reading (the pages print no formula; [CP] "Positional Embedding
+ * Handling" shows per-token cos/sin tables): pair i of an axis segment, dims
+ * (2i, 2i+1) of that segment, turns by pos * theta^(-2i/d_axis) as a complex
+ * product.
+ */
+typedef struct {
+    int B, H, d;
+    k6attn_dtype dtype;
+    int grid_t, grid_h, grid_w;
+    int axis_dim[3];
+    double theta;
+    int n_joint;
+    int joint_rope;
+} k6attn_desc;
+
+typedef struct k6attn_handle *k6attn_t;
+
+/* Validate `desc`, build the per-axis rotary tables on the current device and
+ * allocate the handle's device error word.  On success *out owns them. */
+k6attn_status k6attn_create(const k6attn_desc *desc, k6attn_t *out);
+
+/* Free the handle and what it owns (synchronises the device first).  NULL is a no-op. */
+void k6attn_destroy(k6attn_t h);
+
+/* Device pointer and byte size of the handle-owned rotary tables (fp32 cos/sin
+ * pairs: axis t [grid_t][axis_dim0/2], axis h [grid_h][axis_dim1/2], axis w
+ * [grid_w][axis_dim2/2], then, when joint_rope == 1, joint [Nj][d/2]).
+ * Pass this pointer as `rope_tables` below. */
+const void *k6attn_rope_tables(k6attn_t h);
+size_t k6attn_rope_tables_bytes(k6attn_t h);
+
+/* Workspace bytes k6attn_forward needs for `n_chunks` K/V chunks, with
+ * (with_rope = 1) or without the rotated copies of q/k/joint_k:
+ *   rotated copies  (B*Sq*H*d + B*Nv*H*d + B*Nj*H*d) * elem   if with_rope
+ *   partial outputs n * B*Sq*H*d * 4 + n * B*H*Sq * 4          if n_chunks > 1
+ * (each region rounded up to 256 bytes).  0 when neither applies. */
+size_t k6attn_workspace_bytes(k6attn_t h, int n_chunks, int with_rope);
+
+/*
+ * Rotary embedding of q, k and joint_k, in place, one fused launch
+ * ([CP] "Self-Attention with Context Parallelism": `apply_rotary_emb_wan`
+ * on query and key; [K6] RoPE travels with the visual tokens).
+ *  q        [B][Sq][H][d]; row n < Nv at its video grid position, row n >= Nv
+ *           is joint token n - Nv.
+ *  k        [B][Nv][H][d] video keys.
+ *  joint_k  [B][Nj][H][d] (may be NULL when Nj == 0).
+ *  rope_tables  k6attn_rope_tables(h) or a caller copy in the same layout.
+ * bf16 tensors are rotated in fp32 and rounded to nearest even.
+ */
+k6attn_status k6attn_rope_qk(k6attn_t h, void *q, void *k, void *joint_k, const void *rope_tables,
+                             void *stream);
+
+/*
+ * Joint-sequence attention forward ([USP] `_attention`; [CP] "Ring attention
+ * (current implementation)": each K/V chunk is attended separately and the
+ * partials combine through their log-sum-exp).
+ *  q, k, v, joint_k, joint_v  inputs in the layouts above (joint_* may be NULL
+ *           when Nj == 0).  Not modified.
+ *  rope_tables  NULL: q/k/joint_k are already rotated.  Otherwise the rotated
+ *           copies are written to the workspace first (k6attn_rope_qk math).
+ *  n_chunks K/V chunks: chunk c covers keys [c*Sk/n, (c+1)*Sk/n) of
+ *           concat(k, joint_k); Sk % n_chunks must be 0 ([CP] "Sequence
+ *           Length Constraints").  n_chunks == 1 writes out/lse directly;
+ *           n_chunks > 1 writes per-chunk fp32 partials [n][B][Sq][H][d] and
+ *           [n][B][H][Sq] into the workspace and merges them (k6attn_lse_merge).
+ *  out      [B][Sq][H][d], same element type as q.  Must not alias any input.
+ *  lse      fp32 [B][H][Sq] (may be NULL: not written).
+ *  workspace, workspace_bytes  caller-owned device scratch of at least
+ *           k6attn_workspace_bytes(h, n_chunks, rope_tables != NULL); may be
+ *           NULL when that is 0.
+ */
+k6attn_status k6attn_forward(k6attn_t h, const void *q, const void *k, const void *v, const void *joint_k,
+                             const void *joint_v, const void *rope_tables, int n_chunks, void *out, float *lse,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The attention step alone, on already-rotated inputs: for each K/V chunk c
+ * (as in k6attn_forward) the chunk's softmax(q k^T / sqrt(d)) v and its
+ * log-sum-exp ([CP] "Ring attention (current implementation)").
+ *  n_chunks == 1: out is [B][Sq][H][d] in the handle's element type and lse
+ *           fp32 [B][H][Sq] (may be NULL).
+ *  n_chunks > 1:  out is fp32 partials [n_chunks][B][Sq][H][d] and lse fp32
+ *           [n_chunks][B][H][Sq] (required); combine them with
+ *           k6attn_lse_merge.
+ * Inputs as in k6attn_forward; outputs must not alias them.
+ */
+k6attn_status k6attn_attention_chunks(k6attn_t h, const void *q, const void *k, const void *v, const void *joint_k,
+                                      const void *joint_v, int n_chunks, void *out, float *lse, void *stream);
+
+/*
+ * Log-sum-exp merge of per-chunk partials (ring attention's combine step,
+ * [CP] "Ring attention (current implementation)", "Scaling Properties"):
+ *   LSE = log sum_c exp(LSE_c),  out = sum_c exp(LSE_c - LSE) * O_c.
+ *  part_o   fp32 [n_chunks][B][Sq][H][d];  part_lse fp32 [n_chunks][B][H][Sq].
+ *  out      [B][Sq][H][d] in the handle's element type;  lse fp32 [B][H][Sq]
+ *           (may be NULL).  Outputs must not alias the partials.
+ */
+k6attn_status k6attn_lse_merge(k6attn_t h, const float *part_o, const float *part_lse, int n_chunks, void *out,
+                               float *lse, void *stream);
+
+/*
+ * Sequence-partitioned <-> head-partitioned relayout, the single-GPU form of
+ * the Ulysses all-to-all ([USP] `_ft_c_input_all_to_all` /
+ * `_ft_c_output_all_to_all`; [CP] "Comparison with Other CP Strategies").
+ * A bit-exact permutation; no arithmetic.  With Sl = S/P and Hl = H/P:
+ *   seq  buffer [P][B][Sl][H][d]  (part r holds tokens [r*Sl, (r+1)*Sl))
+ *   head buffer [P][B][S][Hl][d]  (part p holds heads  [p*Hl, (p+1)*Hl))
+ *   direction 0 (seq -> head): head[p][b][r*Sl+s][hh][e] = seq[r][b][s][p*Hl+hh][e]
+ *   direction 1 (head -> seq): the inverse.
+ * For B == 1 the seq buffer is byte-identical to a contiguous [1][S][H][d].
+ *  elem_bytes 2 or 4.  Requires S % P == 0 and H % P == 0 (INVALID_ARG
+ *  otherwise, like [CP]'s ValueError for 3645 tokens on 8 ranks), and
+ *  non-overlapping src/dst.  No handle needed.
+ */
+k6attn_status k6attn_seq2head_relayout(const void *src, void *dst, int B, long S, int H, int d, int elem_bytes,
+                                       int P, int direction, void *stream);
+
+/* Synchronise `stream`, then read and clear the handle's device error word:
+ * K6ATTN_ERR_TIMEOUT if any kernel of this handle gave up on a wait,
+ * K6ATTN_ERR_CUDA on an asynchronous CUDA error, else K6ATTN_OK. */
+k6attn_status k6attn_sync(k6attn_t h, void *stream);
+
+/* Handle options.
+ *  K6ATTN_OPT_WAIT_LIMIT_NS   upper bound, in nanoseconds, on any single
+ *      device-side wait of this handle's kernels (default 2e9).  0 makes every
+ *      wait give up at once, which tests use to exercise the timeout path
+ *      without hanging the GPU.
+ *  K6ATTN_OPT_STRICT_MMA_ORDER  1: the bf16 kernel waits for each P.V product
+ *      to finish reading P (which shares tensor memory with the next S tile)
+ *      before issuing the next Q.K^T product; 0 (default): relies on the
+ *      tensor pipe executing one thread's MMAs in issue order.
+ * Returns K6ATTN_ERR_INVALID_ARG for an unknown option or a negative value. */
+typedef enum { K6ATTN_OPT_WAIT_LIMIT_NS = 0, K6ATTN_OPT_STRICT_MMA_ORDER = 1 } k6attn_option;
+k6attn_status k6attn_set_option(k6attn_t h, k6attn_option opt, long long value);
+
+/* Static description of a status code, and the last error message of the
+ * calling thread ("" if none). */
+const char *k6attn_status_string(k6attn_status s);
+const char *k6attn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* K6ATTN_H */

@@ -1,0 +1,362 @@
+// k6_api.cu -- the C ABI of libk6attn: handle, argument checks, workspace
+// layout and the launch sequence of one forward pass.  Every check runs on
+// the host before any launch; nothing here aborts.
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "k6attn.h"
+#include "k6_internal.h"
+
+struct k6attn_handle {
+    k6attn_desc desc;
+    k6::Geom g;
+    float2 *tables = nullptr;
+    size_t table_bytes = 0;
+    int *err = nullptr;                 // device error word
+    unsigned long long wait_limit_ns = 2000000000ull;
+    int strict_order = 0;
+    int device = 0;
+};
+
+namespace k6 {
+
+static thread_local char g_msg[512];
+
+k6attn_status set_error(k6attn_status s, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+k6attn_status cuda_check(cudaError_t e, const char *what) {
+    if (e == cudaSuccess) return K6ATTN_OK;
+    return set_error(K6ATTN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+static size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+static bool overlap(const void *a, size_t na, const void *b, size_t nb) {
+    if (!a || !b || !na || !nb) return false;
+    uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+struct WsLayout {
+    size_t q_rot = 0, k_rot = 0, jk_rot = 0, part_o = 0, part_lse = 0, total = 0;
+};
+
+static WsLayout ws_layout(const Geom &g, int n, bool rope) {
+    WsLayout L;
+    size_t off = 0;
+    const size_t row = (size_t)g.H * g.d;
+    if (rope) {
+        L.q_rot = off;
+        off += round256((size_t)g.B * g.S * row * g.elem);
+        L.k_rot = off;
+        off += round256((size_t)g.B * g.Nv * row * g.elem);
+        L.jk_rot = off;
+        off += round256((size_t)g.B * g.Nj * row * g.elem);
+    }
+    if (n > 1) {
+        L.part_o = off;
+        off += round256((size_t)n * g.B * g.S * row * 4);
+        L.part_lse = off;
+        off += round256((size_t)n * g.B * g.H * g.S * 4);
+    }
+    L.total = off;
+    return L;
+}
+
+// The attention kernels on rotated inputs: n_chunks == 1 writes out/lse,
+// n_chunks > 1 writes fp32 partials into out/lse (see k6attn_attention_chunks).
+static k6attn_status run_attention(k6attn_handle *h, const void *q, const void *k, const void *v, const void *jk,
+                                   const void *jv, int n_chunks, void *out, float *lse, cudaStream_t st) {
+    const Geom &g = h->g;
+    if (g.elem == 2) {
+        AttnTcOptions opt{h->wait_limit_ns, h->err, h->strict_order};
+        const char *why = nullptr;
+        cudaError_t e = launch_attn_tc(g, q, k, v, jk, jv, n_chunks, out, lse, opt, st, &why);
+        if (e != cudaSuccess) {
+            if (why) return set_error(K6ATTN_ERR_CUDA, "attention: %s", why);
+            return cuda_check(e, "attention launch");
+        }
+        return K6ATTN_OK;
+    }
+    const size_t o_stride = (size_t)g.B * g.S * g.H * g.d, l_stride = (size_t)g.B * g.H * g.S;
+    return cuda_check(launch_attn_f32(g, static_cast<const float *>(q), static_cast<const float *>(k),
+                                      static_cast<const float *>(v), static_cast<const float *>(jk),
+                                      static_cast<const float *>(jv), n_chunks, static_cast<float *>(out), o_stride,
+                                      lse, l_stride, st),
+                      "fp32 attention launch");
+}
+
+// Checks shared by the two attention entry points.
+static k6attn_status check_inputs(const char *fn, const Geom &g, const void *q, const void *k, const void *v,
+                                  const void *jk, const void *jv, int n_chunks, const void *out, size_t out_bytes,
+                                  const float *lse, size_t lse_bytes) {
+    if (!q || !k || !v || !out) return set_error(K6ATTN_ERR_INVALID_ARG, "%s: null q, k, v or out", fn);
+    if (g.Nj > 0 && (!jk || !jv))
+        return set_error(K6ATTN_ERR_INVALID_ARG, "%s: %ld joint tokens but joint_k/joint_v is null", fn, g.Nj);
+    if (n_chunks < 1) return set_error(K6ATTN_ERR_INVALID_ARG, "%s: n_chunks must be >= 1", fn);
+    if (g.S % n_chunks)
+        return set_error(K6ATTN_ERR_INVALID_ARG, "%s: sequence length %ld is not divisible by %d chunks", fn, g.S,
+                         n_chunks);
+    const void *ptrs[] = {q, k, v, jk, jv, out};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return set_error(K6ATTN_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", fn);
+    if (reinterpret_cast<uintptr_t>(lse) & 3) return set_error(K6ATTN_ERR_INVALID_ARG, "%s: lse misaligned", fn);
+    const size_t row = (size_t)g.H * g.d * g.elem;
+    const size_t qb = g.B * g.S * row, kvb = g.B * g.Nv * row, jb = g.B * g.Nj * row;
+    const void *ins[] = {q, k, v, jk, jv};
+    const size_t insz[] = {qb, kvb, kvb, jb, jb};
+    for (int i = 0; i < 5; i++)
+        if (overlap(out, out_bytes, ins[i], insz[i]) || overlap(lse, lse_bytes, ins[i], insz[i]))
+            return set_error(K6ATTN_ERR_INVALID_ARG, "%s: out or lse overlaps an input", fn);
+    if (overlap(out, out_bytes, lse, lse_bytes)) return set_error(K6ATTN_ERR_INVALID_ARG, "%s: out overlaps lse", fn);
+    return K6ATTN_OK;
+}
+
+}  // namespace k6
+
+using namespace k6;
+
+extern "C" {
+
+const char *k6attn_status_string(k6attn_status s) {
+    switch (s) {
+        case K6ATTN_OK: return "ok";
+        case K6ATTN_ERR_INVALID_ARG: return "invalid argument";
+        case K6ATTN_ERR_UNSUPPORTED: return "unsupported";
+        case K6ATTN_ERR_CUDA: return "CUDA error";
+        case K6ATTN_ERR_TIMEOUT: return "device wait timed out";
+        case K6ATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+const char *k6attn_last_error(void) { return g_msg; }
+
+k6attn_status k6attn_create(const k6attn_desc *desc, k6attn_t *out) {
+    g_msg[0] = 0;
+    if (!desc || !out) return set_error(K6ATTN_ERR_INVALID_ARG, "create: null descriptor or output pointer");
+    *out = nullptr;
+    const k6attn_desc &d = *desc;
+    if (d.B < 1 || d.H < 1 || d.grid_t < 1 || d.grid_h < 1 || d.grid_w < 1 || d.n_joint < 0)
+        return set_error(K6ATTN_ERR_INVALID_ARG, "create: B, H and the grid must be >= 1, n_joint >= 0");
+    if (d.dtype != K6ATTN_BF16 && d.dtype != K6ATTN_F32)
+        return set_error(K6ATTN_ERR_INVALID_ARG, "create: unknown dtype %d", (int)d.dtype);
+    if (d.d != 64 && d.d != 128) return set_error(K6ATTN_ERR_UNSUPPORTED, "create: head dim %d (want 64 or 128)", d.d);
+    if (d.dtype == K6ATTN_BF16 && d.d != 128)
+        return set_error(K6ATTN_ERR_UNSUPPORTED, "create: bf16 path needs head dim 128 (got %d)", d.d);
+    int sum = 0;
+    for (int a = 0; a < 3; a++) {
+        if (d.axis_dim[a] < 0 || (d.axis_dim[a] & 1))
+            return set_error(K6ATTN_ERR_INVALID_ARG, "create: axis_dim[%d] = %d must be even and >= 0", a,
+                             d.axis_dim[a]);
+        sum += d.axis_dim[a];
+    }
+    if (sum != d.d) return set_error(K6ATTN_ERR_INVALID_ARG, "create: axis dims sum to %d, head dim is %d", sum, d.d);
+    if (!(d.theta > 0.0)) return set_error(K6ATTN_ERR_INVALID_ARG, "create: theta must be > 0");
+    if (d.joint_rope != 0 && d.joint_rope != 1)
+        return set_error(K6ATTN_ERR_INVALID_ARG, "create: joint_rope must be 0 or 1");
+    const long Nv = (long)d.grid_t * d.grid_h * d.grid_w;
+    const long S = Nv + d.n_joint;
+    // TMA coordinates and several index products are 32-bit
+    if (S >= (1L << 30) || (long)d.B * S * d.H >= (1L << 31))
+        return set_error(K6ATTN_ERR_UNSUPPORTED, "create: problem too large (B*S*H = %ld)", (long)d.B * S * d.H);
+
+    k6attn_handle *h = new k6attn_handle();
+    h->desc = d;
+    Geom &g = h->g;
+    g.B = d.B, g.H = d.H, g.d = d.d;
+    g.Nv = Nv, g.Nj = d.n_joint, g.S = S;
+    g.grid_t = d.grid_t, g.grid_h = d.grid_h, g.grid_w = d.grid_w;
+    for (int a = 0; a < 3; a++) g.axis_dim[a] = d.axis_dim[a];
+    g.joint_rope = d.joint_rope;
+    g.elem = d.dtype == K6ATTN_BF16 ? 2 : 4;
+    cudaGetDevice(&h->device);
+    RopeLayout L = rope_layout(g);
+    h->table_bytes = (size_t)L.total * sizeof(float2);
+    k6attn_status st = cuda_check(cudaMalloc(&h->err, sizeof(int)), "create: error word");
+    if (st == K6ATTN_OK) st = cuda_check(cudaMemset(h->err, 0, sizeof(int)), "create: error word");
+    if (st == K6ATTN_OK && h->table_bytes)
+        st = cuda_check(cudaMalloc(&h->tables, h->table_bytes), "create: rotary tables");
+    if (st == K6ATTN_OK) st = cuda_check(launch_rope_tables(g, d.theta, h->tables, 0), "create: rotary tables");
+    if (st == K6ATTN_OK) st = cuda_check(cudaDeviceSynchronize(), "create: rotary tables");
+    if (st != K6ATTN_OK) {
+        cudaFree(h->tables);
+        cudaFree(h->err);
+        delete h;
+        return st;
+    }
+    *out = h;
+    return K6ATTN_OK;
+}
+
+void k6attn_destroy(k6attn_t h) {
+    if (!h) return;
+    cudaDeviceSynchronize();
+    cudaFree(h->tables);
+    cudaFree(h->err);
+    delete h;
+}
+
+const void *k6attn_rope_tables(k6attn_t h) { return h ? h->tables : nullptr; }
+size_t k6attn_rope_tables_bytes(k6attn_t h) { return h ? h->table_bytes : 0; }
+
+size_t k6attn_workspace_bytes(k6attn_t h, int n_chunks, int with_rope) {
+    if (!h || n_chunks < 1) return 0;
+    return ws_layout(h->g, n_chunks, with_rope != 0).total;
+}
+
+k6attn_status k6attn_set_option(k6attn_t h, k6attn_option opt, long long value) {
+    if (!h) return set_error(K6ATTN_ERR_INVALID_ARG, "set_option: null handle");
+    if (value < 0) return set_error(K6ATTN_ERR_INVALID_ARG, "set_option: negative value");
+    switch (opt) {
+        case K6ATTN_OPT_WAIT_LIMIT_NS: h->wait_limit_ns = (unsigned long long)value; return K6ATTN_OK;
+        case K6ATTN_OPT_STRICT_MMA_ORDER: h->strict_order = value ? 1 : 0; return K6ATTN_OK;
+    }
+    return set_error(K6ATTN_ERR_INVALID_ARG, "set_option: unknown option %d", (int)opt);
+}
+
+k6attn_status k6attn_rope_qk(k6attn_t h, void *q, void *k, void *joint_k, const void *rope_tables, void *stream) {
+    g_msg[0] = 0;
+    if (!h) return set_error(K6ATTN_ERR_INVALID_ARG, "rope_qk: null handle");
+    const Geom &g = h->g;
+    if (!q || !k || (g.Nj > 0 && !joint_k) || (!rope_tables && h->table_bytes))
+        return set_error(K6ATTN_ERR_INVALID_ARG, "rope_qk: null tensor or table pointer");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(joint_k) || !aligned16(rope_tables))
+        return set_error(K6ATTN_ERR_INVALID_ARG, "rope_qk: pointers must be 16-byte aligned");
+    const size_t row = (size_t)g.H * g.d * g.elem;
+    if (overlap(q, g.B * g.S * row, k, g.B * g.Nv * row) || overlap(q, g.B * g.S * row, joint_k, g.B * g.Nj * row) ||
+        overlap(k, g.B * g.Nv * row, joint_k, g.B * g.Nj * row))
+        return set_error(K6ATTN_ERR_INVALID_ARG, "rope_qk: q, k and joint_k overlap");
+    return cuda_check(launch_rope_qk(g, static_cast<const float2 *>(rope_tables), q, q, k, k, joint_k, joint_k,
+                                     static_cast<cudaStream_t>(stream)),
+                      "rope_qk launch");
+}
+
+k6attn_status k6attn_lse_merge(k6attn_t h, const float *part_o, const float *part_lse, int n_chunks, void *out,
+                               float *lse, void *stream) {
+    g_msg[0] = 0;
+    if (!h) return set_error(K6ATTN_ERR_INVALID_ARG, "lse_merge: null handle");
+    const Geom &g = h->g;
+    if (!part_o || !part_lse || !out) return set_error(K6ATTN_ERR_INVALID_ARG, "lse_merge: null pointer");
+    if (n_chunks < 1) return set_error(K6ATTN_ERR_INVALID_ARG, "lse_merge: n_chunks must be >= 1");
+    if (!aligned16(part_o) || !aligned16(out) || (reinterpret_cast<uintptr_t>(part_lse) & 3) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3))
+        return set_error(K6ATTN_ERR_INVALID_ARG, "lse_merge: partials/out must be 16-byte aligned, lse 4-byte");
+    const size_t po = (size_t)n_chunks * g.B * g.S * g.H * g.d * 4, pl = (size_t)n_chunks * g.B * g.H * g.S * 4;
+    const size_t ob = (size_t)g.B * g.S * g.H * g.d * g.elem, lb = (size_t)g.B * g.H * g.S * 4;
+    if (overlap(out, ob, part_o, po) || overlap(out, ob, part_lse, pl) || overlap(lse, lb, part_o, po) ||
+        overlap(lse, lb, part_lse, pl) || overlap(out, ob, lse, lb))
+        return set_error(K6ATTN_ERR_INVALID_ARG, "lse_merge: outputs overlap the partials");
+    return cuda_check(launch_lse_merge(g, n_chunks, part_o, part_lse, out, lse, static_cast<cudaStream_t>(stream)),
+                      "lse_merge launch");
+}
+
+k6attn_status k6attn_forward(k6attn_t h, const void *q, const void *k, const void *v, const void *joint_k,
+                             const void *joint_v, const void *rope_tables, int n_chunks, void *out, float *lse,
+                             void *workspace, size_t workspace_bytes, void *stream) {
+    g_msg[0] = 0;
+    if (!h) return set_error(K6ATTN_ERR_INVALID_ARG, "forward: null handle");
+    const Geom &g = h->g;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t qb = (size_t)g.B * g.S * g.H * g.d * g.elem, lb = (size_t)g.B * g.H * g.S * 4;
+    k6attn_status s = check_inputs("forward", g, q, k, v, joint_k, joint_v, n_chunks, out, qb, lse, lb);
+    if (s != K6ATTN_OK) return s;
+    if (!aligned16(rope_tables) || !aligned16(workspace))
+        return set_error(K6ATTN_ERR_INVALID_ARG, "forward: pointers must be 16-byte aligned");
+    const bool rope = rope_tables != nullptr;
+    const WsLayout L = ws_layout(g, n_chunks, rope);
+    if (L.total) {
+        if (!workspace || workspace_bytes < L.total)
+            return set_error(K6ATTN_ERR_WORKSPACE, "forward: workspace of %zu bytes needed, %zu given", L.total,
+                             workspace ? workspace_bytes : (size_t)0);
+        const size_t row = (size_t)g.H * g.d * g.elem;
+        const void *ins[] = {q, k, v, joint_k, joint_v};
+        const size_t insz[] = {g.B * g.S * row, g.B * g.Nv * row, g.B * g.Nv * row, g.B * g.Nj * row,
+                               g.B * g.Nj * row};
+        for (int i = 0; i < 5; i++)
+            if (overlap(workspace, L.total, ins[i], insz[i]))
+                return set_error(K6ATTN_ERR_INVALID_ARG, "forward: workspace overlaps an input");
+        if (overlap(workspace, L.total, out, qb) || overlap(workspace, L.total, lse, lb))
+            return set_error(K6ATTN_ERR_INVALID_ARG, "forward: workspace overlaps out or lse");
+    }
+    char *ws = static_cast<char *>(workspace);
+    const void *qa = q, *ka = k, *jka = joint_k;
+    if (rope) {
+        void *qr = ws + L.q_rot, *kr = ws + L.k_rot, *jkr = g.Nj ? ws + L.jk_rot : nullptr;
+        s = cuda_check(launch_rope_qk(g, static_cast<const float2 *>(rope_tables), q, qr, k, kr, joint_k, jkr, st),
+                       "forward: rope launch");
+        if (s != K6ATTN_OK) return s;
+        qa = qr, ka = kr, jka = jkr;
+    }
+    if (n_chunks == 1) return run_attention(h, qa, ka, v, jka, joint_v, 1, out, lse, st);
+    float *part_o = reinterpret_cast<float *>(ws + L.part_o);
+    float *part_lse = reinterpret_cast<float *>(ws + L.part_lse);
+    s = run_attention(h, qa, ka, v, jka, joint_v, n_chunks, part_o, part_lse, st);
+    if (s != K6ATTN_OK) return s;
+    return cuda_check(launch_lse_merge(g, n_chunks, part_o, part_lse, out, lse, st), "forward: merge launch");
+}
+
+k6attn_status k6attn_attention_chunks(k6attn_t h, const void *q, const void *k, const void *v, const void *joint_k,
+                                      const void *joint_v, int n_chunks, void *out, float *lse, void *stream) {
+    g_msg[0] = 0;
+    if (!h) return set_error(K6ATTN_ERR_INVALID_ARG, "attention_chunks: null handle");
+    const Geom &g = h->g;
+    if (n_chunks > 1 && !lse)
+        return set_error(K6ATTN_ERR_INVALID_ARG, "attention_chunks: partial lse is required when n_chunks > 1");
+    const int n = n_chunks > 1 ? n_chunks : 1;
+    const size_t ob = (size_t)n * g.B * g.S * g.H * g.d * (n_chunks > 1 ? 4 : g.elem);
+    const size_t lb = (size_t)n * g.B * g.H * g.S * 4;
+    k6attn_status s = check_inputs("attention_chunks", g, q, k, v, joint_k, joint_v, n_chunks, out, ob, lse, lb);
+    if (s != K6ATTN_OK) return s;
+    return run_attention(h, q, k, v, joint_k, joint_v, n_chunks, out, lse, static_cast<cudaStream_t>(stream));
+}
+
+k6attn_status k6attn_seq2head_relayout(const void *src, void *dst, int B, long S, int H, int d, int elem_bytes,
+                                       int P, int direction, void *stream) {
+    g_msg[0] = 0;
+    if (!src || !dst) return set_error(K6ATTN_ERR_INVALID_ARG, "relayout: null pointer");
+    if (B < 1 || S < 1 || H < 1 || d < 1 || P < 1)
+        return set_error(K6ATTN_ERR_INVALID_ARG, "relayout: B, S, H, d, P must be >= 1");
+    if (elem_bytes != 2 && elem_bytes != 4) return set_error(K6ATTN_ERR_INVALID_ARG, "relayout: elem_bytes 2 or 4");
+    if (direction != 0 && direction != 1) return set_error(K6ATTN_ERR_INVALID_ARG, "relayout: direction 0 or 1");
+    if (S % P)
+        return set_error(K6ATTN_ERR_INVALID_ARG, "relayout: sequence length %ld is not divisible by %d", S, P);
+    if (H % P) return set_error(K6ATTN_ERR_INVALID_ARG, "relayout: %d heads are not divisible by %d", H, P);
+    if ((long long)P * B * S >= (1LL << 32) || (long long)(H / P) * d * elem_bytes >= (1LL << 31))
+        return set_error(K6ATTN_ERR_UNSUPPORTED, "relayout: too large");
+    if (!aligned16(src) || !aligned16(dst))
+        return set_error(K6ATTN_ERR_INVALID_ARG, "relayout: pointers must be 16-byte aligned");
+    const size_t bytes = (size_t)B * S * H * d * elem_bytes;
+    if (overlap(src, bytes, dst, bytes)) return set_error(K6ATTN_ERR_INVALID_ARG, "relayout: src and dst overlap");
+    return cuda_check(launch_relayout(src, dst, B, S, H, d, elem_bytes, P, direction, static_cast<cudaStream_t>(stream)),
+                      "relayout launch");
+}
+
+k6attn_status k6attn_sync(k6attn_t h, void *stream) {
+    g_msg[0] = 0;
+    if (!h) return set_error(K6ATTN_ERR_INVALID_ARG, "sync: null handle");
+    k6attn_status s = cuda_check(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "sync");
+    if (s != K6ATTN_OK) return s;
+    int word = 0;
+    s = cuda_check(cudaMemcpy(&word, h->err, sizeof word, cudaMemcpyDeviceToHost), "sync: error word");
+    if (s != K6ATTN_OK) return s;
+    if (word) {
+        cudaMemset(h->err, 0, sizeof(int));
+        return set_error(K6ATTN_ERR_TIMEOUT, "a device-side wait gave up (code %d)", word);
+    }
+    return K6ATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,68 @@
+// k6_internal.h -- host-side declarations shared by the translation units of
+// libk6attn (launchers, geometry, rotary table layout).  Not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "k6attn.h"
+
+namespace k6 {
+
+// Geometry of one joint attention problem, as the kernels see it.
+struct Geom {
+    int B, H, d;
+    long Nv, Nj, S;          // S = Nv + Nj (query rows = key rows)
+    int grid_t, grid_h, grid_w;
+    int axis_dim[3];
+    int joint_rope;
+    int elem;                // bytes per element (2 bf16, 4 f32)
+};
+
+// Offsets (in float2 entries) of the rotary tables inside one buffer.
+struct RopeLayout {
+    long off[4];             // axis t, h, w, joint
+    long total;              // entries
+};
+
+RopeLayout rope_layout(const Geom &g);
+
+// Error reporting of the host side (thread-local message).
+k6attn_status set_error(k6attn_status s, const char *fmt, ...);
+k6attn_status cuda_check(cudaError_t e, const char *what);
+
+// ---- launchers (return cudaSuccess or the launch error) ----
+
+cudaError_t launch_rope_tables(const Geom &g, double theta, float2 *tables, cudaStream_t st);
+
+// Rotary embedding of q [B][S][H][d], k [B][Nv][H][d], jk [B][Nj][H][d]
+// from src_* into dst_* (dst may equal src).
+cudaError_t launch_rope_qk(const Geom &g, const float2 *tables, const void *src_q, void *dst_q, const void *src_k,
+                           void *dst_k, const void *src_jk, void *dst_jk, cudaStream_t st);
+
+cudaError_t launch_lse_merge(const Geom &g, int n, const float *part_o, const float *part_lse, void *out, float *lse,
+                             cudaStream_t st);
+
+cudaError_t launch_relayout(const void *src, void *dst, int B, long S, int H, int d, int elem_bytes, int P,
+                            int direction, cudaStream_t st);
+
+// fp32 attention (SIMT): per chunk c writes out_c [B][S][H][d] and lse_c
+// [B][H][S], at out + c*o_stride / lse + c*l_stride.
+cudaError_t launch_attn_f32(const Geom &g, const float *q, const float *k, const float *v, const float *jk,
+                            const float *jv, int n_chunks, float *out, size_t o_stride, float *lse, size_t l_stride,
+                            cudaStream_t st);
+
+// bf16 attention on tcgen05 tensor cores.  n_chunks == 1: out is bf16
+// [B][S][H][d]; n_chunks > 1: out is fp32 partials [n][B][S][H][d].
+// lse is fp32 [n][B][H][S] (may be null when n_chunks == 1).
+struct AttnTcOptions {
+    unsigned long long wait_limit_ns;
+    int *err;
+    int strict_order;        // 1: wait for P.V to finish before reusing its TMEM
+};
+cudaError_t launch_attn_tc(const Geom &g, const void *q, const void *k, const void *v, const void *jk,
+                           const void *jv, int n_chunks, void *out, float *lse, const AttnTcOptions &opt,
+                           cudaStream_t st, const char **why);
+
+}  // namespace k6

@@ -1,0 +1,212 @@
+// k6_rope.cu -- rotary embedding of Q and K for the joint video/text sequence.
+//
+// "Context Parallelism in vLLM Omni Neuron", sections "Self-Attention with
+// Context Parallelism" (`apply_rotary_emb_wan` on query and key after QK-norm,
+// before attention) and "Positional Embedding Handling" (per-token cos/sin
+// tables, sliced by token range).  The pages print no formula; this library
+// reads it as: each axis (t, h, w) owns a contiguous segment of axis_dim[a]
+// head dims, in that order; pair i of the segment, dims (2i, 2i+1), turns by
+// pos_a * theta^(-2i/axis_dim[a]) as the complex product (x + iy) e^{i angle};
+// joint tokens are unrotated, or (joint_rope) turn over the full head dim by
+// their 0-based joint index.
+//
+// Tables are factorised per axis (grid_t + grid_h + grid_w rows instead of
+// one row per token), fp32 (cos, sin), built once per handle in fp64.
+// The rotation kernel is HBM-bound: one 16-byte load and one 16-byte store
+// per 8 bf16 (or 4 f32) elements; Q, K and joint K are rotated in one launch.
+#include <cuda_bf16.h>
+
+#include "k6_internal.h"
+
+namespace k6 {
+
+RopeLayout rope_layout(const Geom &g) {
+    RopeLayout L;
+    L.off[0] = 0;
+    L.off[1] = L.off[0] + (long)g.grid_t * (g.axis_dim[0] / 2);
+    L.off[2] = L.off[1] + (long)g.grid_h * (g.axis_dim[1] / 2);
+    L.off[3] = L.off[2] + (long)g.grid_w * (g.axis_dim[2] / 2);
+    L.total = L.off[3] + (g.joint_rope ? g.Nj * (g.d / 2) : 0);
+    return L;
+}
+
+struct TableArgs {
+    long off[4];
+    long total;
+    int half[4];    // pairs per row: axis_dim[a]/2, and d/2 for the joint table
+    int dims[4];    // rotating dims of each table: axis_dim[a], d
+    double theta;
+};
+
+__global__ void rope_table_kernel(TableArgs a, float2 *tab) {
+    long i = blockIdx.x * (long)blockDim.x + threadIdx.x;
+    if (i >= a.total) return;
+    int t = 0;
+    while (t < 3 && i >= a.off[t + 1]) t++;
+    long local = i - a.off[t];
+    long pos = local / a.half[t];
+    int pair = (int)(local % a.half[t]);
+    double omega = pow(a.theta, -2.0 * pair / a.dims[t]);
+    double s, c;
+    sincos((double)pos * omega, &s, &c);
+    tab[i] = make_float2((float)c, (float)s);
+}
+
+cudaError_t launch_rope_tables(const Geom &g, double theta, float2 *tables, cudaStream_t st) {
+    RopeLayout L = rope_layout(g);
+    TableArgs a;
+    for (int t = 0; t < 4; t++) a.off[t] = L.off[t];
+    a.total = L.total;
+    for (int t = 0; t < 3; t++) {
+        a.half[t] = g.axis_dim[t] / 2 > 0 ? g.axis_dim[t] / 2 : 1;
+        a.dims[t] = g.axis_dim[t] > 0 ? g.axis_dim[t] : 1;
+    }
+    a.half[3] = g.d / 2;
+    a.dims[3] = g.d;
+    a.theta = theta;
+    if (L.total == 0) return cudaSuccess;
+    int threads = 256;
+    long blocks = (L.total + threads - 1) / threads;
+    rope_table_kernel<<<(unsigned)blocks, threads, 0, st>>>(a, tables);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ rotate
+
+struct RopeArgs {
+    const void *src[3];
+    void *dst[3];
+    long tokens[3];      // B*S, B*Nv, B*Nj
+    long seq[3];         // S, Nv, Nj  (tokens per batch)
+    long Nv;
+    int H, d;
+    int grid_h, grid_w;
+    int seg1, seg2;      // first pair index of the h and w segments
+    int joint_rope;
+    long off[4];         // table offsets (float2 entries)
+    int half[3];         // pairs per axis row
+};
+
+// (cos, sin) of pair `i` for a token with video position (t, h, w), or joint
+// index j (j >= 0 means joint).
+__device__ __forceinline__ float2 rope_cs(const RopeArgs &a, const float2 *tab, int i, int t, int h, int w,
+                                          long j) {
+    if (j >= 0) {
+        if (!a.joint_rope) return make_float2(1.f, 0.f);
+        return tab[a.off[3] + j * (a.d / 2) + i];
+    }
+    if (i < a.seg1) return tab[a.off[0] + (long)t * a.half[0] + i];
+    if (i < a.seg2) return tab[a.off[1] + (long)h * a.half[1] + (i - a.seg1)];
+    return tab[a.off[2] + (long)w * a.half[2] + (i - a.seg2)];
+}
+
+template <typename T>
+struct Vec;
+template <>
+struct Vec<__nv_bfloat16> {
+    static constexpr int kPairs = 4;
+    __device__ static void load(const void *p, float (&x)[8]) {
+        uint4 u = *reinterpret_cast<const uint4 *>(p);
+        const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&u);
+        for (int k = 0; k < 4; k++) {
+            float2 f = __bfloat1622float2(b[k]);
+            x[2 * k] = f.x;
+            x[2 * k + 1] = f.y;
+        }
+    }
+    __device__ static void store(void *p, const float (&x)[8]) {
+        uint4 u;
+        __nv_bfloat162 *b = reinterpret_cast<__nv_bfloat162 *>(&u);
+        for (int k = 0; k < 4; k++) b[k] = __floats2bfloat162_rn(x[2 * k], x[2 * k + 1]);
+        *reinterpret_cast<uint4 *>(p) = u;
+    }
+};
+template <>
+struct Vec<float> {
+    static constexpr int kPairs = 2;
+    __device__ static void load(const void *p, float (&x)[8]) {
+        float4 u = *reinterpret_cast<const float4 *>(p);
+        x[0] = u.x, x[1] = u.y, x[2] = u.z, x[3] = u.w;
+    }
+    __device__ static void store(void *p, const float (&x)[8]) {
+        *reinterpret_cast<float4 *>(p) = make_float4(x[0], x[1], x[2], x[3]);
+    }
+};
+
+// One block-iteration per token: its H*d elements are contiguous, so the
+// block sweeps them with 16-byte vectors; the token's position is uniform.
+template <typename T>
+__global__ void __launch_bounds__(128) rope_kernel(RopeArgs a, const float2 *__restrict__ tab) {
+    constexpr int kPairs = Vec<T>::kPairs;
+    const long total = a.tokens[0] + a.tokens[1] + a.tokens[2];
+    const int vecs_per_token = a.H * a.d / (2 * kPairs);
+    const int vecs_per_head = a.d / (2 * kPairs);
+    for (long tok = blockIdx.x; tok < total; tok += gridDim.x) {
+        int which = 0;
+        long local = tok;
+        while (which < 2 && local >= a.tokens[which]) {
+            local -= a.tokens[which];
+            which++;
+        }
+        long n = local % a.seq[which];  // token index within its sequence
+        long j = -1;                    // joint index, or -1 for video
+        if (which == 2) j = n;
+        else if (n >= a.Nv) j = n - a.Nv;
+        int t = 0, h = 0, w = 0;
+        if (j < 0) {
+            long hw = (long)a.grid_h * a.grid_w;
+            t = (int)(n / hw);
+            h = (int)((n / a.grid_w) % a.grid_h);
+            w = (int)(n % a.grid_w);
+        }
+        const char *src = static_cast<const char *>(a.src[which]) + local * (long)a.H * a.d * sizeof(T);
+        char *dst = static_cast<char *>(a.dst[which]) + local * (long)a.H * a.d * sizeof(T);
+        for (int v = threadIdx.x; v < vecs_per_token; v += blockDim.x) {
+            float x[8];
+            Vec<T>::load(src + (long)v * 16, x);
+            int pair0 = (v % vecs_per_head) * kPairs;
+#pragma unroll
+            for (int k = 0; k < kPairs; k++) {
+                float2 cs = rope_cs(a, tab, pair0 + k, t, h, w, j);
+                float xr = x[2 * k], xi = x[2 * k + 1];
+                x[2 * k] = xr * cs.x - xi * cs.y;
+                x[2 * k + 1] = xr * cs.y + xi * cs.x;
+            }
+            Vec<T>::store(dst + (long)v * 16, x);
+        }
+    }
+}
+
+cudaError_t launch_rope_qk(const Geom &g, const float2 *tables, const void *src_q, void *dst_q, const void *src_k,
+                           void *dst_k, const void *src_jk, void *dst_jk, cudaStream_t st) {
+    RopeArgs a;
+    a.src[0] = src_q, a.dst[0] = dst_q;
+    a.src[1] = src_k, a.dst[1] = dst_k;
+    a.src[2] = src_jk, a.dst[2] = dst_jk;
+    a.tokens[0] = (long)g.B * g.S;
+    a.tokens[1] = (long)g.B * g.Nv;
+    a.tokens[2] = (long)g.B * g.Nj;
+    a.seq[0] = g.S, a.seq[1] = g.Nv > 0 ? g.Nv : 1, a.seq[2] = g.Nj > 0 ? g.Nj : 1;
+    a.Nv = g.Nv;
+    a.H = g.H, a.d = g.d;
+    a.grid_h = g.grid_h, a.grid_w = g.grid_w;
+    a.seg1 = g.axis_dim[0] / 2;
+    a.seg2 = (g.axis_dim[0] + g.axis_dim[1]) / 2;
+    a.joint_rope = g.joint_rope;
+    RopeLayout L = rope_layout(g);
+    for (int t = 0; t < 4; t++) a.off[t] = L.off[t];
+    for (int t = 0; t < 3; t++) a.half[t] = g.axis_dim[t] / 2;
+    long total = a.tokens[0] + a.tokens[1] + a.tokens[2];
+    if (total == 0) return cudaSuccess;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    long blocks = total < (long)sms * 16 ? total : (long)sms * 16;
+    if (g.elem == 2)
+        rope_kernel<__nv_bfloat16><<<(unsigned)blocks, 128, 0, st>>>(a, tables);
+    else
+        rope_kernel<float><<<(unsigned)blocks, 128, 0, st>>>(a, tables);
+    return cudaGetLastError();
+}
+
+}  // namespace k6

@@ -1,0 +1,173 @@
+"""Thin ctypes binding of libk6attn (argument marshalling only).
+
+Every function mirrors a C entry point of include/k6attn.h under the same
+name without the `k6attn_` prefix.  Tensors are torch CUDA tensors; their
+device pointers are passed straight through, and the current torch stream is
+used unless one is given.  All compute runs in the library's CUDA kernels;
+there is no fallback: if the library is missing, loading raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE = range(6)
+BF16, F32 = 0, 1
+OPT_WAIT_LIMIT_NS, OPT_STRICT_MMA_ORDER = 0, 1
+
+# every symbol the header declares
+SYMBOLS = ["k6attn_create", "k6attn_destroy", "k6attn_rope_tables", "k6attn_rope_tables_bytes",
+           "k6attn_workspace_bytes", "k6attn_rope_qk", "k6attn_forward", "k6attn_attention_chunks", "k6attn_lse_merge",
+           "k6attn_seq2head_relayout", "k6attn_sync", "k6attn_set_option", "k6attn_status_string",
+           "k6attn_last_error"]
+
+
+class K6Error(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"k6attn status {status}: {msg}")
+        self.status = status
+
+
+class Desc(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("d", ctypes.c_int), ("dtype", ctypes.c_int),
+                ("grid_t", ctypes.c_int), ("grid_h", ctypes.c_int), ("grid_w", ctypes.c_int),
+                ("axis_dim", ctypes.c_int * 3), ("theta", ctypes.c_double), ("n_joint", ctypes.c_int),
+                ("joint_rope", ctypes.c_int)]
+
+
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libk6attn.so (building it first if asked and absent)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise OSError(f"libk6attn.so not built ({path})")
+        _build.build()
+    L = ctypes.CDLL(path)
+    P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    L.k6attn_create.argtypes = [ctypes.POINTER(Desc), ctypes.POINTER(P)]
+    L.k6attn_destroy.argtypes = [P]
+    L.k6attn_destroy.restype = None
+    L.k6attn_rope_tables.argtypes = [P]
+    L.k6attn_rope_tables.restype = P
+    L.k6attn_rope_tables_bytes.argtypes = [P]
+    L.k6attn_rope_tables_bytes.restype = Z
+    L.k6attn_workspace_bytes.argtypes = [P, I, I]
+    L.k6attn_workspace_bytes.restype = Z
+    L.k6attn_rope_qk.argtypes = [P, P, P, P, P, P]
+    L.k6attn_forward.argtypes = [P, P, P, P, P, P, P, I, P, P, P, Z, P]
+    L.k6attn_attention_chunks.argtypes = [P, P, P, P, P, P, I, P, P, P]
+    L.k6attn_lse_merge.argtypes = [P, P, P, I, P, P, P]
+    L.k6attn_seq2head_relayout.argtypes = [P, P, I, ctypes.c_long, I, I, I, I, I, P]
+    L.k6attn_sync.argtypes = [P, P]
+    L.k6attn_set_option.argtypes = [P, I, ctypes.c_longlong]
+    L.k6attn_status_string.argtypes = [I]
+    L.k6attn_status_string.restype = ctypes.c_char_p
+    L.k6attn_last_error.argtypes = []
+    L.k6attn_last_error.restype = ctypes.c_char_p
+    for name in ("k6attn_create", "k6attn_rope_qk", "k6attn_forward", "k6attn_attention_chunks", "k6attn_lse_merge",
+                 "k6attn_seq2head_relayout", "k6attn_sync", "k6attn_set_option"):
+        getattr(L, name).restype = I
+    _lib = L
+    return L
+
+
+def _check(status: int):
+    if status != OK:
+        L = load()
+        raise K6Error(status, (L.k6attn_last_error() or b"").decode() or L.k6attn_status_string(status).decode())
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(getattr(stream, "cuda_stream", stream))
+
+
+class Handle:
+    """Owns a k6attn handle (rotary tables + device error word)."""
+
+    def __init__(self, B, H, d, dtype, grid, n_joint, axis_dim, theta=10000.0, joint_rope=0):
+        L = load()
+        self._desc = Desc(B, H, d, BF16 if dtype in ("bf16", BF16) else F32, grid[0], grid[1], grid[2],
+                          (ctypes.c_int * 3)(*axis_dim), float(theta), n_joint, joint_rope)
+        h = ctypes.c_void_p()
+        _check(L.k6attn_create(ctypes.byref(self._desc), ctypes.byref(h)))
+        self.h = h
+        self.dtype = dtype
+
+    @classmethod
+    def for_workload(cls, w, B=None):
+        return cls(w.B if B is None else B, w.H, w.d, w.dtype, w.grid, w.Nj, w.axis_dim, w.theta, w.joint_rope)
+
+    def close(self):
+        if getattr(self, "h", None):
+            load().k6attn_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ---- ABI wrappers
+    def rope_tables(self) -> int:
+        return load().k6attn_rope_tables(self.h) or 0
+
+    def rope_tables_bytes(self) -> int:
+        return load().k6attn_rope_tables_bytes(self.h)
+
+    def workspace_bytes(self, n_chunks: int, with_rope: bool) -> int:
+        return load().k6attn_workspace_bytes(self.h, n_chunks, int(bool(with_rope)))
+
+    def set_option(self, opt: int, value: int):
+        _check(load().k6attn_set_option(self.h, opt, int(value)))
+
+    def rope_qk(self, q, k, joint_k, tables=None, stream=None):
+        tab = ctypes.c_void_p(self.rope_tables() if tables is None else tables)
+        _check(load().k6attn_rope_qk(self.h, _ptr(q), _ptr(k), _ptr(joint_k), tab, _stream(stream)))
+
+    def forward(self, q, k, v, joint_k, joint_v, out, lse=None, *, rope=True, n_chunks=1, workspace=None,
+                tables=None, stream=None):
+        tab = None
+        if rope:
+            tab = ctypes.c_void_p(self.rope_tables() if tables is None else tables)
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        _check(load().k6attn_forward(self.h, _ptr(q), _ptr(k), _ptr(v), _ptr(joint_k), _ptr(joint_v), tab,
+                                     int(n_chunks), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
+                                     _stream(stream)))
+
+    def attention_chunks(self, q, k, v, joint_k, joint_v, n_chunks, out, lse=None, stream=None):
+        _check(load().k6attn_attention_chunks(self.h, _ptr(q), _ptr(k), _ptr(v), _ptr(joint_k), _ptr(joint_v),
+                                              int(n_chunks), _ptr(out), _ptr(lse), _stream(stream)))
+
+    def lse_merge(self, part_o, part_lse, n_chunks, out, lse=None, stream=None):
+        _check(load().k6attn_lse_merge(self.h, _ptr(part_o), _ptr(part_lse), int(n_chunks), _ptr(out), _ptr(lse),
+                                       _stream(stream)))
+
+    def sync(self, stream=None):
+        _check(load().k6attn_sync(self.h, _stream(stream)))
+
+
+def seq2head_relayout(src, dst, B, S, H, d, P, direction, stream=None):
+    _check(load().k6attn_seq2head_relayout(_ptr(src), _ptr(dst), B, S, H, d, src.element_size(), P, direction,
+                                           _stream(stream)))
