@@ -1,0 +1,443 @@
+#!/usr/bin/env python
+"""Throughput of the joint-sequence attention path on one GB300.
+
+One step = the whole hot path over one batch of synthetic input, each row a
+separate C-ABI call with CUDA events between them:
+  seq->head relayout of q, k, v, joint_k, joint_v (the Ulysses layout change,
+  8-way, done on one GPU) -> rotary on q/k (head layout, into fp16 copies) ->
+  attention over n K/V chunks (fp32 partials + LSE) -> LSE merge ->
+  head->seq relayout of the output.
+The headline metric is attention TFLOP/s (4*B*H*S^2*d per step) over the whole
+step; the attention kernel alone gives the roofline fraction against the
+measured dense-bf16 peak.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--config pro|long|lite|image] [--chunks n] [--no-secondary]
+
+`--impl reference` times the fp64 CPU oracle on bounded row samples of the
+same workload (rank 0 only).  Under torchrun (N > 1) every rank runs an
+independent replica of the workload (the path does not shard across GPUs);
+`value` counts the work of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from video_dit_long_gb300 import configs, inputs  # noqa: E402
+
+METRIC = "attention TFLOP/s & % of GB300 BF16 tensor peak at 52K/119K-token video DiT shapes"
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        out = {}
+        for k in FALLBACK:
+            v = d.get(k)
+            if isinstance(v, dict):
+                v = v.get("value")
+            out[k] = float(v) if v is not None else None
+        if all(out[k] for k in FALLBACK):
+            out["source"] = "measured"
+            return out
+    return dict(FALLBACK, source="fallback")
+
+
+def traffic_record(kernel: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken on
+    the current source of the kernel (source sha256 recorded beside it)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    src = os.path.join(ROOT, "video_dit_long_gb300", "csrc", "k6_attn_tc.cu")
+    if not os.path.exists(path):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    with open(path) as f:
+        for line in f:
+            parts = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+            if parts.get("kernel") == kernel and parts.get("source_sha256") == sha:
+                return float(parts["dram_bytes_per_launch"])
+    return None
+
+
+class Clocks:
+    """nvidia-smi sampler (200 ms) running while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our path
+
+
+class Path:
+    """Device buffers and handles for one workload; step() runs the hot path."""
+
+    def __init__(self, w, n_chunks, P, x):
+        import torch
+        from video_dit_long_gb300 import k6attn as K
+        self.torch, self.K = torch, K
+        self.w, self.n, self.P = w, n_chunks, P
+        B, S, H, d, Nv, Nj = w.B, w.S, w.H, w.d, w.Nv, w.Nj
+        self.Hl = H // P
+        bf = torch.bfloat16
+
+        def dev(a):
+            return torch.from_numpy(a.view(np.int16)).view(bf).cuda()
+
+        self.host = {k: torch.from_numpy(v.view(np.int16)).view(bf).pin_memory() for k, v in x.items()}
+        self.seq = {k: dev(v) for k, v in x.items()}
+        self.head = {k: torch.empty_like(v) for k, v in self.seq.items()}
+        # rotated q/k/joint_k in fp16 (finer rounding than bf16, same tensor-core rate)
+        self.rot = {k: torch.empty(self.head[k].shape, dtype=torch.float16, device="cuda") for k in ("q", "k", "jk")}
+        self.rows = {"q": S, "k": Nv, "v": Nv, "jk": Nj, "jv": Nj}
+        # attention runs on the head-partitioned layout: P*B independent problems of H/P heads
+        self.h = K.Handle(P * B, self.Hl, d, "bf16", w.grid, Nj, w.axis_dim, w.theta, w.joint_rope)
+        self.part_o = torch.empty((n_chunks, P * B, S, self.Hl, d), dtype=torch.float32, device="cuda")
+        self.part_lse = torch.empty((n_chunks, P * B, self.Hl, S), dtype=torch.float32, device="cuda")
+        self.out_h = torch.empty((P * B, S, self.Hl, d), dtype=bf, device="cuda")
+        self.lse = torch.empty((P * B, self.Hl, S), dtype=torch.float32, device="cuda")
+        self.out = torch.empty((B, S, H, d), dtype=bf, device="cuda")
+        self.ws = torch.empty(self.h.workspace_bytes(n_chunks, True), dtype=torch.uint8, device="cuda")
+        self.out_host = torch.empty(self.out.shape, dtype=bf).pin_memory()
+        self.lse_host = torch.empty(self.lse.shape, dtype=torch.float32).pin_memory()
+        self.launches_per_step = 5 + 1 + 1 + 1 + 1
+
+    def relayout_in(self):
+        w, K = self.w, self.K
+        for name in ("q", "k", "v", "jk", "jv"):
+            if self.rows[name]:
+                K.seq2head_relayout(self.seq[name], self.head[name], w.B, self.rows[name], w.H, w.d, self.P, 0)
+
+    def step(self, ev=None):
+        w, K, hd = self.w, self.K, self.head
+        if ev:
+            ev[0].record()
+        self.relayout_in()
+        if ev:
+            ev[1].record()
+        rt = self.rot
+        self.h.rope_qk(hd["q"], hd["k"], hd["jk"] if w.Nj else None, q_out=rt["q"], k_out=rt["k"],
+                       joint_k_out=rt["jk"] if w.Nj else None, out_dtype=K.F16)
+        if ev:
+            ev[2].record()
+        jk, jv = (rt["jk"], hd["jv"]) if w.Nj else (None, None)
+        self.h.attention_chunks(rt["q"], rt["k"], hd["v"], jk, jv, self.n, self.part_o, self.part_lse,
+                                qk_dtype=K.F16)
+        if ev:
+            ev[3].record()
+        self.h.lse_merge(self.part_o, self.part_lse, self.n, self.out_h, self.lse)
+        if ev:
+            ev[4].record()
+        K.seq2head_relayout(self.out_h, self.out, w.B, w.S, w.H, w.d, self.P, 1)
+        if ev:
+            ev[5].record()
+
+    def e2e_step(self):
+        """Public API from pinned host buffers: H2D, relayout, k6attn_forward
+        (rotary + chunks + merge), relayout back, D2H of out and lse."""
+        w, K, hd = self.w, self.K, self.head
+        for k in self.seq:
+            self.seq[k].copy_(self.host[k], non_blocking=True)
+        self.relayout_in()
+        jk, jv = (hd["jk"], hd["jv"]) if w.Nj else (None, None)
+        self.h.forward(hd["q"], hd["k"], hd["v"], jk, jv, self.out_h, self.lse, rope=True, n_chunks=self.n,
+                       workspace=self.ws)
+        K.seq2head_relayout(self.out_h, self.out, w.B, w.S, w.H, w.d, self.P, 1)
+        self.out_host.copy_(self.out, non_blocking=True)
+        self.lse_host.copy_(self.lse, non_blocking=True)
+
+    def h2d_bytes(self):
+        return sum(t.numel() * t.element_size() for t in self.host.values())
+
+    def d2h_bytes(self):
+        return self.out_host.numel() * 2 + self.lse_host.numel() * 4
+
+
+def gpu_index() -> str:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local < len(ids):
+            return ids[local]
+    return str(local)
+
+
+def barrier(dist_on):
+    import torch
+    if dist_on:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+def max_over_ranks(x: float, dist_on) -> float:
+    if not dist_on:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measure(w, n_chunks, P, steps, warmup, dist_on, with_e2e=True, clocks=True):
+    import torch
+    x = inputs.make_inputs(w)
+    path = Path(w, n_chunks, P, x)
+    for _ in range(warmup):
+        path.step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist_on)
+    clk = Clocks(gpu_index())
+    with (clk if clocks else _Null()):
+        t0.record()
+        for s in range(steps):
+            path.step(evs[s])
+        t1.record()
+        barrier(dist_on)
+    total_ms = max_over_ranks(t0.elapsed_time(t1), dist_on)
+    path.h.sync()
+    per = np.array([[evs[s][i].elapsed_time(evs[s][i + 1]) for i in range(5)] for s in range(steps)])
+    res = {"total_ms": total_ms, "per_kernel_ms": per.mean(axis=0).tolist(),
+           "clocks": clk.summary() if clocks else None, "launches": path.launches_per_step * steps}
+    if with_e2e:
+        for _ in range(max(1, warmup)):
+            path.e2e_step()
+        torch.cuda.synchronize()
+        barrier(dist_on)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            path.e2e_step()
+        e1.record()
+        barrier(dist_on)
+        res["e2e_ms"] = max_over_ranks(e0.elapsed_time(e1), dist_on)
+        res["h2d"] = path.h2d_bytes()
+        res["d2h"] = path.d2h_bytes()
+        path.h.sync()
+    del path
+    torch.cuda.empty_cache()
+    return res, x
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        pass
+
+
+def merge_bytes(w, n, P):
+    rows = w.B * w.S * w.H
+    return n * (rows * w.d * 4 + rows * 4) + rows * w.d * 2 + rows * 4
+
+
+def cpu_sample(w, x, rows_count, seed=7):
+    """Oracle on `rows_count` query rows (all heads, all keys); returns (seconds, flops, threads)."""
+    from oracle import oracle as O
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(w.S, size=rows_count, replace=False))
+    g = O.Geom(w.B, w.H, w.d, w.grid, w.Nj, w.axis_dim, w.theta, w.joint_rope)
+    t = time.perf_counter()
+    O.attention(g, x["q"], x["k"], x["v"], x["jk"], x["jv"], rows=rows)
+    dt = time.perf_counter() - t
+    return dt, 4.0 * w.B * w.H * rows_count * w.S * w.d, O.num_threads()
+
+
+def run_ours(args, rank, world, dist_on):
+    import torch
+    w = configs.WORKLOADS[args.config]
+    n = args.chunks or w.chunks[0]
+    P = w.relayout_P[-1]
+    pk = peaks()
+    res, x = measure(w, n, P, args.steps, args.warmup, dist_on)
+    flops = w.flops()
+    ms = res["total_ms"] / args.steps
+    value = flops * world / (res["total_ms"] / args.steps * 1e-3) / 1e12
+    k_ms = res["per_kernel_ms"]  # relayout_in, rope, attention, merge, relayout_out
+    attn_tflops = flops / (k_ms[2] * 1e-3) / 1e12
+    peak_s = pk["bf16_tflops_sustained"]
+    tag = "of measured" if pk["source"] == "measured" else "of fallback"
+    io = {k: w.H * w.d * 2 * r for k, r in {"q": w.S, "k": w.Nv, "v": w.Nv, "jk": w.Nj, "jv": w.Nj}.items()}
+    relayout_in_bytes = 2 * sum(io.values())
+    rope_bytes = 2 * (io["q"] + io["k"] + io["jk"])
+    mb = merge_bytes(w, n, P)
+    relayout_out_bytes = 2 * io["q"]
+    hbm = pk["hbm_gbs"]
+
+    def gbs(b, t_ms):
+        return b / (t_ms * 1e-3) / 1e9
+
+    kernels = {
+        "relayout_seq2head_qkv": {"ms": k_ms[0], "GB/s": gbs(relayout_in_bytes, k_ms[0]),
+                                  "frac": gbs(relayout_in_bytes, k_ms[0]) / hbm},
+        "rope_qk": {"ms": k_ms[1], "GB/s": gbs(rope_bytes, k_ms[1]), "frac": gbs(rope_bytes, k_ms[1]) / hbm},
+        "attention_chunks": {"ms": k_ms[2], "TFLOP/s": attn_tflops, "frac_sustained": attn_tflops / peak_s,
+                             "frac_burst": attn_tflops / pk["bf16_tflops"]},
+        "lse_merge": {"ms": k_ms[3], "GB/s": gbs(mb, k_ms[3]), "frac": gbs(mb, k_ms[3]) / hbm},
+        "relayout_head2seq_out": {"ms": k_ms[4], "GB/s": gbs(relayout_out_bytes, k_ms[4]),
+                                  "frac": gbs(relayout_out_bytes, k_ms[4]) / hbm},
+    }
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "pct_of_peak": round(100 * value / world / peak_s, 2), "peak_basis": f"bf16 sustained {peak_s} {tag}",
+        "config": {"workload": f"{w.name}: {w.note}", "B": w.B, "H": w.H, "d": w.d, "S": w.S, "Nv": w.Nv,
+                   "Nj": w.Nj, "grid": list(w.grid), "n_chunks": n, "relayout_P": P, "parallelism": "replicas",
+                   "l2": "inputs larger than L2 (q, k, v are %d MB each)" % (io["q"] // 2**20)},
+        "roofline": {"bound": "tensor", "achieved": round(attn_tflops, 2), "peak": peak_s, "unit": "TFLOP/s",
+                     "frac": round(attn_tflops / peak_s, 4), "traffic": traffic_record("attn_tc_kernel"),
+                     "kernel": "attn_tc_kernel", "peak_kind": f"bf16 sustained, {tag}",
+                     "algorithmic_flops_per_launch": flops},
+        "kernels": kernels,
+        "gpu_launches": res["launches"],
+        "clocks": res["clocks"],
+        "peaks": pk,
+    }
+    if "e2e_ms" in res:
+        line["e2e"] = {"value": round(flops * world / (res["e2e_ms"] / args.steps * 1e-3) / 1e12, 2),
+                       "unit": "TFLOP/s", "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
+                       "ms_per_step": round(res["e2e_ms"] / args.steps, 4)}
+    if args.secondary:
+        w2 = configs.WORKLOADS["long"]
+        n2 = w2.chunks[-1]
+        r2, _ = measure(w2, n2, w2.relayout_P[-1], max(3, args.steps // 5), max(3, args.warmup), dist_on,
+                        with_e2e=False, clocks=False)
+        f2 = w2.flops()
+        t2 = r2["total_ms"] / max(3, args.steps // 5)
+        line["long_video"] = {"workload": f"{w2.name}: {w2.note}", "n_chunks": n2,
+                              "value": round(f2 * world / (t2 * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                              "ms_per_step": round(t2, 3),
+                              "attention_TFLOP/s": round(f2 / (r2["per_kernel_ms"][2] * 1e-3) / 1e12, 2),
+                              "merge_GB/s": round(gbs(merge_bytes(w2, n2, 8), r2["per_kernel_ms"][3]), 1)}
+    if rank == 0 and world == 1 and not args.no_cpu:
+        dt, fl, thr = cpu_sample(w, x, args.cpu_rows)
+        line["cpu_baseline"] = {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+                                "sample": f"{args.cpu_rows} query rows x {w.H} heads x all {w.S} keys of "
+                                          f"{w.name}, fp64, {dt:.1f} s"}
+    return line
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    w = configs.WORKLOADS[args.config]
+    x = inputs.make_inputs(w)
+    for _ in range(args.warmup):
+        cpu_sample(w, x, args.ref_rows)
+    times, flops, thr = [], 0.0, 1
+    for s in range(args.steps):
+        dt, fl, thr = cpu_sample(w, x, args.ref_rows, seed=100 + s)
+        times.append(dt)
+        flops = fl
+    total = sum(times)
+    value = flops * args.steps / total / 1e12
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{w.name}: {w.note}", "B": w.B, "H": w.H, "d": w.d, "S": w.S,
+                       "parallelism": "replicas"},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+                             "sample": f"per step {args.ref_rows} query rows x {w.H} heads x all {w.S} keys"},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="pro", choices=["pro", "long", "lite", "image", "mid"])
+    ap.add_argument("--chunks", type=int, default=0)
+    ap.add_argument("--no-secondary", dest="secondary", action="store_false")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=192)
+    ap.add_argument("--ref-rows", type=int, default=4)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    import torch
+    dist_on = world > 1
+    if dist_on:
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    line = run_ours(args, rank, world, dist_on)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist_on:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

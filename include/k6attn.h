@@ -54,10 +54,17 @@ typedef enum {
     K6ATTN_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (e.g. bf16 with d != 128) */
     K6ATTN_ERR_CUDA = 3,        /* a CUDA runtime call failed; message in k6attn_last_error() */
     K6ATTN_ERR_TIMEOUT = 4,     /* a device-side wait ran out (reported by k6attn_sync) */
-    K6ATTN_ERR_WORKSPACE = 5    /* workspace pointer null or smaller than k6attn_workspace_bytes() */
+    K6ATTN_ERR_WORKSPACE = 5,   /* workspace pointer null or smaller than k6attn_workspace_bytes() */
+    K6ATTN_ERR_RANGE = 6        /* a rotated q/k value is not finite in fp16 (reported by k6attn_sync) */
 } k6attn_status;
 
-typedef enum { K6ATTN_BF16 = 0, K6ATTN_F32 = 1 } k6attn_dtype;
+/* Storage types.  A handle's dtype (BF16 or F32) is the type of q, k, v,
+ * joint_k, joint_v and out.  F16 is only a type for ROTATED q/k/joint_k of a
+ * BF16 handle: rounding the rotated values to fp16 (11-bit significand)
+ * instead of bf16 (8-bit) cuts the error they add to the logits 8-fold, at the
+ * same tensor-core rate (Q.K^T runs fp16 x fp16, P.V bf16 x bf16, both with
+ * fp32 accumulation). */
+typedef enum { K6ATTN_BF16 = 0, K6ATTN_F32 = 1, K6ATTN_F16 = 2 } k6attn_dtype;
 
 /*
  * Problem descriptor, fixed at handle creation.
@@ -111,18 +118,24 @@ size_t k6attn_rope_tables_bytes(k6attn_t h);
 size_t k6attn_workspace_bytes(k6attn_t h, int n_chunks, int with_rope);
 
 /*
- * Rotary embedding of q, k and joint_k, in place, one fused launch
- * ([CP] "Self-Attention with Context Parallelism": `apply_rotary_emb_wan`
- * on query and key; [K6] RoPE travels with the visual tokens).
+ * Rotary embedding of q, k and joint_k, one fused launch ([CP]
+ * "Self-Attention with Context Parallelism": `apply_rotary_emb_wan` on query
+ * and key; [K6] RoPE travels with the visual tokens).
  *  q        [B][Sq][H][d]; row n < Nv at its video grid position, row n >= Nv
  *           is joint token n - Nv.
  *  k        [B][Nv][H][d] video keys.
  *  joint_k  [B][Nj][H][d] (may be NULL when Nj == 0).
  *  rope_tables  k6attn_rope_tables(h) or a caller copy in the same layout.
- * bf16 tensors are rotated in fp32 and rounded to nearest even.
+ *  q_out, k_out, joint_k_out  destinations in the same layouts, of type
+ *           out_dtype.  Equal to the sources for in-place rotation (then
+ *           out_dtype must be the handle's dtype); otherwise disjoint from
+ *           every source.  out_dtype F16 is allowed for BF16 handles.
+ * Rotation in fp32, rounded to nearest even.  Writing F16, a value that is
+ * not finite in fp16 sets the handle's error word (K6ATTN_ERR_RANGE at
+ * k6attn_sync).
  */
-k6attn_status k6attn_rope_qk(k6attn_t h, void *q, void *k, void *joint_k, const void *rope_tables,
-                             void *stream);
+k6attn_status k6attn_rope_qk(k6attn_t h, const void *q, const void *k, const void *joint_k, const void *rope_tables,
+                             void *q_out, void *k_out, void *joint_k_out, k6attn_dtype out_dtype, void *stream);
 
 /*
  * Joint-sequence attention forward ([USP] `_attention`; [CP] "Ring attention
@@ -130,8 +143,11 @@ k6attn_status k6attn_rope_qk(k6attn_t h, void *q, void *k, void *joint_k, const 
  * partials combine through their log-sum-exp).
  *  q, k, v, joint_k, joint_v  inputs in the layouts above (joint_* may be NULL
  *           when Nj == 0).  Not modified.
- *  rope_tables  NULL: q/k/joint_k are already rotated.  Otherwise the rotated
- *           copies are written to the workspace first (k6attn_rope_qk math).
+ *  rope_tables  NULL: q/k/joint_k are already rotated (handle dtype).
+ *           Otherwise rotated copies are written to the workspace first
+ *           (k6attn_rope_qk math; fp16 copies for a BF16 handle, so a
+ *           rotated value must be finite in fp16: K6ATTN_ERR_RANGE at
+ *           k6attn_sync otherwise).
  *  n_chunks K/V chunks: chunk c covers keys [c*Sk/n, (c+1)*Sk/n) of
  *           concat(k, joint_k); Sk % n_chunks must be 0 ([CP] "Sequence
  *           Length Constraints").  n_chunks == 1 writes out/lse directly;
@@ -156,10 +172,13 @@ k6attn_status k6attn_forward(k6attn_t h, const void *q, const void *k, const voi
  *  n_chunks > 1:  out is fp32 partials [n_chunks][B][Sq][H][d] and lse fp32
  *           [n_chunks][B][H][Sq] (required); combine them with
  *           k6attn_lse_merge.
+ *  qk_dtype the type of q, k and joint_k: the handle's dtype, or F16 for a
+ *           BF16 handle (v and joint_v always have the handle's dtype).
  * Inputs as in k6attn_forward; outputs must not alias them.
  */
 k6attn_status k6attn_attention_chunks(k6attn_t h, const void *q, const void *k, const void *v, const void *joint_k,
-                                      const void *joint_v, int n_chunks, void *out, float *lse, void *stream);
+                                      const void *joint_v, k6attn_dtype qk_dtype, int n_chunks, void *out, float *lse,
+                                      void *stream);
 
 /*
  * Log-sum-exp merge of per-chunk partials (ring attention's combine step,
@@ -191,6 +210,7 @@ k6attn_status k6attn_seq2head_relayout(const void *src, void *dst, int B, long S
 
 /* Synchronise `stream`, then read and clear the handle's device error word:
  * K6ATTN_ERR_TIMEOUT if any kernel of this handle gave up on a wait,
+ * K6ATTN_ERR_RANGE if a rotation into fp16 overflowed,
  * K6ATTN_ERR_CUDA on an asynchronous CUDA error, else K6ATTN_OK. */
 k6attn_status k6attn_sync(k6attn_t h, void *stream);
 

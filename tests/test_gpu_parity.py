@@ -134,6 +134,63 @@ def test_rope_matches_oracle(name):
         assert (np.abs(got - ref) <= bound).all(), float(np.abs(got - ref).max())
 
 
+@pytest.mark.parametrize("name", ["lite", "ragged"])
+def test_rope_into_fp16_copies_matches_oracle(name):
+    w = configs.WORKLOADS.get(name) or SMALL[name]
+    x = inputs.make_inputs(w)
+    k6 = K()
+    h = k6.Handle.for_workload(w)
+    q, k, jk = (to_dev(x[n], w.dtype) for n in ("q", "k", "jk"))
+    qo, ko, jo = (torch.empty(t.shape, dtype=torch.float16, device="cuda") for t in (q, k, jk))
+    h.rope_qk(q, k, jk, q_out=qo, k_out=ko, joint_k_out=jo, out_dtype=k6.F16)
+    h.sync()
+    g = geom(w)
+    ref_q = O.rope(g, x["q"])
+    ref_k = O.rope(g, np.concatenate([x["k"], x["jk"]], axis=1))
+    got_k = np.concatenate([to_host(ko), to_host(jo)], axis=1)
+    for got, ref in ((to_host(qo), ref_q), (got_k, ref_k)):
+        # one rounding to fp16 (2^-11 relative, or half its subnormal step) plus fp32 table error
+        bound = np.abs(ref) * 2.0**-10 + 2.0**-24 + 1e-6
+        assert (np.abs(got - ref) <= bound).all(), float(np.abs(got - ref).max())
+    # inputs untouched
+    assert np.array_equal(q.cpu().view(torch.int16).numpy().view(np.uint16), x["q"])
+
+
+def test_rope_into_fp16_reports_overflow():
+    w = SMALL["ragged"]
+    x = inputs.make_inputs(w)
+    x["k"][0, 5, 1, 7] = inputs.bf16_bits(np.array([1.0e5], np.float32))[0]  # beyond fp16 range
+    k6 = K()
+    h = k6.Handle.for_workload(w)
+    q, k, jk = (to_dev(x[n], w.dtype) for n in ("q", "k", "jk"))
+    qo, ko, jo = (torch.empty(t.shape, dtype=torch.float16, device="cuda") for t in (q, k, jk))
+    h.rope_qk(q, k, jk, q_out=qo, k_out=ko, joint_k_out=jo, out_dtype=k6.F16)
+    with pytest.raises(k6.K6Error) as e:
+        h.sync()
+    assert e.value.status == k6.ERR_RANGE
+    h.sync()  # the error word was cleared
+
+
+def test_split_calls_equal_forward():
+    """rope into fp16 copies -> attention_chunks -> lse_merge gives forward's bits."""
+    w = SMALL["audio1d"]
+    x = inputs.make_inputs(w)
+    k6 = K()
+    out_f, lse_f, h = run_forward(w, x, 3)
+    q, k, v, jk, jv = (to_dev(x[n], w.dtype) for n in ("q", "k", "v", "jk", "jv"))
+    qo, ko, jo = (torch.empty(t.shape, dtype=torch.float16, device="cuda") for t in (q, k, jk))
+    h.rope_qk(q, k, jk, q_out=qo, k_out=ko, joint_k_out=jo, out_dtype=k6.F16)
+    po = torch.empty((3, w.B, w.S, w.H, w.d), dtype=torch.float32, device="cuda")
+    pl = torch.empty((3, w.B, w.H, w.S), dtype=torch.float32, device="cuda")
+    h.attention_chunks(qo, ko, v, jo, jv, 3, po, pl, qk_dtype=k6.F16)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device="cuda")
+    h.lse_merge(po, pl, 3, out, lse)
+    h.sync()
+    assert np.array_equal(to_host(out), out_f)
+    assert np.array_equal(lse.cpu().numpy().astype(np.float64), lse_f)
+
+
 # --------------------------------------------------------------------- merge
 
 

@@ -65,6 +65,9 @@ WORKLOADS = {
                       note="image DiT 4096 image + 256 text tokens, 2-D rotary"),
     "pro": Workload("pro", 1, 24, 128, "bf16", (32, 30, 54), 520, (32, 48, 48), 0, 0.5, 1.0, (8,), (8,),
                     note="Kandinsky 6 Pro geometry, 51840 video + 520 audio tokens = 52360"),
+    # profiling case: half the Pro video grid in time (inputs still larger than L2, a few GB on device)
+    "mid": Workload("mid", 1, 24, 128, "bf16", (16, 30, 54), 520, (32, 48, 48), 0, 0.5, 1.0, (2,), (8,),
+                    note="half-length Pro geometry, 25920 video + 520 audio tokens = 26440"),
     "long": Workload("long", 1, 24, 128, "bf16", (33, 45, 80), 256, (32, 48, 48), 0, 1.0, 1.0, (8, 16), (8,),
                      note="HunyuanVideo 720x1280x129 geometry, 118800 video + 256 text tokens = 119056"),
 }

@@ -78,10 +78,10 @@ static WsLayout ws_layout(const Geom &g, int n, bool rope) {
 // The attention kernels on rotated inputs: n_chunks == 1 writes out/lse,
 // n_chunks > 1 writes fp32 partials into out/lse (see k6attn_attention_chunks).
 static k6attn_status run_attention(k6attn_handle *h, const void *q, const void *k, const void *v, const void *jk,
-                                   const void *jv, int n_chunks, void *out, float *lse, cudaStream_t st) {
+                                   const void *jv, bool qk_f16, int n_chunks, void *out, float *lse, cudaStream_t st) {
     const Geom &g = h->g;
     if (g.elem == 2) {
-        AttnTcOptions opt{h->wait_limit_ns, h->err, h->strict_order};
+        AttnTcOptions opt{h->wait_limit_ns, h->err, h->strict_order, qk_f16 ? 1 : 0};
         const char *why = nullptr;
         cudaError_t e = launch_attn_tc(g, q, k, v, jk, jv, n_chunks, out, lse, opt, st, &why);
         if (e != cudaSuccess) {
@@ -138,6 +138,7 @@ const char *k6attn_status_string(k6attn_status s) {
         case K6ATTN_ERR_CUDA: return "CUDA error";
         case K6ATTN_ERR_TIMEOUT: return "device wait timed out";
         case K6ATTN_ERR_WORKSPACE: return "workspace missing or too small";
+        case K6ATTN_ERR_RANGE: return "rotated value out of fp16 range";
     }
     return "unknown status";
 }
@@ -182,6 +183,7 @@ k6attn_status k6attn_create(const k6attn_desc *desc, k6attn_t *out) {
     for (int a = 0; a < 3; a++) g.axis_dim[a] = d.axis_dim[a];
     g.joint_rope = d.joint_rope;
     g.elem = d.dtype == K6ATTN_BF16 ? 2 : 4;
+    g.dtype = d.dtype;
     cudaGetDevice(&h->device);
     RopeLayout L = rope_layout(g);
     h->table_bytes = (size_t)L.total * sizeof(float2);
@@ -227,20 +229,34 @@ k6attn_status k6attn_set_option(k6attn_t h, k6attn_option opt, long long value) 
     return set_error(K6ATTN_ERR_INVALID_ARG, "set_option: unknown option %d", (int)opt);
 }
 
-k6attn_status k6attn_rope_qk(k6attn_t h, void *q, void *k, void *joint_k, const void *rope_tables, void *stream) {
+k6attn_status k6attn_rope_qk(k6attn_t h, const void *q, const void *k, const void *joint_k, const void *rope_tables,
+                             void *q_out, void *k_out, void *joint_k_out, k6attn_dtype out_dtype, void *stream) {
     g_msg[0] = 0;
     if (!h) return set_error(K6ATTN_ERR_INVALID_ARG, "rope_qk: null handle");
     const Geom &g = h->g;
-    if (!q || !k || (g.Nj > 0 && !joint_k) || (!rope_tables && h->table_bytes))
+    if (!q || !k || !q_out || !k_out || (g.Nj > 0 && (!joint_k || !joint_k_out)) || (!rope_tables && h->table_bytes))
         return set_error(K6ATTN_ERR_INVALID_ARG, "rope_qk: null tensor or table pointer");
-    if (!aligned16(q) || !aligned16(k) || !aligned16(joint_k) || !aligned16(rope_tables))
-        return set_error(K6ATTN_ERR_INVALID_ARG, "rope_qk: pointers must be 16-byte aligned");
+    if (out_dtype != g.dtype && !(g.dtype == K6ATTN_BF16 && out_dtype == K6ATTN_F16))
+        return set_error(K6ATTN_ERR_INVALID_ARG, "rope_qk: output type %d not allowed for this handle", (int)out_dtype);
+    const void *ptrs[] = {q, k, joint_k, q_out, k_out, joint_k_out, rope_tables};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return set_error(K6ATTN_ERR_INVALID_ARG, "rope_qk: pointers must be 16-byte aligned");
     const size_t row = (size_t)g.H * g.d * g.elem;
-    if (overlap(q, g.B * g.S * row, k, g.B * g.Nv * row) || overlap(q, g.B * g.S * row, joint_k, g.B * g.Nj * row) ||
-        overlap(k, g.B * g.Nv * row, joint_k, g.B * g.Nj * row))
-        return set_error(K6ATTN_ERR_INVALID_ARG, "rope_qk: q, k and joint_k overlap");
-    return cuda_check(launch_rope_qk(g, static_cast<const float2 *>(rope_tables), q, q, k, k, joint_k, joint_k,
-                                     static_cast<cudaStream_t>(stream)),
+    const size_t nb[3] = {g.B * g.S * row, g.B * g.Nv * row, g.B * g.Nj * row};
+    const void *src[3] = {q, k, joint_k};
+    const void *dst[3] = {q_out, k_out, joint_k_out};
+    for (int a = 0; a < 3; a++) {
+        if (dst[a] == src[a] && nb[a] && out_dtype != g.dtype)
+            return set_error(K6ATTN_ERR_INVALID_ARG, "rope_qk: in-place rotation keeps the handle's type");
+        for (int b = 0; b < 3; b++) {
+            if (a != b && (overlap(src[a], nb[a], src[b], nb[b]) || overlap(dst[a], nb[a], dst[b], nb[b])))
+                return set_error(K6ATTN_ERR_INVALID_ARG, "rope_qk: tensors overlap");
+            if (dst[a] != src[a] && overlap(dst[a], nb[a], src[b], nb[b]))
+                return set_error(K6ATTN_ERR_INVALID_ARG, "rope_qk: an output overlaps an input");
+        }
+    }
+    return cuda_check(launch_rope_qk(g, static_cast<const float2 *>(rope_tables), q, q_out, k, k_out, joint_k,
+                                     joint_k_out, out_dtype, h->err, static_cast<cudaStream_t>(stream)),
                       "rope_qk launch");
 }
 
@@ -295,21 +311,25 @@ k6attn_status k6attn_forward(k6attn_t h, const void *q, const void *k, const voi
     const void *qa = q, *ka = k, *jka = joint_k;
     if (rope) {
         void *qr = ws + L.q_rot, *kr = ws + L.k_rot, *jkr = g.Nj ? ws + L.jk_rot : nullptr;
-        s = cuda_check(launch_rope_qk(g, static_cast<const float2 *>(rope_tables), q, qr, k, kr, joint_k, jkr, st),
+        // a bf16 handle keeps its rotated copies in fp16 (8x finer rounding of the logits' inputs)
+        s = cuda_check(launch_rope_qk(g, static_cast<const float2 *>(rope_tables), q, qr, k, kr, joint_k, jkr,
+                                      g.dtype == K6ATTN_BF16 ? K6ATTN_F16 : g.dtype, h->err, st),
                        "forward: rope launch");
         if (s != K6ATTN_OK) return s;
         qa = qr, ka = kr, jka = jkr;
     }
-    if (n_chunks == 1) return run_attention(h, qa, ka, v, jka, joint_v, 1, out, lse, st);
+    const bool qk_f16 = rope && g.dtype == K6ATTN_BF16;
+    if (n_chunks == 1) return run_attention(h, qa, ka, v, jka, joint_v, qk_f16, 1, out, lse, st);
     float *part_o = reinterpret_cast<float *>(ws + L.part_o);
     float *part_lse = reinterpret_cast<float *>(ws + L.part_lse);
-    s = run_attention(h, qa, ka, v, jka, joint_v, n_chunks, part_o, part_lse, st);
+    s = run_attention(h, qa, ka, v, jka, joint_v, qk_f16, n_chunks, part_o, part_lse, st);
     if (s != K6ATTN_OK) return s;
     return cuda_check(launch_lse_merge(g, n_chunks, part_o, part_lse, out, lse, st), "forward: merge launch");
 }
 
 k6attn_status k6attn_attention_chunks(k6attn_t h, const void *q, const void *k, const void *v, const void *joint_k,
-                                      const void *joint_v, int n_chunks, void *out, float *lse, void *stream) {
+                                      const void *joint_v, k6attn_dtype qk_dtype, int n_chunks, void *out, float *lse,
+                                      void *stream) {
     g_msg[0] = 0;
     if (!h) return set_error(K6ATTN_ERR_INVALID_ARG, "attention_chunks: null handle");
     const Geom &g = h->g;
@@ -318,9 +338,13 @@ k6attn_status k6attn_attention_chunks(k6attn_t h, const void *q, const void *k, 
     const int n = n_chunks > 1 ? n_chunks : 1;
     const size_t ob = (size_t)n * g.B * g.S * g.H * g.d * (n_chunks > 1 ? 4 : g.elem);
     const size_t lb = (size_t)n * g.B * g.H * g.S * 4;
+    if (qk_dtype != g.dtype && !(g.dtype == K6ATTN_BF16 && qk_dtype == K6ATTN_F16))
+        return set_error(K6ATTN_ERR_INVALID_ARG, "attention_chunks: q/k type %d not allowed for this handle",
+                         (int)qk_dtype);
     k6attn_status s = check_inputs("attention_chunks", g, q, k, v, joint_k, joint_v, n_chunks, out, ob, lse, lb);
     if (s != K6ATTN_OK) return s;
-    return run_attention(h, q, k, v, joint_k, joint_v, n_chunks, out, lse, static_cast<cudaStream_t>(stream));
+    return run_attention(h, q, k, v, joint_k, joint_v, qk_dtype == K6ATTN_F16, n_chunks, out, lse,
+                         static_cast<cudaStream_t>(stream));
 }
 
 k6attn_status k6attn_seq2head_relayout(const void *src, void *dst, int B, long S, int H, int d, int elem_bytes,
@@ -334,7 +358,7 @@ k6attn_status k6attn_seq2head_relayout(const void *src, void *dst, int B, long S
     if (S % P)
         return set_error(K6ATTN_ERR_INVALID_ARG, "relayout: sequence length %ld is not divisible by %d", S, P);
     if (H % P) return set_error(K6ATTN_ERR_INVALID_ARG, "relayout: %d heads are not divisible by %d", H, P);
-    if ((long long)P * B * S >= (1LL << 32) || (long long)(H / P) * d * elem_bytes >= (1LL << 31))
+    if ((long long)P * B * S >= (1LL << 31) || (long long)(H / P) * d * elem_bytes >= (1LL << 31))
         return set_error(K6ATTN_ERR_UNSUPPORTED, "relayout: too large");
     if (!aligned16(src) || !aligned16(dst))
         return set_error(K6ATTN_ERR_INVALID_ARG, "relayout: pointers must be 16-byte aligned");
@@ -354,6 +378,7 @@ k6attn_status k6attn_sync(k6attn_t h, void *stream) {
     if (s != K6ATTN_OK) return s;
     if (word) {
         cudaMemset(h->err, 0, sizeof(int));
+        if (word == DEV_RANGE) return set_error(K6ATTN_ERR_RANGE, "a rotated q/k value does not fit fp16");
         return set_error(K6ATTN_ERR_TIMEOUT, "a device-side wait gave up (code %d)", word);
     }
     return K6ATTN_OK;

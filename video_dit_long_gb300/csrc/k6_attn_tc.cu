@@ -13,7 +13,8 @@
 // workspace for the merge kernel.
 //
 // How (one CTA = one work unit = 256 query rows of one (batch, head, chunk)):
-//   warp 8      TMA producer: Q0/Q1 (2 x 128 rows) once, then K_j, V_j tiles of
+//   warp 8      TMA producer (warps 8-11 form the control warpgroup, which
+//               gives registers to the two softmax warpgroups): Q0/Q1 (2 x 128 rows) once, then K_j, V_j tiles of
 //               128 keys x 128 dims through a 4-slot ring (32 KB per tile, two
 //               128-byte-swizzled 64-dim panels per tile).
 //   warp 9      MMA issuer (one thread): S_i = Q_i K_j^T (SS, K-major) into
@@ -57,7 +58,11 @@ constexpr int SMEM_BAR = SMEM_KV + NSTAGE * TILE;
 constexpr int NBAR = 1 + 2 * NSTAGE + 3 * NQ + NQ + 1;  // q_full, kv_full/empty, s/p/o_final, o_step, drain
 constexpr int SMEM_TOTAL = SMEM_BAR + NBAR * 8 + 16;
 constexpr int SMEM_ALLOC = SMEM_TOTAL + 1024;  // room to align the base to 1024 bytes
-constexpr int THREADS = 320;
+constexpr int THREADS = 384;                  // 3 warpgroups: softmax 0, softmax 1, producer/MMA/spare
+// Register split (launch: 384 x 168 = 64512): softmax groups grow to 200,
+// the producer/MMA group shrinks to 104: 2*128*200 + 128*104 = 64512.
+constexpr int REGS_SOFTMAX = 200;
+constexpr int REGS_CONTROL = 104;
 constexpr int TMEM_COLS = 512;
 constexpr float RESCALE_THRESHOLD = 8.0f;     // log2 units: rescale when the max grows past 2^8
 constexpr unsigned long long DRAIN_NS = 1000000000ull;
@@ -74,6 +79,7 @@ struct TcParams {
     unsigned long long wait_limit_ns;
     int *err;
     int strict_order;
+    uint32_t idesc_qk;                        // instruction descriptor of Q.K^T (bf16 or fp16 operands)
 };
 
 // K/V tile j of a chunk: which tensor map (0 video, 1 joint), first row, valid keys.
@@ -169,7 +175,9 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
     const uint32_t tmem = *tmem_slot;
     const WaitCtx w{p.wait_limit_ns, p.err, abort_flag};
 
-    if (warp == 8) {
+    if (warp >= 8) {
+        regs_decrease<REGS_CONTROL>();
+        if (warp == 8) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             prefetch_tmap(&tm_q);
@@ -206,10 +214,10 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                 mbar_drain(&kv_full[idx % NSTAGE], (idx / NSTAGE) & 1, DRAIN_NS);
         }
         __syncwarp();
-    } else if (warp == 9) {
+        } else if (warp == 9) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            const uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false);
+            const uint32_t idesc_qk = p.idesc_qk;
             const uint32_t idesc_pv = idesc_bf16_f32(BM, D, true);
             const uint32_t sQ = smem_u32(smem + SMEM_Q), sKV = smem_u32(smem + SMEM_KV);
             auto issue_s = [&](int i, int slot) {
@@ -229,7 +237,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                            smem_desc_sw128(vb + kk * 16 * 128, PANEL, 1024), idesc_pv, (acc || kk > 0) ? 1u : 0u);
                 }
             };
-            uint32_t step_phase[NQ] = {0, 0};
+            uint32_t step_phase0 = 0, step_phase1 = 0;
             bool ok = mbar_wait(q_full, 0, w) && mbar_wait(&kv_full[0], 0, w);
             if (ok) {
                 tc_fence_after();
@@ -239,44 +247,46 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                 tc_commit(&s_full[1]);
                 tc_commit(&kv_empty[0]);
             }
+            // P.V of Q tile i for K/V tile j, then (if another tile follows) S_i(j+1)
+            auto pv_then_s = [&](int i, int j, int vs, int ks, int kidx, uint32_t &step_phase) -> bool {
+                if (!mbar_wait(&p_full[i], j & 1, w)) return false;
+                tc_fence_after();
+                issue_pv(i, vs, j > 0);
+                if (i == NQ - 1) tc_commit(&kv_empty[vs]);
+                if (j + 1 >= T) {
+                    tc_commit(&o_final[i]);
+                    return true;
+                }
+                if (p.strict_order) {
+                    // P_i lives in S_i's columns: let P.V finish reading it first
+                    tc_commit(&o_step[i]);
+                    const bool done = mbar_wait(&o_step[i], step_phase, w);
+                    step_phase ^= 1;
+                    if (!done) return false;
+                }
+                if (i == 0) {
+                    if (!mbar_wait(&kv_full[ks], (kidx / NSTAGE) & 1, w)) return false;
+                    tc_fence_after();
+                }
+                issue_s(i, ks);
+                tc_commit(&s_full[i]);
+                if (i == NQ - 1) tc_commit(&kv_empty[ks]);
+                return true;
+            };
             for (int j = 0; j < T && ok; j++) {
                 const int vidx = 2 * j + 1, vs = vidx % NSTAGE;
                 const int kidx = 2 * j + 2, ks = kidx % NSTAGE;
-                const bool more = j + 1 < T;
-                ok = mbar_wait(&kv_full[vs], (vidx / NSTAGE) & 1, w);
-                for (int i = 0; i < NQ && ok; i++) {
-                    ok = mbar_wait(&p_full[i], j & 1, w);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_pv(i, vs, j > 0);
-                    if (i == NQ - 1) tc_commit(&kv_empty[vs]);
-                    if (!more) {
-                        tc_commit(&o_final[i]);
-                        continue;
-                    }
-                    if (p.strict_order) {
-                        // P_i lives in S_i's columns: let P.V finish reading it first
-                        tc_commit(&o_step[i]);
-                        ok = mbar_wait(&o_step[i], step_phase[i], w);
-                        step_phase[i] ^= 1;
-                        if (!ok) break;
-                    }
-                    if (i == 0) {
-                        ok = mbar_wait(&kv_full[ks], (kidx / NSTAGE) & 1, w);
-                        if (!ok) break;
-                        tc_fence_after();
-                    }
-                    issue_s(i, ks);
-                    tc_commit(&s_full[i]);
-                    if (i == NQ - 1) tc_commit(&kv_empty[ks]);
-                }
+                ok = mbar_wait(&kv_full[vs], (vidx / NSTAGE) & 1, w) && pv_then_s(0, j, vs, ks, kidx, step_phase0) &&
+                     pv_then_s(1, j, vs, ks, kidx, step_phase1);
             }
             // every MMA issued so far must complete before tensor memory is freed
             tc_commit(drain);
             mbar_drain(drain, 0, DRAIN_NS);
         }
         __syncwarp();
+        }
     } else {
+        regs_increase<REGS_SOFTMAX>();
         // ------------------------------------------------ softmax / epilogue
         const int i = warp / 4;                       // Q tile of this warpgroup
         const int r = threadIdx.x % BM;               // row within the tile = TMEM lane
@@ -463,6 +473,9 @@ cudaError_t launch_attn_tc(const Geom &g, const void *q, const void *k, const vo
     p.wait_limit_ns = opt.wait_limit_ns;
     p.err = opt.err;
     p.strict_order = opt.strict_order;
+    // Q.K^T operands: bf16 (A/B format 1) or fp16 (format 0); P.V stays bf16
+    p.idesc_qk = opt.qk_f16 ? (idesc_bf16_f32(tc::BM, tc::BN, false) & ~((7u << 7) | (7u << 10)))
+                            : idesc_bf16_f32(tc::BM, tc::BN, false);
     const long units = (long)g.B * g.H * n_chunks * p.q_pairs;
     if (units == 0) return cudaSuccess;
     attn_tc_kernel<<<(unsigned)units, tc::THREADS, tc::SMEM_ALLOC, st>>>(mq, mk, mv, mjk, mjv, p);

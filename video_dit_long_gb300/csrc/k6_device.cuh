@@ -6,10 +6,10 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "k6_internal.h"
+
 namespace k6 {
 
-// Device error word codes (written with atomicCAS, first error wins).
-enum : int { DEV_OK = 0, DEV_TIMEOUT = 1 };
 
 // Everything a bounded wait needs: the deadline length, the handle's error
 // word in global memory, and the CTA's abort flag in shared memory.
@@ -64,7 +64,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // Wait for the phase of `bar` with the given parity to complete.  Gives up
 // (returns false) when another warp of the CTA has aborted, or after
 // w.limit_ns, in which case it records DEV_TIMEOUT and aborts the CTA.
-__device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const WaitCtx &w) {
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const WaitCtx &w) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (true) {
@@ -80,7 +80,7 @@ __device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const Wai
 
 // Same, with a fixed deadline and no abort check: used on the way out to let
 // asynchronous copies and MMAs already in flight land before the CTA exits.
-__device__ __noinline__ bool mbar_drain(uint64_t *bar, uint32_t parity, unsigned long long limit_ns) {
+__device__ __forceinline__ bool mbar_drain(uint64_t *bar, uint32_t parity, unsigned long long limit_ns) {
     const unsigned long long t0 = global_ns();
     while (!mbar_try_wait(bar, parity)) {
         if (global_ns() - t0 >= limit_ns) return false;
@@ -205,6 +205,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Warpgroup register rebalancing (all 128 threads of a warpgroup execute it).
+template <int N>
+__device__ __forceinline__ void regs_increase() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_decrease() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
 
 // ----------------------------------------------------------------- math
 

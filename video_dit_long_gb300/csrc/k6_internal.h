@@ -10,6 +10,9 @@
 
 namespace k6 {
 
+// Device error word codes (written with atomicCAS, first error wins).
+enum : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_RANGE = 2 };
+
 // Geometry of one joint attention problem, as the kernels see it.
 struct Geom {
     int B, H, d;
@@ -18,6 +21,7 @@ struct Geom {
     int axis_dim[3];
     int joint_rope;
     int elem;                // bytes per element (2 bf16, 4 f32)
+    k6attn_dtype dtype;      // storage type of q, k, v, out (BF16 or F32)
 };
 
 // Offsets (in float2 entries) of the rotary tables inside one buffer.
@@ -37,9 +41,12 @@ k6attn_status cuda_check(cudaError_t e, const char *what);
 cudaError_t launch_rope_tables(const Geom &g, double theta, float2 *tables, cudaStream_t st);
 
 // Rotary embedding of q [B][S][H][d], k [B][Nv][H][d], jk [B][Nj][H][d]
-// from src_* into dst_* (dst may equal src).
+// from src_* (type g.dtype) into dst_* (type out_dtype; dst may equal src
+// when the types match).  Writing F16, a value that is not finite in fp16
+// sets *err to DEV_RANGE.
 cudaError_t launch_rope_qk(const Geom &g, const float2 *tables, const void *src_q, void *dst_q, const void *src_k,
-                           void *dst_k, const void *src_jk, void *dst_jk, cudaStream_t st);
+                           void *dst_k, const void *src_jk, void *dst_jk, k6attn_dtype out_dtype, int *err,
+                           cudaStream_t st);
 
 cudaError_t launch_lse_merge(const Geom &g, int n, const float *part_o, const float *part_lse, void *out, float *lse,
                              cudaStream_t st);
@@ -60,6 +67,7 @@ struct AttnTcOptions {
     unsigned long long wait_limit_ns;
     int *err;
     int strict_order;        // 1: wait for P.V to finish before reusing its TMEM
+    int qk_f16;              // 1: q/k/joint_k are fp16 (Q.K^T in fp16), else bf16
 };
 cudaError_t launch_attn_tc(const Geom &g, const void *q, const void *k, const void *v, const void *jk,
                            const void *jv, int n_chunks, void *out, float *lse, const AttnTcOptions &opt,

@@ -41,13 +41,28 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(int n, long rows, long S
         const float L = m + logf(sum);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         const float *po = part_o + r * D + sub * 4;
-        for (int c = 0; c < n; c++) {
-            const float wgt = expf(__ldg(part_lse + c * l_stride + li) - L);
-            const float4 x = __ldcs(reinterpret_cast<const float4 *>(po + c * o_stride));
-            acc.x += wgt * x.x;
-            acc.y += wgt * x.y;
-            acc.z += wgt * x.z;
-            acc.w += wgt * x.w;
+        // four chunks per pass, loads issued before the arithmetic
+        for (int c0 = 0; c0 < n; c0 += 4) {
+            float4 x[4];
+            float wgt[4];
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const int c = c0 + u;
+                if (c < n) {
+                    x[u] = __ldcs(reinterpret_cast<const float4 *>(po + c * o_stride));
+                    wgt[u] = __ldg(part_lse + c * l_stride + li);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                if (c0 + u < n) {
+                    const float wt = expf(wgt[u] - L);
+                    acc.x += wt * x[u].x;
+                    acc.y += wt * x[u].y;
+                    acc.z += wt * x[u].z;
+                    acc.w += wt * x[u].w;
+                }
+            }
         }
         if constexpr (sizeof(OutT) == 2) {
             __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);

@@ -12,8 +12,11 @@
 // Every head-buffer row (p, b, token) is one contiguous run of Hl*d elements,
 // and so is its source.  One warp copies one run per iteration with 16-byte
 // vectors (narrower only when the run is not a multiple of 16 bytes), so the
-// index arithmetic (32-bit) is paid once per run, not per element.  Pure
-// byte moves: bit-exact by construction.
+// index arithmetic (32-bit) is paid once per run, not per element; four runs
+// per warp-iteration with every load issued before the stores keep enough
+// bytes in flight.  Pure byte moves: bit-exact by construction.
+#include <cuda_runtime.h>
+
 #include "k6_internal.h"
 
 namespace k6 {
@@ -22,25 +25,50 @@ template <typename V>
 __global__ void __launch_bounds__(256) relayout_kernel(const char *__restrict__ src, char *__restrict__ dst,
                                                        unsigned B, unsigned S, unsigned Sl, unsigned H, unsigned Hl,
                                                        unsigned run_bytes, unsigned rows, int direction) {
+    constexpr int kRows = 4;     // runs per warp-iteration
+    constexpr int kPerLane = 2;  // words per lane per run and pass
     const unsigned lane = threadIdx.x & 31;
     const unsigned warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const unsigned nwarps = (gridDim.x * blockDim.x) >> 5;
     const unsigned nvec = run_bytes / sizeof(V);
     const unsigned long long row_bytes_seq = (unsigned long long)run_bytes * (H / Hl);  // H*d*eb
-    for (unsigned hr = warp; hr < rows; hr += nwarps) {
-        // hr = (p*B + b)*S + token
-        const unsigned token = hr % S;
-        const unsigned pb = hr / S;
-        const unsigned b = pb % B;
-        const unsigned p = pb / B;
-        const unsigned r = token / Sl;
-        const unsigned s = token % Sl;
-        const unsigned long long head_off = (unsigned long long)hr * run_bytes;
-        const unsigned long long seq_off =
-            ((unsigned long long)(r * B + b) * Sl + s) * row_bytes_seq + (unsigned long long)p * run_bytes;
-        const V *from = reinterpret_cast<const V *>(src + (direction == 0 ? seq_off : head_off));
-        V *to = reinterpret_cast<V *>(dst + (direction == 0 ? head_off : seq_off));
-        for (unsigned k = lane; k < nvec; k += 32) to[k] = __ldcs(from + k);
+    for (unsigned hr0 = warp * kRows; hr0 < rows; hr0 += nwarps * kRows) {
+        const V *from[kRows];
+        V *to[kRows];
+#pragma unroll
+        for (int i = 0; i < kRows; i++) {
+            // hr = (p*B + b)*S + token
+            const unsigned hr = min(hr0 + i, rows - 1);
+            const unsigned token = hr % S;
+            const unsigned pb = hr / S;
+            const unsigned b = pb % B;
+            const unsigned p = pb / B;
+            const unsigned r = token / Sl;
+            const unsigned s = token % Sl;
+            const unsigned long long head_off = (unsigned long long)hr * run_bytes;
+            const unsigned long long seq_off =
+                ((unsigned long long)(r * B + b) * Sl + s) * row_bytes_seq + (unsigned long long)p * run_bytes;
+            from[i] = reinterpret_cast<const V *>(src + (direction == 0 ? seq_off : head_off));
+            to[i] = reinterpret_cast<V *>(dst + (direction == 0 ? head_off : seq_off));
+        }
+        const int live = (int)min((unsigned)kRows, rows - hr0);
+        for (unsigned base = 0; base < nvec; base += 32 * kPerLane) {
+            V x[kRows][kPerLane];
+#pragma unroll
+            for (int i = 0; i < kRows; i++)
+#pragma unroll
+                for (int u = 0; u < kPerLane; u++) {
+                    const unsigned k = base + u * 32 + lane;
+                    if (i < live && k < nvec) x[i][u] = __ldcs(from[i] + k);
+                }
+#pragma unroll
+            for (int i = 0; i < kRows; i++)
+#pragma unroll
+                for (int u = 0; u < kPerLane; u++) {
+                    const unsigned k = base + u * 32 + lane;
+                    if (i < live && k < nvec) __stcs(to[i] + k, x[i][u]);
+                }
+        }
     }
 }
 
@@ -54,8 +82,8 @@ static cudaError_t launch_relayout_t(const void *src, void *dst, int B, long S, 
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const unsigned warps_per_block = 8;
-    unsigned blocks = (rows + warps_per_block - 1) / warps_per_block;
+    const unsigned runs_per_block = 8 * 4;  // 8 warps x 4 runs
+    unsigned blocks = (rows + runs_per_block - 1) / runs_per_block;
     unsigned cap = (unsigned)sms * 8;
     if (blocks > cap) blocks = cap;
     relayout_kernel<V><<<blocks, 256, 0, st>>>(static_cast<const char *>(src), static_cast<char *>(dst), (unsigned)B,

@@ -15,7 +15,11 @@
 // The rotation kernel is HBM-bound: one 16-byte load and one 16-byte store
 // per 8 bf16 (or 4 f32) elements; Q, K and joint K are rotated in one launch.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
+#include <type_traits>
+
+#include "k6_device.cuh"
 #include "k6_internal.h"
 
 namespace k6 {
@@ -74,6 +78,7 @@ cudaError_t launch_rope_tables(const Geom &g, double theta, float2 *tables, cuda
 // ------------------------------------------------------------------ rotate
 
 struct RopeArgs {
+    int *err;            // device error word (range check of fp16 output)
     const void *src[3];
     void *dst[3];
     long tokens[3];      // B*S, B*Nv, B*Nj
@@ -122,6 +127,16 @@ struct Vec<__nv_bfloat16> {
     }
 };
 template <>
+struct Vec<__half> {
+    static constexpr int kPairs = 4;
+    __device__ static void store(void *p, const float (&x)[8]) {
+        uint4 u;
+        __half2 *b = reinterpret_cast<__half2 *>(&u);
+        for (int k = 0; k < 4; k++) b[k] = __floats2half2_rn(x[2 * k], x[2 * k + 1]);
+        *reinterpret_cast<uint4 *>(p) = u;
+    }
+};
+template <>
 struct Vec<float> {
     static constexpr int kPairs = 2;
     __device__ static void load(const void *p, float (&x)[8]) {
@@ -133,53 +148,77 @@ struct Vec<float> {
     }
 };
 
-// One block-iteration per token: its H*d elements are contiguous, so the
-// block sweeps them with 16-byte vectors; the token's position is uniform.
-template <typename T>
-__global__ void __launch_bounds__(128) rope_kernel(RopeArgs a, const float2 *__restrict__ tab) {
+// One warp per token: its H*d elements are contiguous, the token's position
+// (and so its rotation angles) is uniform across the warp, and each lane
+// moves up to 4 16-byte vectors per pass with all loads issued before any
+// store, so that enough bytes are in flight for HBM.
+template <typename T, typename Tout>
+__global__ void __launch_bounds__(256) rope_kernel(RopeArgs a, const float2 *__restrict__ tab) {
     constexpr int kPairs = Vec<T>::kPairs;
+    constexpr int kUnroll = 4;
+    static_assert(sizeof(T) == sizeof(Tout), "rotation keeps the element size");
     const long total = a.tokens[0] + a.tokens[1] + a.tokens[2];
     const int vecs_per_token = a.H * a.d / (2 * kPairs);
     const int vecs_per_head = a.d / (2 * kPairs);
-    for (long tok = blockIdx.x; tok < total; tok += gridDim.x) {
+    const int lane = threadIdx.x & 31;
+    const long warp0 = (blockIdx.x * (long)blockDim.x + threadIdx.x) >> 5;
+    const long nwarps = ((long)gridDim.x * blockDim.x) >> 5;
+    for (long tok = warp0; tok < total; tok += nwarps) {
         int which = 0;
         long local = tok;
         while (which < 2 && local >= a.tokens[which]) {
             local -= a.tokens[which];
             which++;
         }
-        long n = local % a.seq[which];  // token index within its sequence
-        long j = -1;                    // joint index, or -1 for video
+        const long n = local % a.seq[which];  // token index within its sequence
+        long j = -1;                          // joint index, or -1 for video
         if (which == 2) j = n;
         else if (n >= a.Nv) j = n - a.Nv;
         int t = 0, h = 0, w = 0;
         if (j < 0) {
-            long hw = (long)a.grid_h * a.grid_w;
+            const long hw = (long)a.grid_h * a.grid_w;
             t = (int)(n / hw);
             h = (int)((n / a.grid_w) % a.grid_h);
             w = (int)(n % a.grid_w);
         }
         const char *src = static_cast<const char *>(a.src[which]) + local * (long)a.H * a.d * sizeof(T);
         char *dst = static_cast<char *>(a.dst[which]) + local * (long)a.H * a.d * sizeof(T);
-        for (int v = threadIdx.x; v < vecs_per_token; v += blockDim.x) {
-            float x[8];
-            Vec<T>::load(src + (long)v * 16, x);
-            int pair0 = (v % vecs_per_head) * kPairs;
+        bool bad = false;
+        for (int base = 0; base < vecs_per_token; base += 32 * kUnroll) {
+            float x[kUnroll][8];
 #pragma unroll
-            for (int k = 0; k < kPairs; k++) {
-                float2 cs = rope_cs(a, tab, pair0 + k, t, h, w, j);
-                float xr = x[2 * k], xi = x[2 * k + 1];
-                x[2 * k] = xr * cs.x - xi * cs.y;
-                x[2 * k + 1] = xr * cs.y + xi * cs.x;
+            for (int u = 0; u < kUnroll; u++) {
+                const int v = base + u * 32 + lane;
+                if (v < vecs_per_token) Vec<T>::load(src + (long)v * 16, x[u]);
             }
-            Vec<T>::store(dst + (long)v * 16, x);
+#pragma unroll
+            for (int u = 0; u < kUnroll; u++) {
+                const int v = base + u * 32 + lane;
+                if (v >= vecs_per_token) continue;
+                const int pair0 = (v % vecs_per_head) * kPairs;
+#pragma unroll
+                for (int k = 0; k < kPairs; k++) {
+                    const float2 cs = rope_cs(a, tab, pair0 + k, t, h, w, j);
+                    const float xr = x[u][2 * k], xi = x[u][2 * k + 1];
+                    x[u][2 * k] = xr * cs.x - xi * cs.y;
+                    x[u][2 * k + 1] = xr * cs.y + xi * cs.x;
+                }
+                if constexpr (!std::is_same<T, Tout>::value) {
+#pragma unroll
+                    for (int k = 0; k < 2 * kPairs; k++) bad |= !(fabsf(x[u][k]) < 65520.f);  // a finite half
+                }
+                Vec<Tout>::store(dst + (long)v * 16, x[u]);
+            }
         }
+        if (bad) atomicCAS(a.err, DEV_OK, DEV_RANGE);
     }
 }
 
 cudaError_t launch_rope_qk(const Geom &g, const float2 *tables, const void *src_q, void *dst_q, const void *src_k,
-                           void *dst_k, const void *src_jk, void *dst_jk, cudaStream_t st) {
+                           void *dst_k, const void *src_jk, void *dst_jk, k6attn_dtype out_dtype, int *err,
+                           cudaStream_t st) {
     RopeArgs a;
+    a.err = err;
     a.src[0] = src_q, a.dst[0] = dst_q;
     a.src[1] = src_k, a.dst[1] = dst_k;
     a.src[2] = src_jk, a.dst[2] = dst_jk;
@@ -201,11 +240,14 @@ cudaError_t launch_rope_qk(const Geom &g, const float2 *tables, const void *src_
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    long blocks = total < (long)sms * 16 ? total : (long)sms * 16;
-    if (g.elem == 2)
-        rope_kernel<__nv_bfloat16><<<(unsigned)blocks, 128, 0, st>>>(a, tables);
+    long blocks = (total + 7) / 8;  // 8 warps per block, one token per warp-iteration
+    if (blocks > (long)sms * 8) blocks = (long)sms * 8;
+    if (g.dtype == K6ATTN_BF16 && out_dtype == K6ATTN_F16)
+        rope_kernel<__nv_bfloat16, __half><<<(unsigned)blocks, 256, 0, st>>>(a, tables);
+    else if (g.dtype == K6ATTN_BF16)
+        rope_kernel<__nv_bfloat16, __nv_bfloat16><<<(unsigned)blocks, 256, 0, st>>>(a, tables);
     else
-        rope_kernel<float><<<(unsigned)blocks, 128, 0, st>>>(a, tables);
+        rope_kernel<float, float><<<(unsigned)blocks, 256, 0, st>>>(a, tables);
     return cudaGetLastError();
 }
 

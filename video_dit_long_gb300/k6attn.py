@@ -13,8 +13,8 @@ import os
 
 from . import build as _build
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE = range(6)
-BF16, F32 = 0, 1
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_RANGE = range(7)
+BF16, F32, F16 = 0, 1, 2
 OPT_WAIT_LIMIT_NS, OPT_STRICT_MMA_ORDER = 0, 1
 
 # every symbol the header declares
@@ -65,9 +65,9 @@ def load(build_if_missing: bool = True):
     L.k6attn_rope_tables_bytes.restype = Z
     L.k6attn_workspace_bytes.argtypes = [P, I, I]
     L.k6attn_workspace_bytes.restype = Z
-    L.k6attn_rope_qk.argtypes = [P, P, P, P, P, P]
+    L.k6attn_rope_qk.argtypes = [P, P, P, P, P, P, P, P, I, P]
     L.k6attn_forward.argtypes = [P, P, P, P, P, P, P, I, P, P, P, Z, P]
-    L.k6attn_attention_chunks.argtypes = [P, P, P, P, P, P, I, P, P, P]
+    L.k6attn_attention_chunks.argtypes = [P, P, P, P, P, P, I, I, P, P, P]
     L.k6attn_lse_merge.argtypes = [P, P, P, I, P, P, P]
     L.k6attn_seq2head_relayout.argtypes = [P, P, I, ctypes.c_long, I, I, I, I, I, P]
     L.k6attn_sync.argtypes = [P, P]
@@ -142,9 +142,16 @@ class Handle:
     def set_option(self, opt: int, value: int):
         _check(load().k6attn_set_option(self.h, opt, int(value)))
 
-    def rope_qk(self, q, k, joint_k, tables=None, stream=None):
+    def rope_qk(self, q, k, joint_k, tables=None, q_out=None, k_out=None, joint_k_out=None, out_dtype=None,
+                stream=None):
+        """Rotate q/k/joint_k; in place unless outputs are given (out_dtype F16 for fp16 copies)."""
         tab = ctypes.c_void_p(self.rope_tables() if tables is None else tables)
-        _check(load().k6attn_rope_qk(self.h, _ptr(q), _ptr(k), _ptr(joint_k), tab, _stream(stream)))
+        qo = q if q_out is None else q_out
+        ko = k if k_out is None else k_out
+        jo = joint_k if joint_k_out is None else joint_k_out
+        od = self._desc.dtype if out_dtype is None else out_dtype
+        _check(load().k6attn_rope_qk(self.h, _ptr(q), _ptr(k), _ptr(joint_k), tab, _ptr(qo), _ptr(ko), _ptr(jo),
+                                     int(od), _stream(stream)))
 
     def forward(self, q, k, v, joint_k, joint_v, out, lse=None, *, rope=True, n_chunks=1, workspace=None,
                 tables=None, stream=None):
@@ -156,9 +163,10 @@ class Handle:
                                      int(n_chunks), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
                                      _stream(stream)))
 
-    def attention_chunks(self, q, k, v, joint_k, joint_v, n_chunks, out, lse=None, stream=None):
+    def attention_chunks(self, q, k, v, joint_k, joint_v, n_chunks, out, lse=None, qk_dtype=None, stream=None):
+        qd = self._desc.dtype if qk_dtype is None else qk_dtype
         _check(load().k6attn_attention_chunks(self.h, _ptr(q), _ptr(k), _ptr(v), _ptr(joint_k), _ptr(joint_v),
-                                              int(n_chunks), _ptr(out), _ptr(lse), _stream(stream)))
+                                              int(qd), int(n_chunks), _ptr(out), _ptr(lse), _stream(stream)))
 
     def lse_merge(self, part_o, part_lse, n_chunks, out, lse=None, stream=None):
         _check(load().k6attn_lse_merge(self.h, _ptr(part_o), _ptr(part_lse), int(n_chunks), _ptr(out), _ptr(lse),
