@@ -414,7 +414,7 @@ def main():
     ap.add_argument("--chunks", type=int, default=0)
     ap.add_argument("--no-secondary", dest="secondary", action="store_false")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--cpu-rows", type=int, default=192)
+    ap.add_argument("--cpu-rows", type=int, default=1536)
     ap.add_argument("--ref-rows", type=int, default=4)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

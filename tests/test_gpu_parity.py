@@ -38,7 +38,7 @@ def K():
 SMALL = {
     "ragged": Workload("ragged", 1, 2, 128, "bf16", (3, 10, 20), 40, (32, 48, 48), 0, 1.0, 1.0, (1, 2, 4, 5)),
     "one_tile": Workload("one_tile", 1, 3, 128, "bf16", (1, 7, 9), 0, (32, 48, 48), 0, 1.0, 1.0, (1, 3)),
-    "audio1d": Workload("audio1d", 2, 2, 128, "bf16", (2, 8, 16), 61, (32, 48, 48), 1, 1.0, 1.0, (1, 3)),
+    "audio1d": Workload("audio1d", 2, 2, 128, "bf16", (2, 8, 16), 62, (32, 48, 48), 1, 1.0, 1.0, (1, 3)),
     "f32_d128": Workload("f32_d128", 1, 2, 128, "f32", (2, 6, 10), 8, (32, 48, 48), 0, 1.0, 1.0, (1, 4)),
 }
 

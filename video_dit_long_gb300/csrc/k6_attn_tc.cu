@@ -308,14 +308,22 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
 #pragma unroll
             for (int cc = 0; cc < BN / 32; cc++) tmem_ld32(tS + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[cc * 32]));
             tmem_ld_wait();
-            float mx = -INFINITY;
+            if (valid < BN) {  // ragged tile end (warp-uniform): keys past the segment get -inf
 #pragma unroll
-            for (int k = 0; k < BN; k++) {
-                float x = __uint_as_float(s[k]);
-                if (k >= valid) x = -INFINITY;
-                s[k] = __float_as_uint(x);
-                mx = fmaxf(mx, x);
+                for (int k = 0; k < BN; k++)
+                    if (k >= valid) s[k] = 0xff800000u;
             }
+            // row max: four independent 3-input chains
+            float mc[4];
+#pragma unroll
+            for (int c4 = 0; c4 < 4; c4++) {
+                const uint32_t *x = &s[c4 * 32];
+                float m = fmax3(__uint_as_float(x[0]), __uint_as_float(x[1]), __uint_as_float(x[2]));
+#pragma unroll
+                for (int k = 3; k < 31; k += 2) m = fmax3(m, __uint_as_float(x[k]), __uint_as_float(x[k + 1]));
+                mc[c4] = fmaxf(m, __uint_as_float(x[31]));
+            }
+            const float mx = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]));
             const float mt = mx * sl2;
             bool need = false;
             if (j == 0) m_run = mt;
@@ -338,14 +346,24 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                     tmem_st32(tO + cc * 32, o);
                 }
             }
-            float sum = 0.f;
+            // p = 2^(s * scale*log2e - m): packed FMA, then the SFU; row sum on packed adds
+            const uint64_t scale2 = f2(sl2, sl2), negm2 = f2(-m_run, -m_run);
+            uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
             uint32_t pk[BN / 2];
 #pragma unroll
             for (int k = 0; k < BN; k += 2) {
-                const float p0 = ex2(fmaf(__uint_as_float(s[k]), sl2, -m_run));
-                const float p1 = ex2(fmaf(__uint_as_float(s[k + 1]), sl2, -m_run));
-                sum += p0 + p1;
+                float a, b;
+                f2_split(ffma2(f2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])), scale2, negm2), a, b);
+                const float p0 = ex2(a), p1 = ex2(b);
                 pk[k / 2] = pack_bf16x2(p0, p1);
+                acc[(k / 2) & 3] = fadd2(acc[(k / 2) & 3], f2(p0, p1));
+            }
+            float sum;
+            {
+                float a0, a1, b0, b1;
+                f2_split(fadd2(acc[0], acc[1]), a0, a1);
+                f2_split(fadd2(acc[2], acc[3]), b0, b1);
+                sum = (a0 + a1) + (b0 + b1);
             }
             l_run += sum;
             tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));

@@ -164,25 +164,27 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a, const float2 *__r
     const long warp0 = (blockIdx.x * (long)blockDim.x + threadIdx.x) >> 5;
     const long nwarps = ((long)gridDim.x * blockDim.x) >> 5;
     for (long tok = warp0; tok < total; tok += nwarps) {
+        // 32-bit index arithmetic: the host guarantees B*S*H < 2^31
         int which = 0;
-        long local = tok;
-        while (which < 2 && local >= a.tokens[which]) {
-            local -= a.tokens[which];
+        unsigned local = (unsigned)tok;
+        while (which < 2 && local >= (unsigned)a.tokens[which]) {
+            local -= (unsigned)a.tokens[which];
             which++;
         }
-        const long n = local % a.seq[which];  // token index within its sequence
-        long j = -1;                          // joint index, or -1 for video
+        const unsigned n = local % (unsigned)a.seq[which];  // token index within its sequence
+        long j = -1;                                        // joint index, or -1 for video
         if (which == 2) j = n;
-        else if (n >= a.Nv) j = n - a.Nv;
+        else if (n >= (unsigned)a.Nv) j = n - (unsigned)a.Nv;
         int t = 0, h = 0, w = 0;
         if (j < 0) {
-            const long hw = (long)a.grid_h * a.grid_w;
-            t = (int)(n / hw);
-            h = (int)((n / a.grid_w) % a.grid_h);
-            w = (int)(n % a.grid_w);
+            const unsigned gw = (unsigned)a.grid_w, gh = (unsigned)a.grid_h;
+            const unsigned nw = n / gw;
+            w = (int)(n - nw * gw);
+            t = (int)(nw / gh);
+            h = (int)(nw - (unsigned)t * gh);
         }
-        const char *src = static_cast<const char *>(a.src[which]) + local * (long)a.H * a.d * sizeof(T);
-        char *dst = static_cast<char *>(a.dst[which]) + local * (long)a.H * a.d * sizeof(T);
+        const char *src = static_cast<const char *>(a.src[which]) + (long)local * a.H * a.d * sizeof(T);
+        char *dst = static_cast<char *>(a.dst[which]) + (long)local * a.H * a.d * sizeof(T);
         bool bad = false;
         for (int base = 0; base < vecs_per_token; base += 32 * kUnroll) {
             float x[kUnroll][8];
