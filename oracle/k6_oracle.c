@@ -32,6 +32,11 @@
  *     "Context Parallelism in vLLM Omni Neuron", sections "Ring attention
  *     (current implementation)" and "Scaling Properties".  The merge formula
  *     is a reading: LSE = log sum_c exp(LSE_c), out = sum_c exp(LSE_c - LSE) O_c.
+ *   - Cross-attention, queries of one stream over the keys/values of another
+ *     (Sq != Sk, no rotary): vLLM-Omni recipe "Kandinsky 6 TI2VA -- H100"
+ *     ("Audio queries gather the full visual sequence"); "Context Parallelism
+ *     in vLLM Omni Neuron", "Forward Pass Flow" ("Cross-attention uses full
+ *     encoder states").
  *   - The sequence-partitioned <-> head-partitioned relayout that Ulysses does
  *     with all-to-all: xDiT PR #586 USP listing (`_ft_c_input_all_to_all`,
  *     `_ft_c_output_all_to_all`); "Context Parallelism in vLLM Omni Neuron",
@@ -244,6 +249,58 @@ int k6o_attention(const k6o_geom *g, int rope, const void *q, const void *k, con
     free(kr);
     free(vr);
     return 0;
+}
+
+/*
+ * Cross-attention: Sq query rows of q [B][Sq][H][d] over keys [kv_begin,
+ * kv_end) of k, v [B][Sk][H][d]; no rotary.  out [B][Sq][H][d], lse
+ * [B][H][Sq], the same definitions as k6o_attention.
+ */
+int k6o_cross_attention(int B, int H, int d, long Sq, long Sk, const void *q, const void *k, const void *v,
+                        int type, long kv_begin, long kv_end, double *out, double *lse) {
+    if (B < 1 || H < 1 || d < 1 || Sq < 0 || Sk < 1) return -1;
+    if (kv_begin < 0 || kv_end > Sk || kv_begin >= kv_end) return -2;
+    const long L = kv_end - kv_begin;
+    const double scale = 1.0 / sqrt((double)d);
+    const long tasks = (long)B * H * Sq;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)L);
+        if (!s) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(dynamic, 16)
+        for (long t = 0; t < tasks; t++) {
+            if (!s) continue;
+            const long i = t % Sq;
+            const int h = (int)((t / Sq) % H);
+            const int b = (int)(t / ((long)Sq * H));
+            const size_t qoff = (((size_t)b * Sq + i) * H + h) * d;
+            double m = -INFINITY;
+            for (long j = 0; j < L; j++) {
+                const size_t koff = (((size_t)b * Sk + kv_begin + j) * H + h) * d;
+                double acc = 0.0;
+                for (int e = 0; e < d; e++) acc += load_elem(q, type, qoff + e) * load_elem(k, type, koff + e);
+                s[j] = acc * scale;
+                if (s[j] > m) m = s[j];
+            }
+            double sum = 0.0;
+            for (long j = 0; j < L; j++) sum += exp(s[j] - m);
+            const double lse_i = m + log(sum);
+            double *o = out + qoff;
+            for (int e = 0; e < d; e++) o[e] = 0.0;
+            for (long j = 0; j < L; j++) {
+                const double pj = exp(s[j] - lse_i);
+                const size_t voff = (((size_t)b * Sk + kv_begin + j) * H + h) * d;
+                for (int e = 0; e < d; e++) o[e] += pj * load_elem(v, type, voff + e);
+            }
+            lse[((size_t)b * H + h) * Sq + i] = lse_i;
+        }
+        free(s);
+    }
+    return bad ? -4 : 0;
 }
 
 /*

@@ -83,6 +83,8 @@ def lib():
         _lib.k6o_rope_vec.restype = None
         _lib.k6o_attention.argtypes = [ctypes.POINTER(_Geom), ctypes.c_int, P, P, P, P, P, ctypes.c_int,
                                        ctypes.c_long, ctypes.c_long, P, ctypes.c_long, P, P]
+        _lib.k6o_cross_attention.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_long,
+                                             ctypes.c_long, P, P, P, ctypes.c_int, ctypes.c_long, ctypes.c_long, P, P]
         _lib.k6o_lse_merge.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_long, ctypes.c_int, ctypes.c_int,
                                        P, P, ctypes.c_int, P, P]
         _lib.k6o_relayout.argtypes = [P, P, ctypes.c_int, ctypes.c_long, ctypes.c_int, ctypes.c_int,
@@ -165,6 +167,27 @@ def attention(g: Geom, q, k, v, jk=None, jv=None, *, rope: bool = True, kv_range
                              t, int(kb), int(ke), _ptr(rows), n, _ptr(out), _ptr(lse))
     if rc:
         raise ValueError(f"k6o_attention: {rc}")
+    return out, lse
+
+
+def cross_attention(q, k, v, *, kv_range=None):
+    """Cross-attention (no rotary) of q [B][Sq][H][d] over k, v [B][Sk][H][d].
+
+    Returns (out [B][Sq][H][d], lse [B][H][Sq]), float64.
+    """
+    (q_, t1), (k_, t2), (v_, t3) = _typed(q), _typed(k), _typed(v)
+    if len({t1, t2, t3}) != 1:
+        raise TypeError("q, k, v must share one dtype")
+    B, Sq, H, d = q_.shape
+    Sk = k_.shape[1]
+    assert k_.shape == (B, Sk, H, d) and v_.shape == (B, Sk, H, d)
+    kb, ke = (0, Sk) if kv_range is None else kv_range
+    out = np.empty((B, Sq, H, d), np.float64)
+    lse = np.empty((B, H, Sq), np.float64)
+    rc = lib().k6o_cross_attention(B, H, d, Sq, Sk, _ptr(q_), _ptr(k_), _ptr(v_), t1, int(kb), int(ke), _ptr(out),
+                                   _ptr(lse))
+    if rc:
+        raise ValueError(f"k6o_cross_attention: {rc}")
     return out, lse
 
 

@@ -226,6 +226,49 @@ def test_merge_accepts_f32_partials_exactly():
     np.testing.assert_array_equal(a[1], b[1])
 
 
+# ------------------------------------------------------------ cross-attention
+
+
+@pytest.mark.parametrize("Sq,Sk,d", [(3, 11, 4), (13, 5, 8), (1, 1, 4)])
+def test_cross_attention_matches_decimal_brute_force(Sq, Sk, d):
+    B, H = 2, 2
+    q, k, v = rnd((B, Sq, H, d), Sq, 2.0), rnd((B, Sk, H, d), Sk + 1, 2.0), rnd((B, Sk, H, d), Sk + 2)
+    out, lse = O.cross_attention(q, k, v)
+    for b in range(B):
+        for h in range(H):
+            K = [k[b, j, h] for j in range(Sk)]
+            V = [v[b, j, h] for j in range(Sk)]
+            for i in range(Sq):
+                ref_o, ref_l = brute_attention_decimal(q[b, i, h], K, V)
+                np.testing.assert_allclose(out[b, i, h], ref_o, rtol=0, atol=1e-13)
+                assert abs(lse[b, h, i] - ref_l) < 1e-13
+
+
+def test_cross_attention_matches_torch_sdpa_and_merges():
+    torch = pytest.importorskip("torch")
+    B, Sq, Sk, H, d = 2, 9, 40, 3, 16
+    q, k, v = rnd((B, Sq, H, d), 1, 1.5), rnd((B, Sk, H, d), 2, 1.5), rnd((B, Sk, H, d), 3)
+    out, lse = O.cross_attention(q, k, v)
+    tq, tk, tv = (torch.from_numpy(a).permute(0, 2, 1, 3) for a in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv).permute(0, 2, 1, 3).numpy()
+    ref_lse = torch.logsumexp(tq @ tk.transpose(-1, -2) / math.sqrt(d), dim=-1).numpy()
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse, rtol=0, atol=1e-12)
+    parts = [O.cross_attention(q, k, v, kv_range=r) for r in O.chunk_bounds(Sk, 4)]
+    mo, ml = O.lse_merge(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+    np.testing.assert_allclose(mo, out, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(ml, lse, rtol=0, atol=1e-12)
+
+
+def test_cross_attention_equals_self_attention_without_rotary():
+    g = tiny_geom(B=1, H=2, d=8, grid=(1, 3, 4), Nj=0)
+    q, k, v, _, _ = tiny_inputs(g, seed=12)
+    a = O.attention(g, q, k, v, rope=False)
+    b = O.cross_attention(q, k, v)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
 # ------------------------------------------------------------------- rotary
 
 
