@@ -288,6 +288,38 @@ class _Null:
         pass
 
 
+def measure_cross(w, steps, warmup, n_chunks=8):
+    """Audio queries (the workload's joint tokens) over the full visual sequence, K/V in n chunks."""
+    import torch
+    from video_dit_long_gb300 import k6attn as K
+    B, H, d, Sq, Sk = w.B, w.H, w.d, w.Nj, w.Nv
+
+    def dev(tid, rows, std):
+        return torch.from_numpy(inputs.tensor(42, tid, (B, rows, H, d), "bf16", std).view(np.int16)).view(
+            torch.bfloat16).cuda()
+
+    q, k, v = dev(30, Sq, w.qk_std), dev(31, Sk, w.qk_std), dev(32, Sk, w.v_std)
+    h = K.Handle(B, H, d, "bf16", (1, 1, 1), 0, (d, 0, 0))
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, Sq), dtype=torch.float32, device="cuda")
+    ws = torch.empty(h.cross_workspace_bytes(Sq, n_chunks), dtype=torch.uint8, device="cuda")
+    for _ in range(warmup):
+        h.cross_forward(q, k, v, out, lse, n_chunks=n_chunks, workspace=ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        h.cross_forward(q, k, v, out, lse, n_chunks=n_chunks, workspace=ws)
+    e1.record()
+    torch.cuda.synchronize()
+    h.sync()
+    ms = e0.elapsed_time(e1) / steps
+    flops = 4.0 * B * H * Sq * Sk * d
+    return {"workload": f"{Sq} audio queries over {Sk} video keys (B={B}, H={H}, d={d}), {n_chunks} K/V chunks",
+            "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_call": round(ms, 4),
+            "launches_per_call": 2}
+
+
 def merge_bytes(w, n, P):
     rows = w.B * w.S * w.H
     return n * (rows * w.d * 4 + rows * 4) + rows * w.d * 2 + rows * 4
@@ -372,6 +404,8 @@ def run_ours(args, rank, world, dist_on):
                               "ms_per_step": round(t2, 3),
                               "attention_TFLOP/s": round(f2 / (r2["per_kernel_ms"][2] * 1e-3) / 1e12, 2),
                               "merge_GB/s": round(gbs(merge_bytes(w2, n2, 8), r2["per_kernel_ms"][3]), 1)}
+    if args.secondary:
+        line["cross_attention"] = measure_cross(w, max(5, args.steps // 2), args.warmup)
     if rank == 0 and world == 1 and not args.no_cpu:
         dt, fl, thr = cpu_sample(w, x, args.cpu_rows)
         line["cpu_baseline"] = {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": thr, "kind": "oracle",

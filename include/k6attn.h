@@ -192,6 +192,24 @@ k6attn_status k6attn_lse_merge(k6attn_t h, const float *part_o, const float *par
                                float *lse, void *stream);
 
 /*
+ * Cross-attention: Sq query rows of one stream over Sk keys/values of another
+ * ([K6] "Audio queries gather the full visual sequence"; [CP] "Forward Pass
+ * Flow": cross-attention uses the full encoder states).  No rotary, no joint
+ * tokens; the handle supplies B, H, d, the element type and the error word
+ * (its video grid and joint settings are not used).
+ *  q        [B][Sq][H][d];  k, v [B][Sk][H][d]  (handle dtype).
+ *  n_chunks K/V chunks of Sk/n_chunks keys each (Sk % n_chunks == 0),
+ *           combined by their log-sum-exp as in k6attn_forward.
+ *  out      [B][Sq][H][d];  lse fp32 [B][H][Sq] (may be NULL).
+ *  workspace  at least k6attn_cross_workspace_bytes(h, Sq, n_chunks) bytes
+ *           (0, and NULL allowed, when n_chunks == 1).
+ */
+size_t k6attn_cross_workspace_bytes(k6attn_t h, long Sq, int n_chunks);
+k6attn_status k6attn_cross_forward(k6attn_t h, const void *q, long Sq, const void *k, const void *v, long Sk,
+                                   int n_chunks, void *out, float *lse, void *workspace, size_t workspace_bytes,
+                                   void *stream);
+
+/*
  * Sequence-partitioned <-> head-partitioned relayout, the single-GPU form of
  * the Ulysses all-to-all ([USP] `_ft_c_input_all_to_all` /
  * `_ft_c_output_all_to_all`; [CP] "Comparison with Other CP Strategies").

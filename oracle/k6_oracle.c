@@ -37,6 +37,12 @@
  *     ("Audio queries gather the full visual sequence"); "Context Parallelism
  *     in vLLM Omni Neuron", "Forward Pass Flow" ("Cross-attention uses full
  *     encoder states").
+ *   - QK-norm before the rotary embedding: "Context Parallelism in vLLM Omni
+ *     Neuron", "Self-Attention with Context Parallelism" (`norm_q(q)`,
+ *     `norm_k(k)` on the projected rows before they are split into heads) and
+ *     "Distributed Normalization" (an RMS statistic over the hidden dim).  Read
+ *     as RMSNorm over each token's full hidden row of H*d values:
+ *     y = x / sqrt(mean(x^2) + eps) * w.
  *   - The sequence-partitioned <-> head-partitioned relayout that Ulysses does
  *     with all-to-all: xDiT PR #586 USP listing (`_ft_c_input_all_to_all`,
  *     `_ft_c_output_all_to_all`); "Context Parallelism in vLLM Omni Neuron",
@@ -155,6 +161,22 @@ int k6o_rope(const k6o_geom *g, const void *x, int type, double *y) {
         double *out = y + (size_t)r * d;
         for (int e = 0; e < d; e++) out[e] = load_elem(x, type, (size_t)r * d + e);
         k6o_rope_vec(g, n, out);
+    }
+    return 0;
+}
+
+/* RMSNorm of `rows` rows of n values each: y = x / sqrt(mean(x^2) + eps) * w. */
+int k6o_rms_norm(const void *x, int type, long rows, long n, const double *w, double eps, double *y) {
+    if (rows < 0 || n < 1 || eps < 0) return -1;
+#pragma omp parallel for schedule(static)
+    for (long r = 0; r < rows; r++) {
+        double ss = 0.0;
+        for (long e = 0; e < n; e++) {
+            double v = load_elem(x, type, (size_t)r * n + e);
+            ss += v * v;
+        }
+        double inv = 1.0 / sqrt(ss / (double)n + eps);
+        for (long e = 0; e < n; e++) y[(size_t)r * n + e] = load_elem(x, type, (size_t)r * n + e) * inv * w[e];
     }
     return 0;
 }

@@ -85,6 +85,7 @@ def lib():
                                        ctypes.c_long, ctypes.c_long, P, ctypes.c_long, P, P]
         _lib.k6o_cross_attention.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_long,
                                              ctypes.c_long, P, P, P, ctypes.c_int, ctypes.c_long, ctypes.c_long, P, P]
+        _lib.k6o_rms_norm.argtypes = [P, ctypes.c_int, ctypes.c_long, ctypes.c_long, P, ctypes.c_double, P]
         _lib.k6o_lse_merge.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_long, ctypes.c_int, ctypes.c_int,
                                        P, P, ctypes.c_int, P, P]
         _lib.k6o_relayout.argtypes = [P, P, ctypes.c_int, ctypes.c_long, ctypes.c_int, ctypes.c_int,
@@ -128,6 +129,19 @@ def rope(g: Geom, x: np.ndarray) -> np.ndarray:
     rc = lib().k6o_rope(ctypes.byref(g.c()), _ptr(x), t, _ptr(y))
     if rc:
         raise ValueError(f"k6o_rope: {rc}")
+    return y
+
+
+def rms_norm(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
+    """RMSNorm over the last dim of x (a token's H*d hidden row for QK-norm)."""
+    x_, t = _typed(x)
+    n = x_.shape[-1]
+    w_ = np.ascontiguousarray(w, np.float64)
+    assert w_.shape == (n,)
+    y = np.empty(x_.shape, np.float64)
+    rc = lib().k6o_rms_norm(_ptr(x_), t, x_.size // n, n, _ptr(w_), float(eps), _ptr(y))
+    if rc:
+        raise ValueError(f"k6o_rms_norm: {rc}")
     return y
 
 

@@ -269,6 +269,32 @@ def test_cross_attention_equals_self_attention_without_rotary():
     np.testing.assert_array_equal(a[1], b[1])
 
 
+# ----------------------------------------------------------------- QK-norm
+
+
+def test_rms_norm_unit_rms_scale_invariance_and_weights():
+    x = rnd((5, 3, 48), 40, 3.0)
+    flat = x.reshape(5, 3 * 48)
+    ones = np.ones(3 * 48)
+    y = O.rms_norm(flat, ones, 0.0)
+    np.testing.assert_allclose(np.sqrt((y ** 2).mean(axis=1)), 1.0, rtol=1e-14)   # unit RMS per row
+    np.testing.assert_allclose(O.rms_norm(7.5 * flat, ones, 0.0), y, rtol=1e-13)   # scale invariance
+    w = rnd(3 * 48, 41)
+    np.testing.assert_allclose(O.rms_norm(flat, w, 0.0), y * w, rtol=1e-14)        # weights scale per dim
+    # eps: a row of zeros stays zero; a constant row c gives c / sqrt(c^2 + eps)
+    z = O.rms_norm(np.zeros((1, 8)), np.ones(8), 1e-6)
+    assert not z.any()
+    c = O.rms_norm(np.full((1, 8), 2.0), np.ones(8), 0.25)
+    np.testing.assert_allclose(c, 2.0 / np.sqrt(4.25), rtol=1e-15)
+
+
+def test_rms_norm_accepts_bf16_rows_exactly():
+    raw = inputs.tensor(42, 50, (4, 256), "bf16")
+    w = rnd(256, 51)
+    np.testing.assert_array_equal(O.rms_norm(raw, w, 1e-6),
+                                  O.rms_norm(inputs.bf16_to_f32(raw).astype(np.float64), w, 1e-6))
+
+
 # ------------------------------------------------------------------- rotary
 
 

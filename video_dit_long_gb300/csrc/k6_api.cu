@@ -67,9 +67,9 @@ static WsLayout ws_layout(const Geom &g, int n, bool rope) {
     }
     if (n > 1) {
         L.part_o = off;
-        off += round256((size_t)n * g.B * g.S * row * 4);
+        off += round256((size_t)n * g.B * g.Sq * row * 4);
         L.part_lse = off;
-        off += round256((size_t)n * g.B * g.H * g.S * 4);
+        off += round256((size_t)n * g.B * g.H * g.Sq * 4);
     }
     L.total = off;
     return L;
@@ -77,9 +77,9 @@ static WsLayout ws_layout(const Geom &g, int n, bool rope) {
 
 // The attention kernels on rotated inputs: n_chunks == 1 writes out/lse,
 // n_chunks > 1 writes fp32 partials into out/lse (see k6attn_attention_chunks).
-static k6attn_status run_attention(k6attn_handle *h, const void *q, const void *k, const void *v, const void *jk,
-                                   const void *jv, bool qk_f16, int n_chunks, void *out, float *lse, cudaStream_t st) {
-    const Geom &g = h->g;
+static k6attn_status run_attention(k6attn_handle *h, const Geom &g, const void *q, const void *k, const void *v,
+                                   const void *jk, const void *jv, bool qk_f16, int n_chunks, void *out, float *lse,
+                                   cudaStream_t st) {
     if (g.elem == 2) {
         AttnTcOptions opt{h->wait_limit_ns, h->err, h->strict_order, qk_f16 ? 1 : 0};
         const char *why = nullptr;
@@ -90,7 +90,7 @@ static k6attn_status run_attention(k6attn_handle *h, const void *q, const void *
         }
         return K6ATTN_OK;
     }
-    const size_t o_stride = (size_t)g.B * g.S * g.H * g.d, l_stride = (size_t)g.B * g.H * g.S;
+    const size_t o_stride = (size_t)g.B * g.Sq * g.H * g.d, l_stride = (size_t)g.B * g.H * g.Sq;
     return cuda_check(launch_attn_f32(g, static_cast<const float *>(q), static_cast<const float *>(k),
                                       static_cast<const float *>(v), static_cast<const float *>(jk),
                                       static_cast<const float *>(jv), n_chunks, static_cast<float *>(out), o_stride,
@@ -114,7 +114,7 @@ static k6attn_status check_inputs(const char *fn, const Geom &g, const void *q, 
         if (!aligned16(p)) return set_error(K6ATTN_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", fn);
     if (reinterpret_cast<uintptr_t>(lse) & 3) return set_error(K6ATTN_ERR_INVALID_ARG, "%s: lse misaligned", fn);
     const size_t row = (size_t)g.H * g.d * g.elem;
-    const size_t qb = g.B * g.S * row, kvb = g.B * g.Nv * row, jb = g.B * g.Nj * row;
+    const size_t qb = g.B * g.Sq * row, kvb = g.B * g.Nv * row, jb = g.B * g.Nj * row;
     const void *ins[] = {q, k, v, jk, jv};
     const size_t insz[] = {qb, kvb, kvb, jb, jb};
     for (int i = 0; i < 5; i++)
@@ -178,7 +178,7 @@ k6attn_status k6attn_create(const k6attn_desc *desc, k6attn_t *out) {
     h->desc = d;
     Geom &g = h->g;
     g.B = d.B, g.H = d.H, g.d = d.d;
-    g.Nv = Nv, g.Nj = d.n_joint, g.S = S;
+    g.Nv = Nv, g.Nj = d.n_joint, g.S = S, g.Sq = S;
     g.grid_t = d.grid_t, g.grid_h = d.grid_h, g.grid_w = d.grid_w;
     for (int a = 0; a < 3; a++) g.axis_dim[a] = d.axis_dim[a];
     g.joint_rope = d.joint_rope;
@@ -319,10 +319,10 @@ k6attn_status k6attn_forward(k6attn_t h, const void *q, const void *k, const voi
         qa = qr, ka = kr, jka = jkr;
     }
     const bool qk_f16 = rope && g.dtype == K6ATTN_BF16;
-    if (n_chunks == 1) return run_attention(h, qa, ka, v, jka, joint_v, qk_f16, 1, out, lse, st);
+    if (n_chunks == 1) return run_attention(h, g, qa, ka, v, jka, joint_v, qk_f16, 1, out, lse, st);
     float *part_o = reinterpret_cast<float *>(ws + L.part_o);
     float *part_lse = reinterpret_cast<float *>(ws + L.part_lse);
-    s = run_attention(h, qa, ka, v, jka, joint_v, qk_f16, n_chunks, part_o, part_lse, st);
+    s = run_attention(h, g, qa, ka, v, jka, joint_v, qk_f16, n_chunks, part_o, part_lse, st);
     if (s != K6ATTN_OK) return s;
     return cuda_check(launch_lse_merge(g, n_chunks, part_o, part_lse, out, lse, st), "forward: merge launch");
 }
@@ -343,8 +343,55 @@ k6attn_status k6attn_attention_chunks(k6attn_t h, const void *q, const void *k, 
                          (int)qk_dtype);
     k6attn_status s = check_inputs("attention_chunks", g, q, k, v, joint_k, joint_v, n_chunks, out, ob, lse, lb);
     if (s != K6ATTN_OK) return s;
-    return run_attention(h, q, k, v, joint_k, joint_v, qk_dtype == K6ATTN_F16, n_chunks, out, lse,
+    return run_attention(h, g, q, k, v, joint_k, joint_v, qk_dtype == K6ATTN_F16, n_chunks, out, lse,
                          static_cast<cudaStream_t>(stream));
+}
+
+// The handle's batch, heads, head dim and type with Sq query rows over Sk keys.
+static Geom cross_geom(const Geom &base, long Sq, long Sk) {
+    Geom g = base;
+    g.Nv = Sk, g.Nj = 0, g.S = Sk, g.Sq = Sq;
+    g.grid_t = 1, g.grid_h = 1, g.grid_w = (int)(Sk < (1L << 30) ? Sk : 1);
+    g.joint_rope = 0;
+    return g;
+}
+
+size_t k6attn_cross_workspace_bytes(k6attn_t h, long Sq, int n_chunks) {
+    if (!h || n_chunks < 1 || Sq < 1) return 0;
+    return ws_layout(cross_geom(h->g, Sq, 1), n_chunks, false).total;
+}
+
+k6attn_status k6attn_cross_forward(k6attn_t h, const void *q, long Sq, const void *k, const void *v, long Sk,
+                                   int n_chunks, void *out, float *lse, void *workspace, size_t workspace_bytes,
+                                   void *stream) {
+    g_msg[0] = 0;
+    if (!h) return set_error(K6ATTN_ERR_INVALID_ARG, "cross_forward: null handle");
+    if (Sq < 1 || Sk < 1) return set_error(K6ATTN_ERR_INVALID_ARG, "cross_forward: Sq and Sk must be >= 1");
+    if (Sq >= (1L << 30) || Sk >= (1L << 30) || (long)h->g.B * Sq * h->g.H >= (1L << 31) ||
+        (long)h->g.B * Sk * h->g.H >= (1L << 31))
+        return set_error(K6ATTN_ERR_UNSUPPORTED, "cross_forward: problem too large");
+    const Geom g = cross_geom(h->g, Sq, Sk);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t qb = (size_t)g.B * Sq * g.H * g.d * g.elem, lb = (size_t)g.B * g.H * Sq * 4;
+    k6attn_status s = check_inputs("cross_forward", g, q, k, v, nullptr, nullptr, n_chunks, out, qb, lse, lb);
+    if (s != K6ATTN_OK) return s;
+    if (!aligned16(workspace)) return set_error(K6ATTN_ERR_INVALID_ARG, "cross_forward: workspace misaligned");
+    if (n_chunks == 1) return run_attention(h, g, q, k, v, nullptr, nullptr, false, 1, out, lse, st);
+    const WsLayout L = ws_layout(g, n_chunks, false);
+    if (!workspace || workspace_bytes < L.total)
+        return set_error(K6ATTN_ERR_WORKSPACE, "cross_forward: workspace of %zu bytes needed, %zu given", L.total,
+                         workspace ? workspace_bytes : (size_t)0);
+    const size_t kvb = (size_t)g.B * Sk * g.H * g.d * g.elem;
+    if (overlap(workspace, L.total, q, qb) || overlap(workspace, L.total, k, kvb) ||
+        overlap(workspace, L.total, v, kvb) || overlap(workspace, L.total, out, qb) ||
+        overlap(workspace, L.total, lse, lb))
+        return set_error(K6ATTN_ERR_INVALID_ARG, "cross_forward: workspace overlaps a tensor");
+    char *ws = static_cast<char *>(workspace);
+    float *part_o = reinterpret_cast<float *>(ws + L.part_o);
+    float *part_lse = reinterpret_cast<float *>(ws + L.part_lse);
+    s = run_attention(h, g, q, k, v, nullptr, nullptr, false, n_chunks, part_o, part_lse, st);
+    if (s != K6ATTN_OK) return s;
+    return cuda_check(launch_lse_merge(g, n_chunks, part_o, part_lse, out, lse, st), "cross_forward: merge launch");
 }
 
 k6attn_status k6attn_seq2head_relayout(const void *src, void *dst, int B, long S, int H, int d, int elem_bytes,

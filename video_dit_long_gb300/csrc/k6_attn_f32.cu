@@ -21,7 +21,7 @@ constexpr int F32_KEYS = 32;
 template <int D>
 __global__ void __launch_bounds__(F32_ROWS *(D / 64)) attn_f32_kernel(
     const float *__restrict__ q, const float *__restrict__ k, const float *__restrict__ v,
-    const float *__restrict__ jk, const float *__restrict__ jv, long S, long Nv, int H, int n_chunks,
+    const float *__restrict__ jk, const float *__restrict__ jv, long Sq, long S, long Nv, int H, int n_chunks,
     float *__restrict__ out, size_t o_stride, float *__restrict__ lse, size_t l_stride, float scale) {
     constexpr int TPR = D / 64;  // threads per query row
     __shared__ float ks[F32_KEYS][D];
@@ -36,8 +36,8 @@ __global__ void __launch_bounds__(F32_ROWS *(D / 64)) attn_f32_kernel(
     const long Nj = S - Nv;
 
     float qr[64], o[64];
-    const bool live = row < S;
-    const float *qp = q + (((long)b * S + (live ? row : 0)) * H + h) * D + part * 64;
+    const bool live = row < Sq;
+    const float *qp = q + (((long)b * Sq + (live ? row : 0)) * H + h) * D + part * 64;
 #pragma unroll
     for (int e = 0; e < 64; e++) {
         qr[e] = live ? qp[e] : 0.f;
@@ -95,23 +95,23 @@ __global__ void __launch_bounds__(F32_ROWS *(D / 64)) attn_f32_kernel(
     }
     if (!live) return;
     const float inv = 1.f / l;
-    float *op = out + c * o_stride + (((long)b * S + row) * H + h) * D + part * 64;
+    float *op = out + c * o_stride + (((long)b * Sq + row) * H + h) * D + part * 64;
 #pragma unroll
     for (int e = 0; e < 64; e += 4)
         *reinterpret_cast<float4 *>(op + e) = make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv);
-    if (lse && part == 0) lse[c * l_stride + ((long)b * H + h) * S + row] = m + logf(l);
+    if (lse && part == 0) lse[c * l_stride + ((long)b * H + h) * Sq + row] = m + logf(l);
 }
 
 cudaError_t launch_attn_f32(const Geom &g, const float *q, const float *k, const float *v, const float *jk,
                             const float *jv, int n_chunks, float *out, size_t o_stride, float *lse, size_t l_stride,
                             cudaStream_t st) {
-    dim3 grid((unsigned)((g.S + F32_ROWS - 1) / F32_ROWS), (unsigned)g.H, (unsigned)(g.B * n_chunks));
+    dim3 grid((unsigned)((g.Sq + F32_ROWS - 1) / F32_ROWS), (unsigned)g.H, (unsigned)(g.B * n_chunks));
     const float scale = 1.0f / sqrtf((float)g.d);
     if (g.d == 64)
-        attn_f32_kernel<64><<<grid, F32_ROWS, 0, st>>>(q, k, v, jk, jv, g.S, g.Nv, g.H, n_chunks, out, o_stride, lse,
+        attn_f32_kernel<64><<<grid, F32_ROWS, 0, st>>>(q, k, v, jk, jv, g.Sq, g.S, g.Nv, g.H, n_chunks, out, o_stride, lse,
                                                        l_stride, scale);
     else
-        attn_f32_kernel<128><<<grid, F32_ROWS * 2, 0, st>>>(q, k, v, jk, jv, g.S, g.Nv, g.H, n_chunks, out, o_stride,
+        attn_f32_kernel<128><<<grid, F32_ROWS * 2, 0, st>>>(q, k, v, jk, jv, g.Sq, g.S, g.Nv, g.H, n_chunks, out, o_stride,
                                                             lse, l_stride, scale);
     return cudaGetLastError();
 }

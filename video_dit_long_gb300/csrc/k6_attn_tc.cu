@@ -55,7 +55,7 @@ constexpr int TILE = 2 * PANEL;               // 32 KB
 constexpr int SMEM_Q = 0;
 constexpr int SMEM_KV = NQ * TILE;
 constexpr int SMEM_BAR = SMEM_KV + NSTAGE * TILE;
-constexpr int NBAR = 1 + 2 * NSTAGE + 3 * NQ + NQ + 1;  // q_full, kv_full/empty, s/p/o_final, o_step, drain
+constexpr int NBAR = 2 + 2 * NSTAGE + 4 * NQ + NQ + 1;  // q_full/empty, kv_full/empty, s/p_half/p/o_final, o_step, drain
 constexpr int SMEM_TOTAL = SMEM_BAR + NBAR * 8 + 16;
 constexpr int SMEM_ALLOC = SMEM_TOTAL + 1024;  // room to align the base to 1024 bytes
 constexpr int THREADS = 384;                  // 3 warpgroups: softmax 0, softmax 1, producer/MMA/spare
@@ -69,7 +69,8 @@ constexpr unsigned long long DRAIN_NS = 1000000000ull;
 }  // namespace tc
 
 struct TcParams {
-    long S, Nv, Nj;
+    long S, Nv, Nj;                           // keys (video then joint)
+    long Sq;                                  // query rows
     int H, n_chunks, q_pairs;
     float scale_log2;                         // log2(e) / sqrt(d)
     void *out;                                // bf16 [B][S][H][d] or fp32 partials
@@ -80,6 +81,7 @@ struct TcParams {
     int *err;
     int strict_order;
     uint32_t idesc_qk;                        // instruction descriptor of Q.K^T (bf16 or fp16 operands)
+    long units;                               // B * H * n_chunks * q_pairs work units
 };
 
 // K/V tile j of a chunk: which tensor map (0 video, 1 joint), first row, valid keys.
@@ -115,6 +117,28 @@ __device__ __forceinline__ TileRange chunk_tiles(const TcParams &p, int c) {
     return t;
 }
 
+// Work unit u -> (b, h, chunk, query-tile pair), pairs fastest, so that the
+// CTAs working at the same time share one chunk's K/V in L2.
+struct Unit {
+    int b, h, c, q0;
+};
+__device__ __forceinline__ Unit decode_unit(const TcParams &p, long u) {
+    Unit r;
+    const int qp = (int)(u % p.q_pairs);
+    u /= p.q_pairs;
+    r.c = (int)(u % p.n_chunks);
+    u /= p.n_chunks;
+    r.h = (int)(u % p.H);
+    r.b = (int)(u / p.H);
+    r.q0 = qp * (tc::NQ * tc::BM);
+    return r;
+}
+
+// Persistent: each CTA takes units blockIdx.x, blockIdx.x + gridDim.x, ...
+// The K/V ring, the barrier phases and tensor memory carry over from one unit
+// to the next; the next unit's Q is loaded as soon as the last Q.K^T of the
+// current one has read Q (q_empty), so it overlaps the last P.V products and
+// the epilogue.
 __global__ void __launch_bounds__(tc::THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_jk,
@@ -124,10 +148,12 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SMEM_BAR);
     uint64_t *q_full = bars;
-    uint64_t *kv_full = bars + 1;
+    uint64_t *q_empty = q_full + 1;
+    uint64_t *kv_full = q_empty + 1;
     uint64_t *kv_empty = kv_full + NSTAGE;
     uint64_t *s_full = kv_empty + NSTAGE;
-    uint64_t *p_full = s_full + NQ;
+    uint64_t *p_half = s_full + NQ;
+    uint64_t *p_full = p_half + NQ;
     uint64_t *o_final = p_full + NQ;
     uint64_t *o_step = o_final + NQ;
     uint64_t *drain = o_step + NQ;
@@ -136,27 +162,16 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-    // work unit: (b, h, chunk, query-tile pair), pairs fastest so that CTAs
-    // running together share one chunk's K/V in L2
-    long unit = blockIdx.x;
-    const int qp = (int)(unit % p.q_pairs);
-    unit /= p.q_pairs;
-    const int c = (int)(unit % p.n_chunks);
-    unit /= p.n_chunks;
-    const int h = (int)(unit % p.H);
-    const int b = (int)(unit / p.H);
-    const int q0 = qp * (NQ * BM);
-    const TileRange tr = chunk_tiles(p, c);
-    const int T = tr.T;
-
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
         for (int s = 0; s < NSTAGE; s++) {
             mbar_init(&kv_full[s], 1);
             mbar_init(&kv_empty[s], 1);
         }
         for (int i = 0; i < NQ; i++) {
             mbar_init(&s_full[i], 1);
+            mbar_init(&p_half[i], BM);
             mbar_init(&p_full[i], BM);
             mbar_init(&o_final[i], 1);
             mbar_init(&o_step[i], 1);
@@ -177,50 +192,56 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
 
     if (warp >= 8) {
         regs_decrease<REGS_CONTROL>();
-        if (warp == 8) {
-        // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
+        if (warp == 8 && lane == 0) {
+            // -------------------------------------------------- TMA producer
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
             prefetch_tmap(&tm_jk);
             prefetch_tmap(&tm_jv);
-            mbar_arrive_expect_tx(q_full, NQ * TILE);
-            for (int i = 0; i < NQ; i++)
-                for (int half = 0; half < 2; half++)
-                    tma_load_4d(smem + SMEM_Q + i * TILE + half * PANEL, &tm_q, q_full, half * 64, h, q0 + i * BM, b);
-            int issued = 0;
+            uint32_t kv_idx = 0;  // K/V tile loads issued so far (K_j, V_j alternate)
+            uint32_t uc = 0;      // units started by this CTA
             bool ok = true;
-            for (int j = 0; j < T && ok; j++) {
-                int map, row, valid;
-                tr.at(j, map, row, valid);
-                for (int kv = 0; kv < 2; kv++) {
-                    const int idx = 2 * j + kv, slot = idx % NSTAGE;
-                    if (!mbar_wait(&kv_empty[slot], ((idx / NSTAGE) & 1) ^ 1, w)) {
-                        ok = false;
-                        break;
+            for (long u = blockIdx.x; u < p.units && ok; u += gridDim.x, uc++) {
+                const Unit un = decode_unit(p, u);
+                const TileRange tr = chunk_tiles(p, un.c);
+                // Q of this unit once the previous unit's last Q.K^T has read Q
+                if (!mbar_wait(q_empty, (uc & 1) ^ 1, w)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(q_full, NQ * TILE);
+                for (int i = 0; i < NQ; i++)
+                    for (int half = 0; half < 2; half++)
+                        tma_load_4d(smem + SMEM_Q + i * TILE + half * PANEL, &tm_q, q_full, half * 64, un.h,
+                                    un.q0 + i * BM, un.b);
+                for (int j = 0; j < tr.T && ok; j++) {
+                    int map, row, valid;
+                    tr.at(j, map, row, valid);
+                    for (int kv = 0; kv < 2; kv++, kv_idx++) {
+                        const uint32_t slot = kv_idx % NSTAGE;
+                        if (!mbar_wait(&kv_empty[slot], ((kv_idx / NSTAGE) & 1) ^ 1, w)) {
+                            ok = false;
+                            break;
+                        }
+                        const CUtensorMap *tm = kv == 0 ? (map == 0 ? &tm_k : &tm_jk) : (map == 0 ? &tm_v : &tm_jv);
+                        mbar_arrive_expect_tx(&kv_full[slot], TILE);
+                        uint8_t *dst = smem + SMEM_KV + slot * TILE;
+                        tma_load_4d(dst, tm, &kv_full[slot], 0, un.h, row, un.b);
+                        tma_load_4d(dst + PANEL, tm, &kv_full[slot], 64, un.h, row, un.b);
                     }
-                    const CUtensorMap *tm = kv == 0 ? (map == 0 ? &tm_k : &tm_jk) : (map == 0 ? &tm_v : &tm_jv);
-                    mbar_arrive_expect_tx(&kv_full[slot], TILE);
-                    uint8_t *dst = smem + SMEM_KV + slot * TILE;
-                    tma_load_4d(dst, tm, &kv_full[slot], 0, h, row, b);
-                    tma_load_4d(dst + PANEL, tm, &kv_full[slot], 64, h, row, b);
-                    issued++;
                 }
             }
             // let every copy issued into shared memory land before the CTA can exit
-            mbar_drain(q_full, 0, DRAIN_NS);
-            for (int idx = issued > NSTAGE ? issued - NSTAGE : 0; idx < issued; idx++)
+            if (uc > 0) mbar_drain(q_full, (uc - 1) & 1, DRAIN_NS);
+            for (uint32_t idx = kv_idx > NSTAGE ? kv_idx - NSTAGE : 0; idx < kv_idx; idx++)
                 mbar_drain(&kv_full[idx % NSTAGE], (idx / NSTAGE) & 1, DRAIN_NS);
-        }
-        __syncwarp();
-        } else if (warp == 9) {
-        // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        } else if (warp == 9 && lane == 0) {
+            // --------------------------------------------------- MMA issuer
             const uint32_t idesc_qk = p.idesc_qk;
             const uint32_t idesc_pv = idesc_bf16_f32(BM, D, true);
             const uint32_t sQ = smem_u32(smem + SMEM_Q), sKV = smem_u32(smem + SMEM_KV);
-            auto issue_s = [&](int i, int slot) {
+            auto issue_s = [&](int i, uint32_t slot) {
                 const uint32_t qa = sQ + i * TILE, kb = sKV + slot * TILE;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; kk++) {
@@ -229,62 +250,84 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                            idesc_qk, kk > 0);
                 }
             };
-            auto issue_pv = [&](int i, int slot, bool acc) {
+            // keys [16*k0, 16*k1) of P_i . V
+            auto issue_pv = [&](int i, uint32_t slot, bool acc, int k0, int k1) {
                 const uint32_t vb = sKV + slot * TILE;
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; kk++) {
+                for (int kk = k0; kk < k1; kk++) {
                     mma_ts(tmem + 2 * BN + i * D, tmem + i * BN + kk * 8,
                            smem_desc_sw128(vb + kk * 16 * 128, PANEL, 1024), idesc_pv, (acc || kk > 0) ? 1u : 0u);
                 }
             };
-            uint32_t step_phase0 = 0, step_phase1 = 0;
-            bool ok = mbar_wait(q_full, 0, w) && mbar_wait(&kv_full[0], 0, w);
-            if (ok) {
-                tc_fence_after();
-                issue_s(0, 0);
-                tc_commit(&s_full[0]);
-                issue_s(1, 0);
-                tc_commit(&s_full[1]);
-                tc_commit(&kv_empty[0]);
-            }
-            // P.V of Q tile i for K/V tile j, then (if another tile follows) S_i(j+1)
-            auto pv_then_s = [&](int i, int j, int vs, int ks, int kidx, uint32_t &step_phase) -> bool {
-                if (!mbar_wait(&p_full[i], j & 1, w)) return false;
-                tc_fence_after();
-                issue_pv(i, vs, j > 0);
-                if (i == NQ - 1) tc_commit(&kv_empty[vs]);
-                if (j + 1 >= T) {
-                    tc_commit(&o_final[i]);
-                    return true;
-                }
-                if (p.strict_order) {
-                    // P_i lives in S_i's columns: let P.V finish reading it first
-                    tc_commit(&o_step[i]);
-                    const bool done = mbar_wait(&o_step[i], step_phase, w);
-                    step_phase ^= 1;
-                    if (!done) return false;
-                }
-                if (i == 0) {
-                    if (!mbar_wait(&kv_full[ks], (kidx / NSTAGE) & 1, w)) return false;
-                    tc_fence_after();
-                }
-                issue_s(i, ks);
-                tc_commit(&s_full[i]);
-                if (i == NQ - 1) tc_commit(&kv_empty[ks]);
-                return true;
+            uint32_t step_phase[2] = {0, 0};
+            // P_i lives in S_i's columns: in strict mode let the P.V that read it finish before S_i is rewritten
+            auto strict_wait = [&](int i) -> bool {
+                if (!p.strict_order) return true;
+                tc_commit(&o_step[i]);
+                const bool done = mbar_wait(&o_step[i], step_phase[i], w);
+                step_phase[i] ^= 1;
+                return done;
             };
-            for (int j = 0; j < T && ok; j++) {
-                const int vidx = 2 * j + 1, vs = vidx % NSTAGE;
-                const int kidx = 2 * j + 2, ks = kidx % NSTAGE;
-                ok = mbar_wait(&kv_full[vs], (vidx / NSTAGE) & 1, w) && pv_then_s(0, j, vs, ks, kidx, step_phase0) &&
-                     pv_then_s(1, j, vs, ks, kidx, step_phase1);
+            uint32_t kv_idx = 0;  // K/V tiles consumed (K_j, V_j alternate)
+            uint32_t tile = 0;    // K/V tiles finished over all units: phase of s_full / p_full
+            uint32_t uc = 0;
+            bool started = false;  // any P.V issued yet (the strict hazard exists from then on)
+            bool ok = true;
+            for (long u = blockIdx.x; u < p.units && ok; u += gridDim.x, uc++) {
+                const Unit un = decode_unit(p, u);
+                const int T = chunk_tiles(p, un.c).T;
+                ok = mbar_wait(q_full, uc & 1, w) && mbar_wait(&kv_full[kv_idx % NSTAGE], (kv_idx / NSTAGE) & 1, w);
+                if (!ok) break;
+                tc_fence_after();
+                for (int i = 0; i < NQ && ok; i++) {
+                    if (started && !(ok = strict_wait(i))) break;
+                    issue_s(i, kv_idx % NSTAGE);
+                    tc_commit(&s_full[i]);
+                }
+                if (!ok) break;
+                tc_commit(&kv_empty[kv_idx % NSTAGE]);
+                if (T == 1) tc_commit(q_empty);
+                for (int j = 0; j < T && ok; j++) {
+                    const uint32_t vidx = kv_idx + 2 * j + 1, kidx = vidx + 1;
+                    const uint32_t vs = vidx % NSTAGE, ks = kidx % NSTAGE;
+                    const bool more = j + 1 < T;
+                    ok = mbar_wait(&kv_full[vs], (vidx / NSTAGE) & 1, w);
+                    for (int i = 0; i < NQ && ok; i++) {
+                        // P.V of Q tile i for K/V tile j (the first 64 keys as soon as
+                        // their P is in tensor memory), then S_i(j+1)
+                        if (!(ok = mbar_wait(&p_half[i], (tile + j) & 1, w))) break;
+                        tc_fence_after();
+                        issue_pv(i, vs, j > 0, 0, BN / 32);
+                        if (!(ok = mbar_wait(&p_full[i], (tile + j) & 1, w))) break;
+                        tc_fence_after();
+                        issue_pv(i, vs, true, BN / 32, BN / 16);
+                        started = true;
+                        if (i == NQ - 1) tc_commit(&kv_empty[vs]);
+                        if (!more) {
+                            tc_commit(&o_final[i]);
+                            continue;
+                        }
+                        if (!(ok = strict_wait(i))) break;
+                        if (i == 0) {
+                            if (!(ok = mbar_wait(&kv_full[ks], (kidx / NSTAGE) & 1, w))) break;
+                            tc_fence_after();
+                        }
+                        issue_s(i, ks);
+                        tc_commit(&s_full[i]);
+                        if (i == NQ - 1) {
+                            tc_commit(&kv_empty[ks]);
+                            if (j + 2 == T) tc_commit(q_empty);  // the unit's last Q.K^T has been issued
+                        }
+                    }
+                }
+                kv_idx += 2 * T;
+                tile += T;
             }
             // every MMA issued so far must complete before tensor memory is freed
             tc_commit(drain);
             mbar_drain(drain, 0, DRAIN_NS);
         }
         __syncwarp();
-        }
     } else {
         regs_increase<REGS_SOFTMAX>();
         // ------------------------------------------------ softmax / epilogue
@@ -294,90 +337,107 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
         const uint32_t tS = lane_base + i * BN;
         const uint32_t tO = lane_base + 2 * BN + i * D;
         const float sl2 = p.scale_log2;
-        float m_run = -INFINITY, l_run = 0.f;
+        uint32_t tile = 0, uc = 0;
         bool ok = true;
-        for (int j = 0; j < T; j++) {
-            int map, row, valid;
-            tr.at(j, map, row, valid);
-            if (!mbar_wait(&s_full[i], j & 1, w)) {
+        for (long u = blockIdx.x; u < p.units && ok; u += gridDim.x, uc++) {
+            const Unit un = decode_unit(p, u);
+            const TileRange tr = chunk_tiles(p, un.c);
+            const int T = tr.T;
+            float m_run = -INFINITY, l_run = 0.f;
+            for (int j = 0; j < T; j++) {
+                int map, row, valid;
+                tr.at(j, map, row, valid);
+                if (!mbar_wait(&s_full[i], (tile + j) & 1, w)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t s[BN];
+#pragma unroll
+                for (int cc = 0; cc < BN / 32; cc++)
+                    tmem_ld32(tS + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[cc * 32]));
+                tmem_ld_wait();
+                if (valid < BN) {  // ragged tile end (warp-uniform): keys past the segment get -inf
+#pragma unroll
+                    for (int k = 0; k < BN; k++)
+                        if (k >= valid) s[k] = 0xff800000u;
+                }
+                // row max: four independent 3-input chains
+                float mc[4];
+#pragma unroll
+                for (int c4 = 0; c4 < 4; c4++) {
+                    const uint32_t *x = &s[c4 * 32];
+                    float m = fmax3(__uint_as_float(x[0]), __uint_as_float(x[1]), __uint_as_float(x[2]));
+#pragma unroll
+                    for (int k = 3; k < 31; k += 2) m = fmax3(m, __uint_as_float(x[k]), __uint_as_float(x[k + 1]));
+                    mc[c4] = fmaxf(m, __uint_as_float(x[31]));
+                }
+                const float mx = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]));
+                const float mt = mx * sl2;
+                bool need = false;
+                if (j == 0) m_run = mt;
+                else need = mt > m_run + RESCALE_THRESHOLD;
+                if (__any_sync(0xffffffffu, need)) {
+                    // O_i already holds P.V of tiles < j: S_i(j) was committed after it
+                    float alpha = 1.f;
+                    if (need) {
+                        alpha = ex2(m_run - mt);
+                        m_run = mt;
+                        l_run *= alpha;
+                    }
+#pragma unroll
+                    for (int cc = 0; cc < D / 32; cc++) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + cc * 32, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int k = 0; k < 32; k++) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                        tmem_st32(tO + cc * 32, o);
+                    }
+                }
+                // p = 2^(s * scale*log2e - m): packed FMA, then the SFU; row sum on
+                // packed adds.  The first 64 keys' P is published on its own so
+                // that the first half of P.V can start while the rest is computed.
+                const uint64_t scale2 = f2(sl2, sl2), negm2 = f2(-m_run, -m_run);
+                uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+                for (int half = 0; half < 2; half++) {
+                    uint32_t pk[BN / 4];
+#pragma unroll
+                    for (int k = 0; k < BN / 2; k += 2) {
+                        const int kk = half * (BN / 2) + k;
+                        float a, b2;
+                        f2_split(ffma2(f2(__uint_as_float(s[kk]), __uint_as_float(s[kk + 1])), scale2, negm2), a,
+                                 b2);
+                        const float p0 = ex2(a), p1 = ex2(b2);
+                        pk[k / 2] = pack_bf16x2(p0, p1);
+                        acc[(k / 2) & 3] = fadd2(acc[(k / 2) & 3], f2(p0, p1));
+                    }
+                    tmem_st32(tS + half * 32, pk);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(half == 0 ? &p_half[i] : &p_full[i]);
+                }
+                float sum;
+                {
+                    float a0, a1, b0, b1;
+                    f2_split(fadd2(acc[0], acc[1]), a0, a1);
+                    f2_split(fadd2(acc[2], acc[3]), b0, b1);
+                    sum = (a0 + a1) + (b0 + b1);
+                }
+                l_run += sum;
+            }
+            if (!ok || !mbar_wait(&o_final[i], uc & 1, w)) {
                 ok = false;
                 break;
             }
+            // epilogue: O_i / l to the output (or fp32 partial), LSE; the next
+            // unit's first P.V into O_i waits for this warpgroup's next P
             tc_fence_after();
-            uint32_t s[BN];
-#pragma unroll
-            for (int cc = 0; cc < BN / 32; cc++) tmem_ld32(tS + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[cc * 32]));
-            tmem_ld_wait();
-            if (valid < BN) {  // ragged tile end (warp-uniform): keys past the segment get -inf
-#pragma unroll
-                for (int k = 0; k < BN; k++)
-                    if (k >= valid) s[k] = 0xff800000u;
-            }
-            // row max: four independent 3-input chains
-            float mc[4];
-#pragma unroll
-            for (int c4 = 0; c4 < 4; c4++) {
-                const uint32_t *x = &s[c4 * 32];
-                float m = fmax3(__uint_as_float(x[0]), __uint_as_float(x[1]), __uint_as_float(x[2]));
-#pragma unroll
-                for (int k = 3; k < 31; k += 2) m = fmax3(m, __uint_as_float(x[k]), __uint_as_float(x[k + 1]));
-                mc[c4] = fmaxf(m, __uint_as_float(x[31]));
-            }
-            const float mx = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]));
-            const float mt = mx * sl2;
-            bool need = false;
-            if (j == 0) m_run = mt;
-            else need = mt > m_run + RESCALE_THRESHOLD;
-            if (__any_sync(0xffffffffu, need)) {
-                // O_i already holds P.V of tiles < j: S_i(j) was committed after it
-                float alpha = 1.f;
-                if (need) {
-                    alpha = ex2(m_run - mt);
-                    m_run = mt;
-                    l_run *= alpha;
-                }
-#pragma unroll
-                for (int cc = 0; cc < D / 32; cc++) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + cc * 32, o);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int k = 0; k < 32; k++) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-                    tmem_st32(tO + cc * 32, o);
-                }
-            }
-            // p = 2^(s * scale*log2e - m): packed FMA, then the SFU; row sum on packed adds
-            const uint64_t scale2 = f2(sl2, sl2), negm2 = f2(-m_run, -m_run);
-            uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-            uint32_t pk[BN / 2];
-#pragma unroll
-            for (int k = 0; k < BN; k += 2) {
-                float a, b;
-                f2_split(ffma2(f2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])), scale2, negm2), a, b);
-                const float p0 = ex2(a), p1 = ex2(b);
-                pk[k / 2] = pack_bf16x2(p0, p1);
-                acc[(k / 2) & 3] = fadd2(acc[(k / 2) & 3], f2(p0, p1));
-            }
-            float sum;
-            {
-                float a0, a1, b0, b1;
-                f2_split(fadd2(acc[0], acc[1]), a0, a1);
-                f2_split(fadd2(acc[2], acc[3]), b0, b1);
-                sum = (a0 + a1) + (b0 + b1);
-            }
-            l_run += sum;
-            tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-            tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(&p_full[i]);
-        }
-        if (ok && T > 0 && mbar_wait(&o_final[i], 0, w)) {
-            tc_fence_after();
-            const long grow = (long)q0 + i * BM + r;
-            const bool live = grow < p.S;
+            const long grow = (long)un.q0 + i * BM + r;
+            const bool live = grow < p.Sq;
             const float inv = 1.f / l_run;
-            const long obase = (((long)b * p.S + (live ? grow : 0)) * p.H + h) * D;
+            const long obase = (((long)un.b * p.Sq + (live ? grow : 0)) * p.H + un.h) * D;
 #pragma unroll
             for (int cc = 0; cc < D / 32; cc++) {
                 uint32_t o[32];
@@ -385,7 +445,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                 tmem_ld_wait();
                 if (live) {
                     if (p.out_f32) {
-                        float *dst = static_cast<float *>(p.out) + (long long)c * p.o_stride + obase + cc * 32;
+                        float *dst = static_cast<float *>(p.out) + (long long)un.c * p.o_stride + obase + cc * 32;
 #pragma unroll
                         for (int k = 0; k < 32; k += 4)
                             *reinterpret_cast<float4 *>(dst + k) =
@@ -395,19 +455,20 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                         __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.out) + obase + cc * 32;
 #pragma unroll
                         for (int k = 0; k < 32; k += 8) {
-                            uint4 u;
-                            u.x = pack_bf16x2(__uint_as_float(o[k]) * inv, __uint_as_float(o[k + 1]) * inv);
-                            u.y = pack_bf16x2(__uint_as_float(o[k + 2]) * inv, __uint_as_float(o[k + 3]) * inv);
-                            u.z = pack_bf16x2(__uint_as_float(o[k + 4]) * inv, __uint_as_float(o[k + 5]) * inv);
-                            u.w = pack_bf16x2(__uint_as_float(o[k + 6]) * inv, __uint_as_float(o[k + 7]) * inv);
-                            *reinterpret_cast<uint4 *>(dst + k) = u;
+                            uint4 v;
+                            v.x = pack_bf16x2(__uint_as_float(o[k]) * inv, __uint_as_float(o[k + 1]) * inv);
+                            v.y = pack_bf16x2(__uint_as_float(o[k + 2]) * inv, __uint_as_float(o[k + 3]) * inv);
+                            v.z = pack_bf16x2(__uint_as_float(o[k + 4]) * inv, __uint_as_float(o[k + 5]) * inv);
+                            v.w = pack_bf16x2(__uint_as_float(o[k + 6]) * inv, __uint_as_float(o[k + 7]) * inv);
+                            *reinterpret_cast<uint4 *>(dst + k) = v;
                         }
                     }
                 }
             }
             if (live && p.lse)
-                p.lse[(long long)c * p.l_stride + ((long)b * p.H + h) * p.S + grow] =
+                p.lse[(long long)un.c * p.l_stride + ((long)un.b * p.H + un.h) * p.Sq + grow] =
                     (m_run + log2f(l_run)) * 0.69314718055994531f;
+            tile += T;
         }
     }
 
@@ -464,7 +525,7 @@ cudaError_t launch_attn_tc(const Geom &g, const void *q, const void *k, const vo
     // an empty segment never issues loads; give its maps a valid stand-in
     const void *kk = has_video ? k : jk, *vv = has_video ? v : jv;
     const long kv_rows = has_video ? g.Nv : g.Nj;
-    if (!make_map(&mq, q, g.S, g.H, g.B, why) || !make_map(&mk, kk, kv_rows, g.H, g.B, why) ||
+    if (!make_map(&mq, q, g.Sq, g.H, g.B, why) || !make_map(&mk, kk, kv_rows, g.H, g.B, why) ||
         !make_map(&mv, vv, kv_rows, g.H, g.B, why) ||
         !make_map(&mjk, has_joint ? jk : kk, has_joint ? g.Nj : kv_rows, g.H, g.B, why) ||
         !make_map(&mjv, has_joint ? jv : vv, has_joint ? g.Nj : kv_rows, g.H, g.B, why))
@@ -477,26 +538,31 @@ cudaError_t launch_attn_tc(const Geom &g, const void *q, const void *k, const vo
     if (attr_err != cudaSuccess) return attr_err;
     TcParams p;
     p.S = g.S;
+    p.Sq = g.Sq;
     p.Nv = g.Nv;
     p.Nj = g.Nj;
     p.H = g.H;
     p.n_chunks = n_chunks;
-    p.q_pairs = (int)((g.S + tc::NQ * tc::BM - 1) / (tc::NQ * tc::BM));
+    p.q_pairs = (int)((g.Sq + tc::NQ * tc::BM - 1) / (tc::NQ * tc::BM));
     p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)g.d));
     p.out = out;
     p.lse = lse;
     p.out_f32 = n_chunks > 1;
-    p.o_stride = (long long)g.B * g.S * g.H * g.d;
-    p.l_stride = (long long)g.B * g.H * g.S;
+    p.o_stride = (long long)g.B * g.Sq * g.H * g.d;
+    p.l_stride = (long long)g.B * g.H * g.Sq;
     p.wait_limit_ns = opt.wait_limit_ns;
     p.err = opt.err;
     p.strict_order = opt.strict_order;
     // Q.K^T operands: bf16 (A/B format 1) or fp16 (format 0); P.V stays bf16
     p.idesc_qk = opt.qk_f16 ? (idesc_bf16_f32(tc::BM, tc::BN, false) & ~((7u << 7) | (7u << 10)))
                             : idesc_bf16_f32(tc::BM, tc::BN, false);
-    const long units = (long)g.B * g.H * n_chunks * p.q_pairs;
-    if (units == 0) return cudaSuccess;
-    attn_tc_kernel<<<(unsigned)units, tc::THREADS, tc::SMEM_ALLOC, st>>>(mq, mk, mv, mjk, mjv, p);
+    p.units = (long)g.B * g.H * n_chunks * p.q_pairs;
+    if (p.units == 0) return cudaSuccess;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long grid = p.units < sms ? p.units : sms;  // persistent: one CTA per SM
+    attn_tc_kernel<<<(unsigned)grid, tc::THREADS, tc::SMEM_ALLOC, st>>>(mq, mk, mv, mjk, mjv, p);
     return cudaGetLastError();
 }
 

@@ -16,7 +16,8 @@ enum : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_RANGE = 2 };
 // Geometry of one joint attention problem, as the kernels see it.
 struct Geom {
     int B, H, d;
-    long Nv, Nj, S;          // S = Nv + Nj (query rows = key rows)
+    long Nv, Nj, S;          // keys: S = Nv + Nj (video keys, then joint keys)
+    long Sq;                 // query rows: S for self-attention, any length for cross-attention
     int grid_t, grid_h, grid_w;
     int axis_dim[3];
     int joint_rope;

@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(int n, long rows, long S
 
 cudaError_t launch_lse_merge(const Geom &g, int n, const float *part_o, const float *part_lse, void *out, float *lse,
                              cudaStream_t st) {
-    const long rows = (long)g.B * g.S * g.H;
+    const long rows = (long)g.B * g.Sq * g.H;
     if (rows == 0) return cudaSuccess;
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
@@ -93,17 +93,17 @@ cudaError_t launch_lse_merge(const Geom &g, int n, const float *part_o, const fl
     if (g.d == 128) {
         if (g.elem == 2)
             lse_merge_kernel<__nv_bfloat16, 128><<<blocks, threads, 0, st>>>(
-                n, rows, g.S, g.H, part_o, part_lse, static_cast<__nv_bfloat16 *>(out), lse);
+                n, rows, g.Sq, g.H, part_o, part_lse, static_cast<__nv_bfloat16 *>(out), lse);
         else
             lse_merge_kernel<float, 128>
-                <<<blocks, threads, 0, st>>>(n, rows, g.S, g.H, part_o, part_lse, static_cast<float *>(out), lse);
+                <<<blocks, threads, 0, st>>>(n, rows, g.Sq, g.H, part_o, part_lse, static_cast<float *>(out), lse);
     } else {
         if (g.elem == 2)
             lse_merge_kernel<__nv_bfloat16, 64><<<blocks, threads, 0, st>>>(
-                n, rows, g.S, g.H, part_o, part_lse, static_cast<__nv_bfloat16 *>(out), lse);
+                n, rows, g.Sq, g.H, part_o, part_lse, static_cast<__nv_bfloat16 *>(out), lse);
         else
             lse_merge_kernel<float, 64>
-                <<<blocks, threads, 0, st>>>(n, rows, g.S, g.H, part_o, part_lse, static_cast<float *>(out), lse);
+                <<<blocks, threads, 0, st>>>(n, rows, g.Sq, g.H, part_o, part_lse, static_cast<float *>(out), lse);
     }
     return cudaGetLastError();
 }

@@ -21,7 +21,8 @@ OPT_WAIT_LIMIT_NS, OPT_STRICT_MMA_ORDER = 0, 1
 SYMBOLS = ["k6attn_create", "k6attn_destroy", "k6attn_rope_tables", "k6attn_rope_tables_bytes",
            "k6attn_workspace_bytes", "k6attn_rope_qk", "k6attn_forward", "k6attn_attention_chunks", "k6attn_lse_merge",
            "k6attn_seq2head_relayout", "k6attn_sync", "k6attn_set_option", "k6attn_status_string",
-           "k6attn_last_error"]
+           "k6attn_last_error", "k6attn_cross_workspace_bytes",
+           "k6attn_cross_forward"]
 
 
 class K6Error(RuntimeError):
@@ -67,6 +68,9 @@ def load(build_if_missing: bool = True):
     L.k6attn_workspace_bytes.restype = Z
     L.k6attn_rope_qk.argtypes = [P, P, P, P, P, P, P, P, I, P]
     L.k6attn_forward.argtypes = [P, P, P, P, P, P, P, I, P, P, P, Z, P]
+    L.k6attn_cross_workspace_bytes.argtypes = [P, ctypes.c_long, I]
+    L.k6attn_cross_workspace_bytes.restype = Z
+    L.k6attn_cross_forward.argtypes = [P, P, ctypes.c_long, P, P, ctypes.c_long, I, P, P, P, Z, P]
     L.k6attn_attention_chunks.argtypes = [P, P, P, P, P, P, I, I, P, P, P]
     L.k6attn_lse_merge.argtypes = [P, P, P, I, P, P, P]
     L.k6attn_seq2head_relayout.argtypes = [P, P, I, ctypes.c_long, I, I, I, I, I, P]
@@ -76,7 +80,8 @@ def load(build_if_missing: bool = True):
     L.k6attn_status_string.restype = ctypes.c_char_p
     L.k6attn_last_error.argtypes = []
     L.k6attn_last_error.restype = ctypes.c_char_p
-    for name in ("k6attn_create", "k6attn_rope_qk", "k6attn_forward", "k6attn_attention_chunks", "k6attn_lse_merge",
+    for name in ("k6attn_create", "k6attn_rope_qk", "k6attn_forward",
+                 "k6attn_attention_chunks", "k6attn_lse_merge", "k6attn_cross_forward",
                  "k6attn_seq2head_relayout", "k6attn_sync", "k6attn_set_option"):
         getattr(L, name).restype = I
     _lib = L
@@ -167,6 +172,16 @@ class Handle:
         qd = self._desc.dtype if qk_dtype is None else qk_dtype
         _check(load().k6attn_attention_chunks(self.h, _ptr(q), _ptr(k), _ptr(v), _ptr(joint_k), _ptr(joint_v),
                                               int(qd), int(n_chunks), _ptr(out), _ptr(lse), _stream(stream)))
+
+    def cross_workspace_bytes(self, Sq: int, n_chunks: int) -> int:
+        return load().k6attn_cross_workspace_bytes(self.h, int(Sq), int(n_chunks))
+
+    def cross_forward(self, q, k, v, out, lse=None, *, n_chunks=1, workspace=None, stream=None):
+        """Cross-attention of q [B][Sq][H][d] over k, v [B][Sk][H][d] (no rotary)."""
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        _check(load().k6attn_cross_forward(self.h, _ptr(q), int(q.shape[1]), _ptr(k), _ptr(v), int(k.shape[1]),
+                                           int(n_chunks), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
+                                           _stream(stream)))
 
     def lse_merge(self, part_o, part_lse, n_chunks, out, lse=None, stream=None):
         _check(load().k6attn_lse_merge(self.h, _ptr(part_o), _ptr(part_lse), int(n_chunks), _ptr(out), _ptr(lse),
