@@ -226,6 +226,39 @@ k6attn_status k6attn_cross_forward(k6attn_t h, const void *q, long Sq, const voi
 k6attn_status k6attn_seq2head_relayout(const void *src, void *dst, int B, long S, int H, int d, int elem_bytes,
                                        int P, int direction, void *stream);
 
+/*
+ * Forward pass with library-held scratch, for callers that cannot allocate
+ * device memory.  The pages have no counterpart to this entry point; it exists
+ * for users of the library, not for the method.
+ *
+ * Same arguments, computation and results as k6attn_forward without the
+ * workspace: the scratch (rotated q/k copies, per-chunk partials) lives in one
+ * statically sized device array inside the library, so the call never
+ * allocates device memory (no cudaMalloc, no cudaFree, no allocating library
+ * routine).  It is meant for code that may not or cannot allocate: a plugin
+ * whose host framework owns every device allocation, a deployment held to a
+ * memory budget fixed at start-up, a binding that only receives tensors.
+ *  - Limit: k6attn_workspace_bytes(h, n_chunks, rope_tables != NULL) must not
+ *    exceed K6ATTN_STATIC_SCRATCH_BYTES (32 MiB); a larger problem returns
+ *    K6ATTN_ERR_WORKSPACE with a message and launches nothing (use
+ *    k6attn_forward with a caller workspace then).
+ *  - Every GPU that loads the library reserves the array until the process
+ *    exits.
+ *  - The first call on a device, made with that device current, looks up the
+ *    array's device address once (cudaGetSymbolAddress); make that first call
+ *    before any stream capture begins.
+ *  - All calls on one device share the array, which keeps the last call's
+ *    contents: calls that can overlap on the GPU (several streams, or several
+ *    host threads without ordering between them) race on it.  Keep such calls
+ *    on one stream, or use k6attn_forward.
+ *  - Nothing in the array needs to start at zero: a call writes every scratch
+ *    byte before reading it.
+ */
+#define K6ATTN_STATIC_SCRATCH_BYTES (32u << 20)
+k6attn_status k6attn_forward_static_scratch(k6attn_t h, const void *q, const void *k, const void *v,
+                                            const void *joint_k, const void *joint_v, const void *rope_tables,
+                                            int n_chunks, void *out, float *lse, void *stream);
+
 /* Synchronise `stream`, then read and clear the handle's device error word:
  * K6ATTN_ERR_TIMEOUT if any kernel of this handle gave up on a wait,
  * K6ATTN_ERR_RANGE if a rotation into fp16 overflowed,

@@ -21,7 +21,7 @@ OPT_WAIT_LIMIT_NS, OPT_STRICT_MMA_ORDER = 0, 1
 SYMBOLS = ["k6attn_create", "k6attn_destroy", "k6attn_rope_tables", "k6attn_rope_tables_bytes",
            "k6attn_workspace_bytes", "k6attn_rope_qk", "k6attn_forward", "k6attn_attention_chunks", "k6attn_lse_merge",
            "k6attn_seq2head_relayout", "k6attn_sync", "k6attn_set_option", "k6attn_status_string",
-           "k6attn_last_error", "k6attn_cross_workspace_bytes",
+           "k6attn_last_error", "k6attn_forward_static_scratch", "k6attn_cross_workspace_bytes",
            "k6attn_cross_forward"]
 
 
@@ -68,6 +68,7 @@ def load(build_if_missing: bool = True):
     L.k6attn_workspace_bytes.restype = Z
     L.k6attn_rope_qk.argtypes = [P, P, P, P, P, P, P, P, I, P]
     L.k6attn_forward.argtypes = [P, P, P, P, P, P, P, I, P, P, P, Z, P]
+    L.k6attn_forward_static_scratch.argtypes = [P, P, P, P, P, P, P, I, P, P, P]
     L.k6attn_cross_workspace_bytes.argtypes = [P, ctypes.c_long, I]
     L.k6attn_cross_workspace_bytes.restype = Z
     L.k6attn_cross_forward.argtypes = [P, P, ctypes.c_long, P, P, ctypes.c_long, I, P, P, P, Z, P]
@@ -80,7 +81,7 @@ def load(build_if_missing: bool = True):
     L.k6attn_status_string.restype = ctypes.c_char_p
     L.k6attn_last_error.argtypes = []
     L.k6attn_last_error.restype = ctypes.c_char_p
-    for name in ("k6attn_create", "k6attn_rope_qk", "k6attn_forward",
+    for name in ("k6attn_create", "k6attn_rope_qk", "k6attn_forward", "k6attn_forward_static_scratch",
                  "k6attn_attention_chunks", "k6attn_lse_merge", "k6attn_cross_forward",
                  "k6attn_seq2head_relayout", "k6attn_sync", "k6attn_set_option"):
         getattr(L, name).restype = I
@@ -167,6 +168,15 @@ class Handle:
         _check(load().k6attn_forward(self.h, _ptr(q), _ptr(k), _ptr(v), _ptr(joint_k), _ptr(joint_v), tab,
                                      int(n_chunks), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
                                      _stream(stream)))
+
+    def forward_static_scratch(self, q, k, v, joint_k, joint_v, out, lse=None, *, rope=True, n_chunks=1,
+                               tables=None, stream=None):
+        """k6attn_forward with the library's static scratch array (no allocation, no workspace)."""
+        tab = None
+        if rope:
+            tab = ctypes.c_void_p(self.rope_tables() if tables is None else tables)
+        _check(load().k6attn_forward_static_scratch(self.h, _ptr(q), _ptr(k), _ptr(v), _ptr(joint_k), _ptr(joint_v),
+                                                    tab, int(n_chunks), _ptr(out), _ptr(lse), _stream(stream)))
 
     def attention_chunks(self, q, k, v, joint_k, joint_v, n_chunks, out, lse=None, qk_dtype=None, stream=None):
         qd = self._desc.dtype if qk_dtype is None else qk_dtype
