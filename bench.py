@@ -221,21 +221,30 @@ def gpu_index() -> str:
 
 
 def barrier(dist_on):
+    """Barrier across ranks (when distributed) and a device synchronize (when CUDA is up)."""
     import torch
     if dist_on:
         import torch.distributed as dist
         dist.barrier()
-    torch.cuda.synchronize()
+    if torch.cuda.is_available() and torch.cuda.is_initialized():
+        torch.cuda.synchronize()
 
 
 def max_over_ranks(x: float, dist_on) -> float:
+    """The slowest rank's time: all-reduce MAX over the process group (NCCL on GPUs, gloo on CPU)."""
     if not dist_on:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(work_per_rank: float, world: int, seconds_max: float) -> float:
+    """Units all ranks processed over the slowest rank's time (replicas: every rank does the same work)."""
+    return work_per_rank * world / seconds_max
 
 
 def measure(w, n_chunks, P, steps, warmup, dist_on, with_e2e=True, clocks=True):
@@ -346,7 +355,7 @@ def run_ours(args, rank, world, dist_on):
     res, x = measure(w, n, P, args.steps, args.warmup, dist_on)
     flops = w.flops()
     ms = res["total_ms"] / args.steps
-    value = flops * world / (res["total_ms"] / args.steps * 1e-3) / 1e12
+    value = whole_job_rate(flops, world, res["total_ms"] / args.steps * 1e-3) / 1e12
     k_ms = res["per_kernel_ms"]  # relayout_in, rope, attention, merge, relayout_out
     attn_tflops = flops / (k_ms[2] * 1e-3) / 1e12
     peak_s = pk["bf16_tflops_sustained"]

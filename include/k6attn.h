@@ -138,6 +138,25 @@ k6attn_status k6attn_rope_qk(k6attn_t h, const void *q, const void *k, const voi
                              void *q_out, void *k_out, void *joint_k_out, k6attn_dtype out_dtype, void *stream);
 
 /*
+ * QK-norm, then rotary embedding, in one launch ([CP] "Self-Attention with
+ * Context Parallelism": `norm_q(q)` / `norm_k(k)` on the projected rows, then
+ * `apply_rotary_emb_wan`; "Distributed Normalization": the RMS statistic is
+ * taken over the hidden dim).  Each token row of H*d values is RMS-normalised
+ * in fp32 as y = x / sqrt(mean(x^2) + eps) * w, then rotated exactly as
+ * k6attn_rope_qk does; arguments and outputs as there, plus:
+ *  q_weight, k_weight   fp32 [H*d] device arrays for video query / key rows.
+ *  joint_q_weight, joint_k_weight  fp32 [H*d] for the joint query rows (the
+ *           rear Nj rows of q) and for joint_k; NULL = use q_weight/k_weight.
+ *  eps      >= 0.
+ * The norm needs each token's full row, so call it on sequence-partitioned
+ * (full-head) tensors, before a seq->head relayout.
+ */
+k6attn_status k6attn_norm_rope_qk(k6attn_t h, const void *q, const void *k, const void *joint_k,
+                                  const float *q_weight, const float *k_weight, const float *joint_q_weight,
+                                  const float *joint_k_weight, float eps, const void *rope_tables, void *q_out,
+                                  void *k_out, void *joint_k_out, k6attn_dtype out_dtype, void *stream);
+
+/*
  * Joint-sequence attention forward ([USP] `_attention`; [CP] "Ring attention
  * (current implementation)": each K/V chunk is attended separately and the
  * partials combine through their log-sum-exp).

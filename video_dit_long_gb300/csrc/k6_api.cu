@@ -229,35 +229,58 @@ k6attn_status k6attn_set_option(k6attn_t h, k6attn_option opt, long long value) 
     return set_error(K6ATTN_ERR_INVALID_ARG, "set_option: unknown option %d", (int)opt);
 }
 
-k6attn_status k6attn_rope_qk(k6attn_t h, const void *q, const void *k, const void *joint_k, const void *rope_tables,
-                             void *q_out, void *k_out, void *joint_k_out, k6attn_dtype out_dtype, void *stream) {
-    g_msg[0] = 0;
-    if (!h) return set_error(K6ATTN_ERR_INVALID_ARG, "rope_qk: null handle");
+// Shared checks and launch of the two rotary entry points.
+static k6attn_status rope_common(const char *fn, k6attn_t h, const void *q, const void *k, const void *joint_k,
+                                 const void *rope_tables, void *q_out, void *k_out, void *joint_k_out,
+                                 k6attn_dtype out_dtype, const QkNorm *norm, void *stream) {
+    if (!h) return set_error(K6ATTN_ERR_INVALID_ARG, "%s: null handle", fn);
     const Geom &g = h->g;
     if (!q || !k || !q_out || !k_out || (g.Nj > 0 && (!joint_k || !joint_k_out)) || (!rope_tables && h->table_bytes))
-        return set_error(K6ATTN_ERR_INVALID_ARG, "rope_qk: null tensor or table pointer");
+        return set_error(K6ATTN_ERR_INVALID_ARG, "%s: null tensor or table pointer", fn);
     if (out_dtype != g.dtype && !(g.dtype == K6ATTN_BF16 && out_dtype == K6ATTN_F16))
-        return set_error(K6ATTN_ERR_INVALID_ARG, "rope_qk: output type %d not allowed for this handle", (int)out_dtype);
+        return set_error(K6ATTN_ERR_INVALID_ARG, "%s: output type %d not allowed for this handle", fn, (int)out_dtype);
     const void *ptrs[] = {q, k, joint_k, q_out, k_out, joint_k_out, rope_tables};
     for (const void *p : ptrs)
-        if (!aligned16(p)) return set_error(K6ATTN_ERR_INVALID_ARG, "rope_qk: pointers must be 16-byte aligned");
+        if (!aligned16(p)) return set_error(K6ATTN_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", fn);
     const size_t row = (size_t)g.H * g.d * g.elem;
     const size_t nb[3] = {g.B * g.S * row, g.B * g.Nv * row, g.B * g.Nj * row};
     const void *src[3] = {q, k, joint_k};
     const void *dst[3] = {q_out, k_out, joint_k_out};
     for (int a = 0; a < 3; a++) {
         if (dst[a] == src[a] && nb[a] && out_dtype != g.dtype)
-            return set_error(K6ATTN_ERR_INVALID_ARG, "rope_qk: in-place rotation keeps the handle's type");
+            return set_error(K6ATTN_ERR_INVALID_ARG, "%s: in-place rotation keeps the handle's type", fn);
         for (int b = 0; b < 3; b++) {
             if (a != b && (overlap(src[a], nb[a], src[b], nb[b]) || overlap(dst[a], nb[a], dst[b], nb[b])))
-                return set_error(K6ATTN_ERR_INVALID_ARG, "rope_qk: tensors overlap");
+                return set_error(K6ATTN_ERR_INVALID_ARG, "%s: tensors overlap", fn);
             if (dst[a] != src[a] && overlap(dst[a], nb[a], src[b], nb[b]))
-                return set_error(K6ATTN_ERR_INVALID_ARG, "rope_qk: an output overlaps an input");
+                return set_error(K6ATTN_ERR_INVALID_ARG, "%s: an output overlaps an input", fn);
         }
     }
     return cuda_check(launch_rope_qk(g, static_cast<const float2 *>(rope_tables), q, q_out, k, k_out, joint_k,
-                                     joint_k_out, out_dtype, h->err, static_cast<cudaStream_t>(stream)),
-                      "rope_qk launch");
+                                     joint_k_out, out_dtype, h->err, static_cast<cudaStream_t>(stream), norm),
+                      "rope launch");
+}
+
+k6attn_status k6attn_rope_qk(k6attn_t h, const void *q, const void *k, const void *joint_k, const void *rope_tables,
+                             void *q_out, void *k_out, void *joint_k_out, k6attn_dtype out_dtype, void *stream) {
+    g_msg[0] = 0;
+    return rope_common("rope_qk", h, q, k, joint_k, rope_tables, q_out, k_out, joint_k_out, out_dtype, nullptr,
+                       stream);
+}
+
+k6attn_status k6attn_norm_rope_qk(k6attn_t h, const void *q, const void *k, const void *joint_k,
+                                  const float *q_weight, const float *k_weight, const float *joint_q_weight,
+                                  const float *joint_k_weight, float eps, const void *rope_tables, void *q_out,
+                                  void *k_out, void *joint_k_out, k6attn_dtype out_dtype, void *stream) {
+    g_msg[0] = 0;
+    if (!q_weight || !k_weight) return set_error(K6ATTN_ERR_INVALID_ARG, "norm_rope_qk: null q or k weight");
+    if (!(eps >= 0.f)) return set_error(K6ATTN_ERR_INVALID_ARG, "norm_rope_qk: eps must be >= 0");
+    const uintptr_t al = reinterpret_cast<uintptr_t>(q_weight) | reinterpret_cast<uintptr_t>(k_weight) |
+                         reinterpret_cast<uintptr_t>(joint_q_weight) | reinterpret_cast<uintptr_t>(joint_k_weight);
+    if (al & 3) return set_error(K6ATTN_ERR_INVALID_ARG, "norm_rope_qk: weights must be 4-byte aligned");
+    QkNorm norm{q_weight, joint_q_weight, k_weight, joint_k_weight, eps};
+    return rope_common("norm_rope_qk", h, q, k, joint_k, rope_tables, q_out, k_out, joint_k_out, out_dtype, &norm,
+                       stream);
 }
 
 k6attn_status k6attn_lse_merge(k6attn_t h, const float *part_o, const float *part_lse, int n_chunks, void *out,

@@ -41,13 +41,21 @@ k6attn_status cuda_check(cudaError_t e, const char *what);
 
 cudaError_t launch_rope_tables(const Geom &g, double theta, float2 *tables, cudaStream_t st);
 
+// Optional QK-norm ahead of the rotation: fp32 weights [H*d] for video q rows,
+// joint q rows, video k rows and joint k rows (the joint ones default to the
+// video ones when null).
+struct QkNorm {
+    const float *q_w, *jq_w, *k_w, *jk_w;
+    float eps;
+};
+
 // Rotary embedding of q [B][S][H][d], k [B][Nv][H][d], jk [B][Nj][H][d]
 // from src_* (type g.dtype) into dst_* (type out_dtype; dst may equal src
 // when the types match).  Writing F16, a value that is not finite in fp16
 // sets *err to DEV_RANGE.
 cudaError_t launch_rope_qk(const Geom &g, const float2 *tables, const void *src_q, void *dst_q, const void *src_k,
                            void *dst_k, const void *src_jk, void *dst_jk, k6attn_dtype out_dtype, int *err,
-                           cudaStream_t st);
+                           cudaStream_t st, const QkNorm *norm = nullptr);
 
 cudaError_t launch_lse_merge(const Geom &g, int n, const float *part_o, const float *part_lse, void *out, float *lse,
                              cudaStream_t st);

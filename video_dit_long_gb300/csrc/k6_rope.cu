@@ -90,6 +90,10 @@ struct RopeArgs {
     int joint_rope;
     long off[4];         // table offsets (float2 entries)
     int half[3];         // pairs per axis row
+    // QK-norm weights, fp32 [H*d]: [tensor][0 = video rows, 1 = joint rows]
+    // (tensor 0 = q, 1 = k, 2 = joint_k); all null = no norm
+    const float *norm_w[3][2];
+    float eps;
 };
 
 // (cos, sin) of pair `i` for a token with video position (t, h, w), or joint
@@ -152,7 +156,10 @@ struct Vec<float> {
 // (and so its rotation angles) is uniform across the warp, and each lane
 // moves up to 4 16-byte vectors per pass with all loads issued before any
 // store, so that enough bytes are in flight for HBM.
-template <typename T, typename Tout>
+// With NORM, each token row of H*d values is first RMS-normalised
+// (x * rsqrt(mean(x^2) + eps) * w, fp32): one pass sums the squares (warp
+// reduction), the second pass re-reads the row (an L2 hit) and normalises.
+template <typename T, typename Tout, bool NORM>
 __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a, const float2 *__restrict__ tab) {
     constexpr int kPairs = Vec<T>::kPairs;
     constexpr int kUnroll = 4;
@@ -186,6 +193,21 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a, const float2 *__r
         const char *src = static_cast<const char *>(a.src[which]) + (long)local * a.H * a.d * sizeof(T);
         char *dst = static_cast<char *>(a.dst[which]) + (long)local * a.H * a.d * sizeof(T);
         bool bad = false;
+        float inv_rms = 1.f;
+        const float *wrow = nullptr;
+        if constexpr (NORM) {
+            wrow = a.norm_w[which][j >= 0 ? 1 : 0];
+            float ss = 0.f;
+            for (int v = lane; v < vecs_per_token; v += 32) {
+                float x[8];
+                Vec<T>::load(src + (long)v * 16, x);
+#pragma unroll
+                for (int k = 0; k < 2 * kPairs; k++) ss = fmaf(x[k], x[k], ss);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            inv_rms = rsqrtf(ss / (float)(a.H * a.d) + a.eps);
+        }
         for (int base = 0; base < vecs_per_token; base += 32 * kUnroll) {
             float x[kUnroll][8];
 #pragma unroll
@@ -198,6 +220,11 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a, const float2 *__r
                 const int v = base + u * 32 + lane;
                 if (v >= vecs_per_token) continue;
                 const int pair0 = (v % vecs_per_head) * kPairs;
+                if constexpr (NORM) {
+                    const float *wv = wrow + v * 2 * kPairs;
+#pragma unroll
+                    for (int k = 0; k < 2 * kPairs; k++) x[u][k] *= inv_rms * __ldg(wv + k);
+                }
 #pragma unroll
                 for (int k = 0; k < kPairs; k++) {
                     const float2 cs = rope_cs(a, tab, pair0 + k, t, h, w, j);
@@ -218,9 +245,18 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a, const float2 *__r
 
 cudaError_t launch_rope_qk(const Geom &g, const float2 *tables, const void *src_q, void *dst_q, const void *src_k,
                            void *dst_k, const void *src_jk, void *dst_jk, k6attn_dtype out_dtype, int *err,
-                           cudaStream_t st) {
+                           cudaStream_t st, const QkNorm *norm) {
     RopeArgs a;
     a.err = err;
+    const bool use_norm = norm != nullptr;
+    a.eps = use_norm ? norm->eps : 0.f;
+    for (int t = 0; t < 3; t++) a.norm_w[t][0] = a.norm_w[t][1] = nullptr;
+    if (use_norm) {
+        a.norm_w[0][0] = norm->q_w;
+        a.norm_w[0][1] = norm->jq_w ? norm->jq_w : norm->q_w;
+        a.norm_w[1][0] = a.norm_w[1][1] = norm->k_w;
+        a.norm_w[2][0] = a.norm_w[2][1] = norm->jk_w ? norm->jk_w : norm->k_w;
+    }
     a.src[0] = src_q, a.dst[0] = dst_q;
     a.src[1] = src_k, a.dst[1] = dst_k;
     a.src[2] = src_jk, a.dst[2] = dst_jk;
@@ -244,12 +280,16 @@ cudaError_t launch_rope_qk(const Geom &g, const float2 *tables, const void *src_
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     long blocks = (total + 7) / 8;  // 8 warps per block, one token per warp-iteration
     if (blocks > (long)sms * 8) blocks = (long)sms * 8;
-    if (g.dtype == K6ATTN_BF16 && out_dtype == K6ATTN_F16)
-        rope_kernel<__nv_bfloat16, __half><<<(unsigned)blocks, 256, 0, st>>>(a, tables);
-    else if (g.dtype == K6ATTN_BF16)
-        rope_kernel<__nv_bfloat16, __nv_bfloat16><<<(unsigned)blocks, 256, 0, st>>>(a, tables);
-    else
-        rope_kernel<float, float><<<(unsigned)blocks, 256, 0, st>>>(a, tables);
+    if (g.dtype == K6ATTN_BF16 && out_dtype == K6ATTN_F16) {
+        if (use_norm) rope_kernel<__nv_bfloat16, __half, true><<<(unsigned)blocks, 256, 0, st>>>(a, tables);
+        else rope_kernel<__nv_bfloat16, __half, false><<<(unsigned)blocks, 256, 0, st>>>(a, tables);
+    } else if (g.dtype == K6ATTN_BF16) {
+        if (use_norm) rope_kernel<__nv_bfloat16, __nv_bfloat16, true><<<(unsigned)blocks, 256, 0, st>>>(a, tables);
+        else rope_kernel<__nv_bfloat16, __nv_bfloat16, false><<<(unsigned)blocks, 256, 0, st>>>(a, tables);
+    } else {
+        if (use_norm) rope_kernel<float, float, true><<<(unsigned)blocks, 256, 0, st>>>(a, tables);
+        else rope_kernel<float, float, false><<<(unsigned)blocks, 256, 0, st>>>(a, tables);
+    }
     return cudaGetLastError();
 }
 

@@ -22,7 +22,7 @@ SYMBOLS = ["k6attn_create", "k6attn_destroy", "k6attn_rope_tables", "k6attn_rope
            "k6attn_workspace_bytes", "k6attn_rope_qk", "k6attn_forward", "k6attn_attention_chunks", "k6attn_lse_merge",
            "k6attn_seq2head_relayout", "k6attn_sync", "k6attn_set_option", "k6attn_status_string",
            "k6attn_last_error", "k6attn_forward_static_scratch", "k6attn_cross_workspace_bytes",
-           "k6attn_cross_forward"]
+           "k6attn_cross_forward", "k6attn_norm_rope_qk"]
 
 
 class K6Error(RuntimeError):
@@ -69,6 +69,7 @@ def load(build_if_missing: bool = True):
     L.k6attn_rope_qk.argtypes = [P, P, P, P, P, P, P, P, I, P]
     L.k6attn_forward.argtypes = [P, P, P, P, P, P, P, I, P, P, P, Z, P]
     L.k6attn_forward_static_scratch.argtypes = [P, P, P, P, P, P, P, I, P, P, P]
+    L.k6attn_norm_rope_qk.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P, I, P]
     L.k6attn_cross_workspace_bytes.argtypes = [P, ctypes.c_long, I]
     L.k6attn_cross_workspace_bytes.restype = Z
     L.k6attn_cross_forward.argtypes = [P, P, ctypes.c_long, P, P, ctypes.c_long, I, P, P, P, Z, P]
@@ -82,7 +83,7 @@ def load(build_if_missing: bool = True):
     L.k6attn_last_error.argtypes = []
     L.k6attn_last_error.restype = ctypes.c_char_p
     for name in ("k6attn_create", "k6attn_rope_qk", "k6attn_forward", "k6attn_forward_static_scratch",
-                 "k6attn_attention_chunks", "k6attn_lse_merge", "k6attn_cross_forward",
+                 "k6attn_attention_chunks", "k6attn_lse_merge", "k6attn_cross_forward", "k6attn_norm_rope_qk",
                  "k6attn_seq2head_relayout", "k6attn_sync", "k6attn_set_option"):
         getattr(L, name).restype = I
     _lib = L
@@ -158,6 +159,18 @@ class Handle:
         od = self._desc.dtype if out_dtype is None else out_dtype
         _check(load().k6attn_rope_qk(self.h, _ptr(q), _ptr(k), _ptr(joint_k), tab, _ptr(qo), _ptr(ko), _ptr(jo),
                                      int(od), _stream(stream)))
+
+    def norm_rope_qk(self, q, k, joint_k, q_weight, k_weight, eps, joint_q_weight=None, joint_k_weight=None,
+                     tables=None, q_out=None, k_out=None, joint_k_out=None, out_dtype=None, stream=None):
+        """QK RMSNorm over each token's H*d row, then rotary; in place unless outputs are given."""
+        tab = ctypes.c_void_p(self.rope_tables() if tables is None else tables)
+        qo = q if q_out is None else q_out
+        ko = k if k_out is None else k_out
+        jo = joint_k if joint_k_out is None else joint_k_out
+        od = self._desc.dtype if out_dtype is None else out_dtype
+        _check(load().k6attn_norm_rope_qk(self.h, _ptr(q), _ptr(k), _ptr(joint_k), _ptr(q_weight), _ptr(k_weight),
+                                          _ptr(joint_q_weight), _ptr(joint_k_weight), float(eps), tab, _ptr(qo),
+                                          _ptr(ko), _ptr(jo), int(od), _stream(stream)))
 
     def forward(self, q, k, v, joint_k, joint_v, out, lse=None, *, rope=True, n_chunks=1, workspace=None,
                 tables=None, stream=None):
