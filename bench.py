@@ -3,10 +3,10 @@
 
 One step = the whole hot path over one batch of synthetic input, each row a
 separate C-ABI call with CUDA events between them:
-  seq->head relayout of q, k, v, joint_k, joint_v (the Ulysses layout change,
-  8-way, done on one GPU) -> rotary on q/k (head layout, into fp16 copies) ->
-  attention over n K/V chunks (fp32 partials + LSE) -> LSE merge ->
-  head->seq relayout of the output.
+  rotary on q/k/joint_k (sequence layout, full head rows, into fp16 copies) ->
+  seq->head relayout of q, k, joint_k (fp16), v, joint_v (the Ulysses layout
+  change, 8-way, done on one GPU) -> attention over n K/V chunks (fp32
+  partials + LSE) -> LSE merge -> head->seq relayout of the output.
 The headline metric is attention TFLOP/s (4*B*H*S^2*d per step) over the whole
 step; the attention kernel alone gives the roofline fraction against the
 measured dense-bf16 peak.
@@ -136,17 +136,20 @@ class Path:
         self.w, self.n, self.P = w, n_chunks, P
         B, S, H, d, Nv, Nj = w.B, w.S, w.H, w.d, w.Nv, w.Nj
         self.Hl = H // P
-        bf = torch.bfloat16
+        bf, f16 = torch.bfloat16, torch.float16
 
         def dev(a):
             return torch.from_numpy(a.view(np.int16)).view(bf).cuda()
 
         self.host = {k: torch.from_numpy(v.view(np.int16)).view(bf).pin_memory() for k, v in x.items()}
         self.seq = {k: dev(v) for k, v in x.items()}
-        self.head = {k: torch.empty_like(v) for k, v in self.seq.items()}
-        # rotated q/k/joint_k in fp16 (finer rounding than bf16, same tensor-core rate)
-        self.rot = {k: torch.empty(self.head[k].shape, dtype=torch.float16, device="cuda") for k in ("q", "k", "jk")}
         self.rows = {"q": S, "k": Nv, "v": Nv, "jk": Nj, "jv": Nj}
+        # rotary on the sequence-partitioned tensors (full head rows), into fp16 copies
+        self.hs = K.Handle(B, H, d, "bf16", w.grid, Nj, w.axis_dim, w.theta, w.joint_rope)
+        self.rot = {k: torch.empty(self.seq[k].shape, dtype=f16, device="cuda") for k in ("q", "k", "jk")}
+        # head-partitioned copies: rotated q/k/joint_k (fp16), v/joint_v (bf16)
+        self.head = {k: torch.empty_like(self.rot[k]) for k in ("q", "k", "jk")}
+        self.head.update({k: torch.empty_like(self.seq[k]) for k in ("v", "jv")})
         # attention runs on the head-partitioned layout: P*B independent problems of H/P heads
         self.h = K.Handle(P * B, self.Hl, d, "bf16", w.grid, Nj, w.axis_dim, w.theta, w.joint_rope)
         self.part_o = torch.empty((n_chunks, P * B, S, self.Hl, d), dtype=torch.float32, device="cuda")
@@ -154,31 +157,34 @@ class Path:
         self.out_h = torch.empty((P * B, S, self.Hl, d), dtype=bf, device="cuda")
         self.lse = torch.empty((P * B, self.Hl, S), dtype=torch.float32, device="cuda")
         self.out = torch.empty((B, S, H, d), dtype=bf, device="cuda")
+        self.e2e_head = {k: torch.empty_like(self.seq[k]) for k in self.seq}
+        self.e2e_in = [{k: torch.empty_like(self.seq[k]) for k in self.seq} for _ in range(2)]
+        self.copy_stream = torch.cuda.Stream()
         self.ws = torch.empty(self.h.workspace_bytes(n_chunks, True), dtype=torch.uint8, device="cuda")
         self.out_host = torch.empty(self.out.shape, dtype=bf).pin_memory()
         self.lse_host = torch.empty(self.lse.shape, dtype=torch.float32).pin_memory()
-        self.launches_per_step = 5 + 1 + 1 + 1 + 1
+        self.launches_per_step = 1 + 5 + 1 + 1 + 1
 
-    def relayout_in(self):
+    def relayout(self, src, dst):
         w, K = self.w, self.K
         for name in ("q", "k", "v", "jk", "jv"):
             if self.rows[name]:
-                K.seq2head_relayout(self.seq[name], self.head[name], w.B, self.rows[name], w.H, w.d, self.P, 0)
+                K.seq2head_relayout(src[name], dst[name], w.B, self.rows[name], w.H, w.d, self.P, 0)
 
     def step(self, ev=None):
         w, K, hd = self.w, self.K, self.head
         if ev:
             ev[0].record()
-        self.relayout_in()
+        rt = self.rot
+        self.hs.rope_qk(self.seq["q"], self.seq["k"], self.seq["jk"] if w.Nj else None, q_out=rt["q"], k_out=rt["k"],
+                        joint_k_out=rt["jk"] if w.Nj else None, out_dtype=K.F16)
         if ev:
             ev[1].record()
-        rt = self.rot
-        self.h.rope_qk(hd["q"], hd["k"], hd["jk"] if w.Nj else None, q_out=rt["q"], k_out=rt["k"],
-                       joint_k_out=rt["jk"] if w.Nj else None, out_dtype=K.F16)
+        self.relayout({"q": rt["q"], "k": rt["k"], "jk": rt["jk"], "v": self.seq["v"], "jv": self.seq["jv"]}, hd)
         if ev:
             ev[2].record()
-        jk, jv = (rt["jk"], hd["jv"]) if w.Nj else (None, None)
-        self.h.attention_chunks(rt["q"], rt["k"], hd["v"], jk, jv, self.n, self.part_o, self.part_lse,
+        jk, jv = (hd["jk"], hd["jv"]) if w.Nj else (None, None)
+        self.h.attention_chunks(hd["q"], hd["k"], hd["v"], jk, jv, self.n, self.part_o, self.part_lse,
                                 qk_dtype=K.F16)
         if ev:
             ev[3].record()
@@ -189,19 +195,62 @@ class Path:
         if ev:
             ev[5].record()
 
-    def e2e_step(self):
-        """Public API from pinned host buffers: H2D, relayout, k6attn_forward
-        (rotary + chunks + merge), relayout back, D2H of out and lse."""
+    def const_max_step(self):
+        """Constant-max variant of the attention + merge rows on the head-layout buffers
+        that step() filled: row bounds, bounded attention over the chunks, merge."""
         w, K, hd = self.w, self.K, self.head
-        for k in self.seq:
-            self.seq[k].copy_(self.host[k], non_blocking=True)
-        self.relayout_in()
+        if not hasattr(self, "bounds"):
+            self.bounds = self.torch.empty(self.h.row_bounds_bytes() // 4, dtype=self.torch.float32, device="cuda")
         jk, jv = (hd["jk"], hd["jv"]) if w.Nj else (None, None)
-        self.h.forward(hd["q"], hd["k"], hd["v"], jk, jv, self.out_h, self.lse, rope=True, n_chunks=self.n,
-                       workspace=self.ws)
-        K.seq2head_relayout(self.out_h, self.out, w.B, w.S, w.H, w.d, self.P, 1)
-        self.out_host.copy_(self.out, non_blocking=True)
-        self.lse_host.copy_(self.lse, non_blocking=True)
+        self.h.row_bounds(hd["q"], hd["k"], jk, self.bounds, qk_dtype=K.F16)
+        self.h.attention_chunks_bounded(hd["q"], hd["k"], hd["v"], jk, jv, self.bounds, self.n, self.part_o,
+                                        self.part_lse, qk_dtype=K.F16)
+        self.h.lse_merge(self.part_o, self.part_lse, self.n, self.out_h, self.lse)
+
+    def e2e_run(self, steps):
+        """Public API from pinned host buffers, `steps` steps: per step the H2D copy of its
+        inputs, relayout, k6attn_forward (rotary + chunks + merge), relayout back and the
+        D2H copy of out and lse.  Copies run on their own stream, overlapping the previous
+        and next steps' compute (inputs double-buffered); every copy is inside the timed region."""
+        torch, w, K = self.torch, self.w, self.K
+        comp = torch.cuda.current_stream()
+        copy = self.copy_stream
+        ev_in = [torch.cuda.Event() for _ in range(2)]      # inputs of a buffer landed
+        ev_used = [torch.cuda.Event() for _ in range(2)]    # compute done reading a buffer
+        ev_out = torch.cuda.Event()                         # outputs of a step ready
+        ev_read = torch.cuda.Event()                        # previous outputs copied out
+
+        def h2d(step):
+            buf = self.e2e_in[step % 2]
+            with torch.cuda.stream(copy):
+                copy.wait_event(ev_used[step % 2])
+                for k in buf:
+                    buf[k].copy_(self.host[k], non_blocking=True)
+                ev_in[step % 2].record(copy)
+
+        for e in ev_used:
+            e.record(comp)
+        h2d(0)
+        for step in range(steps):
+            if step + 1 < steps:
+                h2d(step + 1)
+            buf = self.e2e_in[step % 2]
+            comp.wait_event(ev_in[step % 2])
+            self.relayout(buf, self.e2e_head)
+            ev_used[step % 2].record(comp)
+            hd = self.e2e_head
+            jk, jv = (hd["jk"], hd["jv"]) if w.Nj else (None, None)
+            comp.wait_event(ev_read)  # the previous step's outputs have left the device
+            self.h.forward(hd["q"], hd["k"], hd["v"], jk, jv, self.out_h, self.lse, rope=True, n_chunks=self.n,
+                           workspace=self.ws)
+            K.seq2head_relayout(self.out_h, self.out, w.B, w.S, w.H, w.d, self.P, 1)
+            ev_out.record(comp)
+            with torch.cuda.stream(copy):
+                copy.wait_event(ev_out)
+                self.out_host.copy_(self.out, non_blocking=True)
+                self.lse_host.copy_(self.lse, non_blocking=True)
+                ev_read.record(copy)
+        comp.wait_stream(copy)
 
     def h2d_bytes(self):
         return sum(t.numel() * t.element_size() for t in self.host.values())
@@ -270,14 +319,24 @@ def measure(w, n_chunks, P, steps, warmup, dist_on, with_e2e=True, clocks=True):
     res = {"total_ms": total_ms, "per_kernel_ms": per.mean(axis=0).tolist(),
            "clocks": clk.summary() if clocks else None, "launches": path.launches_per_step * steps}
     if with_e2e:
-        for _ in range(max(1, warmup)):
-            path.e2e_step()
+        # the constant-max variant of attention + merge on the same buffers
+        for _ in range(2):
+            path.const_max_step()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record()
+        for _ in range(steps):
+            path.const_max_step()
+        c1.record()
+        torch.cuda.synchronize()
+        path.h.sync()
+        res["const_max_ms"] = c0.elapsed_time(c1) / steps
+    if with_e2e:
+        path.e2e_run(max(1, warmup))
         torch.cuda.synchronize()
         barrier(dist_on)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        for _ in range(steps):
-            path.e2e_step()
+        path.e2e_run(steps)
         e1.record()
         barrier(dist_on)
         res["e2e_ms"] = max_over_ranks(e0.elapsed_time(e1), dist_on)
@@ -356,7 +415,7 @@ def run_ours(args, rank, world, dist_on):
     flops = w.flops()
     ms = res["total_ms"] / args.steps
     value = whole_job_rate(flops, world, res["total_ms"] / args.steps * 1e-3) / 1e12
-    k_ms = res["per_kernel_ms"]  # relayout_in, rope, attention, merge, relayout_out
+    k_ms = res["per_kernel_ms"]  # rope, relayout_in, attention, merge, relayout_out
     attn_tflops = flops / (k_ms[2] * 1e-3) / 1e12
     peak_s = pk["bf16_tflops_sustained"]
     tag = "of measured" if pk["source"] == "measured" else "of fallback"
@@ -371,9 +430,9 @@ def run_ours(args, rank, world, dist_on):
         return b / (t_ms * 1e-3) / 1e9
 
     kernels = {
-        "relayout_seq2head_qkv": {"ms": k_ms[0], "GB/s": gbs(relayout_in_bytes, k_ms[0]),
-                                  "frac": gbs(relayout_in_bytes, k_ms[0]) / hbm},
-        "rope_qk": {"ms": k_ms[1], "GB/s": gbs(rope_bytes, k_ms[1]), "frac": gbs(rope_bytes, k_ms[1]) / hbm},
+        "rope_qk": {"ms": k_ms[0], "GB/s": gbs(rope_bytes, k_ms[0]), "frac": gbs(rope_bytes, k_ms[0]) / hbm},
+        "relayout_seq2head_qkv": {"ms": k_ms[1], "GB/s": gbs(relayout_in_bytes, k_ms[1]),
+                                  "frac": gbs(relayout_in_bytes, k_ms[1]) / hbm},
         "attention_chunks": {"ms": k_ms[2], "TFLOP/s": attn_tflops, "frac_sustained": attn_tflops / peak_s,
                              "frac_burst": attn_tflops / pk["bf16_tflops"]},
         "lse_merge": {"ms": k_ms[3], "GB/s": gbs(mb, k_ms[3]), "frac": gbs(mb, k_ms[3]) / hbm},
@@ -413,6 +472,11 @@ def run_ours(args, rank, world, dist_on):
                               "ms_per_step": round(t2, 3),
                               "attention_TFLOP/s": round(f2 / (r2["per_kernel_ms"][2] * 1e-3) / 1e12, 2),
                               "merge_GB/s": round(gbs(merge_bytes(w2, n2, 8), r2["per_kernel_ms"][3]), 1)}
+    if "const_max_ms" in res:
+        line["const_max"] = {"what": "row bounds + bounded attention (no running max, no rescale) + merge",
+                              "ms": round(res["const_max_ms"], 3),
+                              "TFLOP/s": round(flops / (res["const_max_ms"] * 1e-3) / 1e12, 2),
+                              "standard_attention_plus_merge_ms": round(k_ms[2] + k_ms[3], 3)}
     if args.secondary:
         line["cross_attention"] = measure_cross(w, max(5, args.steps // 2), args.warmup)
     if rank == 0 and world == 1 and not args.no_cpu:

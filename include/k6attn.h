@@ -200,6 +200,33 @@ k6attn_status k6attn_attention_chunks(k6attn_t h, const void *q, const void *k, 
                                       void *stream);
 
 /*
+ * Constant-max softmax ([CP] "Related information": the ring kernel
+ * `ring_attention_const_max_fwd` uses a runtime bound on the softmax maximum
+ * instead of a running maximum, so no partial output is ever rescaled).  The
+ * pages do not give the bound; this library uses Cauchy-Schwarz:
+ *   bound_i = |q_i| * max_j |k_j| / sqrt(d)  >=  every logit of row i,
+ * the maximum taken over all keys of the (batch, head) pair, so one bound
+ * serves every K/V chunk and the partials merge unchanged.
+ *
+ * k6attn_row_bounds: bounds fp32 of k6attn_row_bounds_bytes(h) bytes: the
+ *   first B*H*Sq floats are the row bounds [B][H][Sq] (natural-log units of
+ *   the logits), the last B*H the key-norm maxima.  q/k/joint_k as for
+ *   k6attn_attention_chunks (rotated; qk_dtype the handle's or F16).
+ * k6attn_attention_chunks_bounded: k6attn_attention_chunks with the bounds
+ *   in place of the running maximum (bf16 handles).  Exactly the same
+ *   mathematics; a row whose every term underflows (a bound more than about
+ *   87 above its largest logit) sets the error word (K6ATTN_ERR_RANGE at
+ *   k6attn_sync) and gets a zero output.
+ */
+size_t k6attn_row_bounds_bytes(k6attn_t h);
+k6attn_status k6attn_row_bounds(k6attn_t h, const void *q, const void *k, const void *joint_k, k6attn_dtype qk_dtype,
+                                float *bounds, void *stream);
+k6attn_status k6attn_attention_chunks_bounded(k6attn_t h, const void *q, const void *k, const void *v,
+                                              const void *joint_k, const void *joint_v, k6attn_dtype qk_dtype,
+                                              const float *bounds, int n_chunks, void *out, float *lse,
+                                              void *stream);
+
+/*
  * Log-sum-exp merge of per-chunk partials (ring attention's combine step,
  * [CP] "Ring attention (current implementation)", "Scaling Properties"):
  *   LSE = log sum_c exp(LSE_c),  out = sum_c exp(LSE_c - LSE) * O_c.
@@ -280,7 +307,8 @@ k6attn_status k6attn_forward_static_scratch(k6attn_t h, const void *q, const voi
 
 /* Synchronise `stream`, then read and clear the handle's device error word:
  * K6ATTN_ERR_TIMEOUT if any kernel of this handle gave up on a wait,
- * K6ATTN_ERR_RANGE if a rotation into fp16 overflowed,
+ * K6ATTN_ERR_RANGE if a rotation into fp16 overflowed or a constant-max row
+ * underflowed,
  * K6ATTN_ERR_CUDA on an asynchronous CUDA error, else K6ATTN_OK. */
 k6attn_status k6attn_sync(k6attn_t h, void *stream);
 

@@ -37,6 +37,12 @@
  *     ("Audio queries gather the full visual sequence"); "Context Parallelism
  *     in vLLM Omni Neuron", "Forward Pass Flow" ("Cross-attention uses full
  *     encoder states").
+ *   - The constant-max variant of ring attention ("Context Parallelism in vLLM
+ *     Omni Neuron", "Related information": `ring_attention_const_max_fwd`
+ *     takes the softmax max as a runtime bound instead of a running max).
+ *     Read as the Cauchy-Schwarz bound M_i = |q~_i| * max_j |k~_j| / sqrt(d)
+ *     >= max_j s_ij; the attention result does not depend on which bound is
+ *     used, so the oracle supplies only the bound itself.
  *   - QK-norm before the rotary embedding: "Context Parallelism in vLLM Omni
  *     Neuron", "Self-Attention with Context Parallelism" (`norm_q(q)`,
  *     `norm_k(k)` on the projected rows before they are split into heads) and
@@ -162,6 +168,58 @@ int k6o_rope(const k6o_geom *g, const void *x, int type, double *y) {
         for (int e = 0; e < d; e++) out[e] = load_elem(x, type, (size_t)r * d + e);
         k6o_rope_vec(g, n, out);
     }
+    return 0;
+}
+
+static const void *kv_ptr(const k6o_geom *g, long n, int b, int h, const void *video, const void *joint,
+                          size_t *off);
+
+/*
+ * Row bounds of the constant-max softmax, from rotated (or unrotated when
+ * rope = 0) q and keys: bound [B][H][Sq] = |q~_i| * max_j |k~_j| / sqrt(d),
+ * the maximum over all Sk = Nv + Nj keys of the (b, h) pair.
+ */
+int k6o_row_bounds(const k6o_geom *g, int rope, const void *q, const void *k, const void *jk, int type,
+                   double *bound) {
+    if (!geom_ok(g)) return -1;
+    const long S = g->Nv + g->Nj;
+    const int d = g->d, H = g->H;
+    for (int b = 0; b < g->B; b++)
+        for (int h = 0; h < H; h++) {
+            double kmax = 0.0;
+#pragma omp parallel
+            {
+                double *x = (double *)malloc(sizeof(double) * d);
+                double local = 0.0;
+#pragma omp for schedule(static)
+                for (long n = 0; n < S; n++) {
+                    size_t off;
+                    const void *src = kv_ptr(g, n, b, h, k, jk, &off);
+                    for (int e = 0; e < d; e++) x[e] = load_elem(src, type, off + e);
+                    if (rope) k6o_rope_vec(g, n, x);
+                    double ss = 0.0;
+                    for (int e = 0; e < d; e++) ss += x[e] * x[e];
+                    if (sqrt(ss) > local) local = sqrt(ss);
+                }
+#pragma omp critical
+                if (local > kmax) kmax = local;
+                free(x);
+            }
+#pragma omp parallel
+            {
+                double *x = (double *)malloc(sizeof(double) * d);
+#pragma omp for schedule(static)
+                for (long i = 0; i < S; i++) {
+                    const size_t off = (((size_t)b * S + i) * H + h) * d;
+                    for (int e = 0; e < d; e++) x[e] = load_elem(q, type, off + e);
+                    if (rope) k6o_rope_vec(g, i, x);
+                    double ss = 0.0;
+                    for (int e = 0; e < d; e++) ss += x[e] * x[e];
+                    bound[((size_t)b * H + h) * S + i] = sqrt(ss) * kmax / sqrt((double)d);
+                }
+                free(x);
+            }
+        }
     return 0;
 }
 

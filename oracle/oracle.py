@@ -85,6 +85,7 @@ def lib():
                                        ctypes.c_long, ctypes.c_long, P, ctypes.c_long, P, P]
         _lib.k6o_cross_attention.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_long,
                                              ctypes.c_long, P, P, P, ctypes.c_int, ctypes.c_long, ctypes.c_long, P, P]
+        _lib.k6o_row_bounds.argtypes = [ctypes.POINTER(_Geom), ctypes.c_int, P, P, P, ctypes.c_int, P]
         _lib.k6o_rms_norm.argtypes = [P, ctypes.c_int, ctypes.c_long, ctypes.c_long, P, ctypes.c_double, P]
         _lib.k6o_lse_merge.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_long, ctypes.c_int, ctypes.c_int,
                                        P, P, ctypes.c_int, P, P]
@@ -130,6 +131,18 @@ def rope(g: Geom, x: np.ndarray) -> np.ndarray:
     if rc:
         raise ValueError(f"k6o_rope: {rc}")
     return y
+
+
+def row_bounds(g: Geom, q, k, jk=None, *, rope: bool = True) -> np.ndarray:
+    """Constant-max row bounds [B][H][S]: |q~_i| * max_j |k~_j| / sqrt(d) over all keys."""
+    (q_, t), (k_, t2) = _typed(q), _typed(k)
+    jk_ = _typed(jk)[0] if g.Nj > 0 else None
+    out = np.empty((g.B, g.H, g.S), np.float64)
+    rc = lib().k6o_row_bounds(ctypes.byref(g.c()), int(bool(rope)), _ptr(q_), _ptr(k_),
+                              _ptr(jk_) if jk_ is not None else ctypes.c_void_p(0), t, _ptr(out))
+    if rc:
+        raise ValueError(f"k6o_row_bounds: {rc}")
+    return out
 
 
 def rms_norm(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:

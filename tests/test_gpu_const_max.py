@@ -1,0 +1,90 @@
+"""GPU parity of the constant-max softmax (row bounds in place of the running
+max) against the oracle: the bounds themselves, the attention result, and the
+underflow guard when the Cauchy-Schwarz bound is far above every logit."""
+import numpy as np
+import pytest
+
+from oracle import oracle as O
+from video_dit_long_gb300 import configs, inputs
+from video_dit_long_gb300.configs import Workload
+
+from .helpers import compare, geom, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+CASES = {
+    "ragged": Workload("ragged", 1, 2, 128, "bf16", (3, 10, 20), 40, (32, 48, 48), 0, 1.0, 1.0, (1, 4)),
+    "audio1d": Workload("audio1d", 2, 2, 128, "bf16", (2, 8, 16), 62, (32, 48, 48), 1, 1.0, 1.0, (1, 3)),
+    "lite": configs.WORKLOADS["lite"],
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def run_bounded(w, x, n, rope=True):
+    from video_dit_long_gb300 import k6attn as K
+    h = K.Handle.for_workload(w)
+    q, k, v, jk, jv = (to_dev(x[nm], w.dtype) for nm in ("q", "k", "v", "jk", "jv"))
+    if rope:
+        qo, ko, jo = (torch.empty(t.shape, dtype=torch.float16, device="cuda") for t in (q, k, jk))
+        h.rope_qk(q, k, jk, q_out=qo, k_out=ko, joint_k_out=jo, out_dtype=K.F16)
+        qd = K.F16
+    else:
+        qo, ko, jo, qd = q, k, jk, K.BF16
+    bounds = torch.empty(h.row_bounds_bytes() // 4, dtype=torch.float32, device="cuda")
+    h.row_bounds(qo, ko, jo, bounds, qk_dtype=qd)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device="cuda")
+    if n == 1:
+        h.attention_chunks_bounded(qo, ko, v, jo, jv, bounds, 1, out, lse, qk_dtype=qd)
+    else:
+        po = torch.empty((n, w.B, w.S, w.H, w.d), dtype=torch.float32, device="cuda")
+        pl = torch.empty((n, w.B, w.H, w.S), dtype=torch.float32, device="cuda")
+        h.attention_chunks_bounded(qo, ko, v, jo, jv, bounds, n, po, pl, qk_dtype=qd)
+        h.lse_merge(po, pl, n, out, lse)
+    return h, out, lse, bounds
+
+
+@pytest.mark.parametrize("name", ["ragged", "audio1d", "lite"])
+def test_bounded_attention_matches_oracle(name):
+    w = CASES[name]
+    x = inputs.make_inputs(w)
+    for n in (1, w.chunks[-1]):
+        h, out, lse, bounds = run_bounded(w, x, n)
+        h.sync()
+        ref, ref_lse = O.attention(geom(w), x["q"], x["k"], x["v"], x["jk"], x["jv"])
+        compare(to_host(out), ref, lse.cpu().numpy().astype(np.float64), ref_lse, "bf16")
+        # the bounds: within fp16 rounding of the oracle's, and above every logit
+        rb = O.row_bounds(geom(w), x["q"], x["k"], x["jk"])
+        got = bounds[: w.B * w.H * w.S].cpu().numpy().reshape(w.B, w.H, w.S)
+        np.testing.assert_allclose(got, rb, rtol=2e-3, atol=0)
+
+
+def test_bounded_attention_mildly_peaked():
+    w = CASES["ragged"]
+    x = inputs.make_inputs(w, qk_scale=2.0)
+    h, out, lse, _ = run_bounded(w, x, 4, rope=False)
+    h.sync()
+    ref, ref_lse = O.attention(geom(w), x["q"], x["k"], x["v"], x["jk"], x["jv"], rope=False)
+    compare(to_host(out), ref, lse.cpu().numpy().astype(np.float64), ref_lse, "bf16")
+
+
+def test_loose_bound_underflow_is_reported():
+    from video_dit_long_gb300 import k6attn as K
+    w = CASES["ragged"]
+    x = inputs.make_inputs(w, qk_scale=5.0)  # |q||k|/sqrt(d) ~ 330 against logits ~ 110: exp underflows
+    g = geom(w)
+    rb = O.row_bounds(g, x["q"], x["k"], x["jk"], rope=False)
+    _, ref_lse = O.attention(g, x["q"], x["k"], x["v"], x["jk"], x["jv"], rope=False)
+    assert (rb - ref_lse).max() > 90  # the oracle agrees the bound is that loose somewhere
+    h, out, lse, _ = run_bounded(w, x, 1, rope=False)
+    with pytest.raises(K.K6Error) as e:
+        h.sync()
+    assert e.value.status == K.ERR_RANGE
+    assert torch.isfinite(out.float()).all()

@@ -269,6 +269,26 @@ def test_cross_attention_equals_self_attention_without_rotary():
     np.testing.assert_array_equal(a[1], b[1])
 
 
+# ------------------------------------------------------- constant-max bound
+
+
+def test_row_bounds_dominate_every_logit_and_are_tight_for_aligned_keys():
+    g = O.Geom(2, 3, 16, (2, 3, 4), 5, (4, 6, 6), 10000.0, 1)
+    q, k, v, jk, jv = tiny_inputs(g, seed=61, std=2.0)
+    bound = O.row_bounds(g, q, k, jk)
+    qr = O.rope(g, q)
+    kr = O.rope(g, np.concatenate([k, jk], axis=1))
+    s = np.einsum("bihe,bjhe->bhij", qr, kr) / math.sqrt(g.d)
+    assert (s.max(axis=-1) <= bound + 1e-12).all()          # Cauchy-Schwarz
+    # a key equal to the longest key direction aligned with q reaches the bound
+    g0 = tiny_geom(B=1, H=1, d=8, grid=(1, 1, 3), Nj=0)
+    q0 = rnd((1, 3, 1, 8), 62)
+    k0 = np.stack([q0[0, 0, 0] * 2.0, q0[0, 1, 0] * 0.1, q0[0, 2, 0] * 0.3])[None, :, None, :]
+    b0 = O.row_bounds(g0, q0, k0, rope=False)
+    s00 = q0[0, 0, 0] @ k0[0, 0, 0] / math.sqrt(8)
+    assert abs(b0[0, 0, 0] - s00) < 1e-12
+
+
 # ----------------------------------------------------------------- QK-norm
 
 

@@ -79,9 +79,9 @@ static WsLayout ws_layout(const Geom &g, int n, bool rope) {
 // n_chunks > 1 writes fp32 partials into out/lse (see k6attn_attention_chunks).
 static k6attn_status run_attention(k6attn_handle *h, const Geom &g, const void *q, const void *k, const void *v,
                                    const void *jk, const void *jv, bool qk_f16, int n_chunks, void *out, float *lse,
-                                   cudaStream_t st) {
+                                   cudaStream_t st, const float *row_bound = nullptr) {
     if (g.elem == 2) {
-        AttnTcOptions opt{h->wait_limit_ns, h->err, h->strict_order, qk_f16 ? 1 : 0};
+        AttnTcOptions opt{h->wait_limit_ns, h->err, h->strict_order, qk_f16 ? 1 : 0, row_bound};
         const char *why = nullptr;
         cudaError_t e = launch_attn_tc(g, q, k, v, jk, jv, n_chunks, out, lse, opt, st, &why);
         if (e != cudaSuccess) {
@@ -281,6 +281,58 @@ k6attn_status k6attn_norm_rope_qk(k6attn_t h, const void *q, const void *k, cons
     QkNorm norm{q_weight, joint_q_weight, k_weight, joint_k_weight, eps};
     return rope_common("norm_rope_qk", h, q, k, joint_k, rope_tables, q_out, k_out, joint_k_out, out_dtype, &norm,
                        stream);
+}
+
+size_t k6attn_row_bounds_bytes(k6attn_t h) {
+    if (!h) return 0;
+    return ((size_t)h->g.B * h->g.H * h->g.Sq + (size_t)h->g.B * h->g.H) * sizeof(float);
+}
+
+k6attn_status k6attn_row_bounds(k6attn_t h, const void *q, const void *k, const void *joint_k, k6attn_dtype qk_dtype,
+                                float *bounds, void *stream) {
+    g_msg[0] = 0;
+    if (!h) return set_error(K6ATTN_ERR_INVALID_ARG, "row_bounds: null handle");
+    const Geom &g = h->g;
+    if (!q || !k || !bounds || (g.Nj > 0 && !joint_k))
+        return set_error(K6ATTN_ERR_INVALID_ARG, "row_bounds: null pointer");
+    if (qk_dtype != g.dtype && !(g.dtype == K6ATTN_BF16 && qk_dtype == K6ATTN_F16))
+        return set_error(K6ATTN_ERR_INVALID_ARG, "row_bounds: q/k type %d not allowed for this handle", (int)qk_dtype);
+    if (!aligned16(q) || !aligned16(k) || !aligned16(joint_k) || (reinterpret_cast<uintptr_t>(bounds) & 3))
+        return set_error(K6ATTN_ERR_INVALID_ARG, "row_bounds: misaligned pointer");
+    const size_t row = (size_t)g.H * g.d * (qk_dtype == K6ATTN_F32 ? 4 : 2);
+    const size_t bb = k6attn_row_bounds_bytes(h);
+    if (overlap(bounds, bb, q, g.B * g.Sq * row) || overlap(bounds, bb, k, g.B * g.Nv * row) ||
+        overlap(bounds, bb, joint_k, g.B * g.Nj * row))
+        return set_error(K6ATTN_ERR_INVALID_ARG, "row_bounds: bounds overlap an input");
+    return cuda_check(launch_row_bounds(g, qk_dtype, q, k, joint_k, bounds, static_cast<cudaStream_t>(stream)),
+                      "row_bounds launch");
+}
+
+k6attn_status k6attn_attention_chunks_bounded(k6attn_t h, const void *q, const void *k, const void *v,
+                                              const void *joint_k, const void *joint_v, k6attn_dtype qk_dtype,
+                                              const float *bounds, int n_chunks, void *out, float *lse,
+                                              void *stream) {
+    g_msg[0] = 0;
+    if (!h) return set_error(K6ATTN_ERR_INVALID_ARG, "attention_chunks_bounded: null handle");
+    const Geom &g = h->g;
+    if (g.dtype != K6ATTN_BF16)
+        return set_error(K6ATTN_ERR_UNSUPPORTED, "attention_chunks_bounded: the constant-max path is bf16 only");
+    if (!bounds || (reinterpret_cast<uintptr_t>(bounds) & 3))
+        return set_error(K6ATTN_ERR_INVALID_ARG, "attention_chunks_bounded: null or misaligned bounds");
+    if (n_chunks > 1 && !lse)
+        return set_error(K6ATTN_ERR_INVALID_ARG, "attention_chunks_bounded: partial lse is required when n_chunks > 1");
+    if (qk_dtype != K6ATTN_BF16 && qk_dtype != K6ATTN_F16)
+        return set_error(K6ATTN_ERR_INVALID_ARG, "attention_chunks_bounded: q/k type %d", (int)qk_dtype);
+    const int n = n_chunks > 1 ? n_chunks : 1;
+    const size_t ob = (size_t)n * g.B * g.Sq * g.H * g.d * (n_chunks > 1 ? 4 : g.elem);
+    const size_t lb = (size_t)n * g.B * g.H * g.Sq * 4;
+    k6attn_status s = check_inputs("attention_chunks_bounded", g, q, k, v, joint_k, joint_v, n_chunks, out, ob, lse, lb);
+    if (s != K6ATTN_OK) return s;
+    const size_t bb = k6attn_row_bounds_bytes(h);
+    if (overlap(bounds, bb, out, ob) || overlap(bounds, bb, lse, lb))
+        return set_error(K6ATTN_ERR_INVALID_ARG, "attention_chunks_bounded: bounds overlap an output");
+    return run_attention(h, g, q, k, v, joint_k, joint_v, qk_dtype == K6ATTN_F16, n_chunks, out, lse,
+                         static_cast<cudaStream_t>(stream), bounds);
 }
 
 k6attn_status k6attn_lse_merge(k6attn_t h, const float *part_o, const float *part_lse, int n_chunks, void *out,

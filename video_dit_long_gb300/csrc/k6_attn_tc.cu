@@ -82,6 +82,7 @@ struct TcParams {
     int strict_order;
     uint32_t idesc_qk;                        // instruction descriptor of Q.K^T (bf16 or fp16 operands)
     long units;                               // B * H * n_chunks * q_pairs work units
+    const float *row_bound;                   // constant-max softmax: bound per query row [B][H][Sq], or null
 };
 
 // K/V tile j of a chunk: which tensor map (0 video, 1 joint), first row, valid keys.
@@ -139,6 +140,11 @@ __device__ __forceinline__ Unit decode_unit(const TcParams &p, long u) {
 // to the next; the next unit's Q is loaded as soon as the last Q.K^T of the
 // current one has read Q (q_empty), so it overlaps the last P.V products and
 // the epilogue.
+// BOUNDED: constant-max softmax.  Each row's running max is replaced by the
+// precomputed bound p.row_bound (>= every logit of the row), so the softmax
+// takes no row maximum and never rescales O; a row whose every term
+// underflows (a bound far above the true maximum) is reported as DEV_RANGE.
+template <bool BOUNDED>
 __global__ void __launch_bounds__(tc::THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_jk,
@@ -241,23 +247,26 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
             const uint32_t idesc_qk = p.idesc_qk;
             const uint32_t idesc_pv = idesc_bf16_f32(BM, D, true);
             const uint32_t sQ = smem_u32(smem + SMEM_Q), sKV = smem_u32(smem + SMEM_KV);
+            // Descriptors are built once; per MMA only the start-address field
+            // (bits 0-13, 16-byte units) moves, so each issue is one 64-bit add.
+            const uint64_t dq0 = smem_desc_sw128(sQ, 16, 1024);         // Q / K: K-major, SBO 1024
+            const uint64_t dv0 = smem_desc_sw128(sKV, PANEL, 1024);     // V: MN-major, LBO = panel stride
             auto issue_s = [&](int i, uint32_t slot) {
-                const uint32_t qa = sQ + i * TILE, kb = sKV + slot * TILE;
+                const uint64_t qa = dq0 + ((uint64_t)(i * TILE) >> 4);
+                const uint64_t kb = dq0 + ((uint64_t)(SMEM_KV - SMEM_Q + slot * TILE) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; kk++) {
-                    const uint32_t off = (kk >> 2) * PANEL + (kk & 3) * 32;
-                    mma_ss(tmem + i * BN, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024),
-                           idesc_qk, kk > 0);
+                    const uint64_t off = (uint64_t)((kk >> 2) * PANEL + (kk & 3) * 32) >> 4;
+                    mma_ss(tmem + i * BN, qa + off, kb + off, idesc_qk, kk > 0);
                 }
             };
             // keys [16*k0, 16*k1) of P_i . V
             auto issue_pv = [&](int i, uint32_t slot, bool acc, int k0, int k1) {
-                const uint32_t vb = sKV + slot * TILE;
+                const uint64_t vb = dv0 + ((uint64_t)(slot * TILE) >> 4);
 #pragma unroll
-                for (int kk = k0; kk < k1; kk++) {
-                    mma_ts(tmem + 2 * BN + i * D, tmem + i * BN + kk * 8,
-                           smem_desc_sw128(vb + kk * 16 * 128, PANEL, 1024), idesc_pv, (acc || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = k0; kk < k1; kk++)
+                    mma_ts(tmem + 2 * BN + i * D, tmem + i * BN + kk * 8, vb + ((uint64_t)(kk * 16 * 128) >> 4),
+                           idesc_pv, (acc || kk > 0) ? 1u : 0u);
             };
             uint32_t step_phase[2] = {0, 0};
             // P_i lives in S_i's columns: in strict mode let the P.V that read it finish before S_i is rewritten
@@ -344,6 +353,10 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
             const TileRange tr = chunk_tiles(p, un.c);
             const int T = tr.T;
             float m_run = -INFINITY, l_run = 0.f;
+            const long grow_u = (long)un.q0 + i * BM + r;
+            if constexpr (BOUNDED)
+                m_run = grow_u < p.Sq ? p.row_bound[((long)un.b * p.H + un.h) * p.Sq + grow_u] * 1.4426950408889634f
+                                      : 0.f;
             for (int j = 0; j < T; j++) {
                 int map, row, valid;
                 tr.at(j, map, row, valid);
@@ -362,6 +375,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                     for (int k = 0; k < BN; k++)
                         if (k >= valid) s[k] = 0xff800000u;
                 }
+                if constexpr (!BOUNDED) {
                 // row max: four independent 3-input chains
                 float mc[4];
 #pragma unroll
@@ -394,6 +408,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                         for (int k = 0; k < 32; k++) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
                         tmem_st32(tO + cc * 32, o);
                     }
+                }
                 }
                 // p = 2^(s * scale*log2e - m): packed FMA, then the SFU; row sum on
                 // packed adds.  The first 64 keys' P is published on its own so
@@ -436,7 +451,10 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
             tc_fence_after();
             const long grow = (long)un.q0 + i * BM + r;
             const bool live = grow < p.Sq;
-            const float inv = 1.f / l_run;
+            if constexpr (BOUNDED) {
+                if (live && !(l_run > 0.f)) atomicCAS(p.err, DEV_OK, DEV_RANGE);  // bound too loose: all terms underflowed
+            }
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
             const long obase = (((long)un.b * p.Sq + (live ? grow : 0)) * p.H + un.h) * D;
 #pragma unroll
             for (int cc = 0; cc < D / 32; cc++) {
@@ -533,7 +551,11 @@ cudaError_t launch_attn_tc(const Geom &g, const void *q, const void *k, const vo
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_ALLOC);
+        attr_err = cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        tc::SMEM_ALLOC);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            tc::SMEM_ALLOC);
     });
     if (attr_err != cudaSuccess) return attr_err;
     TcParams p;
@@ -562,7 +584,11 @@ cudaError_t launch_attn_tc(const Geom &g, const void *q, const void *k, const vo
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const long grid = p.units < sms ? p.units : sms;  // persistent: one CTA per SM
-    attn_tc_kernel<<<(unsigned)grid, tc::THREADS, tc::SMEM_ALLOC, st>>>(mq, mk, mv, mjk, mjv, p);
+    p.row_bound = opt.row_bound;
+    if (opt.row_bound)
+        attn_tc_kernel<true><<<(unsigned)grid, tc::THREADS, tc::SMEM_ALLOC, st>>>(mq, mk, mv, mjk, mjv, p);
+    else
+        attn_tc_kernel<false><<<(unsigned)grid, tc::THREADS, tc::SMEM_ALLOC, st>>>(mq, mk, mv, mjk, mjv, p);
     return cudaGetLastError();
 }
 

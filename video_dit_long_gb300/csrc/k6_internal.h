@@ -77,7 +77,13 @@ struct AttnTcOptions {
     int *err;
     int strict_order;        // 1: wait for P.V to finish before reusing its TMEM
     int qk_f16;              // 1: q/k/joint_k are fp16 (Q.K^T in fp16), else bf16
+    const float *row_bound = nullptr;  // constant-max softmax bounds [B][H][Sq] (natural-log units), or null
 };
+
+// Constant-max bounds: bound[(b*H + h)*Sq + s] = |q| * max|k| / sqrt(d);
+// bound must hold B*H*Sq + B*H floats (the tail is the key-norm maximum).
+cudaError_t launch_row_bounds(const Geom &g, k6attn_dtype qk_dtype, const void *q, const void *k, const void *jk,
+                              float *bound, cudaStream_t st);
 cudaError_t launch_attn_tc(const Geom &g, const void *q, const void *k, const void *v, const void *jk,
                            const void *jv, int n_chunks, void *out, float *lse, const AttnTcOptions &opt,
                            cudaStream_t st, const char **why);

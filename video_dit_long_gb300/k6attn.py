@@ -22,7 +22,8 @@ SYMBOLS = ["k6attn_create", "k6attn_destroy", "k6attn_rope_tables", "k6attn_rope
            "k6attn_workspace_bytes", "k6attn_rope_qk", "k6attn_forward", "k6attn_attention_chunks", "k6attn_lse_merge",
            "k6attn_seq2head_relayout", "k6attn_sync", "k6attn_set_option", "k6attn_status_string",
            "k6attn_last_error", "k6attn_forward_static_scratch", "k6attn_cross_workspace_bytes",
-           "k6attn_cross_forward", "k6attn_norm_rope_qk"]
+           "k6attn_cross_forward", "k6attn_norm_rope_qk", "k6attn_row_bounds_bytes", "k6attn_row_bounds",
+           "k6attn_attention_chunks_bounded"]
 
 
 class K6Error(RuntimeError):
@@ -69,6 +70,10 @@ def load(build_if_missing: bool = True):
     L.k6attn_rope_qk.argtypes = [P, P, P, P, P, P, P, P, I, P]
     L.k6attn_forward.argtypes = [P, P, P, P, P, P, P, I, P, P, P, Z, P]
     L.k6attn_forward_static_scratch.argtypes = [P, P, P, P, P, P, P, I, P, P, P]
+    L.k6attn_row_bounds_bytes.argtypes = [P]
+    L.k6attn_row_bounds_bytes.restype = Z
+    L.k6attn_row_bounds.argtypes = [P, P, P, P, I, P, P]
+    L.k6attn_attention_chunks_bounded.argtypes = [P, P, P, P, P, P, I, P, I, P, P, P]
     L.k6attn_norm_rope_qk.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P, I, P]
     L.k6attn_cross_workspace_bytes.argtypes = [P, ctypes.c_long, I]
     L.k6attn_cross_workspace_bytes.restype = Z
@@ -84,6 +89,7 @@ def load(build_if_missing: bool = True):
     L.k6attn_last_error.restype = ctypes.c_char_p
     for name in ("k6attn_create", "k6attn_rope_qk", "k6attn_forward", "k6attn_forward_static_scratch",
                  "k6attn_attention_chunks", "k6attn_lse_merge", "k6attn_cross_forward", "k6attn_norm_rope_qk",
+                 "k6attn_row_bounds", "k6attn_attention_chunks_bounded",
                  "k6attn_seq2head_relayout", "k6attn_sync", "k6attn_set_option"):
         getattr(L, name).restype = I
     _lib = L
@@ -205,6 +211,21 @@ class Handle:
         _check(load().k6attn_cross_forward(self.h, _ptr(q), int(q.shape[1]), _ptr(k), _ptr(v), int(k.shape[1]),
                                            int(n_chunks), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
                                            _stream(stream)))
+
+    def row_bounds_bytes(self) -> int:
+        return load().k6attn_row_bounds_bytes(self.h)
+
+    def row_bounds(self, q, k, joint_k, bounds, qk_dtype=None, stream=None):
+        qd = self._desc.dtype if qk_dtype is None else qk_dtype
+        _check(load().k6attn_row_bounds(self.h, _ptr(q), _ptr(k), _ptr(joint_k), int(qd), _ptr(bounds),
+                                        _stream(stream)))
+
+    def attention_chunks_bounded(self, q, k, v, joint_k, joint_v, bounds, n_chunks, out, lse=None, qk_dtype=None,
+                                 stream=None):
+        qd = self._desc.dtype if qk_dtype is None else qk_dtype
+        _check(load().k6attn_attention_chunks_bounded(self.h, _ptr(q), _ptr(k), _ptr(v), _ptr(joint_k),
+                                                      _ptr(joint_v), int(qd), _ptr(bounds), int(n_chunks), _ptr(out),
+                                                      _ptr(lse), _stream(stream)))
 
     def lse_merge(self, part_o, part_lse, n_chunks, out, lse=None, stream=None):
         _check(load().k6attn_lse_merge(self.h, _ptr(part_o), _ptr(part_lse), int(n_chunks), _ptr(out), _ptr(lse),
