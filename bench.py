@@ -159,6 +159,8 @@ class Path:
         self.out = torch.empty((B, S, H, d), dtype=bf, device="cuda")
         self.e2e_head = {k: torch.empty_like(self.seq[k]) for k in self.seq}
         self.e2e_in = [{k: torch.empty_like(self.seq[k]) for k in self.seq} for _ in range(2)]
+        self.e2e_out = [{"out_h": torch.empty_like(self.out_h), "lse": torch.empty_like(self.lse),
+                         "out": torch.empty_like(self.out)} for _ in range(2)]
         self.copy_stream = torch.cuda.Stream()
         self.ws = torch.empty(self.h.workspace_bytes(n_chunks, True), dtype=torch.uint8, device="cuda")
         self.out_host = torch.empty(self.out.shape, dtype=bf).pin_memory()
@@ -211,14 +213,15 @@ class Path:
         """Public API from pinned host buffers, `steps` steps: per step the H2D copy of its
         inputs, relayout, k6attn_forward (rotary + chunks + merge), relayout back and the
         D2H copy of out and lse.  Copies run on their own stream, overlapping the previous
-        and next steps' compute (inputs double-buffered); every copy is inside the timed region."""
+        and next steps' compute (inputs and outputs double-buffered); every copy is inside
+        the timed region."""
         torch, w, K = self.torch, self.w, self.K
         comp = torch.cuda.current_stream()
         copy = self.copy_stream
         ev_in = [torch.cuda.Event() for _ in range(2)]      # inputs of a buffer landed
-        ev_used = [torch.cuda.Event() for _ in range(2)]    # compute done reading a buffer
-        ev_out = torch.cuda.Event()                         # outputs of a step ready
-        ev_read = torch.cuda.Event()                        # previous outputs copied out
+        ev_used = [torch.cuda.Event() for _ in range(2)]    # compute done reading an input buffer
+        ev_out = [torch.cuda.Event() for _ in range(2)]     # outputs of a buffer ready
+        ev_read = [torch.cuda.Event() for _ in range(2)]    # outputs of a buffer copied out
 
         def h2d(step):
             buf = self.e2e_in[step % 2]
@@ -228,28 +231,29 @@ class Path:
                     buf[k].copy_(self.host[k], non_blocking=True)
                 ev_in[step % 2].record(copy)
 
-        for e in ev_used:
+        for e in ev_used + ev_read:
             e.record(comp)
         h2d(0)
         for step in range(steps):
             if step + 1 < steps:
                 h2d(step + 1)
-            buf = self.e2e_in[step % 2]
-            comp.wait_event(ev_in[step % 2])
+            b = step % 2
+            buf, ob = self.e2e_in[b], self.e2e_out[b]
+            comp.wait_event(ev_in[b])
             self.relayout(buf, self.e2e_head)
-            ev_used[step % 2].record(comp)
+            ev_used[b].record(comp)
             hd = self.e2e_head
             jk, jv = (hd["jk"], hd["jv"]) if w.Nj else (None, None)
-            comp.wait_event(ev_read)  # the previous step's outputs have left the device
-            self.h.forward(hd["q"], hd["k"], hd["v"], jk, jv, self.out_h, self.lse, rope=True, n_chunks=self.n,
+            comp.wait_event(ev_read[b])  # this output buffer's previous contents have left the device
+            self.h.forward(hd["q"], hd["k"], hd["v"], jk, jv, ob["out_h"], ob["lse"], rope=True, n_chunks=self.n,
                            workspace=self.ws)
-            K.seq2head_relayout(self.out_h, self.out, w.B, w.S, w.H, w.d, self.P, 1)
-            ev_out.record(comp)
+            K.seq2head_relayout(ob["out_h"], ob["out"], w.B, w.S, w.H, w.d, self.P, 1)
+            ev_out[b].record(comp)
             with torch.cuda.stream(copy):
-                copy.wait_event(ev_out)
-                self.out_host.copy_(self.out, non_blocking=True)
-                self.lse_host.copy_(self.lse, non_blocking=True)
-                ev_read.record(copy)
+                copy.wait_event(ev_out[b])
+                self.out_host.copy_(ob["out"], non_blocking=True)
+                self.lse_host.copy_(ob["lse"], non_blocking=True)
+                ev_read[b].record(copy)
         comp.wait_stream(copy)
 
     def h2d_bytes(self):

@@ -12,7 +12,7 @@
 // is written as bf16; with several, fp32 partials and LSE go to the caller's
 // workspace for the merge kernel.
 //
-// How (one CTA = one work unit = 256 query rows of one (batch, head, chunk)):
+// How (one CTA per work unit = 256 query rows of one (batch, head, chunk)):
 //   warp 8      TMA producer (warps 8-11 form the control warpgroup, which
 //               gives registers to the two softmax warpgroups): Q0/Q1 (2 x 128 rows) once, then K_j, V_j tiles of
 //               128 keys x 128 dims through a 4-slot ring (32 KB per tile, two
@@ -20,8 +20,9 @@
 //   warp 9      MMA issuer (one thread): S_i = Q_i K_j^T (SS, K-major) into
 //               TMEM, then O_i += P_i V_j with P_i read from TMEM (TS) and V
 //               MN-major from shared memory.  Order per K/V tile:
-//               PV0(j), S0(j+1), PV1(j), S1(j+1), so each softmax group has a
-//               full P.V + S of the other group to hide behind.
+//               PV0(j), then S0(j+1) and PV1(j) interleaved MMA by MMA (two
+//               independent accumulator chains), then S1(j+1); each softmax
+//               group has the other group's work to hide behind.
 //   warps 0-3   softmax of Q tile 0, warps 4-7 of Q tile 1: one thread per
 //               query row (its TMEM lane); online softmax in base 2 with the
 //               scale folded in; the running max is only moved (and O
@@ -135,11 +136,11 @@ __device__ __forceinline__ Unit decode_unit(const TcParams &p, long u) {
     return r;
 }
 
-// Persistent: each CTA takes units blockIdx.x, blockIdx.x + gridDim.x, ...
-// The K/V ring, the barrier phases and tensor memory carry over from one unit
-// to the next; the next unit's Q is loaded as soon as the last Q.K^T of the
-// current one has read Q (q_empty), so it overlaps the last P.V products and
-// the epilogue.
+// Each CTA takes units blockIdx.x, blockIdx.x + gridDim.x, ... (launched with
+// one CTA per unit, so normally one).  When a CTA does take several, the K/V
+// ring, the barrier phases and tensor memory carry over from one unit to the
+// next, and the next unit's Q loads as soon as the current one's last Q.K^T
+// has read Q (q_empty).
 // BOUNDED: constant-max softmax.  Each row's running max is replaced by the
 // precomputed bound p.row_bound (>= every logit of the row), so the softmax
 // takes no row maximum and never rescales O; a row whose every term
@@ -296,38 +297,60 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                 if (!ok) break;
                 tc_commit(&kv_empty[kv_idx % NSTAGE]);
                 if (T == 1) tc_commit(q_empty);
+                // Per K/V tile j: P0.V(j); then S0(j+1) interleaved MMA by MMA with
+                // P1.V(j), two independent accumulator chains for the tensor pipe;
+                // then S1(j+1).  S_i(j+1) always follows P_i.V(j), whose P it overwrites.
                 for (int j = 0; j < T && ok; j++) {
                     const uint32_t vidx = kv_idx + 2 * j + 1, kidx = vidx + 1;
                     const uint32_t vs = vidx % NSTAGE, ks = kidx % NSTAGE;
                     const bool more = j + 1 < T;
-                    ok = mbar_wait(&kv_full[vs], (vidx / NSTAGE) & 1, w);
-                    for (int i = 0; i < NQ && ok; i++) {
-                        // P.V of Q tile i for K/V tile j (the first 64 keys as soon as
-                        // their P is in tensor memory), then S_i(j+1)
-                        if (!(ok = mbar_wait(&p_half[i], (tile + j) & 1, w))) break;
+                    const uint32_t ph = (tile + j) & 1;
+                    ok = mbar_wait(&kv_full[vs], (vidx / NSTAGE) & 1, w) && mbar_wait(&p_half[0], ph, w);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv(0, vs, j > 0, 0, BN / 32);
+                    if (!(ok = mbar_wait(&p_full[0], ph, w))) break;
+                    tc_fence_after();
+                    issue_pv(0, vs, true, BN / 32, BN / 16);
+                    started = true;
+                    if (!more) {
+                        tc_commit(&o_final[0]);
+                        if (!(ok = mbar_wait(&p_half[1], ph, w))) break;
                         tc_fence_after();
-                        issue_pv(i, vs, j > 0, 0, BN / 32);
-                        if (!(ok = mbar_wait(&p_full[i], (tile + j) & 1, w))) break;
+                        issue_pv(1, vs, j > 0, 0, BN / 32);
+                        if (!(ok = mbar_wait(&p_full[1], ph, w))) break;
                         tc_fence_after();
-                        issue_pv(i, vs, true, BN / 32, BN / 16);
-                        started = true;
-                        if (i == NQ - 1) tc_commit(&kv_empty[vs]);
-                        if (!more) {
-                            tc_commit(&o_final[i]);
-                            continue;
-                        }
-                        if (!(ok = strict_wait(i))) break;
-                        if (i == 0) {
-                            if (!(ok = mbar_wait(&kv_full[ks], (kidx / NSTAGE) & 1, w))) break;
-                            tc_fence_after();
-                        }
-                        issue_s(i, ks);
-                        tc_commit(&s_full[i]);
-                        if (i == NQ - 1) {
-                            tc_commit(&kv_empty[ks]);
-                            if (j + 2 == T) tc_commit(q_empty);  // the unit's last Q.K^T has been issued
+                        issue_pv(1, vs, true, BN / 32, BN / 16);
+                        tc_commit(&kv_empty[vs]);
+                        tc_commit(&o_final[1]);
+                        continue;
+                    }
+                    if (!(ok = strict_wait(0))) break;
+                    if (!(ok = mbar_wait(&kv_full[ks], (kidx / NSTAGE) & 1, w) && mbar_wait(&p_half[1], ph, w))) break;
+                    tc_fence_after();
+                    {
+                        const uint64_t kb = dq0 + ((uint64_t)(SMEM_KV - SMEM_Q + ks * TILE) >> 4);
+                        const uint64_t vb = dv0 + ((uint64_t)(vs * TILE) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; kk++) {
+                            const uint64_t off = (uint64_t)((kk >> 2) * PANEL + (kk & 3) * 32) >> 4;
+                            mma_ss(tmem, dq0 + off, kb + off, idesc_qk, kk > 0);  // S0(j+1)
+                            if (kk == BN / 32) {
+                                if (!(ok = mbar_wait(&p_full[1], ph, w))) break;
+                                tc_fence_after();
+                            }
+                            mma_ts(tmem + 2 * BN + D, tmem + BN + kk * 8, vb + ((uint64_t)(kk * 16 * 128) >> 4),
+                                   idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);  // P1.V(j)
                         }
                     }
+                    if (!ok) break;
+                    tc_commit(&s_full[0]);
+                    tc_commit(&kv_empty[vs]);
+                    if (!(ok = strict_wait(1))) break;
+                    issue_s(1, ks);
+                    tc_commit(&s_full[1]);
+                    tc_commit(&kv_empty[ks]);
+                    if (j + 2 == T) tc_commit(q_empty);  // the unit's last Q.K^T has been issued
                 }
                 kv_idx += 2 * T;
                 tile += T;
@@ -583,7 +606,12 @@ cudaError_t launch_attn_tc(const Geom &g, const void *q, const void *k, const vo
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const long grid = p.units < sms ? p.units : sms;  // persistent: one CTA per SM
+    // One CTA per unit: the block scheduler hands each freed SM the next unit,
+    // which keeps the units in flight (and their K/V in L2) in a tight window;
+    // measured faster than a static persistent round-robin.  The kernel loops
+    // over units, so a smaller grid would also be correct.
+    (void)sms;
+    const long grid = p.units;
     p.row_bound = opt.row_bound;
     if (opt.row_bound)
         attn_tc_kernel<true><<<(unsigned)grid, tc::THREADS, tc::SMEM_ALLOC, st>>>(mq, mk, mv, mjk, mjv, p);
