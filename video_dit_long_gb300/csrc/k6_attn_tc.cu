@@ -56,14 +56,14 @@ constexpr int TILE = 2 * PANEL;               // 32 KB
 constexpr int SMEM_Q = 0;
 constexpr int SMEM_KV = NQ * TILE;
 constexpr int SMEM_BAR = SMEM_KV + NSTAGE * TILE;
-constexpr int NBAR = 2 + 2 * NSTAGE + 4 * NQ + NQ + 1;  // q_full/empty, kv_full/empty, s/p_half/p/o_final, o_step, drain
+constexpr int NBAR = 1 + 2 * NSTAGE + 4 * NQ + NQ + 1;  // q_full, kv_full/empty, s/p_half/p/o_final, o_step, drain
 constexpr int SMEM_TOTAL = SMEM_BAR + NBAR * 8 + 16;
 constexpr int SMEM_ALLOC = SMEM_TOTAL + 1024;  // room to align the base to 1024 bytes
 constexpr int THREADS = 384;                  // 3 warpgroups: softmax 0, softmax 1, producer/MMA/spare
-// Register split (launch: 384 x 168 = 64512): softmax groups grow to 200,
-// the producer/MMA group shrinks to 104: 2*128*200 + 128*104 = 64512.
-constexpr int REGS_SOFTMAX = 200;
-constexpr int REGS_CONTROL = 104;
+// Register split (launch: 384 x 168 = 64512): softmax groups grow to 184,
+// the producer/MMA group shrinks to 136: 2*128*184 + 128*136 = 64512.
+constexpr int REGS_SOFTMAX = 184;
+constexpr int REGS_CONTROL = 136;
 constexpr int TMEM_COLS = 512;
 constexpr float RESCALE_THRESHOLD = 8.0f;     // log2 units: rescale when the max grows past 2^8
 constexpr unsigned long long DRAIN_NS = 1000000000ull;
@@ -83,6 +83,7 @@ struct TcParams {
     int strict_order;
     uint32_t idesc_qk;                        // instruction descriptor of Q.K^T (bf16 or fp16 operands)
     long units;                               // B * H * n_chunks * q_pairs work units
+    int group;                                // chunks per CTA, sharing one load of Q (divides n_chunks)
     const float *row_bound;                   // constant-max softmax: bound per query row [B][H][Sq], or null
 };
 
@@ -119,28 +120,34 @@ __device__ __forceinline__ TileRange chunk_tiles(const TcParams &p, int c) {
     return t;
 }
 
-// Work unit u -> (b, h, chunk, query-tile pair), pairs fastest, so that the
-// CTAs working at the same time share one chunk's K/V in L2.
+// Work unit u -> (b, h, chunk group, query-tile pair, chunk within the group),
+// the chunk within the group fastest: CTA x owns units [x*group, (x+1)*group),
+// one Q tile pair over `group` consecutive chunks.  Across CTAs the query-tile
+// pair varies fastest, so the CTAs running at the same time walk through the
+// same chunks and share their K/V in L2.
 struct Unit {
     int b, h, c, q0;
 };
 __device__ __forceinline__ Unit decode_unit(const TcParams &p, long u) {
     Unit r;
+    const int g = (int)(u % p.group);
+    u /= p.group;
     const int qp = (int)(u % p.q_pairs);
     u /= p.q_pairs;
-    r.c = (int)(u % p.n_chunks);
-    u /= p.n_chunks;
+    const int groups = p.n_chunks / p.group;
+    const int cg = (int)(u % groups);
+    u /= groups;
+    r.c = cg * p.group + g;
     r.h = (int)(u % p.H);
     r.b = (int)(u / p.H);
     r.q0 = qp * (tc::NQ * tc::BM);
     return r;
 }
 
-// Each CTA takes units blockIdx.x, blockIdx.x + gridDim.x, ... (launched with
-// one CTA per unit, so normally one).  When a CTA does take several, the K/V
-// ring, the barrier phases and tensor memory carry over from one unit to the
-// next, and the next unit's Q loads as soon as the current one's last Q.K^T
-// has read Q (q_empty).
+// Each CTA loads its Q tile pair once and runs its chunks one after another;
+// the K/V ring, the barrier phases and tensor memory carry over from one chunk
+// to the next, so the next chunk's first Q.K^T overlaps the previous chunk's
+// last P.V and epilogue.
 // BOUNDED: constant-max softmax.  Each row's running max is replaced by the
 // precomputed bound p.row_bound (>= every logit of the row), so the softmax
 // takes no row maximum and never rescales O; a row whose every term
@@ -155,8 +162,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SMEM_BAR);
     uint64_t *q_full = bars;
-    uint64_t *q_empty = q_full + 1;
-    uint64_t *kv_full = q_empty + 1;
+    uint64_t *kv_full = q_full + 1;
     uint64_t *kv_empty = kv_full + NSTAGE;
     uint64_t *s_full = kv_empty + NSTAGE;
     uint64_t *p_half = s_full + NQ;
@@ -171,7 +177,6 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        mbar_init(q_empty, 1);
         for (int s = 0; s < NSTAGE; s++) {
             mbar_init(&kv_full[s], 1);
             mbar_init(&kv_empty[s], 1);
@@ -209,19 +214,17 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
             uint32_t kv_idx = 0;  // K/V tile loads issued so far (K_j, V_j alternate)
             uint32_t uc = 0;      // units started by this CTA
             bool ok = true;
-            for (long u = blockIdx.x; u < p.units && ok; u += gridDim.x, uc++) {
+            const long u0 = (long)blockIdx.x * p.group, u1 = u0 + p.group;
+            for (long u = u0; u < u1 && ok; u++, uc++) {
                 const Unit un = decode_unit(p, u);
                 const TileRange tr = chunk_tiles(p, un.c);
-                // Q of this unit once the previous unit's last Q.K^T has read Q
-                if (!mbar_wait(q_empty, (uc & 1) ^ 1, w)) {
-                    ok = false;
-                    break;
+                if (uc == 0) {  // the CTA's Q tile pair, once
+                    mbar_arrive_expect_tx(q_full, NQ * TILE);
+                    for (int i = 0; i < NQ; i++)
+                        for (int half = 0; half < 2; half++)
+                            tma_load_4d(smem + SMEM_Q + i * TILE + half * PANEL, &tm_q, q_full, half * 64, un.h,
+                                        un.q0 + i * BM, un.b);
                 }
-                mbar_arrive_expect_tx(q_full, NQ * TILE);
-                for (int i = 0; i < NQ; i++)
-                    for (int half = 0; half < 2; half++)
-                        tma_load_4d(smem + SMEM_Q + i * TILE + half * PANEL, &tm_q, q_full, half * 64, un.h,
-                                    un.q0 + i * BM, un.b);
                 for (int j = 0; j < tr.T && ok; j++) {
                     int map, row, valid;
                     tr.at(j, map, row, valid);
@@ -240,7 +243,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                 }
             }
             // let every copy issued into shared memory land before the CTA can exit
-            if (uc > 0) mbar_drain(q_full, (uc - 1) & 1, DRAIN_NS);
+            if (uc > 0) mbar_drain(q_full, 0, DRAIN_NS);
             for (uint32_t idx = kv_idx > NSTAGE ? kv_idx - NSTAGE : 0; idx < kv_idx; idx++)
                 mbar_drain(&kv_full[idx % NSTAGE], (idx / NSTAGE) & 1, DRAIN_NS);
         } else if (warp == 9 && lane == 0) {
@@ -283,10 +286,12 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
             uint32_t uc = 0;
             bool started = false;  // any P.V issued yet (the strict hazard exists from then on)
             bool ok = true;
-            for (long u = blockIdx.x; u < p.units && ok; u += gridDim.x, uc++) {
+            const long u0 = (long)blockIdx.x * p.group, u1 = u0 + p.group;
+            for (long u = u0; u < u1 && ok; u++, uc++) {
                 const Unit un = decode_unit(p, u);
                 const int T = chunk_tiles(p, un.c).T;
-                ok = mbar_wait(q_full, uc & 1, w) && mbar_wait(&kv_full[kv_idx % NSTAGE], (kv_idx / NSTAGE) & 1, w);
+                ok = (uc > 0 || mbar_wait(q_full, 0, w)) &&
+                     mbar_wait(&kv_full[kv_idx % NSTAGE], (kv_idx / NSTAGE) & 1, w);
                 if (!ok) break;
                 tc_fence_after();
                 for (int i = 0; i < NQ && ok; i++) {
@@ -296,7 +301,6 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                 }
                 if (!ok) break;
                 tc_commit(&kv_empty[kv_idx % NSTAGE]);
-                if (T == 1) tc_commit(q_empty);
                 // Per K/V tile j: P0.V(j); then S0(j+1) interleaved MMA by MMA with
                 // P1.V(j), two independent accumulator chains for the tensor pipe;
                 // then S1(j+1).  S_i(j+1) always follows P_i.V(j), whose P it overwrites.
@@ -350,7 +354,6 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                     issue_s(1, ks);
                     tc_commit(&s_full[1]);
                     tc_commit(&kv_empty[ks]);
-                    if (j + 2 == T) tc_commit(q_empty);  // the unit's last Q.K^T has been issued
                 }
                 kv_idx += 2 * T;
                 tile += T;
@@ -371,7 +374,8 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
         const float sl2 = p.scale_log2;
         uint32_t tile = 0, uc = 0;
         bool ok = true;
-        for (long u = blockIdx.x; u < p.units && ok; u += gridDim.x, uc++) {
+        const long u0 = (long)blockIdx.x * p.group, u1 = u0 + p.group;
+        for (long u = u0; u < u1 && ok; u++, uc++) {
             const Unit un = decode_unit(p, u);
             const TileRange tr = chunk_tiles(p, un.c);
             const int T = tr.T;
@@ -393,6 +397,8 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                 for (int cc = 0; cc < BN / 32; cc++)
                     tmem_ld32(tS + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[cc * 32]));
                 tmem_ld_wait();
+                bool rescale = false;  // warp-uniform
+                float alpha = 1.f;
                 if (valid < BN) {  // ragged tile end (warp-uniform): keys past the segment get -inf
 #pragma unroll
                     for (int k = 0; k < BN; k++)
@@ -415,21 +421,13 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                 if (j == 0) m_run = mt;
                 else need = mt > m_run + RESCALE_THRESHOLD;
                 if (__any_sync(0xffffffffu, need)) {
-                    // O_i already holds P.V of tiles < j: S_i(j) was committed after it
-                    float alpha = 1.f;
+                    // O_i holds P.V of tiles < j (S_i(j) was committed after it); it is
+                    // rescaled below, after the first half of P is stored, before P.V(j)
+                    rescale = true;
                     if (need) {
                         alpha = ex2(m_run - mt);
                         m_run = mt;
                         l_run *= alpha;
-                    }
-#pragma unroll
-                    for (int cc = 0; cc < D / 32; cc++) {
-                        uint32_t o[32];
-                        tmem_ld32(tO + cc * 32, o);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int k = 0; k < 32; k++) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-                        tmem_st32(tO + cc * 32, o);
                     }
                 }
                 }
@@ -452,6 +450,17 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                         acc[(k / 2) & 3] = fadd2(acc[(k / 2) & 3], f2(p0, p1));
                     }
                     tmem_st32(tS + half * 32, pk);
+                    if (!BOUNDED && half == 0 && rescale) {
+#pragma unroll
+                        for (int cc = 0; cc < D / 32; cc++) {
+                            uint32_t o[32];
+                            tmem_ld32(tO + cc * 32, o);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int k = 0; k < 32; k++) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                            tmem_st32(tO + cc * 32, o);
+                        }
+                    }
                     tmem_st_wait();
                     tc_fence_before();
                     mbar_arrive(half == 0 ? &p_half[i] : &p_full[i]);
@@ -603,15 +612,22 @@ cudaError_t launch_attn_tc(const Geom &g, const void *q, const void *k, const vo
                             : idesc_bf16_f32(tc::BM, tc::BN, false);
     p.units = (long)g.B * g.H * n_chunks * p.q_pairs;
     if (p.units == 0) return cudaSuccess;
+    // chunks per CTA: the largest divisor of n_chunks up to 4
+    p.group = 1;
+    for (int gsz = 4; gsz > 1; gsz--)
+        if (n_chunks % gsz == 0) {
+            p.group = gsz;
+            break;
+        }
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    // One CTA per unit: the block scheduler hands each freed SM the next unit,
-    // which keeps the units in flight (and their K/V in L2) in a tight window;
-    // measured faster than a static persistent round-robin.  The kernel loops
-    // over units, so a smaller grid would also be correct.
+    // One CTA per Q tile pair and chunk group: the block scheduler hands each
+    // freed SM the next CTA, which keeps the CTAs in flight (and their K/V in
+    // L2) in a tight window; measured faster than a static persistent
+    // round-robin over SMs.
     (void)sms;
-    const long grid = p.units;
+    const long grid = p.units / p.group;
     p.row_bound = opt.row_bound;
     if (opt.row_bound)
         attn_tc_kernel<true><<<(unsigned)grid, tc::THREADS, tc::SMEM_ALLOC, st>>>(mq, mk, mv, mjk, mjv, p);
