@@ -56,7 +56,11 @@ constexpr int TILE = 2 * PANEL;               // 32 KB
 constexpr int SMEM_Q = 0;
 constexpr int SMEM_KV = NQ * TILE;
 constexpr int SMEM_BAR = SMEM_KV + NSTAGE * TILE;
-constexpr int NBAR = 1 + 2 * NSTAGE + 4 * NQ + NQ + 1;  // q_full, kv_full/empty, s/p_half/p/o_final, o_step, drain
+constexpr int P_PARTS = 2;                    // P of a tile is published in this many parts
+constexpr int KP = BN / P_PARTS;              // keys per part
+constexpr int MMA_PER_PART = KP / 16;         // P.V MMAs (K = 16 keys each) per part
+constexpr int NBAR = 1 + 2 * NSTAGE + NQ + NQ * P_PARTS + NQ + NQ + 1;  // q_full, kv_full/empty, s_full,
+                                                                       // p parts, o_final, o_step, drain
 constexpr int SMEM_TOTAL = SMEM_BAR + NBAR * 8 + 16;
 constexpr int SMEM_ALLOC = SMEM_TOTAL + 1024;  // room to align the base to 1024 bytes
 constexpr int THREADS = 384;                  // 3 warpgroups: softmax 0, softmax 1, producer/MMA/spare
@@ -165,9 +169,8 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
     uint64_t *kv_full = q_full + 1;
     uint64_t *kv_empty = kv_full + NSTAGE;
     uint64_t *s_full = kv_empty + NSTAGE;
-    uint64_t *p_half = s_full + NQ;
-    uint64_t *p_full = p_half + NQ;
-    uint64_t *o_final = p_full + NQ;
+    uint64_t *p_part = s_full + NQ;  // [NQ][P_PARTS]
+    uint64_t *o_final = p_part + NQ * P_PARTS;
     uint64_t *o_step = o_final + NQ;
     uint64_t *drain = o_step + NQ;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
@@ -183,8 +186,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
         }
         for (int i = 0; i < NQ; i++) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&p_half[i], BM);
-            mbar_init(&p_full[i], BM);
+            for (int q = 0; q < P_PARTS; q++) mbar_init(&p_part[i * P_PARTS + q], BM);
             mbar_init(&o_final[i], 1);
             mbar_init(&o_step[i], 1);
         }
@@ -282,7 +284,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                 return done;
             };
             uint32_t kv_idx = 0;  // K/V tiles consumed (K_j, V_j alternate)
-            uint32_t tile = 0;    // K/V tiles finished over all units: phase of s_full / p_full
+            uint32_t tile = 0;    // K/V tiles finished over all units: phase of s_full / p_part
             uint32_t uc = 0;
             bool started = false;  // any P.V issued yet (the strict hazard exists from then on)
             bool ok = true;
@@ -309,28 +311,26 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                     const uint32_t vs = vidx % NSTAGE, ks = kidx % NSTAGE;
                     const bool more = j + 1 < T;
                     const uint32_t ph = (tile + j) & 1;
-                    ok = mbar_wait(&kv_full[vs], (vidx / NSTAGE) & 1, w) && mbar_wait(&p_half[0], ph, w);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_pv(0, vs, j > 0, 0, BN / 32);
-                    if (!(ok = mbar_wait(&p_full[0], ph, w))) break;
-                    tc_fence_after();
-                    issue_pv(0, vs, true, BN / 32, BN / 16);
+                    // P_i.V(j), part by part as the softmax publishes P
+                    auto pv_parts = [&](int i) -> bool {
+                        for (int q = 0; q < P_PARTS; q++) {
+                            if (!mbar_wait(&p_part[i * P_PARTS + q], ph, w)) return false;
+                            tc_fence_after();
+                            issue_pv(i, vs, j > 0 || q > 0, q * MMA_PER_PART, (q + 1) * MMA_PER_PART);
+                        }
+                        return true;
+                    };
+                    if (!(ok = mbar_wait(&kv_full[vs], (vidx / NSTAGE) & 1, w) && pv_parts(0))) break;
                     started = true;
                     if (!more) {
                         tc_commit(&o_final[0]);
-                        if (!(ok = mbar_wait(&p_half[1], ph, w))) break;
-                        tc_fence_after();
-                        issue_pv(1, vs, j > 0, 0, BN / 32);
-                        if (!(ok = mbar_wait(&p_full[1], ph, w))) break;
-                        tc_fence_after();
-                        issue_pv(1, vs, true, BN / 32, BN / 16);
+                        if (!(ok = pv_parts(1))) break;
                         tc_commit(&kv_empty[vs]);
                         tc_commit(&o_final[1]);
                         continue;
                     }
                     if (!(ok = strict_wait(0))) break;
-                    if (!(ok = mbar_wait(&kv_full[ks], (kidx / NSTAGE) & 1, w) && mbar_wait(&p_half[1], ph, w))) break;
+                    if (!(ok = mbar_wait(&kv_full[ks], (kidx / NSTAGE) & 1, w))) break;
                     tc_fence_after();
                     {
                         const uint64_t kb = dq0 + ((uint64_t)(SMEM_KV - SMEM_Q + ks * TILE) >> 4);
@@ -339,8 +339,8 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                         for (int kk = 0; kk < D / 16; kk++) {
                             const uint64_t off = (uint64_t)((kk >> 2) * PANEL + (kk & 3) * 32) >> 4;
                             mma_ss(tmem, dq0 + off, kb + off, idesc_qk, kk > 0);  // S0(j+1)
-                            if (kk == BN / 32) {
-                                if (!(ok = mbar_wait(&p_full[1], ph, w))) break;
+                            if (kk % MMA_PER_PART == 0) {
+                                if (!(ok = mbar_wait(&p_part[P_PARTS + kk / MMA_PER_PART], ph, w))) break;
                                 tc_fence_after();
                             }
                             mma_ts(tmem + 2 * BN + D, tmem + BN + kk * 8, vb + ((uint64_t)(kk * 16 * 128) >> 4),
@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                 else need = mt > m_run + RESCALE_THRESHOLD;
                 if (__any_sync(0xffffffffu, need)) {
                     // O_i holds P.V of tiles < j (S_i(j) was committed after it); it is
-                    // rescaled below, after the first half of P is stored, before P.V(j)
+                    // rescaled below, after the first part of P is stored, before P.V(j)
                     rescale = true;
                     if (need) {
                         alpha = ex2(m_run - mt);
@@ -432,16 +432,16 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                 }
                 }
                 // p = 2^(s * scale*log2e - m): packed FMA, then the SFU; row sum on
-                // packed adds.  The first 64 keys' P is published on its own so
-                // that the first half of P.V can start while the rest is computed.
+                // packed adds.  P is published in parts so that P.V can start on
+                // the first keys while the rest is computed.
                 const uint64_t scale2 = f2(sl2, sl2), negm2 = f2(-m_run, -m_run);
                 uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-                for (int half = 0; half < 2; half++) {
-                    uint32_t pk[BN / 4];
+                for (int q = 0; q < P_PARTS; q++) {
+                    uint32_t pk[KP / 2];
 #pragma unroll
-                    for (int k = 0; k < BN / 2; k += 2) {
-                        const int kk = half * (BN / 2) + k;
+                    for (int k = 0; k < KP; k += 2) {
+                        const int kk = q * KP + k;
                         float a, b2;
                         f2_split(ffma2(f2(__uint_as_float(s[kk]), __uint_as_float(s[kk + 1])), scale2, negm2), a,
                                  b2);
@@ -449,8 +449,8 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                         pk[k / 2] = pack_bf16x2(p0, p1);
                         acc[(k / 2) & 3] = fadd2(acc[(k / 2) & 3], f2(p0, p1));
                     }
-                    tmem_st32(tS + half * 32, pk);
-                    if (!BOUNDED && half == 0 && rescale) {
+                    tmem_st_cols<KP / 2>(tS + q * (KP / 2), pk);
+                    if (!BOUNDED && q == 0 && rescale) {
 #pragma unroll
                         for (int cc = 0; cc < D / 32; cc++) {
                             uint32_t o[32];
@@ -463,7 +463,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                     }
                     tmem_st_wait();
                     tc_fence_before();
-                    mbar_arrive(half == 0 ? &p_half[i] : &p_full[i]);
+                    mbar_arrive(&p_part[i * P_PARTS + q]);
                 }
                 float sum;
                 {
