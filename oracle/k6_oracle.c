@@ -72,6 +72,13 @@
 
 enum { K6O_F32 = 0, K6O_BF16 = 1, K6O_F64 = 2 };
 
+/* K6O_MUTANT plants one deliberate mistake, for the test that checks the pins
+ * catch it (tests/test_oracle_mutants.py builds these variants separately).
+ * 0 (the default) is the oracle itself. */
+#ifndef K6O_MUTANT
+#define K6O_MUTANT 0
+#endif
+
 typedef struct {
     int B, H, d;
     long Nv, Nj;              /* video tokens, joint tokens */
@@ -124,7 +131,11 @@ static int geom_ok(const k6o_geom *g) {
 static void rotate_pair(double *x, int i, double angle) {
     double c = cos(angle), s = sin(angle);
     double a = x[2 * i], b = x[2 * i + 1];
+#if K6O_MUTANT == 1
+    x[2 * i] = a * c + b * s; /* planted: wrong sign */
+#else
     x[2 * i] = a * c - b * s;
+#endif
     x[2 * i + 1] = a * s + b * c;
 }
 
@@ -133,14 +144,23 @@ void k6o_rope_vec(const k6o_geom *g, long n, double *x) {
     if (n < g->Nv) {
         long hw = (long)g->grid_h * g->grid_w;
         long pos[3];
+#if K6O_MUTANT == 3
+        pos[1] = n / hw;               /* planted: t and h swapped */
+        pos[0] = (n / g->grid_w) % g->grid_h;
+#else
         pos[0] = n / hw;               /* t */
         pos[1] = (n / g->grid_w) % g->grid_h; /* h */
+#endif
         pos[2] = n % g->grid_w;        /* w */
         int off = 0;                   /* first dim owned by the axis */
         for (int a = 0; a < 3; a++) {
             int da = g->axis_dim[a];
             for (int i = 0; i < da / 2; i++) {
+#if K6O_MUTANT == 2
+                double omega = pow(g->theta, -1.0 * i / da); /* planted: dropped factor 2 */
+#else
                 double omega = pow(g->theta, -2.0 * i / da);
+#endif
                 rotate_pair(x + off, i, (double)pos[a] * omega);
             }
             off += da;
@@ -248,7 +268,11 @@ static const void *kv_ptr(const k6o_geom *g, long n, int b, int h, const void *v
         return video;
     }
     *off = (((size_t)b * g->Nj + (n - g->Nv)) * g->H + h) * g->d;
+#if K6O_MUTANT == 8
+    return video; /* planted: joint rows read from the video tensor */
+#else
     return joint;
+#endif
 }
 
 /*
@@ -271,7 +295,11 @@ int k6o_attention(const k6o_geom *g, int rope, const void *q, const void *k, con
         if (rows[r] < 0 || rows[r] >= S) return -3;
     int d = g->d, H = g->H;
     long L = kv_end - kv_begin;
+#if K6O_MUTANT == 4
+    double scale = 1.0 / (double)d; /* planted: 1/d */
+#else
     double scale = 1.0 / sqrt((double)d);
+#endif
     double *kr = (double *)malloc(sizeof(double) * (size_t)L * d);
     double *vr = (double *)malloc(sizeof(double) * (size_t)L * d);
     if (!kr || !vr) { free(kr); free(vr); return -4; }
@@ -311,7 +339,11 @@ int k6o_attention(const k6o_geom *g, int rope, const void *q, const void *k, con
                     }
                     double sum = 0.0;
                     for (long j = 0; j < L; j++) sum += exp(s[j] - m);
+#if K6O_MUTANT == 7
+                    double lse_i = log(sum); /* planted: dropped the max */
+#else
                     double lse_i = m + log(sum);
+#endif
                     double *o = out + (((size_t)b * nrows + r) * H + h) * d;
                     for (int e = 0; e < d; e++) o[e] = 0.0;
                     for (long j = 0; j < L; j++) {
@@ -413,7 +445,11 @@ int k6o_lse_merge(int n, int B, long Sq, int H, int d, const void *part_o, const
         double *o = out + (size_t)r * d;
         for (int e = 0; e < d; e++) o[e] = 0.0;
         for (int c = 0; c < n; c++) {
+#if K6O_MUTANT == 5
+            double w = exp(load_elem(part_lse, type, c * l_stride + li) - M); /* planted: max, not LSE */
+#else
             double w = exp(load_elem(part_lse, type, c * l_stride + li) - L);
+#endif
             for (int e = 0; e < d; e++)
                 o[e] += w * load_elem(part_o, type, c * o_stride + (size_t)r * d + e);
         }
@@ -441,7 +477,11 @@ int k6o_relayout(const void *src, void *dst, int B, long S, int H, int d, int el
                 for (long s = 0; s < Sl; s++)
                     for (int hh = 0; hh < Hl; hh++)
                         for (int e = 0; e < d; e++) {
+#if K6O_MUTANT == 6
+                            size_t seq_i = ((((size_t)p * B + b) * Sl + s) * H + (size_t)r * Hl + hh) * d + e; /* planted */
+#else
                             size_t seq_i = ((((size_t)r * B + b) * Sl + s) * H + (size_t)p * Hl + hh) * d + e;
+#endif
                             size_t head_i = ((((size_t)p * B + b) * S + (size_t)r * Sl + s) * Hl + hh) * d + e;
                             if (direction == 0)
                                 memcpy(dp + head_i * elem_bytes, sp + seq_i * elem_bytes, elem_bytes);

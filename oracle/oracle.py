@@ -25,15 +25,19 @@ _LIB_PATH = os.path.join(_BUILD, "libk6oracle.so")
 F32, BF16, F64 = 0, 1, 2
 
 
-def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (-O2, OpenMP, no fast-math)."""
+def build(force: bool = False, mutant: int = 0) -> str:
+    """Compile the oracle with gcc (-O2, OpenMP, no fast-math).
+
+    mutant > 0 builds a copy with one planted mistake (see K6O_MUTANT in the
+    source), used only by the test that checks the pins catch it."""
     os.makedirs(_BUILD, exist_ok=True)
-    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
-        tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.run(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"],
-                       check=True)
-        os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+    path = _LIB_PATH if mutant == 0 else os.path.join(_BUILD, f"libk6oracle_mutant{mutant}.so")
+    if force or not os.path.exists(path) or os.path.getmtime(path) < os.path.getmtime(_SRC):
+        tmp = path + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", f"-DK6O_MUTANT={int(mutant)}",
+                        "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, path)
+    return path
 
 
 class _Geom(ctypes.Structure):
@@ -76,27 +80,38 @@ _lib = None
 def lib():
     global _lib
     if _lib is None:
-        _lib = ctypes.CDLL(build())
-        P = ctypes.c_void_p
-        _lib.k6o_rope.argtypes = [ctypes.POINTER(_Geom), P, ctypes.c_int, P]
-        _lib.k6o_rope_vec.argtypes = [ctypes.POINTER(_Geom), ctypes.c_long, P]
-        _lib.k6o_rope_vec.restype = None
-        _lib.k6o_attention.argtypes = [ctypes.POINTER(_Geom), ctypes.c_int, P, P, P, P, P, ctypes.c_int,
-                                       ctypes.c_long, ctypes.c_long, P, ctypes.c_long, P, P]
-        _lib.k6o_cross_attention.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_long,
-                                             ctypes.c_long, P, P, P, ctypes.c_int, ctypes.c_long, ctypes.c_long, P, P]
-        _lib.k6o_row_bounds.argtypes = [ctypes.POINTER(_Geom), ctypes.c_int, P, P, P, ctypes.c_int, P]
-        _lib.k6o_rms_norm.argtypes = [P, ctypes.c_int, ctypes.c_long, ctypes.c_long, P, ctypes.c_double, P]
-        _lib.k6o_lse_merge.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_long, ctypes.c_int, ctypes.c_int,
-                                       P, P, ctypes.c_int, P, P]
-        _lib.k6o_relayout.argtypes = [P, P, ctypes.c_int, ctypes.c_long, ctypes.c_int, ctypes.c_int,
-                                      ctypes.c_int, ctypes.c_int, ctypes.c_int]
-        _lib.k6o_latent_grid.argtypes = [ctypes.c_int] * 3 + [ctypes.POINTER(ctypes.c_int)] * 3
-        _lib.k6o_latent_grid.restype = None
-        _lib.k6o_num_threads.restype = ctypes.c_int
-        _lib.k6o_set_num_threads.argtypes = [ctypes.c_int]
-        _lib.k6o_set_num_threads.restype = None
+        _lib = _declare(ctypes.CDLL(build()))
     return _lib
+
+
+def use_mutant(mutant: int):
+    """Point this module at a planted-mistake build (0 restores the oracle)."""
+    global _lib
+    _lib = _declare(ctypes.CDLL(build(mutant=mutant)))
+
+
+def _declare(L):
+    """Declare the argument and result types of every oracle entry point."""
+    P = ctypes.c_void_p
+    L.k6o_rope.argtypes = [ctypes.POINTER(_Geom), P, ctypes.c_int, P]
+    L.k6o_rope_vec.argtypes = [ctypes.POINTER(_Geom), ctypes.c_long, P]
+    L.k6o_rope_vec.restype = None
+    L.k6o_attention.argtypes = [ctypes.POINTER(_Geom), ctypes.c_int, P, P, P, P, P, ctypes.c_int,
+                                   ctypes.c_long, ctypes.c_long, P, ctypes.c_long, P, P]
+    L.k6o_cross_attention.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_long,
+                                         ctypes.c_long, P, P, P, ctypes.c_int, ctypes.c_long, ctypes.c_long, P, P]
+    L.k6o_row_bounds.argtypes = [ctypes.POINTER(_Geom), ctypes.c_int, P, P, P, ctypes.c_int, P]
+    L.k6o_rms_norm.argtypes = [P, ctypes.c_int, ctypes.c_long, ctypes.c_long, P, ctypes.c_double, P]
+    L.k6o_lse_merge.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_long, ctypes.c_int, ctypes.c_int,
+                                   P, P, ctypes.c_int, P, P]
+    L.k6o_relayout.argtypes = [P, P, ctypes.c_int, ctypes.c_long, ctypes.c_int, ctypes.c_int,
+                                  ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    L.k6o_latent_grid.argtypes = [ctypes.c_int] * 3 + [ctypes.POINTER(ctypes.c_int)] * 3
+    L.k6o_latent_grid.restype = None
+    L.k6o_num_threads.restype = ctypes.c_int
+    L.k6o_set_num_threads.argtypes = [ctypes.c_int]
+    L.k6o_set_num_threads.restype = None
+    return L
 
 
 def num_threads() -> int:
