@@ -498,9 +498,11 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                         float *dst = static_cast<float *>(p.out) + (long long)un.c * p.o_stride + obase + cc * 32;
 #pragma unroll
                         for (int k = 0; k < 32; k += 4)
-                            *reinterpret_cast<float4 *>(dst + k) =
-                                make_float4(__uint_as_float(o[k]) * inv, __uint_as_float(o[k + 1]) * inv,
-                                            __uint_as_float(o[k + 2]) * inv, __uint_as_float(o[k + 3]) * inv);
+                            // streaming stores: the partials are read once, by the merge, and should
+                            // not push this chunk's K/V out of L2
+                            __stcs(reinterpret_cast<float4 *>(dst + k),
+                                   make_float4(__uint_as_float(o[k]) * inv, __uint_as_float(o[k + 1]) * inv,
+                                               __uint_as_float(o[k + 2]) * inv, __uint_as_float(o[k + 3]) * inv));
                     } else {
                         __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.out) + obase + cc * 32;
 #pragma unroll
