@@ -43,6 +43,11 @@
  *     Read as the Cauchy-Schwarz bound M_i = |q~_i| * max_j |k~_j| / sqrt(d)
  *     >= max_j s_ij; the attention result does not depend on which bound is
  *     used, so the oracle supplies only the bound itself.
+ *   - The backward pass of the attention (gradients of q, k, v and the joint
+ *     keys/values for a given output gradient).  The pages describe inference
+ *     only; this is the plain chain rule of softmax(Q K^T / sqrt(d)) V:
+ *     D_i = sum_e dO_ie O_ie, dV = P^T dO, dS = P o (dO V^T - D),
+ *     dQ = dS K / sqrt(d), dK = dS^T Q / sqrt(d), on the rotated q and k.
  *   - QK-norm before the rotary embedding: "Context Parallelism in vLLM Omni
  *     Neuron", "Self-Attention with Context Parallelism" (`norm_q(q)`,
  *     `norm_k(k)` on the projected rows before they are split into heads) and
@@ -413,6 +418,121 @@ int k6o_cross_attention(int B, int H, int d, long Sq, long Sk, const void *q, co
         free(s);
     }
     return bad ? -4 : 0;
+}
+
+/*
+ * Backward of the attention over the full joint sequence, on rotated (or
+ * unrotated, rope = 0) inputs in the layouts of k6o_attention, for the output
+ * gradient dout [B][S][H][d].  Writes dq [B][S][H][d], dk/dv [B][Nv][H][d],
+ * djk/djv [B][Nj][H][d] (double).  With rope = 1 the q/k gradients are with
+ * respect to the rotated q~ and k~.
+ */
+int k6o_attention_backward(const k6o_geom *g, int rope, const void *q, const void *k, const void *v,
+                           const void *jk, const void *jv, int type, const double *dout, double *dq, double *dk,
+                           double *dv, double *djk, double *djv) {
+    if (!geom_ok(g)) return -1;
+    const long S = g->Nv + g->Nj;
+    const int d = g->d, H = g->H;
+    const double scale = 1.0 / sqrt((double)d);
+    double *qr = (double *)malloc(sizeof(double) * (size_t)S * d);
+    double *kr = (double *)malloc(sizeof(double) * (size_t)S * d);
+    double *vr = (double *)malloc(sizeof(double) * (size_t)S * d);
+    double *Pm = (double *)malloc(sizeof(double) * (size_t)S * S);
+    double *dK = (double *)malloc(sizeof(double) * (size_t)S * d);
+    double *dV = (double *)malloc(sizeof(double) * (size_t)S * d);
+    double *Dr = (double *)malloc(sizeof(double) * (size_t)S);
+    if (!qr || !kr || !vr || !Pm || !dK || !dV || !Dr) {
+        free(qr); free(kr); free(vr); free(Pm); free(dK); free(dV); free(Dr);
+        return -4;
+    }
+    for (int b = 0; b < g->B; b++)
+        for (int h = 0; h < H; h++) {
+            for (long n = 0; n < S; n++) {
+                size_t off;
+                const void *kb = kv_ptr(g, n, b, h, k, jk, &off);
+                const void *vb = kv_ptr(g, n, b, h, v, jv, &off);
+                const size_t qoff = (((size_t)b * S + n) * H + h) * d;
+                for (int e = 0; e < d; e++) {
+                    qr[(size_t)n * d + e] = load_elem(q, type, qoff + e);
+                    kr[(size_t)n * d + e] = load_elem(kb, type, off + e);
+                    vr[(size_t)n * d + e] = load_elem(vb, type, off + e);
+                }
+                if (rope) {
+                    k6o_rope_vec(g, n, qr + (size_t)n * d);
+                    k6o_rope_vec(g, n, kr + (size_t)n * d);
+                }
+            }
+            /* P and the row terms, then dQ row by row */
+#pragma omp parallel for schedule(dynamic, 4)
+            for (long i = 0; i < S; i++) {
+                double *p = Pm + (size_t)i * S;
+                double m = -INFINITY;
+                for (long j = 0; j < S; j++) {
+                    double acc = 0.0;
+                    for (int e = 0; e < d; e++) acc += qr[(size_t)i * d + e] * kr[(size_t)j * d + e];
+                    p[j] = acc * scale;
+                    if (p[j] > m) m = p[j];
+                }
+                double sum = 0.0;
+                for (long j = 0; j < S; j++) sum += exp(p[j] - m);
+                const double lse = m + log(sum);
+                for (long j = 0; j < S; j++) p[j] = exp(p[j] - lse);
+                const double *go = dout + (((size_t)b * S + i) * H + h) * d;
+                /* D_i = dO_i . O_i with O_i = sum_j p_j v_j */
+                double Di = 0.0;
+                for (int e = 0; e < d; e++) {
+                    double o = 0.0;
+                    for (long j = 0; j < S; j++) o += p[j] * vr[(size_t)j * d + e];
+                    Di += go[e] * o;
+                }
+#if K6O_MUTANT == 9
+                Di = 0.0; /* planted: dropped the D_i term */
+#endif
+                Dr[i] = Di;
+                /* dQ_i = sum_j dS_ij k_j / sqrt(d),  dS_ij = P_ij (dO_i . v_j - D_i) */
+                double *gq = dq + (((size_t)b * S + i) * H + h) * d;
+                for (int e = 0; e < d; e++) gq[e] = 0.0;
+                for (long j = 0; j < S; j++) {
+                    double dp = 0.0;
+                    for (int e = 0; e < d; e++) dp += go[e] * vr[(size_t)j * d + e];
+                    const double ds = p[j] * (dp - Di);
+                    for (int e = 0; e < d; e++) gq[e] += ds * kr[(size_t)j * d + e] * scale;
+                }
+            }
+            /* dK and dV key by key (P kept in Pm) */
+#pragma omp parallel for schedule(dynamic, 4)
+            for (long j = 0; j < S; j++) {
+                double *gk = dK + (size_t)j * d, *gv = dV + (size_t)j * d;
+                for (int e = 0; e < d; e++) gk[e] = gv[e] = 0.0;
+                for (long i = 0; i < S; i++) {
+                    const double pij = Pm[(size_t)i * S + j];
+                    const double *go = dout + (((size_t)b * S + i) * H + h) * d;
+                    double dp = 0.0;
+                    for (int e = 0; e < d; e++) dp += go[e] * vr[(size_t)j * d + e];
+                    const double ds = pij * (dp - Dr[i]);
+                    for (int e = 0; e < d; e++) {
+                        gv[e] += pij * go[e];
+                        gk[e] += ds * qr[(size_t)i * d + e] * scale;
+                    }
+                }
+            }
+            for (long n = 0; n < S; n++) {
+                double *tk, *tv;
+                if (n < g->Nv) {
+                    const size_t off = (((size_t)b * g->Nv + n) * H + h) * d;
+                    tk = dk + off, tv = dv + off;
+                } else {
+                    const size_t off = (((size_t)b * g->Nj + (n - g->Nv)) * H + h) * d;
+                    tk = djk + off, tv = djv + off;
+                }
+                for (int e = 0; e < d; e++) {
+                    tk[e] = dK[(size_t)n * d + e];
+                    tv[e] = dV[(size_t)n * d + e];
+                }
+            }
+        }
+    free(qr); free(kr); free(vr); free(Pm); free(dK); free(dV); free(Dr);
+    return 0;
 }
 
 /*

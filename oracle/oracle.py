@@ -100,6 +100,8 @@ def _declare(L):
                                    ctypes.c_long, ctypes.c_long, P, ctypes.c_long, P, P]
     L.k6o_cross_attention.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_long,
                                          ctypes.c_long, P, P, P, ctypes.c_int, ctypes.c_long, ctypes.c_long, P, P]
+    L.k6o_attention_backward.argtypes = [ctypes.POINTER(_Geom), ctypes.c_int, P, P, P, P, P, ctypes.c_int, P,
+                                         P, P, P, P, P]
     L.k6o_row_bounds.argtypes = [ctypes.POINTER(_Geom), ctypes.c_int, P, P, P, ctypes.c_int, P]
     L.k6o_rms_norm.argtypes = [P, ctypes.c_int, ctypes.c_long, ctypes.c_long, P, ctypes.c_double, P]
     L.k6o_lse_merge.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_long, ctypes.c_int, ctypes.c_int,
@@ -210,6 +212,30 @@ def attention(g: Geom, q, k, v, jk=None, jv=None, *, rope: bool = True, kv_range
     if rc:
         raise ValueError(f"k6o_attention: {rc}")
     return out, lse
+
+
+def attention_backward(g: Geom, q, k, v, jk, jv, dout, *, rope: bool = True):
+    """Gradients (dq, dk, dv, djk, djv) of sum(out * dout) over the full joint sequence,
+    with respect to the rotated q, k (rope=True) or the given ones (rope=False)."""
+    arrs = [q, k, v] + ([jk, jv] if g.Nj > 0 else [])
+    typed = [_typed(a) for a in arrs]
+    t = typed[0][1]
+    assert all(tt == t for _, tt in typed)
+    do = np.ascontiguousarray(dout, np.float64)
+    dq = np.empty((g.B, g.S, g.H, g.d))
+    dk = np.empty((g.B, g.Nv, g.H, g.d))
+    dv = np.empty((g.B, g.Nv, g.H, g.d))
+    djk = np.empty((g.B, max(g.Nj, 0), g.H, g.d))
+    djv = np.empty((g.B, max(g.Nj, 0), g.H, g.d))
+    nullp = ctypes.c_void_p(0)
+    j0 = _ptr(typed[3][0]) if g.Nj > 0 else nullp
+    j1 = _ptr(typed[4][0]) if g.Nj > 0 else nullp
+    rc = lib().k6o_attention_backward(ctypes.byref(g.c()), int(bool(rope)), _ptr(typed[0][0]), _ptr(typed[1][0]),
+                                      _ptr(typed[2][0]), j0, j1, t, _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
+                                      _ptr(djk), _ptr(djv))
+    if rc:
+        raise ValueError(f"k6o_attention_backward: {rc}")
+    return dq, dk, dv, djk, djv
 
 
 def cross_attention(q, k, v, *, kv_range=None):

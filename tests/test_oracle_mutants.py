@@ -5,7 +5,8 @@ Each mutant is the oracle compiled with one deliberate mistake planted in it
 the rotary frequency, swapped grid axes, the wrong softmax scale, a merge
 weighted by the maximum instead of the log-sum-exp, transposed relayout
 indices, a log-sum-exp without its maximum, joint keys read from the video
-tensor.  Every mutant must fail at least one pin; the oracle itself passes all.
+tensor, a backward pass without its D_i term.  Every mutant must fail at
+least one pin; the oracle itself passes all.
 """
 import numpy as np
 import pytest
@@ -25,6 +26,7 @@ CHECKS = {
     "rope frequency ladder": pins.test_rope_frequency_ladder_and_axis_segments,
     "rope 1-d complex": pins.test_rope_1d_joint_equals_complex_product,
     "relayout transpose": lambda: pins.test_relayout_matches_transpose_and_round_trips(1, 40, 24, 8, 8, np.uint16),
+    "backward differences": pins.test_backward_matches_central_differences_of_the_forward,
 }
 
 
@@ -49,7 +51,7 @@ def test_oracle_itself_passes_every_check(restore_oracle):
     assert run_checks() == []
 
 
-@pytest.mark.parametrize("mutant", range(1, 9))
+@pytest.mark.parametrize("mutant", range(1, 10))
 def test_pins_catch_a_planted_mistake(mutant, restore_oracle):
     O.use_mutant(mutant)
     failed = run_checks()

@@ -226,6 +226,63 @@ def test_merge_accepts_f32_partials_exactly():
     np.testing.assert_array_equal(a[1], b[1])
 
 
+# ---------------------------------------------------------------- backward
+
+
+def test_backward_matches_central_differences_of_the_forward():
+    """d/dx sum(out * G) by central differences through the forward oracle (rope off)."""
+    g = tiny_geom(B=1, H=2, d=8, grid=(1, 2, 3), Nj=2)
+    q, k, v, jk, jv = tiny_inputs(g, seed=71, std=1.5)
+    G = rnd((g.B, g.S, g.H, g.d), 72)
+    grads = dict(zip(("q", "k", "v", "jk", "jv"), O.attention_backward(g, q, k, v, jk, jv, G, rope=False)))
+    x = {"q": q, "k": k, "v": v, "jk": jk, "jv": jv}
+
+    def loss():
+        out, _ = O.attention(g, x["q"], x["k"], x["v"], x["jk"], x["jv"], rope=False)
+        return float((out * G).sum())
+
+    eps = 1e-5
+    rng = np.random.default_rng(73)
+    for name in x:
+        for _ in range(6):
+            idx = tuple(int(rng.integers(0, n)) for n in x[name].shape)
+            keep = x[name][idx]
+            x[name][idx] = keep + eps
+            up = loss()
+            x[name][idx] = keep - eps
+            dn = loss()
+            x[name][idx] = keep
+            fd = (up - dn) / (2 * eps)
+            assert abs(fd - grads[name][idx]) < 1e-7 * max(1.0, abs(fd)), (name, idx, fd, grads[name][idx])
+
+
+def test_backward_with_rope_is_the_rotated_gradient():
+    """With rotary on, dq/dk are gradients w.r.t. the rotated q~, k~: identical to
+    running the rope-off backward on the oracle-rotated inputs."""
+    g = O.Geom(1, 2, 16, (2, 2, 3), 3, (4, 6, 6), 10000.0, 1)
+    q, k, v, jk, jv = tiny_inputs(g, seed=74)
+    G = rnd((g.B, g.S, g.H, g.d), 75)
+    a = O.attention_backward(g, q, k, v, jk, jv, G, rope=True)
+    K = O.rope(g, np.concatenate([k, jk], axis=1))
+    b = O.attention_backward(g, O.rope(g, q), K[:, :g.Nv], v, K[:, g.Nv:], jv, G, rope=False)
+    for x, y in zip(a, b):
+        np.testing.assert_allclose(x, y, rtol=0, atol=1e-13)
+
+
+def test_backward_closed_forms():
+    """sum_j dV_j = sum_i dO_i (each row of P sums to 1); with every value
+    equal, the output does not depend on q or k: their gradients vanish."""
+    g = tiny_geom(B=1, H=1, d=8, grid=(1, 3, 3), Nj=1)
+    q, k, v, jk, jv = tiny_inputs(g, seed=76)
+    G = rnd((g.B, g.S, g.H, g.d), 77)
+    dq, dk, dv, djk, djv = O.attention_backward(g, q, k, v, jk, jv, G, rope=False)
+    np.testing.assert_allclose(dv.sum(axis=1) + djv.sum(axis=1), G.sum(axis=1), rtol=0, atol=1e-12)
+    vc = np.broadcast_to(v[:, :1], v.shape).copy()
+    jvc = np.broadcast_to(v[:, :1], jv.shape).copy()
+    dq, dk, _, djk, _ = O.attention_backward(g, q, k, vc, jk, jvc, G, rope=False)
+    assert np.abs(dq).max() < 1e-13 and np.abs(dk).max() < 1e-13 and np.abs(djk).max() < 1e-13
+
+
 # ------------------------------------------------------------ cross-attention
 
 
