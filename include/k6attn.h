@@ -200,6 +200,36 @@ k6attn_status k6attn_attention_chunks(k6attn_t h, const void *q, const void *k, 
                                       void *stream);
 
 /*
+ * Backward pass of the joint attention (the pages describe inference only;
+ * these are the chain-rule gradients of out = softmax(s) v with
+ * s = q k^T / sqrt(d), over concat(k, joint_k) as in k6attn_attention_chunks
+ * with one chunk):
+ *   D_i = sum_e dout_ie out_ie,  P = exp(s - lse),
+ *   dS  = P o (dout v^T - D),    dv = P^T dout,
+ *   dq  = dS k / sqrt(d),        dk = dS^T q / sqrt(d).
+ * The q/k gradients are with respect to the q, k given (the rotated copies
+ * when rotary embeddings are used).  BF16 handles with d = 128.
+ *  q, k, joint_k  rotated inputs, type qk_dtype (BF16 or F16); v, joint_v
+ *           bf16; layouts as above.  Not modified.
+ *  out, lse the forward result for these inputs (out bf16 [B][Sq][H][d], lse
+ *           fp32 [B][H][Sq], as written by k6attn_attention_chunks with one
+ *           chunk or by k6attn_forward).
+ *  dout     bf16 [B][Sq][H][d], the gradient of the loss with respect to out.
+ *  dq       fp32 [B][Sq][H][d]; dk, dv fp32 [B][Nv][H][d]; djoint_k,
+ *           djoint_v fp32 [B][Nj][H][d] (may be NULL when Nj == 0).  Fully
+ *           overwritten; must not alias any input or one another.
+ *  workspace, workspace_bytes  caller-owned device scratch of at least
+ *           k6attn_backward_workspace_bytes(h) bytes (the D_i rows).
+ * P is rounded to bf16 and dS to qk_dtype before their products; all
+ * products accumulate in fp32.
+ */
+size_t k6attn_backward_workspace_bytes(k6attn_t h);
+k6attn_status k6attn_backward(k6attn_t h, const void *q, const void *k, const void *v, const void *joint_k,
+                              const void *joint_v, k6attn_dtype qk_dtype, const void *out, const void *dout,
+                              const float *lse, float *dq, float *dk, float *dv, float *djoint_k, float *djoint_v,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Constant-max softmax ([CP] "Related information": the ring kernel
  * `ring_attention_const_max_fwd` uses a runtime bound on the softmax maximum
  * instead of a running maximum, so no partial output is ever rescaled).  The

@@ -422,6 +422,60 @@ k6attn_status k6attn_attention_chunks(k6attn_t h, const void *q, const void *k, 
                          static_cast<cudaStream_t>(stream));
 }
 
+size_t k6attn_backward_workspace_bytes(k6attn_t h) {
+    if (!h) return 0;
+    return (((size_t)h->g.B * h->g.H * h->g.S * sizeof(float)) + 255) & ~(size_t)255;
+}
+
+k6attn_status k6attn_backward(k6attn_t h, const void *q, const void *k, const void *v, const void *joint_k,
+                              const void *joint_v, k6attn_dtype qk_dtype, const void *out, const void *dout,
+                              const float *lse, float *dq, float *dk, float *dv, float *djoint_k, float *djoint_v,
+                              void *workspace, size_t workspace_bytes, void *stream) {
+    g_msg[0] = 0;
+    if (!h) return set_error(K6ATTN_ERR_INVALID_ARG, "backward: null handle");
+    const Geom &g = h->g;
+    if (g.dtype != K6ATTN_BF16 || g.d != 128)
+        return set_error(K6ATTN_ERR_UNSUPPORTED, "backward: needs a BF16 handle with d = 128");
+    if (qk_dtype != K6ATTN_BF16 && qk_dtype != K6ATTN_F16)
+        return set_error(K6ATTN_ERR_INVALID_ARG, "backward: q/k type must be BF16 or F16");
+    if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv)
+        return set_error(K6ATTN_ERR_INVALID_ARG, "backward: null pointer");
+    if (g.Nj > 0 && (!joint_k || !joint_v || !djoint_k || !djoint_v))
+        return set_error(K6ATTN_ERR_INVALID_ARG, "backward: %ld joint tokens but a joint pointer is null", g.Nj);
+    const void *ptrs[] = {q, k, v, joint_k, joint_v, out, dout, dq, dk, dv, djoint_k, djoint_v, workspace};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return set_error(K6ATTN_ERR_INVALID_ARG, "backward: pointers must be 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(lse) & 3) return set_error(K6ATTN_ERR_INVALID_ARG, "backward: lse misaligned");
+    const size_t need = k6attn_backward_workspace_bytes(h);
+    if (!workspace || workspace_bytes < need)
+        return set_error(K6ATTN_ERR_WORKSPACE, "backward: workspace of %zu bytes needed, %zu given", need,
+                         workspace ? workspace_bytes : (size_t)0);
+    const size_t row16 = (size_t)g.H * g.d * 2, row32 = (size_t)g.H * g.d * 4;
+    const size_t qb = g.B * g.S * row16, kvb = g.B * g.Nv * row16, jb = g.B * g.Nj * row16;
+    const void *ins[] = {q, k, v, joint_k, joint_v, out, dout, lse};
+    const size_t insz[] = {qb, kvb, kvb, jb, jb, qb, qb, (size_t)g.B * g.H * g.S * 4};
+    const void *outs[] = {dq, dk, dv, djoint_k, djoint_v, workspace};
+    const size_t outsz[] = {g.B * g.S * row32, g.B * g.Nv * row32, g.B * g.Nv * row32, g.B * g.Nj * row32,
+                            g.B * g.Nj * row32, need};
+    for (int i = 0; i < 6; i++) {
+        for (int j = 0; j < 8; j++)
+            if (overlap(outs[i], outsz[i], ins[j], insz[j]))
+                return set_error(K6ATTN_ERR_INVALID_ARG, "backward: an output overlaps an input");
+        for (int j = i + 1; j < 6; j++)
+            if (overlap(outs[i], outsz[i], outs[j], outsz[j]))
+                return set_error(K6ATTN_ERR_INVALID_ARG, "backward: two outputs overlap");
+    }
+    const char *why = nullptr;
+    cudaError_t e = launch_attn_bwd(g, qk_dtype == K6ATTN_F16, q, k, v, joint_k, joint_v, out, dout, lse,
+                                    static_cast<float *>(workspace), dq, dk, dv, djoint_k, djoint_v,
+                                    h->wait_limit_ns, h->err, static_cast<cudaStream_t>(stream), &why);
+    if (e != cudaSuccess) {
+        if (why) return set_error(K6ATTN_ERR_CUDA, "backward: %s", why);
+        return cuda_check(e, "backward launch");
+    }
+    return K6ATTN_OK;
+}
+
 // The handle's batch, heads, head dim and type with Sq query rows over Sk keys.
 static Geom cross_geom(const Geom &base, long Sq, long Sk) {
     Geom g = base;

@@ -23,7 +23,7 @@ SYMBOLS = ["k6attn_create", "k6attn_destroy", "k6attn_rope_tables", "k6attn_rope
            "k6attn_seq2head_relayout", "k6attn_sync", "k6attn_set_option", "k6attn_status_string",
            "k6attn_last_error", "k6attn_forward_static_scratch", "k6attn_cross_workspace_bytes",
            "k6attn_cross_forward", "k6attn_norm_rope_qk", "k6attn_row_bounds_bytes", "k6attn_row_bounds",
-           "k6attn_attention_chunks_bounded"]
+           "k6attn_attention_chunks_bounded", "k6attn_backward_workspace_bytes", "k6attn_backward"]
 
 
 class K6Error(RuntimeError):
@@ -79,6 +79,9 @@ def load(build_if_missing: bool = True):
     L.k6attn_cross_workspace_bytes.restype = Z
     L.k6attn_cross_forward.argtypes = [P, P, ctypes.c_long, P, P, ctypes.c_long, I, P, P, P, Z, P]
     L.k6attn_attention_chunks.argtypes = [P, P, P, P, P, P, I, I, P, P, P]
+    L.k6attn_backward_workspace_bytes.argtypes = [P]
+    L.k6attn_backward_workspace_bytes.restype = Z
+    L.k6attn_backward.argtypes = [P, P, P, P, P, P, I, P, P, P, P, P, P, P, P, P, Z, P]
     L.k6attn_lse_merge.argtypes = [P, P, P, I, P, P, P]
     L.k6attn_seq2head_relayout.argtypes = [P, P, I, ctypes.c_long, I, I, I, I, I, P]
     L.k6attn_sync.argtypes = [P, P]
@@ -201,6 +204,18 @@ class Handle:
         qd = self._desc.dtype if qk_dtype is None else qk_dtype
         _check(load().k6attn_attention_chunks(self.h, _ptr(q), _ptr(k), _ptr(v), _ptr(joint_k), _ptr(joint_v),
                                               int(qd), int(n_chunks), _ptr(out), _ptr(lse), _stream(stream)))
+
+    def backward_workspace_bytes(self) -> int:
+        return load().k6attn_backward_workspace_bytes(self.h)
+
+    def backward(self, q, k, v, joint_k, joint_v, out, dout, lse, dq, dk, dv, djoint_k=None, djoint_v=None, *,
+                 workspace, qk_dtype=None, stream=None):
+        """Gradients of the joint attention (fp32 dq, dk, dv, djoint_k, djoint_v) for the rotated q, k."""
+        qd = self._desc.dtype if qk_dtype is None else qk_dtype
+        ws_bytes = workspace.numel() * workspace.element_size()
+        _check(load().k6attn_backward(self.h, _ptr(q), _ptr(k), _ptr(v), _ptr(joint_k), _ptr(joint_v), int(qd),
+                                      _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                                      _ptr(djoint_k), _ptr(djoint_v), _ptr(workspace), ws_bytes, _stream(stream)))
 
     def cross_workspace_bytes(self, Sq: int, n_chunks: int) -> int:
         return load().k6attn_cross_workspace_bytes(self.h, int(Sq), int(n_chunks))
