@@ -392,6 +392,51 @@ def measure_cross(w, steps, warmup, n_chunks=8):
             "launches_per_call": 2}
 
 
+def measure_backward(w, x, steps, warmup):
+    """Attention backward on the workload: rotary into fp16 copies and the one-chunk
+    forward (out, lse) once, then `steps` timed k6attn_backward calls (D pre-pass,
+    dq kernel, dk/dv kernel).  FLOPs are the 5-GEMM count 10*B*H*S^2*d."""
+    import torch
+    from video_dit_long_gb300 import k6attn as K
+    B, S, Nv, Nj, H, d = w.B, w.S, w.Nv, w.Nj, w.H, w.d
+    h = K.Handle.for_workload(w)
+
+    def dev(a):
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
+
+    q, k, v, jk, jv = (dev(x[n]) for n in ("q", "k", "v", "jk", "jv"))
+    qh, kh, jh = (torch.empty(t.shape, dtype=torch.float16, device="cuda") for t in (q, k, jk))
+    h.rope_qk(q, k, jk, q_out=qh, k_out=kh, joint_k_out=jh, out_dtype=K.F16)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device="cuda")
+    h.attention_chunks(qh, kh, v, jh, jv, 1, out, lse, qk_dtype=K.F16)
+    do = dev(inputs.tensor(42, 20, (B, S, H, d), "bf16"))
+    f32 = dict(dtype=torch.float32, device="cuda")
+    dq = torch.empty((B, S, H, d), **f32)
+    dk, dv = torch.empty((B, Nv, H, d), **f32), torch.empty((B, Nv, H, d), **f32)
+    djk, djv = torch.empty((B, Nj, H, d), **f32), torch.empty((B, Nj, H, d), **f32)
+    ws = torch.empty(h.backward_workspace_bytes(), dtype=torch.uint8, device="cuda")
+
+    def call():
+        h.backward(qh, kh, v, jh, jv, out, do, lse, dq, dk, dv, djk, djv, workspace=ws, qk_dtype=K.F16)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    h.sync()
+    ms = e0.elapsed_time(e1) / steps
+    flops = 10.0 * B * H * S * S * d
+    return {"workload": f"{w.name}: gradients of q, k, v, joint_k, joint_v over {S} tokens (B={B}, H={H}, d={d})",
+            "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s (5-GEMM count)",
+            "ms_per_call": round(ms, 3), "launches_per_call": 3}
+
+
 def merge_bytes(w, n, P):
     rows = w.B * w.S * w.H
     return n * (rows * w.d * 4 + rows * 4) + rows * w.d * 2 + rows * 4
@@ -483,6 +528,9 @@ def run_ours(args, rank, world, dist_on):
                               "standard_attention_plus_merge_ms": round(k_ms[2] + k_ms[3], 3)}
     if args.secondary:
         line["cross_attention"] = measure_cross(w, max(5, args.steps // 2), args.warmup)
+        bwd = measure_backward(w, x, max(3, args.steps // 10), max(3, args.warmup // 2))
+        bwd["frac_sustained"] = round(bwd["value"] / peak_s, 4)
+        line["backward"] = bwd
     if rank == 0 and world == 1 and not args.no_cpu:
         dt, fl, thr = cpu_sample(w, x, args.cpu_rows)
         line["cpu_baseline"] = {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
