@@ -219,7 +219,8 @@ k6attn_status k6attn_attention_chunks(k6attn_t h, const void *q, const void *k, 
  *           djoint_v fp32 [B][Nj][H][d] (may be NULL when Nj == 0).  Fully
  *           overwritten; must not alias any input or one another.
  *  workspace, workspace_bytes  caller-owned device scratch of at least
- *           k6attn_backward_workspace_bytes(h) bytes (the D_i rows).
+ *           k6attn_backward_workspace_bytes(h) bytes (per (b, h, row) the
+ *           row's lse in base 2 and D_i, 8 bytes).
  * P is rounded to bf16 and dS to qk_dtype before their products; all
  * products accumulate in fp32.
  */

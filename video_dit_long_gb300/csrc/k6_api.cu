@@ -424,7 +424,7 @@ k6attn_status k6attn_attention_chunks(k6attn_t h, const void *q, const void *k, 
 
 size_t k6attn_backward_workspace_bytes(k6attn_t h) {
     if (!h) return 0;
-    return (((size_t)h->g.B * h->g.H * h->g.S * sizeof(float)) + 255) & ~(size_t)255;
+    return (((size_t)h->g.B * h->g.H * h->g.S * sizeof(float2)) + 255) & ~(size_t)255;
 }
 
 k6attn_status k6attn_backward(k6attn_t h, const void *q, const void *k, const void *v, const void *joint_k,
@@ -467,7 +467,7 @@ k6attn_status k6attn_backward(k6attn_t h, const void *q, const void *k, const vo
     }
     const char *why = nullptr;
     cudaError_t e = launch_attn_bwd(g, qk_dtype == K6ATTN_F16, q, k, v, joint_k, joint_v, out, dout, lse,
-                                    static_cast<float *>(workspace), dq, dk, dv, djoint_k, djoint_v,
+                                    static_cast<float2 *>(workspace), dq, dk, dv, djoint_k, djoint_v,
                                     h->wait_limit_ns, h->err, static_cast<cudaStream_t>(stream), &why);
     if (e != cudaSuccess) {
         if (why) return set_error(K6ATTN_ERR_CUDA, "backward: %s", why);

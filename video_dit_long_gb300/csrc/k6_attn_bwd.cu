@@ -9,17 +9,23 @@
 // over the full key range (video keys, then joint keys) of each (batch, head).
 //
 // Two kernels, each with one stationary 128-row tile per CTA and the other
-// operand streamed through a two-slot TMA ring:
-//   dq kernel  (Q, dO stationary, K/V streamed): S = Q K_j^T and dP = dO V_j^T
-//              (SS) into tensor memory; four warps turn each row into dS and
-//              store it (Q/K operand type) over the first 64 columns of S;
-//              dQ += dS K_j (TS, K_j MN-major).  Columns: S | dP | dQ.
-//   dkv kernel (K, V stationary, Q/dO streamed): S^T = K Q_i^T, dP^T = V dO_i^T
-//              (SS); each thread (one key) turns its row into P^T and dS^T
-//              (stored over S^T and dP^T); dV += P^T dO_i, dK += dS^T Q_i
-//              (TS).  Columns: S^T | dP^T | dV | dK (all 512).
-// One elected thread issues the MMAs; one warp drives TMA; all waits are
-// bounded like the forward kernel's.  Gradients are written in fp32.
+// operand streamed by TMA.  Warps 0-7 form P/dS (two warpgroups, each owning
+// half of a tile's columns; one TMEM lane = one row per thread), warp 8 drives
+// TMA, warp 9 owns tensor memory and one of its threads issues every MMA.
+//
+//   dq kernel  (Q, dO stationary; K through a 3-slot ring, V through 2 slots):
+//     S = Q K_j^T, dP = dO V_j^T (SS) into columns 0-127 / 128-255; dS (q/k
+//     type) goes to one of two spare buffers (384-447, 448-511), so the MMAs
+//     of tile j+1 start before dQ += dS_j K_j (TS, 256-383) and that product
+//     runs under the next tile's row pass.
+//   dkv kernel (K, V stationary; Q/dO through a 2-slot ring):
+//     S^T = K Q_i^T, dP^T = V dO_i^T (SS) into 0-127 / 128-255; P^T goes to
+//     shared memory (K-major, 128-byte swizzle) and dS^T over dP^T, so
+//     S^T of tile i+1 runs under the row pass of tile i; then
+//     dV += P^T dO_i (SS) and dK += dS^T Q_i (TS) into 256-383 / 384-511.
+// MMAs of one thread run in issue order, so an MMA may overwrite tensor
+// memory that an earlier MMA reads (dP of tile i+1 over dS^T of tile i).
+// All waits are bounded like the forward kernel's.  Gradients are fp32.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -34,25 +40,22 @@ namespace k6 {
 
 namespace bw {
 constexpr int D = 128, BM = 128;
-constexpr int PANEL = BM * 64 * 2;
-constexpr int TILE = 2 * PANEL;             // 32 KB: 128 rows x 128 dims, 16-bit
-constexpr int SMEM_STAT = 0;                // two stationary tiles
-constexpr int SMEM_RING = 2 * TILE;         // two slots of two tiles each
-constexpr int SMEM_BAR = SMEM_RING + 2 * 2 * TILE;
-constexpr int NBAR = 1 + 2 + 2 + 1 + 1 + 1 + 1;  // stat_full, ld_full[2], ld_empty[2], s_full, ds_full, acc_done, drain
-constexpr int SMEM_ALLOC = SMEM_BAR + NBAR * 8 + 64 + 1024;  // barriers, TMEM slot, abort flag, alignment
-constexpr int THREADS = 192;                // warps 0-3 compute, 4 TMA, 5 MMA
+constexpr int PANEL = BM * 64 * 2;          // 128 rows x 64 elements of 16 bits
+constexpr int TILE = 2 * PANEL;             // 32 KB: 128 rows x 128 elements
+constexpr int THREADS = 320;                // warps 0-7 rows, 8 TMA, 9 MMA + TMEM
+constexpr int SMEM_DATA = 7 * TILE;         // both kernels: 224 KB of tiles
+constexpr int SMEM_ALLOC = SMEM_DATA + 256 + 1024;  // barriers, TMEM slot, abort flag, alignment
 constexpr unsigned long long DRAIN_NS = 1000000000ull;
+constexpr float LOG2E = 1.4426950408889634f;
 }  // namespace bw
 
 struct BwParams {
     long S, Nv, Nj;
     int H, q_tiles, kv_tiles_v, kv_tiles_j;
     float scale_log2, scale;                // log2(e)/sqrt(d), 1/sqrt(d)
-    const float *lse;                       // [B][H][S] natural log
-    const float *Dsum;                      // [B][H][S]
+    const float2 *LD;                       // [B][H][S] {lse * log2(e), D}
     float *dq, *dk, *dv, *djk, *djv;        // fp32 gradients
-    uint32_t idesc_qk, idesc_bf16, idesc_ds_q, idesc_ds_k;
+    uint32_t idesc_qk, idesc_bf16, idesc_bf16_mn, idesc_ds_mn;
     int ds_f16;                             // dS stored as fp16 (q/k are fp16) or bf16
     unsigned long long wait_limit_ns;
     int *err;
@@ -66,11 +69,23 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool f16) {
     return pack_bf16x2(lo, hi);
 }
 
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
 // ------------------------------------------------------------- pre-pass D
 
+// LD[(b*H + h)*S + s] = {lse * log2(e), sum_e dout * out} for one head row.
+// Half a warp (16 lanes x 8 elements) covers one d = 128 row.
 __global__ void __launch_bounds__(256) bwd_dsum_kernel(const __nv_bfloat16 *__restrict__ out,
-                                                      const __nv_bfloat16 *__restrict__ dout, long S, int H, int B,
-                                                      float *__restrict__ Dsum) {
+                                                      const __nv_bfloat16 *__restrict__ dout,
+                                                      const float *__restrict__ lse, long S, int H, int B,
+                                                      float2 *__restrict__ LD) {
     const int lane = threadIdx.x & 31, sub = lane & 15;
     const long warp = (blockIdx.x * (long)blockDim.x + threadIdx.x) >> 5;
     const long nwarps = ((long)gridDim.x * blockDim.x) >> 5;
@@ -94,63 +109,46 @@ __global__ void __launch_bounds__(256) bwd_dsum_kernel(const __nv_bfloat16 *__re
         if (r < rows && sub == 0) {
             const int h = (int)(r % H);
             const long bs = r / H;
-            Dsum[((bs / S) * H + h) * S + bs % S] = s;
+            const long li = ((bs / S) * H + h) * S + bs % S;
+            LD[li] = make_float2(lse[li] * bw::LOG2E, s);
         }
     }
 }
 
-// Shared set-up of both kernels: barriers, tensor memory, abort flag.
-struct BwShared {
-    uint64_t *stat_full, *ld_full, *ld_empty, *s_full, *ds_full, *acc_done, *drain;
-    uint32_t *tmem_slot;
-    volatile int *abort;
-};
+// ----------------------------------------------------------- shared set-up
 
-__device__ __forceinline__ BwShared bw_setup(uint8_t *smem) {
-    BwShared b;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + bw::SMEM_BAR);
-    b.stat_full = bars;
-    b.ld_full = bars + 1;
-    b.ld_empty = bars + 3;
-    b.s_full = bars + 5;
-    b.ds_full = bars + 6;
-    b.acc_done = bars + 7;
-    b.drain = bars + 8;
-    b.tmem_slot = reinterpret_cast<uint32_t *>(bars + bw::NBAR);
-    b.abort = reinterpret_cast<volatile int *>(b.tmem_slot + 1);
+// Barriers 0..NB-1 with the given arrival counts, 512 TMEM columns (warp 9).
+template <int NB>
+__device__ __forceinline__ uint32_t bw_setup(uint8_t *smem, const int (&counts)[NB], uint64_t *&bars,
+                                             volatile int *&abort_flag) {
+    bars = reinterpret_cast<uint64_t *>(smem + bw::SMEM_DATA);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NB);
+    abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     if (threadIdx.x == 0) {
-        mbar_init(b.stat_full, 1);
-        for (int s = 0; s < 2; s++) {
-            mbar_init(&b.ld_full[s], 1);
-            mbar_init(&b.ld_empty[s], 1);
-        }
-        mbar_init(b.s_full, 1);
-        mbar_init(b.ds_full, 128);
-        mbar_init(b.acc_done, 1);
-        mbar_init(b.drain, 1);
-        *b.abort = 0;
+        for (int i = 0; i < NB; i++) mbar_init(bars + i, counts[i]);
+        *abort_flag = 0;
         fence_barrier_init();
     }
-    if (threadIdx.x / 32 == 5) {
-        tmem_alloc(b.tmem_slot, 512);
+    if (threadIdx.x / 32 == 9) {
+        tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    return b;
+    return *tmem_slot;
 }
 
 __device__ __forceinline__ void bw_teardown(uint32_t tmem) {
     tc_fence_before();
     __syncthreads();
-    if (threadIdx.x / 32 == 5) {
+    if (threadIdx.x / 32 == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
 }
 
-// Streamed tile t of the key range: which map (0 video, 1 joint) and first row.
+// Key tile t of concat(k, joint_k): which map (0 video, 1 joint) and first row.
 __device__ __forceinline__ void kv_tile(const BwParams &p, int t, int &map, int &row) {
     if (t < p.kv_tiles_v) {
         map = 0;
@@ -161,7 +159,45 @@ __device__ __forceinline__ void kv_tile(const BwParams &p, int t, int &map, int 
     }
 }
 
+// Two 64-element panels of a 128-row tile into dst (32 KB, completes on bar).
+__device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *m, uint64_t *bar, int h, int row, int b) {
+    tma_load_4d(dst, m, bar, 0, h, row, b);
+    tma_load_4d(dst + bw::PANEL, m, bar, 64, h, row, b);
+}
+
+// Step kk of a K-major SS MMA chain over d = 128 (both operands 128-byte swizzled).
+__device__ __forceinline__ void mma_kmajor(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, int kk) {
+    const uint64_t off = (uint64_t)((kk >> 2) * bw::PANEL + (kk & 3) * 32) >> 4;
+    mma_ss(d, a + off, b + off, idesc, kk > 0);
+}
+
+// Epilogue: 64 fp32 columns of this thread's TMEM lane, times `scale`, to dst.
+__device__ __forceinline__ void store_row64(uint32_t taddr, float *dst, float scale, bool live) {
+#pragma unroll
+    for (int c = 0; c < 2; c++) {
+        uint32_t o[32];
+        tmem_ld32(taddr + c * 32, o);
+        tmem_ld_wait();
+        if (live) {
+#pragma unroll
+            for (int k = 0; k < 32; k += 4)
+                *reinterpret_cast<float4 *>(dst + c * 32 + k) =
+                    make_float4(__uint_as_float(o[k]) * scale, __uint_as_float(o[k + 1]) * scale,
+                                __uint_as_float(o[k + 2]) * scale, __uint_as_float(o[k + 3]) * scale);
+        }
+    }
+}
+
 // ------------------------------------------------------------------ dq kernel
+//
+// smem tiles: Q 0, dO 1, K slots 2-4, V slots 5-6.
+// barriers: stat_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full,
+//           ds_full (256 arrivals), acc_done, drain.
+
+namespace dqb {
+constexpr int STAT = 0, KFULL = 1, KEMPTY = 4, VFULL = 7, VEMPTY = 9, SFULL = 11, DSFULL = 12, ACC = 13,
+              DRAIN = 14, NB = 15;
+}
 
 __global__ void __launch_bounds__(bw::THREADS, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -169,138 +205,144 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
                   const __grid_constant__ CUtensorMap tm_jk, const __grid_constant__ CUtensorMap tm_jv,
                   const BwParams p) {
     using namespace bw;
+    using namespace dqb;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const BwShared sh = bw_setup(smem);
-    const uint32_t tmem = *sh.tmem_slot;
-    const WaitCtx w{p.wait_limit_ns, p.err, sh.abort};
+    const int counts[NB] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 256, 1, 1};
+    uint64_t *bar;
+    volatile int *abort_flag;
+    const uint32_t tmem = bw_setup<NB>(smem, counts, bar, abort_flag);
+    const WaitCtx w{p.wait_limit_ns, p.err, abort_flag};
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int qt = blockIdx.x % p.q_tiles;
     const int h = (blockIdx.x / p.q_tiles) % p.H;
     const int b = blockIdx.x / (p.q_tiles * p.H);
     const int q0 = qt * BM;
     const int T = p.kv_tiles_v + p.kv_tiles_j;
+    uint8_t *sQ = smem, *sDO = smem + TILE, *sK = smem + 2 * TILE, *sV = smem + 5 * TILE;
 
-    if (warp == 4) {
+    if (warp == 8) {
         if (lane == 0) {
-            mbar_arrive_expect_tx(sh.stat_full, 2 * TILE);
-            for (int half = 0; half < 2; half++) {
-                tma_load_4d(smem + SMEM_STAT + half * PANEL, &tm_q, sh.stat_full, half * 64, h, q0, b);
-                tma_load_4d(smem + SMEM_STAT + TILE + half * PANEL, &tm_do, sh.stat_full, half * 64, h, q0, b);
-            }
-            int issued = 0;
+            mbar_arrive_expect_tx(bar + STAT, 2 * TILE);
+            load_tile(sQ, &tm_q, bar + STAT, h, q0, b);
+            load_tile(sDO, &tm_do, bar + STAT, h, q0, b);
+            int nk = 0, nv = 0;  // K and V tiles issued
             for (int t = 0; t < T; t++) {
-                const int slot = t & 1;
-                if (!mbar_wait(&sh.ld_empty[slot], ((t >> 1) & 1) ^ 1, w)) break;
+                const int ks = t % 3, vs = t & 1;
                 int map, row;
                 kv_tile(p, t, map, row);
-                mbar_arrive_expect_tx(&sh.ld_full[slot], 2 * TILE);
-                uint8_t *dst = smem + SMEM_RING + slot * 2 * TILE;
-                for (int half = 0; half < 2; half++) {
-                    tma_load_4d(dst + half * PANEL, map ? &tm_jk : &tm_k, &sh.ld_full[slot], half * 64, h, row, b);
-                    tma_load_4d(dst + TILE + half * PANEL, map ? &tm_jv : &tm_v, &sh.ld_full[slot], half * 64, h,
-                                row, b);
-                }
-                issued++;
+                if (!mbar_wait(bar + KEMPTY + ks, ((t / 3) & 1) ^ 1, w)) break;
+                mbar_arrive_expect_tx(bar + KFULL + ks, TILE);
+                load_tile(sK + ks * TILE, map ? &tm_jk : &tm_k, bar + KFULL + ks, h, row, b);
+                nk++;
+                if (!mbar_wait(bar + VEMPTY + vs, ((t >> 1) & 1) ^ 1, w)) break;
+                mbar_arrive_expect_tx(bar + VFULL + vs, TILE);
+                load_tile(sV + vs * TILE, map ? &tm_jv : &tm_v, bar + VFULL + vs, h, row, b);
+                nv++;
             }
-            mbar_drain(sh.stat_full, 0, DRAIN_NS);
-            for (int t = issued > 2 ? issued - 2 : 0; t < issued; t++)
-                mbar_drain(&sh.ld_full[t & 1], (t >> 1) & 1, DRAIN_NS);
+            // let copies in flight land before the CTA exits
+            mbar_drain(bar + STAT, 0, DRAIN_NS);
+            for (int t = nk > 3 ? nk - 3 : 0; t < nk; t++) mbar_drain(bar + KFULL + t % 3, (t / 3) & 1, DRAIN_NS);
+            for (int t = nv > 2 ? nv - 2 : 0; t < nv; t++) mbar_drain(bar + VFULL + (t & 1), (t >> 1) & 1, DRAIN_NS);
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         if (lane == 0) {
-            const uint32_t tS = tmem, tP = tmem + 128, tA = tmem + 256;
-            const uint64_t dq0 = smem_desc_sw128(smem_u32(smem + SMEM_STAT), 16, 1024);        // Q (K-major)
-            const uint64_t ddo = dq0 + (uint64_t)(TILE >> 4);                               // dO (K-major)
-            const uint64_t dring = smem_desc_sw128(smem_u32(smem + SMEM_RING), 16, 1024);    // K / V (K-major)
-            const uint64_t dring_mn = smem_desc_sw128(smem_u32(smem + SMEM_RING), PANEL, 1024);  // K (MN-major)
-            bool ok = mbar_wait(sh.stat_full, 0, w);
-            for (int t = 0; t < T && ok; t++) {
-                const int slot = t & 1;
-                if (!(ok = mbar_wait(&sh.ld_full[slot], (t >> 1) & 1, w))) break;
+            const uint32_t tS = tmem, tP = tmem + 128, tA = tmem + 256, tDS = tmem + 384;
+            const uint64_t dq_ = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+            const uint64_t ddo = smem_desc_sw128(smem_u32(sDO), 16, 1024);
+            const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
+            const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), 16, 1024);
+            const uint64_t dkmn = smem_desc_sw128(smem_u32(sK), PANEL, 1024);
+            // S(t) = Q K^T and dP(t) = dO V^T, two interleaved chains; then free the
+            // V slot and publish S/dP (each commit also covers every earlier MMA).
+            auto issue_sdp = [&](int t) -> bool {
+                const int ks = t % 3, vs = t & 1;
+                if (!mbar_wait(bar + KFULL + ks, (t / 3) & 1, w)) return false;
+                if (!mbar_wait(bar + VFULL + vs, (t >> 1) & 1, w)) return false;
                 tc_fence_after();
-                const uint64_t kdesc = dring + (uint64_t)((slot * 2 * TILE) >> 4);
-                const uint64_t vdesc = kdesc + (uint64_t)(TILE >> 4);
+                const uint64_t kd = dk0 + (uint64_t)((ks * TILE) >> 4), vd = dv0 + (uint64_t)((vs * TILE) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; kk++) {
-                    const uint64_t off = (uint64_t)((kk >> 2) * PANEL + (kk & 3) * 32) >> 4;
-                    mma_ss(tS, dq0 + off, kdesc + off, p.idesc_qk, kk > 0);     // S = Q K^T
-                    mma_ss(tP, ddo + off, vdesc + off, p.idesc_bf16, kk > 0);   // dP = dO V^T
+                    mma_kmajor(tS, dq_, kd, p.idesc_qk, kk);
+                    mma_kmajor(tP, ddo, vd, p.idesc_bf16, kk);
                 }
-                tc_commit(sh.s_full);
-                if (!(ok = mbar_wait(sh.ds_full, t & 1, w))) break;
+                tc_commit(bar + VEMPTY + vs);
+                tc_commit(bar + SFULL);
+                return true;
+            };
+            bool ok = mbar_wait(bar + STAT, 0, w) && T > 0 && issue_sdp(0);
+            for (int t = 0; t < T && ok; t++) {
+                // the row pass has read S(t)/dP(t) and written dS(t) to buffer t & 1
+                if (!(ok = mbar_wait(bar + DSFULL, t & 1, w))) break;
                 tc_fence_after();
-                const uint64_t kmn = dring_mn + (uint64_t)((slot * 2 * TILE) >> 4);
+                if (t + 1 < T && !(ok = issue_sdp(t + 1))) break;
+                const uint64_t kmn = dkmn + (uint64_t)(((t % 3) * TILE) >> 4);
+                const uint32_t ads = tDS + (t & 1) * 64;
 #pragma unroll
                 for (int kk = 0; kk < BM / 16; kk++)
-                    mma_ts(tA, tS + kk * 8, kmn + (uint64_t)((kk * 16 * 128) >> 4), p.idesc_ds_k,
-                           (t > 0 || kk > 0) ? 1u : 0u);                            // dQ += dS K
-                tc_commit(&sh.ld_empty[slot]);
+                    mma_ts(tA, ads + kk * 8, kmn + (uint64_t)((kk * 16 * 128) >> 4), p.idesc_ds_mn,
+                           (t > 0 || kk > 0) ? 1u : 0u);  // dQ += dS K
+                tc_commit(bar + KEMPTY + t % 3);
             }
-            tc_commit(sh.acc_done);
-            tc_commit(sh.drain);
-            mbar_drain(sh.drain, 0, DRAIN_NS);
+            if (ok) tc_commit(bar + ACC);
+            tc_commit(bar + DRAIN);
+            mbar_drain(bar + DRAIN, 0, DRAIN_NS);
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------ compute: one query row per thread
-        const int r = threadIdx.x;
-        const uint32_t lb = tmem + ((uint32_t)(32 * warp) << 16);
+        // ------------------------------------------ rows: lane quarter q4, key half g
+        const int q4 = warp & 3, g = warp >> 2;
+        const int r = 32 * q4 + lane;
+        const uint32_t lb = tmem + ((uint32_t)(32 * q4) << 16);
         const long grow = (long)q0 + r;
         const bool live = grow < p.S;
-        const long li = ((long)b * p.H + h) * p.S + (live ? grow : 0);
-        const float lse2 = live ? p.lse[li] * 1.4426950408889634f : 0.f;
-        const float Di = live ? p.Dsum[li] : 0.f;
+        const float2 ld = live ? p.LD[((long)b * p.H + h) * p.S + grow] : make_float2(0.f, 0.f);
         const float sl2 = p.scale_log2;
         bool ok = true;
         for (int t = 0; t < T; t++) {
-            if (!mbar_wait(sh.s_full, t & 1, w)) {
+            if (!mbar_wait(bar + SFULL, t & 1, w)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < 4; c++) {
+            for (int c = 0; c < 2; c++) {
                 uint32_t sv[32], pv[32], ds[16];
-                tmem_ld32(lb + c * 32, sv);
-                tmem_ld32(lb + 128 + c * 32, pv);
+                tmem_ld32(lb + 64 * g + 32 * c, sv);
+                tmem_ld32(lb + 128 + 64 * g + 32 * c, pv);
                 tmem_ld_wait();
 #pragma unroll
                 for (int k = 0; k < 32; k += 2) {
-                    const float p0 = ex2(fmaf(__uint_as_float(sv[k]), sl2, -lse2));
-                    const float p1 = ex2(fmaf(__uint_as_float(sv[k + 1]), sl2, -lse2));
-                    ds[k / 2] = pack2(p0 * (__uint_as_float(pv[k]) - Di), p1 * (__uint_as_float(pv[k + 1]) - Di),
+                    const float p0 = ex2(fmaf(__uint_as_float(sv[k]), sl2, -ld.x));
+                    const float p1 = ex2(fmaf(__uint_as_float(sv[k + 1]), sl2, -ld.x));
+                    ds[k / 2] = pack2(p0 * (__uint_as_float(pv[k]) - ld.y), p1 * (__uint_as_float(pv[k + 1]) - ld.y),
                                       p.ds_f16);
                 }
-                tmem_st16(lb + c * 16, ds);
+                tmem_st16(lb + 384 + 64 * (t & 1) + 32 * g + 16 * c, ds);
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(sh.ds_full);
+            mbar_arrive(bar + DSFULL);
         }
-        if (ok && mbar_wait(sh.acc_done, 0, w)) {
+        if (ok && mbar_wait(bar + ACC, 0, w)) {
             tc_fence_after();
-            float *dst = p.dq + (((long)b * p.S + (live ? grow : 0)) * p.H + h) * D;
-#pragma unroll
-            for (int c = 0; c < 4; c++) {
-                uint32_t o[32];
-                tmem_ld32(lb + 256 + c * 32, o);
-                tmem_ld_wait();
-                if (live) {
-#pragma unroll
-                    for (int k = 0; k < 32; k += 4)
-                        *reinterpret_cast<float4 *>(dst + c * 32 + k) =
-                            make_float4(__uint_as_float(o[k]) * p.scale, __uint_as_float(o[k + 1]) * p.scale,
-                                        __uint_as_float(o[k + 2]) * p.scale, __uint_as_float(o[k + 3]) * p.scale);
-                }
-            }
+            store_row64(lb + 256 + 64 * g, p.dq + (((long)b * p.S + (live ? grow : 0)) * p.H + h) * D + 64 * g,
+                        p.scale, live);
         }
     }
     bw_teardown(tmem);
 }
 
 // ----------------------------------------------------------------- dkv kernel
+//
+// smem tiles: K 0, V 1, ring slot s: Q 2+2s, dO 3+2s; P^T 6.
+// barriers: stat_full, ld_full[2], ld_empty[2], s_full, consumed (256 arrivals),
+//           pds_ready (256 arrivals), acc_done, drain.
+
+namespace dkvb {
+constexpr int STAT = 0, FULL = 1, EMPTY = 3, SFULL = 5, CONSUMED = 6, PDS = 7, ACC = 8, DRAIN = 9, NB = 10;
+}
 
 __global__ void __launch_bounds__(bw::THREADS, 1)
     bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -308,11 +350,14 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
                    const __grid_constant__ CUtensorMap tm_jk, const __grid_constant__ CUtensorMap tm_jv,
                    const BwParams p) {
     using namespace bw;
+    using namespace dkvb;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const BwShared sh = bw_setup(smem);
-    const uint32_t tmem = *sh.tmem_slot;
-    const WaitCtx w{p.wait_limit_ns, p.err, sh.abort};
+    const int counts[NB] = {1, 1, 1, 1, 1, 1, 256, 256, 1, 1};
+    uint64_t *bar;
+    volatile int *abort_flag;
+    const uint32_t tmem = bw_setup<NB>(smem, counts, bar, abort_flag);
+    const WaitCtx w{p.wait_limit_ns, p.err, abort_flag};
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int KT = p.kv_tiles_v + p.kv_tiles_j;
     const int kt = blockIdx.x % KT;
@@ -321,101 +366,125 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     int map, krow;
     kv_tile(p, kt, map, krow);
     const int T = p.q_tiles;
+    uint8_t *sK = smem, *sV = smem + TILE, *sRing = smem + 2 * TILE, *sP = smem + 6 * TILE;
 
-    if (warp == 4) {
+    if (warp == 8) {
         if (lane == 0) {
-            mbar_arrive_expect_tx(sh.stat_full, 2 * TILE);
-            for (int half = 0; half < 2; half++) {
-                tma_load_4d(smem + SMEM_STAT + half * PANEL, map ? &tm_jk : &tm_k, sh.stat_full, half * 64, h, krow,
-                            b);
-                tma_load_4d(smem + SMEM_STAT + TILE + half * PANEL, map ? &tm_jv : &tm_v, sh.stat_full, half * 64,
-                            h, krow, b);
-            }
+            mbar_arrive_expect_tx(bar + STAT, 2 * TILE);
+            load_tile(sK, map ? &tm_jk : &tm_k, bar + STAT, h, krow, b);
+            load_tile(sV, map ? &tm_jv : &tm_v, bar + STAT, h, krow, b);
             int issued = 0;
             for (int t = 0; t < T; t++) {
-                const int slot = t & 1;
-                if (!mbar_wait(&sh.ld_empty[slot], ((t >> 1) & 1) ^ 1, w)) break;
-                mbar_arrive_expect_tx(&sh.ld_full[slot], 2 * TILE);
-                uint8_t *dst = smem + SMEM_RING + slot * 2 * TILE;
-                for (int half = 0; half < 2; half++) {
-                    tma_load_4d(dst + half * PANEL, &tm_q, &sh.ld_full[slot], half * 64, h, t * BM, b);
-                    tma_load_4d(dst + TILE + half * PANEL, &tm_do, &sh.ld_full[slot], half * 64, h, t * BM, b);
-                }
+                const int s = t & 1;
+                if (!mbar_wait(bar + EMPTY + s, ((t >> 1) & 1) ^ 1, w)) break;
+                mbar_arrive_expect_tx(bar + FULL + s, 2 * TILE);
+                load_tile(sRing + 2 * s * TILE, &tm_q, bar + FULL + s, h, t * BM, b);
+                load_tile(sRing + (2 * s + 1) * TILE, &tm_do, bar + FULL + s, h, t * BM, b);
                 issued++;
             }
-            mbar_drain(sh.stat_full, 0, DRAIN_NS);
+            mbar_drain(bar + STAT, 0, DRAIN_NS);
             for (int t = issued > 2 ? issued - 2 : 0; t < issued; t++)
-                mbar_drain(&sh.ld_full[t & 1], (t >> 1) & 1, DRAIN_NS);
+                mbar_drain(bar + FULL + (t & 1), (t >> 1) & 1, DRAIN_NS);
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         if (lane == 0) {
             const uint32_t tS = tmem, tP = tmem + 128, tV = tmem + 256, tK = tmem + 384;
-            const uint64_t dk0 = smem_desc_sw128(smem_u32(smem + SMEM_STAT), 16, 1024);      // K (K-major)
-            const uint64_t dv0 = dk0 + (uint64_t)(TILE >> 4);                             // V (K-major)
-            const uint64_t dring = smem_desc_sw128(smem_u32(smem + SMEM_RING), 16, 1024);  // Q / dO (K-major)
-            const uint64_t dring_mn = smem_desc_sw128(smem_u32(smem + SMEM_RING), PANEL, 1024);
-            bool ok = mbar_wait(sh.stat_full, 0, w);
-            for (int t = 0; t < T && ok; t++) {
-                const int slot = t & 1;
-                if (!(ok = mbar_wait(&sh.ld_full[slot], (t >> 1) & 1, w))) break;
+            const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
+            const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), 16, 1024);
+            const uint64_t dring = smem_desc_sw128(smem_u32(sRing), 16, 1024);
+            const uint64_t dring_mn = smem_desc_sw128(smem_u32(sRing), PANEL, 1024);
+            const uint64_t dp = smem_desc_sw128(smem_u32(sP), 16, 1024);
+            // descriptor of tile `which` (0 Q, 1 dO) of the ring slot of tile t
+            auto slot = [&](uint64_t base, int t, int which) {
+                return base + (uint64_t)(((2 * (t & 1) + which) * TILE) >> 4);
+            };
+            auto wait_full = [&](int t) { return mbar_wait(bar + FULL + (t & 1), (t >> 1) & 1, w); };
+            bool ok = mbar_wait(bar + STAT, 0, w) && T > 0 && wait_full(0);
+            if (ok) {
                 tc_fence_after();
-                const uint64_t qdesc = dring + (uint64_t)((slot * 2 * TILE) >> 4);
-                const uint64_t odesc = qdesc + (uint64_t)(TILE >> 4);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; kk++) {
-                    const uint64_t off = (uint64_t)((kk >> 2) * PANEL + (kk & 3) * 32) >> 4;
-                    mma_ss(tS, dk0 + off, qdesc + off, p.idesc_qk, kk > 0);     // S^T = K Q^T
-                    mma_ss(tP, dv0 + off, odesc + off, p.idesc_bf16, kk > 0);   // dP^T = V dO^T
+                    mma_kmajor(tS, dk0, slot(dring, 0, 0), p.idesc_qk, kk);    // S^T = K Q^T
+                    mma_kmajor(tP, dv0, slot(dring, 0, 1), p.idesc_bf16, kk);  // dP^T = V dO^T
                 }
-                tc_commit(sh.s_full);
-                if (!(ok = mbar_wait(sh.ds_full, t & 1, w))) break;
+                tc_commit(bar + SFULL);
+            }
+            for (int t = 0; t < T && ok; t++) {
+                // the row pass has read S^T(t), dP^T(t): S^T(t+1) may overwrite its columns
+                if (!(ok = mbar_wait(bar + CONSUMED, t & 1, w))) break;
                 tc_fence_after();
-                const uint64_t qmn = dring_mn + (uint64_t)((slot * 2 * TILE) >> 4);
-                const uint64_t omn = qmn + (uint64_t)(TILE >> 4);
+                const bool next = t + 1 < T;
+                if (next) {
+                    if (!(ok = wait_full(t + 1))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; kk++) mma_kmajor(tS, dk0, slot(dring, t + 1, 0), p.idesc_qk, kk);
+                }
+                // P^T(t) is in shared memory and dS^T(t) over dP^T(t)
+                if (!(ok = mbar_wait(bar + PDS, t & 1, w))) break;
+                tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < BM / 16; kk++) {
-                    const uint64_t off = (uint64_t)((kk * 16 * 128) >> 4);
-                    mma_ts(tV, tS + kk * 8, omn + off, p.idesc_bf16 | (1u << 16), (t > 0 || kk > 0) ? 1u : 0u);
-                    mma_ts(tK, tP + kk * 8, qmn + off, p.idesc_ds_q, (t > 0 || kk > 0) ? 1u : 0u);
+                    const uint64_t poff = (uint64_t)((kk >> 2) * PANEL + (kk & 3) * 32) >> 4;
+                    const uint64_t boff = (uint64_t)((kk * 16 * 128) >> 4);
+                    const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
+                    mma_ss(tV, dp + poff, slot(dring_mn, t, 1) + boff, p.idesc_bf16_mn, acc);  // dV += P^T dO
+                    mma_ts(tK, tP + (kk >> 2) * 64 + (kk & 3) * 8, slot(dring_mn, t, 0) + boff, p.idesc_ds_mn,
+                           acc);                                                               // dK += dS^T Q
                 }
-                tc_commit(&sh.ld_empty[slot]);
+                tc_commit(bar + EMPTY + (t & 1));
+                if (next) {
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; kk++) mma_kmajor(tP, dv0, slot(dring, t + 1, 1), p.idesc_bf16, kk);
+                    tc_commit(bar + SFULL);
+                }
             }
-            tc_commit(sh.acc_done);
-            tc_commit(sh.drain);
-            mbar_drain(sh.drain, 0, DRAIN_NS);
+            if (ok) tc_commit(bar + ACC);
+            tc_commit(bar + DRAIN);
+            mbar_drain(bar + DRAIN, 0, DRAIN_NS);
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------ compute: one key row per thread
-        const int r = threadIdx.x;
-        const uint32_t lb = tmem + ((uint32_t)(32 * warp) << 16);
+        // ------------------------------------------ rows: key row r, query half g
+        const int q4 = warp & 3, g = warp >> 2;
+        const int r = 32 * q4 + lane;
+        const uint32_t lb = tmem + ((uint32_t)(32 * q4) << 16);
         const float sl2 = p.scale_log2;
-        const float *lse_bh = p.lse + ((long)b * p.H + h) * p.S;
-        const float *d_bh = p.Dsum + ((long)b * p.H + h) * p.S;
+        const float2 *ld_bh = p.LD + ((long)b * p.H + h) * p.S;
+        // this thread's row of P^T panel g: 8 chunks of 16 bytes, 128-byte swizzle
+        const uint32_t prow = smem_u32(sP) + g * PANEL + (r >> 3) * 1024 + (r & 7) * 128;
         bool ok = true;
         for (int t = 0; t < T; t++) {
-            if (!mbar_wait(sh.s_full, t & 1, w)) {
+            if (!mbar_wait(bar + SFULL, t & 1, w)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
+            // S^T of this half into registers, then its columns are free for S^T(t+1)
+            uint32_t sv[2][32];
+            tmem_ld32(lb + 64 * g, sv[0]);
+            tmem_ld32(lb + 64 * g + 32, sv[1]);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(bar + CONSUMED);
 #pragma unroll
-            for (int c = 0; c < 4; c++) {
-                uint32_t sv[32], pv[32], pk[16], ds[16];
-                tmem_ld32(lb + c * 32, sv);
-                tmem_ld32(lb + 128 + c * 32, pv);
+            for (int c = 0; c < 2; c++) {
+                // dP^T in 32-column chunks; dS^T goes over columns this thread has read
+                uint32_t pv[32], pk[16], ds[16];
+                tmem_ld32(lb + 128 + 64 * g + 32 * c, pv);
                 tmem_ld_wait();
+                const long qb = (long)t * BM + 64 * g + 32 * c;  // first query of the chunk
 #pragma unroll
                 for (int k = 0; k < 32; k += 2) {
                     float pe[2], de[2];
 #pragma unroll
                     for (int e = 0; e < 2; e++) {
-                        const long qrow = (long)t * BM + c * 32 + k + e;  // column = query row (warp-uniform)
+                        const long qrow = qb + k + e;  // warp-uniform
                         if (qrow < p.S) {
-                            const float l2 = __ldg(lse_bh + qrow) * 1.4426950408889634f;
-                            pe[e] = ex2(fmaf(__uint_as_float(sv[k + e]), sl2, -l2));
-                            de[e] = pe[e] * (__uint_as_float(pv[k + e]) - __ldg(d_bh + qrow));
+                            const float2 ld = __ldg(ld_bh + qrow);
+                            pe[e] = ex2(fmaf(__uint_as_float(sv[c][k + e]), sl2, -ld.x));
+                            de[e] = pe[e] * (__uint_as_float(pv[k + e]) - ld.y);
                         } else {
                             pe[e] = 0.f;
                             de[e] = 0.f;
@@ -424,39 +493,27 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
                     pk[k / 2] = pack_bf16x2(pe[0], pe[1]);
                     ds[k / 2] = pack2(de[0], de[1], p.ds_f16);
                 }
-                tmem_st16(lb + c * 16, pk);        // P^T over S^T
-                tmem_st16(lb + 128 + c * 16, ds);  // dS^T over dP^T
+#pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    const int chunk = 4 * c + j;  // 16-byte chunk of the 128-byte row
+                    st_shared_v4(prow + ((chunk ^ (r & 7)) << 4), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2],
+                                 pk[4 * j + 3]);
+                }
+                tmem_st16(lb + 128 + 64 * g + 16 * c, ds);
             }
+            fence_proxy_async_smem();
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(sh.ds_full);
+            mbar_arrive(bar + PDS);
         }
-        if (ok && mbar_wait(sh.acc_done, 0, w)) {
+        if (ok && mbar_wait(bar + ACC, 0, w)) {
             tc_fence_after();
             const long kr = (long)krow + r;
             const long rows = map ? p.Nj : p.Nv;
             const bool live = kr < rows;
-            const long off = (((long)b * rows + (live ? kr : 0)) * p.H + h) * D;
-            float *dkp = (map ? p.djk : p.dk) + off;
-            float *dvp = (map ? p.djv : p.dv) + off;
-#pragma unroll
-            for (int c = 0; c < 4; c++) {
-                uint32_t gk[32], gv[32];
-                tmem_ld32(lb + 384 + c * 32, gk);
-                tmem_ld32(lb + 256 + c * 32, gv);
-                tmem_ld_wait();
-                if (live) {
-#pragma unroll
-                    for (int k = 0; k < 32; k += 4) {
-                        *reinterpret_cast<float4 *>(dkp + c * 32 + k) =
-                            make_float4(__uint_as_float(gk[k]) * p.scale, __uint_as_float(gk[k + 1]) * p.scale,
-                                        __uint_as_float(gk[k + 2]) * p.scale, __uint_as_float(gk[k + 3]) * p.scale);
-                        *reinterpret_cast<float4 *>(dvp + c * 32 + k) =
-                            make_float4(__uint_as_float(gv[k]), __uint_as_float(gv[k + 1]), __uint_as_float(gv[k + 2]),
-                                        __uint_as_float(gv[k + 3]));
-                    }
-                }
-            }
+            const long off = (((long)b * rows + (live ? kr : 0)) * p.H + h) * D + 64 * g;
+            store_row64(lb + 384 + 64 * g, (map ? p.djk : p.dk) + off, p.scale, live);
+            store_row64(lb + 256 + 64 * g, (map ? p.djv : p.dv) + off, 1.0f, live);
         }
     }
     bw_teardown(tmem);
@@ -465,11 +522,11 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
 // ------------------------------------------------------------------- host
 
 static bool bw_map(CUtensorMap *m, const void *base, long rows, int H, int B, bool f16, const char **why) {
-    void *fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
     static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     static std::once_flag once;
-    std::call_once(once, [&] {
+    std::call_once(once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
@@ -493,7 +550,7 @@ static bool bw_map(CUtensorMap *m, const void *base, long rows, int H, int B, bo
 }
 
 cudaError_t launch_attn_bwd(const Geom &g, bool qk_f16, const void *q, const void *k, const void *v, const void *jk,
-                            const void *jv, const void *out, const void *dout, const float *lse, float *Dsum, float *dq,
+                            const void *jv, const void *out, const void *dout, const float *lse, float2 *LD, float *dq,
                             float *dk, float *dv, float *djk, float *djv, unsigned long long wait_limit_ns, int *err,
                             cudaStream_t st, const char **why) {
     const long rows = (long)g.B * g.S * g.H;
@@ -501,8 +558,6 @@ cudaError_t launch_attn_bwd(const Geom &g, bool qk_f16, const void *q, const voi
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    bwd_dsum_kernel<<<(unsigned)sms * 8, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(out),
-                                                       static_cast<const __nv_bfloat16 *>(dout), g.S, g.H, g.B, Dsum);
     CUtensorMap mq, mdo, mk, mv, mjk, mjv;
     const bool has_joint = g.Nj > 0;
     if (!bw_map(&mq, q, g.S, g.H, g.B, qk_f16, why) || !bw_map(&mdo, dout, g.S, g.H, g.B, false, why) ||
@@ -519,6 +574,9 @@ cudaError_t launch_attn_bwd(const Geom &g, bool qk_f16, const void *q, const voi
                                             bw::SMEM_ALLOC);
     });
     if (attr_err != cudaSuccess) return attr_err;
+    bwd_dsum_kernel<<<(unsigned)sms * 8, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(out),
+                                                       static_cast<const __nv_bfloat16 *>(dout), lse, g.S, g.H, g.B,
+                                                       LD);
     BwParams p;
     p.S = g.S, p.Nv = g.Nv, p.Nj = g.Nj, p.H = g.H;
     p.q_tiles = (int)((g.S + bw::BM - 1) / bw::BM);
@@ -526,15 +584,15 @@ cudaError_t launch_attn_bwd(const Geom &g, bool qk_f16, const void *q, const voi
     p.kv_tiles_j = (int)((g.Nj + bw::BM - 1) / bw::BM);
     p.scale = (float)(1.0 / sqrt((double)g.d));
     p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)g.d));
-    p.lse = lse, p.Dsum = Dsum;
+    p.LD = LD;
     p.dq = dq, p.dk = dk, p.dv = dv, p.djk = djk, p.djv = djv;
     // A/B formats: bits 7-9 and 10-12 (0 = fp16, 1 = bf16); bit 16: B MN-major
     const uint32_t base = idesc_bf16_f32(bw::BM, bw::BM, false) & ~((7u << 7) | (7u << 10));
     const uint32_t f16 = base, bf16 = base | (1u << 7) | (1u << 10);
-    p.idesc_qk = qk_f16 ? f16 : bf16;          // S = Q K^T
-    p.idesc_bf16 = bf16;                       // dP = dO V^T (and dV with the MN bit)
-    p.idesc_ds_k = (qk_f16 ? f16 : bf16) | (1u << 16);  // dQ += dS K  (dS in K's type, K MN-major)
-    p.idesc_ds_q = (qk_f16 ? f16 : bf16) | (1u << 16);  // dK += dS^T Q
+    p.idesc_qk = qk_f16 ? f16 : bf16;                    // S = Q K^T
+    p.idesc_bf16 = bf16;                                 // dP = dO V^T
+    p.idesc_bf16_mn = bf16 | (1u << 16);                 // dV += P^T dO
+    p.idesc_ds_mn = (qk_f16 ? f16 : bf16) | (1u << 16);  // dQ += dS K, dK += dS^T Q (dS in the q/k type)
     p.ds_f16 = qk_f16 ? 1 : 0;
     p.wait_limit_ns = wait_limit_ns;
     p.err = err;

@@ -88,10 +88,10 @@ cudaError_t launch_attn_tc(const Geom &g, const void *q, const void *k, const vo
                            const void *jv, int n_chunks, void *out, float *lse, const AttnTcOptions &opt,
                            cudaStream_t st, const char **why);
 
-// Backward pass (bf16 v/out/dout, q/k bf16 or fp16, d = 128): the D_i pre-pass
-// into Dsum [B][H][S], then the dq kernel and the dk/dv kernel.
+// Backward pass (bf16 v/out/dout, q/k bf16 or fp16, d = 128): the pre-pass
+// into LD [B][H][S] = {lse * log2(e), D_i}, then the dq kernel and the dk/dv kernel.
 cudaError_t launch_attn_bwd(const Geom &g, bool qk_f16, const void *q, const void *k, const void *v, const void *jk,
-                            const void *jv, const void *out, const void *dout, const float *lse, float *Dsum, float *dq,
+                            const void *jv, const void *out, const void *dout, const float *lse, float2 *LD, float *dq,
                             float *dk, float *dv, float *djk, float *djv, unsigned long long wait_limit_ns, int *err,
                             cudaStream_t st, const char **why);
 
