@@ -69,6 +69,30 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool f16) {
     return pack_bf16x2(lo, hi);
 }
 
+// 32 lanes x 16 consecutive 32-bit columns (load) / 8 columns (store).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
+// 2^x on the special function unit, kept in program order (volatile) so the
+// exps of a row pass run before the wait that follows them.
+__device__ __forceinline__ float ex2_here(float x) {
+    float y;
+    asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -337,11 +361,22 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
 // ----------------------------------------------------------------- dkv kernel
 //
 // smem tiles: K 0, V 1, ring slot s: Q 2+2s, dO 3+2s; P^T 6.
-// barriers: stat_full, ld_full[2], ld_empty[2], s_full, consumed (256 arrivals),
-//           pds_ready (256 arrivals), acc_done, drain.
+// barriers: stat_full, q_full[2], do_full[2], q_empty[2], do_empty[2], s_ready
+//           (S^T(i) done), consumed (256 arrivals: S^T(i) read), pds_ready (256
+//           arrivals: P^T(i) in shared memory, dS^T(i) in tensor memory), window
+//           (dV/dK(i-1) and dP^T(i) done), acc_done, drain.
+// Q and dO slots are released separately: Q(i) once dK(i) is done, midway
+// through the window, so Q(i+2) is in flight while the window finishes.
+//
+// Per tile i the MMA thread issues S^T(i+1) as soon as the row pass has read
+// S^T(i), then, once P^T(i)/dS^T(i) are published, the window dK(i) | dV(i)
+// first half, then dP^T(i+1) | dV(i) second half (dP^T(i+1) overwrites dS^T(i),
+// so it follows every dK(i) MMA).  The row pass of tile i+1 computes its P from
+// S^T(i+1) while that window runs, and only the dS / P^T stores wait for it.
 
 namespace dkvb {
-constexpr int STAT = 0, FULL = 1, EMPTY = 3, SFULL = 5, CONSUMED = 6, PDS = 7, ACC = 8, DRAIN = 9, NB = 10;
+constexpr int STAT = 0, QFULL = 1, DOFULL = 3, QEMPTY = 5, DOEMPTY = 7, SREADY = 9, CONSUMED = 10, PDS = 11,
+              WIN = 12, ACC = 13, DRAIN = 14, NB = 15;
 }
 
 __global__ void __launch_bounds__(bw::THREADS, 1)
@@ -353,7 +388,7 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     using namespace dkvb;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int counts[NB] = {1, 1, 1, 1, 1, 1, 256, 256, 1, 1};
+    const int counts[NB] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 256, 256, 1, 1, 1};
     uint64_t *bar;
     volatile int *abort_flag;
     const uint32_t tmem = bw_setup<NB>(smem, counts, bar, abort_flag);
@@ -373,18 +408,23 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
             mbar_arrive_expect_tx(bar + STAT, 2 * TILE);
             load_tile(sK, map ? &tm_jk : &tm_k, bar + STAT, h, krow, b);
             load_tile(sV, map ? &tm_jv : &tm_v, bar + STAT, h, krow, b);
-            int issued = 0;
+            int nq = 0, ndo = 0;  // Q and dO tiles issued
             for (int t = 0; t < T; t++) {
                 const int s = t & 1;
-                if (!mbar_wait(bar + EMPTY + s, ((t >> 1) & 1) ^ 1, w)) break;
-                mbar_arrive_expect_tx(bar + FULL + s, 2 * TILE);
-                load_tile(sRing + 2 * s * TILE, &tm_q, bar + FULL + s, h, t * BM, b);
-                load_tile(sRing + (2 * s + 1) * TILE, &tm_do, bar + FULL + s, h, t * BM, b);
-                issued++;
+                const uint32_t par = ((t >> 1) & 1) ^ 1;
+                if (!mbar_wait(bar + QEMPTY + s, par, w)) break;
+                mbar_arrive_expect_tx(bar + QFULL + s, TILE);
+                load_tile(sRing + 2 * s * TILE, &tm_q, bar + QFULL + s, h, t * BM, b);
+                nq++;
+                if (!mbar_wait(bar + DOEMPTY + s, par, w)) break;
+                mbar_arrive_expect_tx(bar + DOFULL + s, TILE);
+                load_tile(sRing + (2 * s + 1) * TILE, &tm_do, bar + DOFULL + s, h, t * BM, b);
+                ndo++;
             }
             mbar_drain(bar + STAT, 0, DRAIN_NS);
-            for (int t = issued > 2 ? issued - 2 : 0; t < issued; t++)
-                mbar_drain(bar + FULL + (t & 1), (t >> 1) & 1, DRAIN_NS);
+            for (int t = nq > 2 ? nq - 2 : 0; t < nq; t++) mbar_drain(bar + QFULL + (t & 1), (t >> 1) & 1, DRAIN_NS);
+            for (int t = ndo > 2 ? ndo - 2 : 0; t < ndo; t++)
+                mbar_drain(bar + DOFULL + (t & 1), (t >> 1) & 1, DRAIN_NS);
         }
         __syncwarp();
     } else if (warp == 9) {
@@ -399,46 +439,59 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
             auto slot = [&](uint64_t base, int t, int which) {
                 return base + (uint64_t)(((2 * (t & 1) + which) * TILE) >> 4);
             };
-            auto wait_full = [&](int t) { return mbar_wait(bar + FULL + (t & 1), (t >> 1) & 1, w); };
-            bool ok = mbar_wait(bar + STAT, 0, w) && T > 0 && wait_full(0);
+            auto wait_q = [&](int t) { return mbar_wait(bar + QFULL + (t & 1), (t >> 1) & 1, w); };
+            auto wait_do = [&](int t) { return mbar_wait(bar + DOFULL + (t & 1), (t >> 1) & 1, w); };
+            bool ok = mbar_wait(bar + STAT, 0, w) && T > 0 && wait_q(0);
             if (ok) {
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < D / 16; kk++) {
-                    mma_kmajor(tS, dk0, slot(dring, 0, 0), p.idesc_qk, kk);    // S^T = K Q^T
-                    mma_kmajor(tP, dv0, slot(dring, 0, 1), p.idesc_bf16, kk);  // dP^T = V dO^T
-                }
-                tc_commit(bar + SFULL);
+                for (int kk = 0; kk < D / 16; kk++) mma_kmajor(tS, dk0, slot(dring, 0, 0), p.idesc_qk, kk);  // S^T = K Q^T
+                tc_commit(bar + SREADY);
+                ok = wait_do(0);
+            }
+            if (ok) {
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; kk++) mma_kmajor(tP, dv0, slot(dring, 0, 1), p.idesc_bf16, kk);  // dP^T = V dO^T
+                tc_commit(bar + WIN);
             }
             for (int t = 0; t < T && ok; t++) {
-                // the row pass has read S^T(t), dP^T(t): S^T(t+1) may overwrite its columns
+                // the row pass has read S^T(t): S^T(t+1) may overwrite its columns
                 if (!(ok = mbar_wait(bar + CONSUMED, t & 1, w))) break;
                 tc_fence_after();
                 const bool next = t + 1 < T;
                 if (next) {
-                    if (!(ok = wait_full(t + 1))) break;
+                    if (!(ok = wait_q(t + 1))) break;
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < D / 16; kk++) mma_kmajor(tS, dk0, slot(dring, t + 1, 0), p.idesc_qk, kk);
+                    tc_commit(bar + SREADY);
                 }
                 // P^T(t) is in shared memory and dS^T(t) over dP^T(t)
                 if (!(ok = mbar_wait(bar + PDS, t & 1, w))) break;
+                if (next && !(ok = wait_do(t + 1))) break;
                 tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < BM / 16; kk++) {
+                const uint32_t acc = t > 0 ? 1u : 0u;
+                auto dv_step = [&](int kk) {  // dV += P^T dO
                     const uint64_t poff = (uint64_t)((kk >> 2) * PANEL + (kk & 3) * 32) >> 4;
-                    const uint64_t boff = (uint64_t)((kk * 16 * 128) >> 4);
-                    const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
-                    mma_ss(tV, dp + poff, slot(dring_mn, t, 1) + boff, p.idesc_bf16_mn, acc);  // dV += P^T dO
-                    mma_ts(tK, tP + (kk >> 2) * 64 + (kk & 3) * 8, slot(dring_mn, t, 0) + boff, p.idesc_ds_mn,
-                           acc);                                                               // dK += dS^T Q
-                }
-                tc_commit(bar + EMPTY + (t & 1));
-                if (next) {
+                    mma_ss(tV, dp + poff, slot(dring_mn, t, 1) + (uint64_t)((kk * 16 * 128) >> 4), p.idesc_bf16_mn,
+                           acc | (kk > 0 ? 1u : 0u));
+                };
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; kk++) mma_kmajor(tP, dv0, slot(dring, t + 1, 1), p.idesc_bf16, kk);
-                    tc_commit(bar + SFULL);
+                for (int kk = 0; kk < BM / 16; kk++) {  // dK += dS^T Q
+                    mma_ts(tK, tP + (kk >> 2) * 64 + (kk & 3) * 8,
+                           slot(dring_mn, t, 0) + (uint64_t)((kk * 16 * 128) >> 4), p.idesc_ds_mn,
+                           acc | (kk > 0 ? 1u : 0u));
+                    if (kk < 4) dv_step(kk);
                 }
+                tc_commit(bar + QEMPTY + (t & 1));  // Q(t): S^T(t) and dK(t) done
+#pragma unroll
+                for (int kk = 0; kk < D / 16; kk++) {
+                    if (next) mma_kmajor(tP, dv0, slot(dring, t + 1, 1), p.idesc_bf16, kk);  // dP^T(t+1)
+                    if (kk < 4) dv_step(4 + kk);
+                }
+                tc_commit(bar + DOEMPTY + (t & 1));  // dO(t): dP^T(t) and dV(t) done
+                tc_commit(bar + WIN);
             }
             if (ok) tc_commit(bar + ACC);
             tc_commit(bar + DRAIN);
@@ -456,7 +509,7 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
         const uint32_t prow = smem_u32(sP) + g * PANEL + (r >> 3) * 1024 + (r & 7) * 128;
         bool ok = true;
         for (int t = 0; t < T; t++) {
-            if (!mbar_wait(bar + SFULL, t & 1, w)) {
+            if (!mbar_wait(bar + SREADY, t & 1, w)) {
                 ok = false;
                 break;
             }
@@ -468,38 +521,52 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
             tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(bar + CONSUMED);
+            // P = 2^(s log2(e)/sqrt(d) - lse log2(e)); queries past S get lse = +inf, so P = 0
+            const long qb = (long)t * BM + 64 * g;  // first query of this half
+            // P in fp32 registers: rounded to bf16 for dV (through shared memory), exact for dS
+            float pr[64];
 #pragma unroll
             for (int c = 0; c < 2; c++) {
-                // dP^T in 32-column chunks; dS^T goes over columns this thread has read
-                uint32_t pv[32], pk[16], ds[16];
-                tmem_ld32(lb + 128 + 64 * g + 32 * c, pv);
-                tmem_ld_wait();
-                const long qb = (long)t * BM + 64 * g + 32 * c;  // first query of the chunk
 #pragma unroll
-                for (int k = 0; k < 32; k += 2) {
-                    float pe[2], de[2];
+                for (int k = 0; k < 32; k++) {
+                    const long qrow = qb + 32 * c + k;  // warp-uniform
+                    const float l2 = qrow < p.S ? ld_bh[qrow].x : __int_as_float(0x7f800000);
+                    pr[32 * c + k] = ex2_here(fmaf(__uint_as_float(sv[c][k]), sl2, -l2));
+                }
+                asm volatile("" ::: "memory");  // one half's loads at a time (register pressure)
+            }
+            // dV/dK(t-1) and dP^T(t) done: the P^T buffer is free and dP^T(t) is in place
+            if (!mbar_wait(bar + WIN, t & 1, w)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < 4; c++) {
+                // dP^T in 16-column chunks; dS^T goes over columns this thread has read
+                uint32_t pv[16], ds[8], pk[8];
+                tmem_ld16(lb + 128 + 64 * g + 16 * c, pv);
+                tmem_ld_wait();
+#pragma unroll
+                for (int k = 0; k < 16; k += 2) {
+                    float de[2];
 #pragma unroll
                     for (int e = 0; e < 2; e++) {
-                        const long qrow = qb + k + e;  // warp-uniform
-                        if (qrow < p.S) {
-                            const float2 ld = __ldg(ld_bh + qrow);
-                            pe[e] = ex2(fmaf(__uint_as_float(sv[c][k + e]), sl2, -ld.x));
-                            de[e] = pe[e] * (__uint_as_float(pv[k + e]) - ld.y);
-                        } else {
-                            pe[e] = 0.f;
-                            de[e] = 0.f;
-                        }
+                        const long qrow = qb + 16 * c + k + e;
+                        // plain load: the clobber of the tensor-memory load above keeps it in this chunk
+                        const float dd = qrow < p.S ? ld_bh[qrow].y : 0.f;
+                        de[e] = pr[16 * c + k + e] * (__uint_as_float(pv[k + e]) - dd);
                     }
-                    pk[k / 2] = pack_bf16x2(pe[0], pe[1]);
                     ds[k / 2] = pack2(de[0], de[1], p.ds_f16);
+                    pk[k / 2] = pack_bf16x2(pr[16 * c + k], pr[16 * c + k + 1]);
                 }
 #pragma unroll
-                for (int j = 0; j < 4; j++) {
-                    const int chunk = 4 * c + j;  // 16-byte chunk of the 128-byte row
+                for (int j = 0; j < 2; j++) {
+                    const int chunk = 2 * c + j;  // 16-byte chunk of the 128-byte row
                     st_shared_v4(prow + ((chunk ^ (r & 7)) << 4), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2],
                                  pk[4 * j + 3]);
                 }
-                tmem_st16(lb + 128 + 64 * g + 16 * c, ds);
+                tmem_st8(lb + 128 + 64 * g + 8 * c, ds);
             }
             fence_proxy_async_smem();
             tmem_st_wait();
