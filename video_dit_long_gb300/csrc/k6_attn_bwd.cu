@@ -358,6 +358,56 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     bw_teardown(tmem);
 }
 
+// Row pass of the dk/dv kernel for one key row and 64 queries (FULL: all live).
+// P for the 64 queries from S^T in registers; queries j >= nq get P = 0.
+template <bool FULL>
+__device__ __forceinline__ void p_half(float (&pr)[64], const uint32_t (&sv)[2][32], const float2 *ldq, int nq,
+                                       float sl2) {
+#pragma unroll
+    for (int c = 0; c < 2; c++) {
+#pragma unroll
+        for (int k = 0; k < 32; k++) {
+            const int j = 32 * c + k;
+            const float l2 = (FULL || j < nq) ? ldq[j].x : __int_as_float(0x7f800000);
+            pr[j] = ex2_here(fmaf(__uint_as_float(sv[c][k]), sl2, -l2));
+        }
+        asm volatile("" ::: "memory");  // one half's loads at a time (register pressure)
+    }
+}
+
+// dS^T = P (dP^T - D) over the 64 columns at taddr (16-column chunks; each chunk's
+// dS^T lands on columns already read), and P rounded to bf16 into this thread's
+// row of the swizzled P^T panel at prow.
+template <bool FULL>
+__device__ __forceinline__ void ds_half(const float (&pr)[64], const float2 *ldq, int nq, uint32_t taddr,
+                                        uint32_t prow, int r, int ds_f16) {
+#pragma unroll
+    for (int c = 0; c < 4; c++) {
+        uint32_t pv[16], ds[8], pk[8];
+        tmem_ld16(taddr + 16 * c, pv);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 16; k += 2) {
+            float de[2];
+#pragma unroll
+            for (int e = 0; e < 2; e++) {
+                const int j = 16 * c + k + e;
+                // plain load: the clobber of the tensor-memory load above keeps it in this chunk
+                const float dd = (FULL || j < nq) ? ldq[j].y : 0.f;
+                de[e] = pr[j] * (__uint_as_float(pv[k + e]) - dd);
+            }
+            ds[k / 2] = pack2(de[0], de[1], ds_f16);
+            pk[k / 2] = pack_bf16x2(pr[16 * c + k], pr[16 * c + k + 1]);
+        }
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+            const int chunk = 2 * c + i;  // 16-byte chunk of the 128-byte row
+            st_shared_v4(prow + ((chunk ^ (r & 7)) << 4), pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+        tmem_st8(taddr + 8 * c, ds);
+    }
+}
+
 // ----------------------------------------------------------------- dkv kernel
 //
 // smem tiles: K 0, V 1, ring slot s: Q 2+2s, dO 3+2s; P^T 6.
@@ -523,51 +573,23 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
             mbar_arrive(bar + CONSUMED);
             // P = 2^(s log2(e)/sqrt(d) - lse log2(e)); queries past S get lse = +inf, so P = 0
             const long qb = (long)t * BM + 64 * g;  // first query of this half
-            // P in fp32 registers: rounded to bf16 for dV (through shared memory), exact for dS
+            const float2 *ldq = ld_bh + qb;
+            const int nq = p.S - qb >= 64 ? 64 : (int)(p.S - qb);  // live queries of this half (warp-uniform)
             float pr[64];
-#pragma unroll
-            for (int c = 0; c < 2; c++) {
-#pragma unroll
-                for (int k = 0; k < 32; k++) {
-                    const long qrow = qb + 32 * c + k;  // warp-uniform
-                    const float l2 = qrow < p.S ? ld_bh[qrow].x : __int_as_float(0x7f800000);
-                    pr[32 * c + k] = ex2_here(fmaf(__uint_as_float(sv[c][k]), sl2, -l2));
-                }
-                asm volatile("" ::: "memory");  // one half's loads at a time (register pressure)
-            }
+            if (nq == 64)
+                p_half<true>(pr, sv, ldq, 64, sl2);
+            else
+                p_half<false>(pr, sv, ldq, nq, sl2);
             // dV/dK(t-1) and dP^T(t) done: the P^T buffer is free and dP^T(t) is in place
             if (!mbar_wait(bar + WIN, t & 1, w)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < 4; c++) {
-                // dP^T in 16-column chunks; dS^T goes over columns this thread has read
-                uint32_t pv[16], ds[8], pk[8];
-                tmem_ld16(lb + 128 + 64 * g + 16 * c, pv);
-                tmem_ld_wait();
-#pragma unroll
-                for (int k = 0; k < 16; k += 2) {
-                    float de[2];
-#pragma unroll
-                    for (int e = 0; e < 2; e++) {
-                        const long qrow = qb + 16 * c + k + e;
-                        // plain load: the clobber of the tensor-memory load above keeps it in this chunk
-                        const float dd = qrow < p.S ? ld_bh[qrow].y : 0.f;
-                        de[e] = pr[16 * c + k + e] * (__uint_as_float(pv[k + e]) - dd);
-                    }
-                    ds[k / 2] = pack2(de[0], de[1], p.ds_f16);
-                    pk[k / 2] = pack_bf16x2(pr[16 * c + k], pr[16 * c + k + 1]);
-                }
-#pragma unroll
-                for (int j = 0; j < 2; j++) {
-                    const int chunk = 2 * c + j;  // 16-byte chunk of the 128-byte row
-                    st_shared_v4(prow + ((chunk ^ (r & 7)) << 4), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2],
-                                 pk[4 * j + 3]);
-                }
-                tmem_st8(lb + 128 + 64 * g + 8 * c, ds);
-            }
+            if (nq == 64)
+                ds_half<true>(pr, ldq, 64, lb + 128 + 64 * g, prow, r, p.ds_f16);
+            else
+                ds_half<false>(pr, ldq, nq, lb + 128 + 64 * g, prow, r, p.ds_f16);
             fence_proxy_async_smem();
             tmem_st_wait();
             tc_fence_before();
