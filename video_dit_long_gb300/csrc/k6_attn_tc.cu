@@ -40,19 +40,14 @@
 
 #include <mutex>
 
+#include "k6_attn_common.cuh"
 #include "k6_device.cuh"
 #include "k6_internal.h"
 
 namespace k6 {
 
 namespace tc {
-constexpr int D = 128;
-constexpr int BM = 128;                       // query rows per Q tile
-constexpr int BN = 128;                       // keys per K/V tile
-constexpr int NQ = 2;                         // Q tiles per CTA
 constexpr int NSTAGE = 4;                     // K/V tile slots
-constexpr int PANEL = BM * 64 * 2;            // one 128-row x 64-dim bf16 panel: 16 KB
-constexpr int TILE = 2 * PANEL;               // 32 KB
 constexpr int SMEM_Q = 0;
 constexpr int SMEM_KV = NQ * TILE;
 constexpr int SMEM_BAR = SMEM_KV + NSTAGE * TILE;
@@ -69,84 +64,7 @@ constexpr int THREADS = 384;                  // 3 warpgroups: softmax 0, softma
 constexpr int REGS_SOFTMAX = 184;
 constexpr int REGS_CONTROL = 136;
 constexpr int TMEM_COLS = 512;
-constexpr float RESCALE_THRESHOLD = 8.0f;     // log2 units: rescale when the max grows past 2^8
-constexpr unsigned long long DRAIN_NS = 1000000000ull;
 }  // namespace tc
-
-struct TcParams {
-    long S, Nv, Nj;                           // keys (video then joint)
-    long Sq;                                  // query rows
-    int H, n_chunks, q_pairs;
-    float scale_log2;                         // log2(e) / sqrt(d)
-    void *out;                                // bf16 [B][S][H][d] or fp32 partials
-    float *lse;
-    int out_f32;
-    long long o_stride, l_stride;             // elements between chunks
-    unsigned long long wait_limit_ns;
-    int *err;
-    int strict_order;
-    uint32_t idesc_qk;                        // instruction descriptor of Q.K^T (bf16 or fp16 operands)
-    long units;                               // B * H * n_chunks * q_pairs work units
-    int group;                                // chunks per CTA, sharing one load of Q (divides n_chunks)
-    const float *row_bound;                   // constant-max softmax: bound per query row [B][H][Sq], or null
-};
-
-// K/V tile j of a chunk: which tensor map (0 video, 1 joint), first row, valid keys.
-struct TileRange {
-    long v_beg, v_end, j_beg, j_end;
-    int Tv, T;
-    __device__ void at(int j, int &map, int &row, int &valid) const {
-        if (j < Tv) {
-            map = 0;
-            long r = v_beg + (long)j * tc::BN;
-            row = (int)r;
-            valid = (int)min((long)tc::BN, v_end - r);
-        } else {
-            map = 1;
-            long r = j_beg + (long)(j - Tv) * tc::BN;
-            row = (int)r;
-            valid = (int)min((long)tc::BN, j_end - r);
-        }
-    }
-};
-
-__device__ __forceinline__ TileRange chunk_tiles(const TcParams &p, int c) {
-    TileRange t;
-    const long L = (p.S) / p.n_chunks;
-    const long kb = (long)c * L, ke = kb + L;
-    t.v_beg = kb;
-    t.v_end = ke < p.Nv ? ke : p.Nv;
-    t.j_beg = (kb > p.Nv ? kb : p.Nv) - p.Nv;
-    t.j_end = ke > p.Nv ? ke - p.Nv : 0;
-    t.Tv = t.v_end > t.v_beg ? (int)((t.v_end - t.v_beg + tc::BN - 1) / tc::BN) : 0;
-    const int Tj = t.j_end > t.j_beg ? (int)((t.j_end - t.j_beg + tc::BN - 1) / tc::BN) : 0;
-    t.T = t.Tv + Tj;
-    return t;
-}
-
-// Work unit u -> (b, h, chunk group, query-tile pair, chunk within the group),
-// the chunk within the group fastest: CTA x owns units [x*group, (x+1)*group),
-// one Q tile pair over `group` consecutive chunks.  Across CTAs the query-tile
-// pair varies fastest, so the CTAs running at the same time walk through the
-// same chunks and share their K/V in L2.
-struct Unit {
-    int b, h, c, q0;
-};
-__device__ __forceinline__ Unit decode_unit(const TcParams &p, long u) {
-    Unit r;
-    const int g = (int)(u % p.group);
-    u /= p.group;
-    const int qp = (int)(u % p.q_pairs);
-    u /= p.q_pairs;
-    const int groups = p.n_chunks / p.group;
-    const int cg = (int)(u % groups);
-    u /= groups;
-    r.c = cg * p.group + g;
-    r.h = (int)(u % p.H);
-    r.b = (int)(u / p.H);
-    r.q0 = qp * (tc::NQ * tc::BM);
-    return r;
-}
 
 // Each CTA loads its Q tile pair once and runs its chunks one after another;
 // the K/V ring, the barrier phases and tensor memory carry over from one chunk
@@ -614,6 +532,10 @@ cudaError_t launch_attn_tc(const Geom &g, const void *q, const void *k, const vo
                             : idesc_bf16_f32(tc::BM, tc::BN, false);
     p.units = (long)g.B * g.H * n_chunks * p.q_pairs;
     if (p.units == 0) return cudaSuccess;
+    if (p.units >= (1L << 31)) {
+        if (why) *why = "too many work units (batch x heads x chunks x query-tile pairs must stay below 2^31)";
+        return cudaErrorInvalidValue;
+    }
     // chunks per CTA: the largest divisor of n_chunks up to 4
     p.group = 1;
     for (int gsz = 4; gsz > 1; gsz--)
