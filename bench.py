@@ -62,10 +62,13 @@ def traffic_record(kernel: str):
     """dram bytes per launch from the committed ncu summary, if it was taken on
     the current source of the kernel (source sha256 recorded beside it)."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
-    src = os.path.join(ROOT, "video_dit_long_gb300", "csrc", "k6_attn_tc.cu")
+    csrc = os.path.join(ROOT, "video_dit_long_gb300", "csrc")
     if not os.path.exists(path):
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    digest = hashlib.sha256()
+    for name in ("k6_attn_tc.cu", "k6_attn_common.cuh"):  # the kernel's own sources
+        digest.update(open(os.path.join(csrc, name), "rb").read())
+    sha = digest.hexdigest()[:16]
     with open(path) as f:
         for line in f:
             parts = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)

@@ -159,10 +159,13 @@ struct Vec<float> {
 // With NORM, each token row of H*d values is first RMS-normalised
 // (x * rsqrt(mean(x^2) + eps) * w, fp32): one pass sums the squares (warp
 // reduction), the second pass re-reads the row (an L2 hit) and normalises.
+// A lane's vectors are v = lane + 32 u, and a head row holds d / (2 kPairs)
+// vectors, a divisor of 32 for every supported d: so a lane always rotates the
+// same kPairs pairs of every head, and reads their cos/sin once per token.
 template <typename T, typename Tout, bool NORM>
 __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a, const float2 *__restrict__ tab) {
     constexpr int kPairs = Vec<T>::kPairs;
-    constexpr int kUnroll = 4;
+    constexpr int kUnroll = 6;
     static_assert(sizeof(T) == sizeof(Tout), "rotation keeps the element size");
     const long total = a.tokens[0] + a.tokens[1] + a.tokens[2];
     const int vecs_per_token = a.H * a.d / (2 * kPairs);
@@ -208,6 +211,10 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a, const float2 *__r
             for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
             inv_rms = rsqrtf(ss / (float)(a.H * a.d) + a.eps);
         }
+        const int pair0 = (lane % vecs_per_head) * kPairs;
+        float2 cs[kPairs];
+#pragma unroll
+        for (int k = 0; k < kPairs; k++) cs[k] = rope_cs(a, tab, pair0 + k, t, h, w, j);
         for (int base = 0; base < vecs_per_token; base += 32 * kUnroll) {
             float x[kUnroll][8];
 #pragma unroll
@@ -219,7 +226,6 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a, const float2 *__r
             for (int u = 0; u < kUnroll; u++) {
                 const int v = base + u * 32 + lane;
                 if (v >= vecs_per_token) continue;
-                const int pair0 = (v % vecs_per_head) * kPairs;
                 if constexpr (NORM) {
                     const float *wv = wrow + v * 2 * kPairs;
 #pragma unroll
@@ -227,10 +233,9 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a, const float2 *__r
                 }
 #pragma unroll
                 for (int k = 0; k < kPairs; k++) {
-                    const float2 cs = rope_cs(a, tab, pair0 + k, t, h, w, j);
                     const float xr = x[u][2 * k], xi = x[u][2 * k + 1];
-                    x[u][2 * k] = xr * cs.x - xi * cs.y;
-                    x[u][2 * k + 1] = xr * cs.y + xi * cs.x;
+                    x[u][2 * k] = xr * cs[k].x - xi * cs[k].y;
+                    x[u][2 * k + 1] = xr * cs[k].y + xi * cs[k].x;
                 }
                 if constexpr (!std::is_same<T, Tout>::value) {
 #pragma unroll
@@ -278,17 +283,25 @@ cudaError_t launch_rope_qk(const Geom &g, const float2 *tables, const void *src_
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    long blocks = (total + 7) / 8;  // 8 warps per block, one token per warp-iteration
-    if (blocks > (long)sms * 8) blocks = (long)sms * 8;
+    // one wave: as many 256-thread blocks as fit on the SMs at once (the kernel
+    // strides over tokens), at most one token per warp
+    auto launch = [&](auto kernel) {
+        int per_sm = 1;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0);
+        long blocks = (total + 7) / 8;
+        const long wave = (long)sms * (per_sm > 0 ? per_sm : 1);
+        if (blocks > wave) blocks = wave;
+        kernel<<<(unsigned)blocks, 256, 0, st>>>(a, tables);
+    };
     if (g.dtype == K6ATTN_BF16 && out_dtype == K6ATTN_F16) {
-        if (use_norm) rope_kernel<__nv_bfloat16, __half, true><<<(unsigned)blocks, 256, 0, st>>>(a, tables);
-        else rope_kernel<__nv_bfloat16, __half, false><<<(unsigned)blocks, 256, 0, st>>>(a, tables);
+        if (use_norm) launch(rope_kernel<__nv_bfloat16, __half, true>);
+        else launch(rope_kernel<__nv_bfloat16, __half, false>);
     } else if (g.dtype == K6ATTN_BF16) {
-        if (use_norm) rope_kernel<__nv_bfloat16, __nv_bfloat16, true><<<(unsigned)blocks, 256, 0, st>>>(a, tables);
-        else rope_kernel<__nv_bfloat16, __nv_bfloat16, false><<<(unsigned)blocks, 256, 0, st>>>(a, tables);
+        if (use_norm) launch(rope_kernel<__nv_bfloat16, __nv_bfloat16, true>);
+        else launch(rope_kernel<__nv_bfloat16, __nv_bfloat16, false>);
     } else {
-        if (use_norm) rope_kernel<float, float, true><<<(unsigned)blocks, 256, 0, st>>>(a, tables);
-        else rope_kernel<float, float, false><<<(unsigned)blocks, 256, 0, st>>>(a, tables);
+        if (use_norm) launch(rope_kernel<float, float, true>);
+        else launch(rope_kernel<float, float, false>);
     }
     return cudaGetLastError();
 }
