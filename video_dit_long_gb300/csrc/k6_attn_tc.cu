@@ -536,21 +536,22 @@ cudaError_t launch_attn_tc(const Geom &g, const void *q, const void *k, const vo
         if (why) *why = "too many work units (batch x heads x chunks x query-tile pairs must stay below 2^31)";
         return cudaErrorInvalidValue;
     }
-    // chunks per CTA: the largest divisor of n_chunks up to 4
-    p.group = 1;
-    for (int gsz = 4; gsz > 1; gsz--)
-        if (n_chunks % gsz == 0) {
-            p.group = gsz;
-            break;
-        }
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // chunks per CTA (sharing one load of Q): the largest divisor of n_chunks up
+    // to 4 that still leaves at least four waves of CTAs; short query ranges
+    // (cross-attention from a few hundred audio rows) keep one chunk per CTA
+    p.group = 1;
+    for (int gsz = 4; gsz > 1; gsz--)
+        if (n_chunks % gsz == 0 && p.units / gsz >= 4L * sms) {
+            p.group = gsz;
+            break;
+        }
     // One CTA per Q tile pair and chunk group: the block scheduler hands each
     // freed SM the next CTA, which keeps the CTAs in flight (and their K/V in
     // L2) in a tight window; measured faster than a static persistent
     // round-robin over SMs.
-    (void)sms;
     const long grid = p.units / p.group;
     p.row_bound = opt.row_bound;
     if (opt.row_bound)
