@@ -132,6 +132,8 @@ class Clocks:
 class Path:
     """Device buffers and handles for one workload; step() runs the hot path."""
 
+    E2E_BUFS = 3  # input and output buffer sets of the end-to-end loop (uploads run two steps ahead)
+
     def __init__(self, w, n_chunks, P, x):
         import torch
         from video_dit_long_gb300 import k6attn as K
@@ -161,10 +163,11 @@ class Path:
         self.lse = torch.empty((P * B, self.Hl, S), dtype=torch.float32, device="cuda")
         self.out = torch.empty((B, S, H, d), dtype=bf, device="cuda")
         self.e2e_head = {k: torch.empty_like(self.seq[k]) for k in self.seq}
-        self.e2e_in = [{k: torch.empty_like(self.seq[k]) for k in self.seq} for _ in range(2)]
+        self.e2e_in = [{k: torch.empty_like(self.seq[k]) for k in self.seq} for _ in range(self.E2E_BUFS)]
         self.e2e_out = [{"out_h": torch.empty_like(self.out_h), "lse": torch.empty_like(self.lse),
-                         "out": torch.empty_like(self.out)} for _ in range(2)]
-        self.copy_stream = torch.cuda.Stream()
+                         "out": torch.empty_like(self.out)} for _ in range(self.E2E_BUFS)]
+        self.h2d_stream = torch.cuda.Stream()
+        self.d2h_stream = torch.cuda.Stream()
         self.ws = torch.empty(self.h.workspace_bytes(n_chunks, True), dtype=torch.uint8, device="cuda")
         self.out_host = torch.empty(self.out.shape, dtype=bf).pin_memory()
         self.lse_host = torch.empty(self.lse.shape, dtype=torch.float32).pin_memory()
@@ -215,32 +218,35 @@ class Path:
     def e2e_run(self, steps):
         """Public API from pinned host buffers, `steps` steps: per step the H2D copy of its
         inputs, relayout, k6attn_forward (rotary + chunks + merge), relayout back and the
-        D2H copy of out and lse.  Copies run on their own stream, overlapping the previous
-        and next steps' compute (inputs and outputs double-buffered); every copy is inside
-        the timed region."""
+        D2H copy of out and lse.  Uploads and downloads run on their own streams (one per
+        direction, so a slow download never holds up an upload), uploads two steps ahead
+        of the compute with three input and output buffer sets, as a serving loop would
+        run it; every copy is inside the timed region."""
         torch, w, K = self.torch, self.w, self.K
+        nb = self.E2E_BUFS
         comp = torch.cuda.current_stream()
-        copy = self.copy_stream
-        ev_in = [torch.cuda.Event() for _ in range(2)]      # inputs of a buffer landed
-        ev_used = [torch.cuda.Event() for _ in range(2)]    # compute done reading an input buffer
-        ev_out = [torch.cuda.Event() for _ in range(2)]     # outputs of a buffer ready
-        ev_read = [torch.cuda.Event() for _ in range(2)]    # outputs of a buffer copied out
+        up, down = self.h2d_stream, self.d2h_stream
+        ev_in = [torch.cuda.Event() for _ in range(nb)]      # inputs of a buffer landed
+        ev_used = [torch.cuda.Event() for _ in range(nb)]    # compute done reading an input buffer
+        ev_out = [torch.cuda.Event() for _ in range(nb)]     # outputs of a buffer ready
+        ev_read = [torch.cuda.Event() for _ in range(nb)]    # outputs of a buffer copied out
 
         def h2d(step):
-            buf = self.e2e_in[step % 2]
-            with torch.cuda.stream(copy):
-                copy.wait_event(ev_used[step % 2])
+            buf = self.e2e_in[step % nb]
+            with torch.cuda.stream(up):
+                up.wait_event(ev_used[step % nb])
                 for k in buf:
                     buf[k].copy_(self.host[k], non_blocking=True)
-                ev_in[step % 2].record(copy)
+                ev_in[step % nb].record(up)
 
         for e in ev_used + ev_read:
             e.record(comp)
-        h2d(0)
+        for step in range(min(nb - 1, steps)):
+            h2d(step)
         for step in range(steps):
-            if step + 1 < steps:
-                h2d(step + 1)
-            b = step % 2
+            if step + nb - 1 < steps:
+                h2d(step + nb - 1)
+            b = step % nb
             buf, ob = self.e2e_in[b], self.e2e_out[b]
             comp.wait_event(ev_in[b])
             self.relayout(buf, self.e2e_head)
@@ -252,12 +258,13 @@ class Path:
                            workspace=self.ws)
             K.seq2head_relayout(ob["out_h"], ob["out"], w.B, w.S, w.H, w.d, self.P, 1)
             ev_out[b].record(comp)
-            with torch.cuda.stream(copy):
-                copy.wait_event(ev_out[b])
+            with torch.cuda.stream(down):
+                down.wait_event(ev_out[b])
                 self.out_host.copy_(ob["out"], non_blocking=True)
                 self.lse_host.copy_(ob["lse"], non_blocking=True)
-                ev_read[b].record(copy)
-        comp.wait_stream(copy)
+                ev_read[b].record(down)
+        comp.wait_stream(up)
+        comp.wait_stream(down)
 
     def h2d_bytes(self):
         return sum(t.numel() * t.element_size() for t in self.host.values())

@@ -159,6 +159,38 @@ struct Vec<float> {
 // With NORM, each token row of H*d values is first RMS-normalised
 // (x * rsqrt(mean(x^2) + eps) * w, fp32): one pass sums the squares (warp
 // reduction), the second pass re-reads the row (an L2 hit) and normalises.
+// Token `tok` of the concatenation (q rows, k rows, joint_k rows): which
+// tensor, its row there, and its rotary position: video grid (t, h, w), or
+// joint index j >= 0.  32-bit arithmetic: the host keeps B*S*H below 2^31.
+struct TokenPos {
+    int which;
+    unsigned local;
+    int t, h, w;
+    long j;
+};
+__device__ __forceinline__ TokenPos token_pos(const RopeArgs &a, long tok) {
+    TokenPos p;
+    p.which = 0;
+    p.local = (unsigned)tok;
+    while (p.which < 2 && p.local >= (unsigned)a.tokens[p.which]) {
+        p.local -= (unsigned)a.tokens[p.which];
+        p.which++;
+    }
+    const unsigned n = p.local % (unsigned)a.seq[p.which];  // token index within its sequence
+    p.j = -1;
+    if (p.which == 2) p.j = n;
+    else if (n >= (unsigned)a.Nv) p.j = n - (unsigned)a.Nv;
+    p.t = p.h = p.w = 0;
+    if (p.j < 0) {
+        const unsigned gw = (unsigned)a.grid_w, gh = (unsigned)a.grid_h;
+        const unsigned nw = n / gw;
+        p.w = (int)(n - nw * gw);
+        p.t = (int)(nw / gh);
+        p.h = (int)(nw - (unsigned)p.t * gh);
+    }
+    return p;
+}
+
 // A lane's vectors are v = lane + 32 u, and a head row holds d / (2 kPairs)
 // vectors, a divisor of 32 for every supported d: so a lane always rotates the
 // same kPairs pairs of every head, and reads their cos/sin once per token.
@@ -174,25 +206,10 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a, const float2 *__r
     const long warp0 = (blockIdx.x * (long)blockDim.x + threadIdx.x) >> 5;
     const long nwarps = ((long)gridDim.x * blockDim.x) >> 5;
     for (long tok = warp0; tok < total; tok += nwarps) {
-        // 32-bit index arithmetic: the host guarantees B*S*H < 2^31
-        int which = 0;
-        unsigned local = (unsigned)tok;
-        while (which < 2 && local >= (unsigned)a.tokens[which]) {
-            local -= (unsigned)a.tokens[which];
-            which++;
-        }
-        const unsigned n = local % (unsigned)a.seq[which];  // token index within its sequence
-        long j = -1;                                        // joint index, or -1 for video
-        if (which == 2) j = n;
-        else if (n >= (unsigned)a.Nv) j = n - (unsigned)a.Nv;
-        int t = 0, h = 0, w = 0;
-        if (j < 0) {
-            const unsigned gw = (unsigned)a.grid_w, gh = (unsigned)a.grid_h;
-            const unsigned nw = n / gw;
-            w = (int)(n - nw * gw);
-            t = (int)(nw / gh);
-            h = (int)(nw - (unsigned)t * gh);
-        }
+        const TokenPos tp = token_pos(a, tok);
+        const int which = tp.which, t = tp.t, h = tp.h, w = tp.w;
+        const unsigned local = tp.local;
+        const long j = tp.j;
         const char *src = static_cast<const char *>(a.src[which]) + (long)local * a.H * a.d * sizeof(T);
         char *dst = static_cast<char *>(a.dst[which]) + (long)local * a.H * a.d * sizeof(T);
         bool bad = false;
@@ -248,6 +265,63 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a, const float2 *__r
     }
 }
 
+// Short token rows (a head-partitioned layout keeps H/P heads per token, e.g.
+// 3 x 128 elements): one warp pass covers `tpw` whole rows, so that every lane
+// still keeps kUnroll 16-byte loads in flight.  Rotation only (no QK-norm,
+// whose statistic needs the full row).  A lane's vectors stay in the same
+// kPairs pairs of a head (flat index lane + 32 u, rows and heads of whole
+// vectors, a head a divisor of 32 vectors); each vector looks up its own
+// token's cos/sin.
+template <typename T, typename Tout>
+__global__ void __launch_bounds__(256) rope_short_kernel(RopeArgs a, const float2 *__restrict__ tab, int tpw) {
+    constexpr int kPairs = Vec<T>::kPairs;
+    constexpr int kUnroll = 6;
+    const long total = a.tokens[0] + a.tokens[1] + a.tokens[2];
+    const int vpt = a.H * a.d / (2 * kPairs);  // vectors per token row
+    const int vph = a.d / (2 * kPairs);        // vectors per head
+    const int lane = threadIdx.x & 31;
+    const int pair0 = (lane % vph) * kPairs;
+    const long warp0 = (blockIdx.x * (long)blockDim.x + threadIdx.x) >> 5;
+    const long nwarps = ((long)gridDim.x * blockDim.x) >> 5;
+    bool bad = false;
+    for (long tok0 = warp0 * tpw; tok0 < total; tok0 += nwarps * tpw) {
+        float x[kUnroll][8];
+        long tok[kUnroll];
+        int v[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; u++) {
+            const int flat = lane + 32 * u;
+            const int to = flat / vpt;
+            v[u] = flat - to * vpt;
+            tok[u] = (to < tpw) ? tok0 + to : total;  // past the warp's rows: skipped
+            if (tok[u] < total) {
+                const TokenPos tp = token_pos(a, tok[u]);
+                Vec<T>::load(static_cast<const char *>(a.src[tp.which]) +
+                                 ((long)tp.local * vpt + v[u]) * 16,
+                             x[u]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; u++) {
+            if (tok[u] >= total) continue;
+            const TokenPos tp = token_pos(a, tok[u]);
+#pragma unroll
+            for (int k = 0; k < kPairs; k++) {
+                const float2 cs = rope_cs(a, tab, pair0 + k, tp.t, tp.h, tp.w, tp.j);
+                const float xr = x[u][2 * k], xi = x[u][2 * k + 1];
+                x[u][2 * k] = xr * cs.x - xi * cs.y;
+                x[u][2 * k + 1] = xr * cs.y + xi * cs.x;
+            }
+            if constexpr (!std::is_same<T, Tout>::value) {
+#pragma unroll
+                for (int k = 0; k < 2 * kPairs; k++) bad |= !(fabsf(x[u][k]) < 65520.f);  // a finite half
+            }
+            Vec<Tout>::store(static_cast<char *>(a.dst[tp.which]) + ((long)tp.local * vpt + v[u]) * 16, x[u]);
+        }
+    }
+    if (bad) atomicCAS(a.err, DEV_OK, DEV_RANGE);
+}
+
 cudaError_t launch_rope_qk(const Geom &g, const float2 *tables, const void *src_q, void *dst_q, const void *src_k,
                            void *dst_k, const void *src_jk, void *dst_jk, k6attn_dtype out_dtype, int *err,
                            cudaStream_t st, const QkNorm *norm) {
@@ -293,6 +367,24 @@ cudaError_t launch_rope_qk(const Geom &g, const float2 *tables, const void *src_
         if (blocks > wave) blocks = wave;
         kernel<<<(unsigned)blocks, 256, 0, st>>>(a, tables);
     };
+    // short rows (fewer vectors than half of one warp pass): several rows per warp pass
+    const int kpairs = g.dtype == K6ATTN_F32 ? 2 : 4;
+    const int vpt = g.H * g.d / (2 * kpairs);
+    if (!use_norm && 2 * vpt <= 32 * 6) {
+        const int tpw = (32 * 6) / vpt;
+        auto launch_short = [&](auto kernel) {
+            int per_sm = 1;
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0);
+            long blocks = (total + 8L * tpw - 1) / (8L * tpw);
+            const long wave = (long)sms * (per_sm > 0 ? per_sm : 1);
+            if (blocks > wave) blocks = wave;
+            kernel<<<(unsigned)blocks, 256, 0, st>>>(a, tables, tpw);
+        };
+        if (g.dtype == K6ATTN_BF16 && out_dtype == K6ATTN_F16) launch_short(rope_short_kernel<__nv_bfloat16, __half>);
+        else if (g.dtype == K6ATTN_BF16) launch_short(rope_short_kernel<__nv_bfloat16, __nv_bfloat16>);
+        else launch_short(rope_short_kernel<float, float>);
+        return cudaGetLastError();
+    }
     if (g.dtype == K6ATTN_BF16 && out_dtype == K6ATTN_F16) {
         if (use_norm) launch(rope_kernel<__nv_bfloat16, __half, true>);
         else launch(rope_kernel<__nv_bfloat16, __half, false>);
