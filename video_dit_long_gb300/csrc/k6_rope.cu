@@ -266,57 +266,66 @@ __global__ void __launch_bounds__(256) rope_kernel(RopeArgs a, const float2 *__r
 }
 
 // Short token rows (a head-partitioned layout keeps H/P heads per token, e.g.
-// 3 x 128 elements): one warp pass covers `tpw` whole rows, so that every lane
-// still keeps kUnroll 16-byte loads in flight.  Rotation only (no QK-norm,
-// whose statistic needs the full row).  A lane's vectors stay in the same
-// kPairs pairs of a head (flat index lane + 32 u, rows and heads of whole
-// vectors, a head a divisor of 32 vectors); each vector looks up its own
-// token's cos/sin.
+// 3 x 128 elements): a group of `gl` lanes (16, or 32 when a head holds 32
+// vectors) owns whole rows; each lane decodes its rows' positions and reads
+// its 4 cos/sin once per row, then moves `vpl` vectors of each of `rpg` rows,
+// kUnroll 16-byte loads in flight.  Rotation only (no QK-norm, whose statistic
+// needs the full row).  A lane's vectors are sub + gl*u of a row, and a head a
+// divisor of gl vectors, so the lane stays on the same kPairs pairs of every
+// head.
 template <typename T, typename Tout>
-__global__ void __launch_bounds__(256) rope_short_kernel(RopeArgs a, const float2 *__restrict__ tab, int tpw) {
+__global__ void __launch_bounds__(256) rope_short_kernel(RopeArgs a, const float2 *__restrict__ tab, int gl, int vpl,
+                                                         int rpg) {
     constexpr int kPairs = Vec<T>::kPairs;
     constexpr int kUnroll = 6;
+    constexpr int kRows = kUnroll;             // rows per group pass at most (vpl >= 1)
     const long total = a.tokens[0] + a.tokens[1] + a.tokens[2];
     const int vpt = a.H * a.d / (2 * kPairs);  // vectors per token row
     const int vph = a.d / (2 * kPairs);        // vectors per head
     const int lane = threadIdx.x & 31;
-    const int pair0 = (lane % vph) * kPairs;
+    const int sub = lane % gl, grp = lane / gl, groups = 32 / gl;
+    const int pair0 = (sub % vph) * kPairs;
     const long warp0 = (blockIdx.x * (long)blockDim.x + threadIdx.x) >> 5;
     const long nwarps = ((long)gridDim.x * blockDim.x) >> 5;
+    const long per_pass = (long)groups * rpg;  // rows per warp pass
     bool bad = false;
-    for (long tok0 = warp0 * tpw; tok0 < total; tok0 += nwarps * tpw) {
+    for (long row0 = warp0 * per_pass + (long)grp * rpg; row0 < total; row0 += nwarps * per_pass) {
         float x[kUnroll][8];
-        long tok[kUnroll];
-        int v[kUnroll];
+        float2 cs[kRows][kPairs];
+        const char *src[kRows];
+        char *dst[kRows];
 #pragma unroll
-        for (int u = 0; u < kUnroll; u++) {
-            const int flat = lane + 32 * u;
-            const int to = flat / vpt;
-            v[u] = flat - to * vpt;
-            tok[u] = (to < tpw) ? tok0 + to : total;  // past the warp's rows: skipped
-            if (tok[u] < total) {
-                const TokenPos tp = token_pos(a, tok[u]);
-                Vec<T>::load(static_cast<const char *>(a.src[tp.which]) +
-                                 ((long)tp.local * vpt + v[u]) * 16,
-                             x[u]);
+        for (int r = 0; r < kRows; r++) {
+            src[r] = nullptr;
+            if (r < rpg && row0 + r < total) {
+                const TokenPos tp = token_pos(a, row0 + r);
+                src[r] = static_cast<const char *>(a.src[tp.which]) + (long)tp.local * vpt * 16;
+                dst[r] = static_cast<char *>(a.dst[tp.which]) + (long)tp.local * vpt * 16;
+#pragma unroll
+                for (int k = 0; k < kPairs; k++) cs[r][k] = rope_cs(a, tab, pair0 + k, tp.t, tp.h, tp.w, tp.j);
             }
         }
+        // element e = r * vpl + i: row r, the lane's vector sub + gl * i of that row
 #pragma unroll
-        for (int u = 0; u < kUnroll; u++) {
-            if (tok[u] >= total) continue;
-            const TokenPos tp = token_pos(a, tok[u]);
+        for (int e = 0; e < kUnroll; e++) {
+            const int r = e / vpl, v = sub + gl * (e - r * vpl);
+            if (r < rpg && src[r] && v < vpt) Vec<T>::load(src[r] + (long)v * 16, x[e]);
+        }
+#pragma unroll
+        for (int e = 0; e < kUnroll; e++) {
+            const int r = e / vpl, v = sub + gl * (e - r * vpl);
+            if (!(r < rpg && src[r] && v < vpt)) continue;
 #pragma unroll
             for (int k = 0; k < kPairs; k++) {
-                const float2 cs = rope_cs(a, tab, pair0 + k, tp.t, tp.h, tp.w, tp.j);
-                const float xr = x[u][2 * k], xi = x[u][2 * k + 1];
-                x[u][2 * k] = xr * cs.x - xi * cs.y;
-                x[u][2 * k + 1] = xr * cs.y + xi * cs.x;
+                const float xr = x[e][2 * k], xi = x[e][2 * k + 1];
+                x[e][2 * k] = xr * cs[r][k].x - xi * cs[r][k].y;
+                x[e][2 * k + 1] = xr * cs[r][k].y + xi * cs[r][k].x;
             }
             if constexpr (!std::is_same<T, Tout>::value) {
 #pragma unroll
-                for (int k = 0; k < 2 * kPairs; k++) bad |= !(fabsf(x[u][k]) < 65520.f);  // a finite half
+                for (int k = 0; k < 2 * kPairs; k++) bad |= !(fabsf(x[e][k]) < 65520.f);  // a finite half
             }
-            Vec<Tout>::store(static_cast<char *>(a.dst[tp.which]) + ((long)tp.local * vpt + v[u]) * 16, x[u]);
+            Vec<Tout>::store(dst[r] + (long)v * 16, x[e]);
         }
     }
     if (bad) atomicCAS(a.err, DEV_OK, DEV_RANGE);
@@ -371,14 +380,19 @@ cudaError_t launch_rope_qk(const Geom &g, const float2 *tables, const void *src_
     const int kpairs = g.dtype == K6ATTN_F32 ? 2 : 4;
     const int vpt = g.H * g.d / (2 * kpairs);
     if (!use_norm && 2 * vpt <= 32 * 6) {
-        const int tpw = (32 * 6) / vpt;
+        // lanes per row group, vectors per lane per row, rows per group pass (6 vectors in flight)
+        const int vph = g.d / (2 * kpairs);
+        const int gl = vph <= 16 ? 16 : 32;
+        const int vpl = (vpt + gl - 1) / gl;
+        const int rpg = 6 / vpl > 0 ? 6 / vpl : 1;
+        const long rows_per_warp = (long)(32 / gl) * rpg;
         auto launch_short = [&](auto kernel) {
             int per_sm = 1;
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0);
-            long blocks = (total + 8L * tpw - 1) / (8L * tpw);
+            long blocks = (total + 8L * rows_per_warp - 1) / (8L * rows_per_warp);
             const long wave = (long)sms * (per_sm > 0 ? per_sm : 1);
             if (blocks > wave) blocks = wave;
-            kernel<<<(unsigned)blocks, 256, 0, st>>>(a, tables, tpw);
+            kernel<<<(unsigned)blocks, 256, 0, st>>>(a, tables, gl, vpl, rpg);
         };
         if (g.dtype == K6ATTN_BF16 && out_dtype == K6ATTN_F16) launch_short(rope_short_kernel<__nv_bfloat16, __half>);
         else if (g.dtype == K6ATTN_BF16) launch_short(rope_short_kernel<__nv_bfloat16, __nv_bfloat16>);
