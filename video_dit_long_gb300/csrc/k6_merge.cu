@@ -16,7 +16,9 @@
 
 namespace k6 {
 
-template <typename OutT, int D>
+// SHFL (d = 128, n <= 32, one warp per row): lane c holds chunk c's LSE; max and
+// sum by warp shuffles, and lane c's weight is broadcast to the accumulation.
+template <typename OutT, int D, bool SHFL>
 __global__ void __launch_bounds__(256) lse_merge_kernel(int n, long rows, long Sq, int H,
                                                         const float *__restrict__ part_o,
                                                         const float *__restrict__ part_lse, OutT *__restrict__ out,
@@ -34,33 +36,63 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(int n, long rows, long S
         const long s = bs % Sq;
         const long b = bs / Sq;
         const long li = (b * H + h) * Sq + s;
-        float m = -INFINITY;
-        for (int c = 0; c < n; c++) m = fmaxf(m, __ldg(part_lse + c * l_stride + li));
-        float sum = 0.f;
-        for (int c = 0; c < n; c++) sum += expf(__ldg(part_lse + c * l_stride + li) - m);
-        const float L = m + logf(sum);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         const float *po = part_o + r * D + sub * 4;
-        // four chunks per pass, loads issued before the arithmetic (eight measured slower)
-        for (int c0 = 0; c0 < n; c0 += 4) {
-            float4 x[4];
-            float wgt[4];
+        float L;
+        if constexpr (SHFL) {
+            static_assert(TPR == 32, "one warp per row");
+            const float lc = sub < n ? __ldg(part_lse + sub * l_stride + li) : -INFINITY;
+            float m = lc;
 #pragma unroll
-            for (int u = 0; u < 4; u++) {
-                const int c = c0 + u;
-                if (c < n) {
-                    x[u] = __ldcs(reinterpret_cast<const float4 *>(po + c * o_stride));
-                    wgt[u] = __ldg(part_lse + c * l_stride + li);
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            float e = sub < n ? expf(lc - m) : 0.f;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
+            L = m + logf(e);
+            const float wl = sub < n ? expf(lc - L) : 0.f;
+            for (int c0 = 0; c0 < n; c0 += 4) {
+                float4 x[4];
+#pragma unroll
+                for (int u = 0; u < 4; u++)
+                    if (c0 + u < n) x[u] = __ldcs(reinterpret_cast<const float4 *>(po + (c0 + u) * o_stride));
+#pragma unroll
+                for (int u = 0; u < 4; u++) {
+                    const float wt = __shfl_sync(0xffffffffu, wl, (c0 + u) & 31);
+                    if (c0 + u < n) {
+                        acc.x += wt * x[u].x;
+                        acc.y += wt * x[u].y;
+                        acc.z += wt * x[u].z;
+                        acc.w += wt * x[u].w;
+                    }
                 }
             }
+        } else {
+            float m = -INFINITY;
+            for (int c = 0; c < n; c++) m = fmaxf(m, __ldg(part_lse + c * l_stride + li));
+            float sum = 0.f;
+            for (int c = 0; c < n; c++) sum += expf(__ldg(part_lse + c * l_stride + li) - m);
+            L = m + logf(sum);
+            // four chunks per pass, loads issued before the arithmetic (eight measured slower)
+            for (int c0 = 0; c0 < n; c0 += 4) {
+                float4 x[4];
+                float wgt[4];
 #pragma unroll
-            for (int u = 0; u < 4; u++) {
-                if (c0 + u < n) {
-                    const float wt = expf(wgt[u] - L);
-                    acc.x += wt * x[u].x;
-                    acc.y += wt * x[u].y;
-                    acc.z += wt * x[u].z;
-                    acc.w += wt * x[u].w;
+                for (int u = 0; u < 4; u++) {
+                    const int c = c0 + u;
+                    if (c < n) {
+                        x[u] = __ldcs(reinterpret_cast<const float4 *>(po + c * o_stride));
+                        wgt[u] = __ldg(part_lse + c * l_stride + li);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; u++) {
+                    if (c0 + u < n) {
+                        const float wt = expf(wgt[u] - L);
+                        acc.x += wt * x[u].x;
+                        acc.y += wt * x[u].y;
+                        acc.z += wt * x[u].z;
+                        acc.w += wt * x[u].w;
+                    }
                 }
             }
         }
@@ -90,19 +122,26 @@ cudaError_t launch_lse_merge(const Geom &g, int n, const float *part_o, const fl
     long want = (rows * tpr + threads - 1) / threads;
     long cap = (long)sms * 8;  // 2048 threads per SM resident
     unsigned blocks = (unsigned)(want < cap ? want : cap);
-    if (g.d == 128) {
+    if (g.d == 128 && n <= 32) {
         if (g.elem == 2)
-            lse_merge_kernel<__nv_bfloat16, 128><<<blocks, threads, 0, st>>>(
+            lse_merge_kernel<__nv_bfloat16, 128, true><<<blocks, threads, 0, st>>>(
                 n, rows, g.Sq, g.H, part_o, part_lse, static_cast<__nv_bfloat16 *>(out), lse);
         else
-            lse_merge_kernel<float, 128>
+            lse_merge_kernel<float, 128, true>
+                <<<blocks, threads, 0, st>>>(n, rows, g.Sq, g.H, part_o, part_lse, static_cast<float *>(out), lse);
+    } else if (g.d == 128) {
+        if (g.elem == 2)
+            lse_merge_kernel<__nv_bfloat16, 128, false><<<blocks, threads, 0, st>>>(
+                n, rows, g.Sq, g.H, part_o, part_lse, static_cast<__nv_bfloat16 *>(out), lse);
+        else
+            lse_merge_kernel<float, 128, false>
                 <<<blocks, threads, 0, st>>>(n, rows, g.Sq, g.H, part_o, part_lse, static_cast<float *>(out), lse);
     } else {
         if (g.elem == 2)
-            lse_merge_kernel<__nv_bfloat16, 64><<<blocks, threads, 0, st>>>(
+            lse_merge_kernel<__nv_bfloat16, 64, false><<<blocks, threads, 0, st>>>(
                 n, rows, g.Sq, g.H, part_o, part_lse, static_cast<__nv_bfloat16 *>(out), lse);
         else
-            lse_merge_kernel<float, 64>
+            lse_merge_kernel<float, 64, false>
                 <<<blocks, threads, 0, st>>>(n, rows, g.Sq, g.H, part_o, part_lse, static_cast<float *>(out), lse);
     }
     return cudaGetLastError();
