@@ -69,3 +69,10 @@ def test_cross_rejects_indivisible_chunks():
     with pytest.raises(K.K6Error) as e:
         h.cross_forward(q, kv, kv, torch.empty_like(q), n_chunks=4)
     assert e.value.status == K.ERR_INVALID_ARG
+
+
+def test_short_queries_several_chunks_per_cta():
+    # 100 query rows: every CTA runs a single Q tile; 32 heads x 80 chunks make
+    # enough work units that each CTA takes four chunks in turn, carrying its
+    # S buffers and barrier phases from one chunk to the next
+    print(run_cross(1, 32, 128, "bf16", 100, 80 * 130, 80))

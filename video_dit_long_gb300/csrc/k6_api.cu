@@ -83,7 +83,9 @@ static k6attn_status run_attention(k6attn_handle *h, const Geom &g, const void *
     if (g.elem == 2) {
         AttnTcOptions opt{h->wait_limit_ns, h->err, h->strict_order, qk_f16 ? 1 : 0, row_bound};
         const char *why = nullptr;
-        cudaError_t e = launch_attn_tc(g, q, k, v, jk, jv, n_chunks, out, lse, opt, st, &why);
+        // a query range of one 128-row tile runs the single-tile kernel
+        cudaError_t e = (g.Sq <= 128 ? launch_attn_tc_single : launch_attn_tc)(g, q, k, v, jk, jv, n_chunks, out, lse,
+                                                                           opt, st, &why);
         if (e != cudaSuccess) {
             if (why) return set_error(K6ATTN_ERR_CUDA, "attention: %s", why);
             return cuda_check(e, "attention launch");

@@ -87,6 +87,10 @@ cudaError_t launch_row_bounds(const Geom &g, k6attn_dtype qk_dtype, const void *
 cudaError_t launch_attn_tc(const Geom &g, const void *q, const void *k, const void *v, const void *jk,
                            const void *jv, int n_chunks, void *out, float *lse, const AttnTcOptions &opt,
                            cudaStream_t st, const char **why);
+// The same attention for at most 128 query rows (one Q tile per CTA).
+cudaError_t launch_attn_tc_single(const Geom &g, const void *q, const void *k, const void *v, const void *jk,
+                                  const void *jv, int n_chunks, void *out, float *lse, const AttnTcOptions &opt,
+                                  cudaStream_t st, const char **why);
 
 // Backward pass (bf16 v/out/dout, q/k bf16 or fp16, d = 128): the pre-pass
 // into LD [B][H][S] = {lse * log2(e), D_i}, then the dq kernel and the dk/dv kernel.
