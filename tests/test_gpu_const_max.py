@@ -18,6 +18,8 @@ CASES = {
     "ragged": Workload("ragged", 1, 2, 128, "bf16", (3, 10, 20), 40, (32, 48, 48), 0, 1.0, 1.0, (1, 4)),
     "audio1d": Workload("audio1d", 2, 2, 128, "bf16", (2, 8, 16), 62, (32, 48, 48), 1, 1.0, 1.0, (1, 3)),
     "lite": configs.WORKLOADS["lite"],
+    # 63 tokens: a query range of one tile (the single-tile kernel), chunks of 21 keys
+    "one_tile": Workload("one_tile", 1, 3, 128, "bf16", (1, 7, 9), 0, (32, 48, 48), 0, 1.0, 1.0, (1, 3)),
 }
 
 
@@ -31,8 +33,11 @@ def run_bounded(w, x, n, rope=True):
     from video_dit_long_gb300 import k6attn as K
     h = K.Handle.for_workload(w)
     q, k, v, jk, jv = (to_dev(x[nm], w.dtype) for nm in ("q", "k", "v", "jk", "jv"))
+    if w.Nj == 0:
+        jk = jv = None
     if rope:
-        qo, ko, jo = (torch.empty(t.shape, dtype=torch.float16, device="cuda") for t in (q, k, jk))
+        qo, ko = (torch.empty(t.shape, dtype=torch.float16, device="cuda") for t in (q, k))
+        jo = torch.empty(jk.shape, dtype=torch.float16, device="cuda") if jk is not None else None
         h.rope_qk(q, k, jk, q_out=qo, k_out=ko, joint_k_out=jo, out_dtype=K.F16)
         qd = K.F16
     else:
@@ -51,17 +56,18 @@ def run_bounded(w, x, n, rope=True):
     return h, out, lse, bounds
 
 
-@pytest.mark.parametrize("name", ["ragged", "audio1d", "lite"])
+@pytest.mark.parametrize("name", ["ragged", "audio1d", "lite", "one_tile"])
 def test_bounded_attention_matches_oracle(name):
     w = CASES[name]
     x = inputs.make_inputs(w)
     for n in (1, w.chunks[-1]):
         h, out, lse, bounds = run_bounded(w, x, n)
         h.sync()
-        ref, ref_lse = O.attention(geom(w), x["q"], x["k"], x["v"], x["jk"], x["jv"])
+        ref, ref_lse = O.attention(geom(w), x["q"], x["k"], x["v"], x["jk"] if w.Nj else None,
+                                   x["jv"] if w.Nj else None)
         compare(to_host(out), ref, lse.cpu().numpy().astype(np.float64), ref_lse, "bf16")
         # the bounds: within fp16 rounding of the oracle's, and above every logit
-        rb = O.row_bounds(geom(w), x["q"], x["k"], x["jk"])
+        rb = O.row_bounds(geom(w), x["q"], x["k"], x["jk"] if w.Nj else None)
         got = bounds[: w.B * w.H * w.S].cpu().numpy().reshape(w.B, w.H, w.S)
         np.testing.assert_allclose(got, rb, rtol=2e-3, atol=0)
 

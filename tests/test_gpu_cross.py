@@ -24,12 +24,14 @@ def _need_gpu():
         pytest.skip("no CUDA device")
 
 
-def run_cross(B, H, d, dtype, Sq, Sk, n, seed=42, std=1.0):
+def run_cross(B, H, d, dtype, Sq, Sk, n, seed=42, std=1.0, strict=False, raw=False):
     from video_dit_long_gb300 import k6attn as K
     q = inputs.tensor(seed, 30, (B, Sq, H, d), dtype, std)
     k = inputs.tensor(seed, 31, (B, Sk, H, d), dtype, std)
     v = inputs.tensor(seed, 32, (B, Sk, H, d), dtype)
     h = K.Handle(B, H, d, dtype, (1, 1, 1), 0, (d, 0, 0))
+    if strict:
+        h.set_option(K.OPT_STRICT_MMA_ORDER, 1)
     tq, tk, tv = (to_dev(a, dtype) for a in (q, k, v))
     out = torch.empty_like(tq)
     lse = torch.empty((B, H, Sq), dtype=torch.float32, device="cuda")
@@ -37,6 +39,8 @@ def run_cross(B, H, d, dtype, Sq, Sk, n, seed=42, std=1.0):
     ws = torch.empty(nb, dtype=torch.uint8, device="cuda") if nb else None
     h.cross_forward(tq, tk, tv, out, lse, n_chunks=n, workspace=ws)
     h.sync()
+    if raw:
+        return to_host(out), lse.cpu().numpy()
     ref, ref_lse = O.cross_attention(q, k, v)
     return compare(to_host(out), ref, lse.cpu().numpy().astype(np.float64), ref_lse, dtype)
 
@@ -51,7 +55,8 @@ def test_visual_queries_over_text(n):
     run_cross(2, 24, 128, "bf16", 4096, 256, n)
 
 
-@pytest.mark.parametrize("Sq,Sk,n", [(333, 700, 7), (1, 128, 1), (129, 1, 1), (257, 255, 5)])
+@pytest.mark.parametrize("Sq,Sk,n", [(333, 700, 7), (1, 128, 1), (129, 1, 1), (257, 255, 5),
+                                     (77, 1000, 1), (128, 2000, 1)])
 def test_ragged_cross_bf16(Sq, Sk, n):
     run_cross(1, 2, 128, "bf16", Sq, Sk, n, std=2.0)
 
@@ -76,3 +81,13 @@ def test_short_queries_several_chunks_per_cta():
     # enough work units that each CTA takes four chunks in turn, carrying its
     # S buffers and barrier phases from one chunk to the next
     print(run_cross(1, 32, 128, "bf16", 100, 80 * 130, 80))
+
+
+@pytest.mark.parametrize("n", [1, 2])
+def test_single_tile_strict_mma_order_gives_identical_bits(n):
+    # 77 queries (the single-tile kernel) over 16 K/V tiles per chunk, logits peaked
+    # enough to rescale O: waiting for every P.V before S(j+2) reuses its tensor memory
+    # must change nothing
+    a = run_cross(1, 2, 128, "bf16", 77, 2048, n, std=2.0, raw=True)
+    b = run_cross(1, 2, 128, "bf16", 77, 2048, n, std=2.0, raw=True, strict=True)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
