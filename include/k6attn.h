@@ -16,9 +16,10 @@
  *         implementation)", "Self-Attention with Context Parallelism",
  *         "Comparison with Other CP Strategies", "Positional Embedding
  *         Handling", "Scaling Properties", "Sequence Length Constraints".
- *  [K6]   vLLM-Omni recipe "Kandinsky 6 TI2VA -- H100": parallel features
- *         ("visual tokens (and their RoPE) are sharded", "Audio queries gather
- *         the full visual sequence").
+ *  [K6]   vLLM-Omni recipe "Kandinsky 6 TI2VA -- H100", section "Notes", its
+ *         sequence-parallel item: the visual tokens and their rotary tables are
+ *         split across ranks, and the audio queries attend over every visual
+ *         token.
  *
  * Conventions shared by every call:
  *  - Tensors are caller-owned DEVICE pointers, 16-byte aligned, densely packed
@@ -270,8 +271,9 @@ k6attn_status k6attn_lse_merge(k6attn_t h, const float *part_o, const float *par
 
 /*
  * Cross-attention: Sq query rows of one stream over Sk keys/values of another
- * ([K6] "Audio queries gather the full visual sequence"; [CP] "Forward Pass
- * Flow": cross-attention uses the full encoder states).  No rotary, no joint
+ * ([K6] "Notes", sequence-parallel item: audio queries attend over every
+ * visual token; [CP] "Forward Pass Flow": cross-attention reads the encoder
+ * states unsharded).  No rotary, no joint
  * tokens; the handle supplies B, H, d, the element type and the error word
  * (its video grid and joint settings are not used).
  *  q        [B][Sq][H][d];  k, v [B][Sk][H][d]  (handle dtype).

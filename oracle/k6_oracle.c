@@ -33,10 +33,10 @@
  *     (current implementation)" and "Scaling Properties".  The merge formula
  *     is a reading: LSE = log sum_c exp(LSE_c), out = sum_c exp(LSE_c - LSE) O_c.
  *   - Cross-attention, queries of one stream over the keys/values of another
- *     (Sq != Sk, no rotary): vLLM-Omni recipe "Kandinsky 6 TI2VA -- H100"
- *     ("Audio queries gather the full visual sequence"); "Context Parallelism
- *     in vLLM Omni Neuron", "Forward Pass Flow" ("Cross-attention uses full
- *     encoder states").
+ *     (Sq != Sk, no rotary): vLLM-Omni recipe "Kandinsky 6 TI2VA -- H100",
+ *     section "Notes" (in sequence parallelism the audio queries attend over
+ *     every visual token); "Context Parallelism in vLLM Omni Neuron", "Forward
+ *     Pass Flow" (cross-attention reads the encoder states unsharded).
  *   - The constant-max variant of ring attention ("Context Parallelism in vLLM
  *     Omni Neuron", "Related information": `ring_attention_const_max_fwd`
  *     takes the softmax max as a runtime bound instead of a running max).

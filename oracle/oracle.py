@@ -262,7 +262,7 @@ def cross_attention(q, k, v, *, kv_range=None):
 def chunk_bounds(S: int, n: int):
     """Equal contiguous K/V chunks [c*S/n, (c+1)*S/n), as ring ranks hold them."""
     if S % n:
-        raise ValueError(f"sequence length {S} is not divisible by {n} chunks")
+        raise ValueError(f"{n} equal chunks cannot cover {S} keys")
     L = S // n
     return [(c * L, (c + 1) * L) for c in range(n)]
 
