@@ -404,8 +404,10 @@ def measure_cross(w, steps, warmup, n_chunks=8):
 
 def measure_backward(w, x, steps, warmup):
     """Attention backward on the workload: rotary into fp16 copies and the one-chunk
-    forward (out, lse) once, then `steps` timed k6attn_backward calls (D pre-pass,
-    dq kernel, dk/dv kernel).  FLOPs are the 5-GEMM count 10*B*H*S^2*d."""
+    forward (out, lse), then `steps` timed k6attn_backward calls (D pre-pass,
+    dq kernel, dk/dv kernel).  FLOPs are the 5-GEMM count 10*B*H*S^2*d.  The
+    one-chunk forward (bf16 out and lse written directly, no merge) is timed
+    too, over the same number of calls: returns (backward, forward_n1)."""
     import torch
     from video_dit_long_gb300 import k6attn as K
     B, S, Nv, Nj, H, d = w.B, w.S, w.Nv, w.Nj, w.H, w.d
@@ -419,7 +421,24 @@ def measure_backward(w, x, steps, warmup):
     h.rope_qk(q, k, jk, q_out=qh, k_out=kh, joint_k_out=jh, out_dtype=K.F16)
     out = torch.empty_like(q)
     lse = torch.empty((B, H, S), dtype=torch.float32, device="cuda")
-    h.attention_chunks(qh, kh, v, jh, jv, 1, out, lse, qk_dtype=K.F16)
+
+    def forward():
+        h.attention_chunks(qh, kh, v, jh, jv, 1, out, lse, qk_dtype=K.F16)
+
+    for _ in range(warmup):
+        forward()
+    torch.cuda.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record()
+    for _ in range(steps):
+        forward()
+    f1.record()
+    torch.cuda.synchronize()
+    h.sync()
+    fwd_ms = f0.elapsed_time(f1) / steps
+    fwd = {"what": f"{w.name}: attention with one K/V chunk (bf16 out and lse written directly, no merge), "
+                   "rotated fp16 q/k", "value": round(4.0 * B * H * S * S * d / (fwd_ms * 1e-3) / 1e12, 2),
+           "unit": "TFLOP/s", "ms_per_call": round(fwd_ms, 3), "launches_per_call": 1}
     do = dev(inputs.tensor(42, 20, (B, S, H, d), "bf16"))
     f32 = dict(dtype=torch.float32, device="cuda")
     dq = torch.empty((B, S, H, d), **f32)
@@ -442,9 +461,9 @@ def measure_backward(w, x, steps, warmup):
     h.sync()
     ms = e0.elapsed_time(e1) / steps
     flops = 10.0 * B * H * S * S * d
-    return {"workload": f"{w.name}: gradients of q, k, v, joint_k, joint_v over {S} tokens (B={B}, H={H}, d={d})",
-            "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s (5-GEMM count)",
-            "ms_per_call": round(ms, 3), "launches_per_call": 3}
+    return ({"workload": f"{w.name}: gradients of q, k, v, joint_k, joint_v over {S} tokens (B={B}, H={H}, d={d})",
+             "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s (5-GEMM count)",
+             "ms_per_call": round(ms, 3), "launches_per_call": 3}, fwd)
 
 
 def merge_bytes(w, n, P):
@@ -538,8 +557,10 @@ def run_ours(args, rank, world, dist_on):
                               "standard_attention_plus_merge_ms": round(k_ms[2] + k_ms[3], 3)}
     if args.secondary:
         line["cross_attention"] = measure_cross(w, max(5, args.steps // 2), args.warmup)
-        bwd = measure_backward(w, x, max(3, args.steps // 10), max(3, args.warmup // 2))
+        bwd, fwd1 = measure_backward(w, x, max(3, args.steps // 10), max(3, args.warmup // 2))
         bwd["frac_sustained"] = round(bwd["value"] / peak_s, 4)
+        fwd1["frac_sustained"] = round(fwd1["value"] / peak_s, 4)
+        line["attention_n1"] = fwd1
         line["backward"] = bwd
     if rank == 0 and world == 1 and not args.no_cpu:
         dt, fl, thr = cpu_sample(w, x, args.cpu_rows)
