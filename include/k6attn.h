@@ -34,6 +34,11 @@
  *    s_ij = q~_i . k~_j / sqrt(d).
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
  *    asynchronous on that stream and returns after enqueueing.
+ *  - A handle belongs to the device that was current at k6attn_create (its
+ *    rotary tables and error word live there).  Every call that takes a handle,
+ *    except k6attn_destroy and the host-only queries, must be made with that
+ *    device current; otherwise it returns K6ATTN_ERR_INVALID_ARG and launches
+ *    nothing.
  *  - Calls never abort or trap.  Argument errors are found on the host before
  *    any launch and return K6ATTN_ERR_INVALID_ARG / _UNSUPPORTED /
  *    _WORKSPACE; k6attn_last_error() then holds a message (thread-local).
@@ -323,9 +328,12 @@ k6attn_status k6attn_seq2head_relayout(const void *src, void *dst, int B, long S
  *    k6attn_forward with a caller workspace then).
  *  - Every GPU that loads the library reserves the array until the process
  *    exits.
- *  - The first call on a device, made with that device current, looks up the
- *    array's device address once (cudaGetSymbolAddress); make that first call
- *    before any stream capture begins.
+ *  - The first call in a CUDA context looks up the array's device address
+ *    (cudaGetSymbolAddress) and keeps it for that context: once per device,
+ *    and once more after cudaDeviceReset, which gives the device a new context
+ *    with a new copy of the array (the old copy's contents are gone).  Make
+ *    that first call, with the handle's device current, before any stream
+ *    capture begins.
  *  - All calls on one device share the array, which keeps the last call's
  *    contents: calls that can overlap on the GPU (several streams, or several
  *    host threads without ordering between them) race on it.  Keep such calls

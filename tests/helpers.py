@@ -49,3 +49,17 @@ def compare(out, ref, lse=None, ref_lse=None, dtype="bf16"):
     if lse is not None:
         assert m["lse_max_abs"] <= LSE_MAX_ABS, m
     return m
+
+
+_ORACLE_ROWS = {}
+
+
+def oracle_sampled(w, x, rows):
+    """Oracle output and LSE of the workload's inputs `x` on query `rows` (all
+    heads, all keys), cached per (workload, rows): the full-size workloads cost
+    seconds of CPU per call and several tests check the same sample."""
+    key = (w.name, w.B, np.asarray(rows, np.int64).tobytes())
+    if key not in _ORACLE_ROWS:
+        _ORACLE_ROWS[key] = O.attention(geom(w), x["q"], x["k"], x["v"], x["jk"] if w.Nj else None,
+                                        x["jv"] if w.Nj else None, rows=rows)
+    return _ORACLE_ROWS[key]

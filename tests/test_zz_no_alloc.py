@@ -4,18 +4,18 @@ results as k6attn_forward with a caller workspace.
 It serves callers that cannot allocate device memory (a plugin whose host
 framework owns all allocations, a fixed memory budget, a binding that only
 receives tensors): the scratch comes from one device array inside the
-library.  Two calls in a row, with different inputs and chunk counts, check
-that the second call is not disturbed by what the first left in the array.
-This file is collected last so that a stop at its first failure has already
-run every other test.
+library.  Both entry points run the same kernels on the same inputs, so their
+outputs must agree bit for bit.  Two calls in a row, with different inputs,
+the larger chunk count first, check that the second call is not disturbed by
+the partials the first left in the array.  This file is collected last so
+that a stop at its first failure has already run every other test.
 """
-import numpy as np
 import pytest
 
 from video_dit_long_gb300 import inputs
 from video_dit_long_gb300.configs import Workload
 
-from .helpers import BF16_MAX_ABS, BF16_MEAN_ABS, BF16_REL_L2, LSE_MAX_ABS, to_dev, to_host
+from .helpers import to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -30,17 +30,10 @@ def _need_gpu():
         pytest.skip("no CUDA device")
 
 
-def within(a, b, la, lb):
-    err = np.abs(a - b)
-    assert err.max() <= BF16_MAX_ABS and err.mean() <= BF16_MEAN_ABS
-    assert np.linalg.norm(a - b) <= BF16_REL_L2 * np.linalg.norm(b)
-    assert np.abs(la - lb).max() <= LSE_MAX_ABS
-
-
 def test_static_scratch_forward_matches_workspace_forward_twice():
     from video_dit_long_gb300 import k6attn as K
     h = K.Handle.for_workload(W)
-    for seed, n in ((42, 2), (7, 4)):
+    for seed, n in ((42, 4), (7, 2)):
         x = inputs.make_inputs(W, seed=seed)
         q, k, v, jk, jv = (to_dev(x[name], W.dtype) for name in ("q", "k", "v", "jk", "jv"))
         ws = torch.empty(h.workspace_bytes(n, True), dtype=torch.uint8, device="cuda")
@@ -51,7 +44,8 @@ def test_static_scratch_forward_matches_workspace_forward_twice():
         lse = torch.full_like(ref_lse, float("nan"))
         h.forward_static_scratch(q, k, v, jk, jv, out, lse, rope=True, n_chunks=n)
         h.sync()
-        within(to_host(out), to_host(ref), lse.cpu().numpy(), ref_lse.cpu().numpy())
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), (seed, n)
+        assert torch.equal(lse.view(torch.int32), ref_lse.view(torch.int32)), (seed, n)
 
 
 def test_static_scratch_rejects_problems_beyond_its_size():

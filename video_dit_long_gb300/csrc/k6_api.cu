@@ -126,6 +126,16 @@ static k6attn_status check_inputs(const char *fn, const Geom &g, const void *q, 
     return K6ATTN_OK;
 }
 
+k6attn_status check_handle(const char *fn, k6attn_t h) {
+    if (!h) return set_error(K6ATTN_ERR_INVALID_ARG, "%s: null handle", fn);
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return set_error(K6ATTN_ERR_CUDA, "%s: no current device", fn);
+    if (dev != h->device)
+        return set_error(K6ATTN_ERR_INVALID_ARG, "%s: the handle was created on device %d but device %d is current",
+                         fn, h->device, dev);
+    return K6ATTN_OK;
+}
+
 }  // namespace k6
 
 using namespace k6;
@@ -207,9 +217,14 @@ k6attn_status k6attn_create(const k6attn_desc *desc, k6attn_t *out) {
 
 void k6attn_destroy(k6attn_t h) {
     if (!h) return;
+    // free on the handle's own device, whichever device the caller has current
+    int cur = -1;
+    const bool other = cudaGetDevice(&cur) == cudaSuccess && cur != h->device;
+    if (other) cudaSetDevice(h->device);
     cudaDeviceSynchronize();
     cudaFree(h->tables);
     cudaFree(h->err);
+    if (other) cudaSetDevice(cur);
     delete h;
 }
 
@@ -222,7 +237,7 @@ size_t k6attn_workspace_bytes(k6attn_t h, int n_chunks, int with_rope) {
 }
 
 k6attn_status k6attn_set_option(k6attn_t h, k6attn_option opt, long long value) {
-    if (!h) return set_error(K6ATTN_ERR_INVALID_ARG, "set_option: null handle");
+    if (!h) return set_error(K6ATTN_ERR_INVALID_ARG, "set_option: null handle");  // host-side only
     if (value < 0) return set_error(K6ATTN_ERR_INVALID_ARG, "set_option: negative value");
     switch (opt) {
         case K6ATTN_OPT_WAIT_LIMIT_NS: h->wait_limit_ns = (unsigned long long)value; return K6ATTN_OK;
@@ -235,7 +250,10 @@ k6attn_status k6attn_set_option(k6attn_t h, k6attn_option opt, long long value) 
 static k6attn_status rope_common(const char *fn, k6attn_t h, const void *q, const void *k, const void *joint_k,
                                  const void *rope_tables, void *q_out, void *k_out, void *joint_k_out,
                                  k6attn_dtype out_dtype, const QkNorm *norm, void *stream) {
-    if (!h) return set_error(K6ATTN_ERR_INVALID_ARG, "%s: null handle", fn);
+    {
+        k6attn_status hs = check_handle(fn, h);
+        if (hs != K6ATTN_OK) return hs;
+    }
     const Geom &g = h->g;
     if (!q || !k || !q_out || !k_out || (g.Nj > 0 && (!joint_k || !joint_k_out)) || (!rope_tables && h->table_bytes))
         return set_error(K6ATTN_ERR_INVALID_ARG, "%s: null tensor or table pointer", fn);
@@ -293,7 +311,10 @@ size_t k6attn_row_bounds_bytes(k6attn_t h) {
 k6attn_status k6attn_row_bounds(k6attn_t h, const void *q, const void *k, const void *joint_k, k6attn_dtype qk_dtype,
                                 float *bounds, void *stream) {
     g_msg[0] = 0;
-    if (!h) return set_error(K6ATTN_ERR_INVALID_ARG, "row_bounds: null handle");
+    {
+        k6attn_status hs = check_handle("row_bounds", h);
+        if (hs != K6ATTN_OK) return hs;
+    }
     const Geom &g = h->g;
     if (!q || !k || !bounds || (g.Nj > 0 && !joint_k))
         return set_error(K6ATTN_ERR_INVALID_ARG, "row_bounds: null pointer");
@@ -315,7 +336,10 @@ k6attn_status k6attn_attention_chunks_bounded(k6attn_t h, const void *q, const v
                                               const float *bounds, int n_chunks, void *out, float *lse,
                                               void *stream) {
     g_msg[0] = 0;
-    if (!h) return set_error(K6ATTN_ERR_INVALID_ARG, "attention_chunks_bounded: null handle");
+    {
+        k6attn_status hs = check_handle("attention_chunks_bounded", h);
+        if (hs != K6ATTN_OK) return hs;
+    }
     const Geom &g = h->g;
     if (g.dtype != K6ATTN_BF16)
         return set_error(K6ATTN_ERR_UNSUPPORTED, "attention_chunks_bounded: the constant-max path is bf16 only");
@@ -340,7 +364,10 @@ k6attn_status k6attn_attention_chunks_bounded(k6attn_t h, const void *q, const v
 k6attn_status k6attn_lse_merge(k6attn_t h, const float *part_o, const float *part_lse, int n_chunks, void *out,
                                float *lse, void *stream) {
     g_msg[0] = 0;
-    if (!h) return set_error(K6ATTN_ERR_INVALID_ARG, "lse_merge: null handle");
+    {
+        k6attn_status hs = check_handle("lse_merge", h);
+        if (hs != K6ATTN_OK) return hs;
+    }
     const Geom &g = h->g;
     if (!part_o || !part_lse || !out) return set_error(K6ATTN_ERR_INVALID_ARG, "lse_merge: null pointer");
     if (n_chunks < 1) return set_error(K6ATTN_ERR_INVALID_ARG, "lse_merge: n_chunks must be >= 1");
@@ -360,7 +387,10 @@ k6attn_status k6attn_forward(k6attn_t h, const void *q, const void *k, const voi
                              const void *joint_v, const void *rope_tables, int n_chunks, void *out, float *lse,
                              void *workspace, size_t workspace_bytes, void *stream) {
     g_msg[0] = 0;
-    if (!h) return set_error(K6ATTN_ERR_INVALID_ARG, "forward: null handle");
+    {
+        k6attn_status hs = check_handle("forward", h);
+        if (hs != K6ATTN_OK) return hs;
+    }
     const Geom &g = h->g;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t qb = (size_t)g.B * g.S * g.H * g.d * g.elem, lb = (size_t)g.B * g.H * g.S * 4;
@@ -408,7 +438,10 @@ k6attn_status k6attn_attention_chunks(k6attn_t h, const void *q, const void *k, 
                                       const void *joint_v, k6attn_dtype qk_dtype, int n_chunks, void *out, float *lse,
                                       void *stream) {
     g_msg[0] = 0;
-    if (!h) return set_error(K6ATTN_ERR_INVALID_ARG, "attention_chunks: null handle");
+    {
+        k6attn_status hs = check_handle("attention_chunks", h);
+        if (hs != K6ATTN_OK) return hs;
+    }
     const Geom &g = h->g;
     if (n_chunks > 1 && !lse)
         return set_error(K6ATTN_ERR_INVALID_ARG, "attention_chunks: partial lse is required when n_chunks > 1");
@@ -434,7 +467,10 @@ k6attn_status k6attn_backward(k6attn_t h, const void *q, const void *k, const vo
                               const float *lse, float *dq, float *dk, float *dv, float *djoint_k, float *djoint_v,
                               void *workspace, size_t workspace_bytes, void *stream) {
     g_msg[0] = 0;
-    if (!h) return set_error(K6ATTN_ERR_INVALID_ARG, "backward: null handle");
+    {
+        k6attn_status hs = check_handle("backward", h);
+        if (hs != K6ATTN_OK) return hs;
+    }
     const Geom &g = h->g;
     if (g.dtype != K6ATTN_BF16 || g.d != 128)
         return set_error(K6ATTN_ERR_UNSUPPORTED, "backward: needs a BF16 handle with d = 128");
@@ -496,7 +532,10 @@ k6attn_status k6attn_cross_forward(k6attn_t h, const void *q, long Sq, const voi
                                    int n_chunks, void *out, float *lse, void *workspace, size_t workspace_bytes,
                                    void *stream) {
     g_msg[0] = 0;
-    if (!h) return set_error(K6ATTN_ERR_INVALID_ARG, "cross_forward: null handle");
+    {
+        k6attn_status hs = check_handle("cross_forward", h);
+        if (hs != K6ATTN_OK) return hs;
+    }
     if (Sq < 1 || Sk < 1) return set_error(K6ATTN_ERR_INVALID_ARG, "cross_forward: Sq and Sk must be >= 1");
     if (Sq >= (1L << 30) || Sk >= (1L << 30) || (long)h->g.B * Sq * h->g.H >= (1L << 31) ||
         (long)h->g.B * Sk * h->g.H >= (1L << 31))
@@ -548,7 +587,10 @@ k6attn_status k6attn_seq2head_relayout(const void *src, void *dst, int B, long S
 
 k6attn_status k6attn_sync(k6attn_t h, void *stream) {
     g_msg[0] = 0;
-    if (!h) return set_error(K6ATTN_ERR_INVALID_ARG, "sync: null handle");
+    {
+        k6attn_status hs = check_handle("sync", h);
+        if (hs != K6ATTN_OK) return hs;
+    }
     k6attn_status s = cuda_check(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "sync");
     if (s != K6ATTN_OK) return s;
     int word = 0;

@@ -31,7 +31,6 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
-#include <mutex>
 
 #include "k6_device.cuh"
 #include "k6_internal.h"
@@ -610,34 +609,6 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
 
 // ------------------------------------------------------------------- host
 
-static bool bw_map(CUtensorMap *m, const void *base, long rows, int H, int B, bool f16, const char **why) {
-    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    });
-    if (!encode) {
-        if (why) *why = "cuTensorMapEncodeTiled is not available from the driver";
-        return false;
-    }
-    cuuint64_t dims[4] = {(cuuint64_t)bw::D, (cuuint64_t)H, (cuuint64_t)rows, (cuuint64_t)B};
-    cuuint64_t strides[3] = {(cuuint64_t)bw::D * 2, (cuuint64_t)H * bw::D * 2, (cuuint64_t)rows * H * bw::D * 2};
-    cuuint32_t box[4] = {64, 1, (cuuint32_t)bw::BM, 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    if (encode(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base),
-               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
-        if (why) *why = "cuTensorMapEncodeTiled rejected a tensor";
-        return false;
-    }
-    return true;
-}
-
 cudaError_t launch_attn_bwd(const Geom &g, bool qk_f16, const void *q, const void *k, const void *v, const void *jk,
                             const void *jv, const void *out, const void *dout, const float *lse, float2 *LD, float *dq,
                             float *dk, float *dv, float *djk, float *djv, unsigned long long wait_limit_ns, int *err,
@@ -649,19 +620,13 @@ cudaError_t launch_attn_bwd(const Geom &g, bool qk_f16, const void *q, const voi
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     CUtensorMap mq, mdo, mk, mv, mjk, mjv;
     const bool has_joint = g.Nj > 0;
-    if (!bw_map(&mq, q, g.S, g.H, g.B, qk_f16, why) || !bw_map(&mdo, dout, g.S, g.H, g.B, false, why) ||
-        !bw_map(&mk, k, g.Nv, g.H, g.B, qk_f16, why) || !bw_map(&mv, v, g.Nv, g.H, g.B, false, why) ||
-        !bw_map(&mjk, has_joint ? jk : k, has_joint ? g.Nj : g.Nv, g.H, g.B, qk_f16, why) ||
-        !bw_map(&mjv, has_joint ? jv : v, has_joint ? g.Nj : g.Nv, g.H, g.B, false, why))
+    if (!make_bshd_map(&mq, q, g.S, g.H, g.B, qk_f16, why) || !make_bshd_map(&mdo, dout, g.S, g.H, g.B, false, why) ||
+        !make_bshd_map(&mk, k, g.Nv, g.H, g.B, qk_f16, why) || !make_bshd_map(&mv, v, g.Nv, g.H, g.B, false, why) ||
+        !make_bshd_map(&mjk, has_joint ? jk : k, has_joint ? g.Nj : g.Nv, g.H, g.B, qk_f16, why) ||
+        !make_bshd_map(&mjv, has_joint ? jv : v, has_joint ? g.Nj : g.Nv, g.H, g.B, false, why))
         return cudaErrorInvalidValue;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bw::SMEM_ALLOC);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(bwd_dkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            bw::SMEM_ALLOC);
-    });
+    cudaError_t attr_err = set_max_dynamic_smem((const void *)bwd_dq_kernel, bw::SMEM_ALLOC);
+    if (attr_err == cudaSuccess) attr_err = set_max_dynamic_smem((const void *)bwd_dkv_kernel, bw::SMEM_ALLOC);
     if (attr_err != cudaSuccess) return attr_err;
     bwd_dsum_kernel<<<(unsigned)sms * 8, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(out),
                                                        static_cast<const __nv_bfloat16 *>(dout), lse, g.S, g.H, g.B,

@@ -28,7 +28,6 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
-#include <mutex>
 
 #include "k6_attn_common.cuh"
 #include "k6_device.cuh"
@@ -433,37 +432,6 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
 
 // ------------------------------------------------------------------- host
 
-// Tensor map over a BSHD bf16 tensor [B][rows][H][128] with the two-tile
-// kernel's box: 64 dims x 1 head x 128 rows x 1 batch, 128-byte swizzle, zero
-// fill out of bounds.
-static bool single_map(CUtensorMap *m, const void *base, long rows, int H, int B, const char **why) {
-    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    });
-    if (!encode) {
-        if (why) *why = "cuTensorMapEncodeTiled is not available from the driver";
-        return false;
-    }
-    cuuint64_t dims[4] = {(cuuint64_t)tc::D, (cuuint64_t)H, (cuuint64_t)rows, (cuuint64_t)B};
-    cuuint64_t strides[3] = {(cuuint64_t)tc::D * 2, (cuuint64_t)H * tc::D * 2, (cuuint64_t)rows * H * tc::D * 2};
-    cuuint32_t box[4] = {64, 1, (cuuint32_t)tc::BM, 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    if (encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
-        if (why) *why = "cuTensorMapEncodeTiled rejected a tensor";
-        return false;
-    }
-    return true;
-}
-
 cudaError_t launch_attn_tc_single(const Geom &g, const void *q, const void *k, const void *v, const void *jk,
                                   const void *jv, int n_chunks, void *out, float *lse, const AttnTcOptions &opt,
                                   cudaStream_t st, const char **why) {
@@ -477,20 +445,14 @@ cudaError_t launch_attn_tc_single(const Geom &g, const void *q, const void *k, c
     // an empty segment never issues loads; give its maps a valid stand-in
     const void *kk = has_video ? k : jk, *vv = has_video ? v : jv;
     const long kv_rows = has_video ? g.Nv : g.Nj;
-    if (!single_map(&mq, q, g.Sq, g.H, g.B, why) || !single_map(&mk, kk, kv_rows, g.H, g.B, why) ||
-        !single_map(&mv, vv, kv_rows, g.H, g.B, why) ||
-        !single_map(&mjk, has_joint ? jk : kk, has_joint ? g.Nj : kv_rows, g.H, g.B, why) ||
-        !single_map(&mjv, has_joint ? jv : vv, has_joint ? g.Nj : kv_rows, g.H, g.B, why))
+    if (!make_bshd_map(&mq, q, g.Sq, g.H, g.B, false, why) || !make_bshd_map(&mk, kk, kv_rows, g.H, g.B, false, why) ||
+        !make_bshd_map(&mv, vv, kv_rows, g.H, g.B, false, why) ||
+        !make_bshd_map(&mjk, has_joint ? jk : kk, has_joint ? g.Nj : kv_rows, g.H, g.B, false, why) ||
+        !make_bshd_map(&mjv, has_joint ? jv : vv, has_joint ? g.Nj : kv_rows, g.H, g.B, false, why))
         return cudaErrorInvalidValue;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(attn_tc_single_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        ts::SMEM_ALLOC);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(attn_tc_single_kernel<true>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize, ts::SMEM_ALLOC);
-    });
+    cudaError_t attr_err = set_max_dynamic_smem((const void *)attn_tc_single_kernel<false>, ts::SMEM_ALLOC);
+    if (attr_err == cudaSuccess)
+        attr_err = set_max_dynamic_smem((const void *)attn_tc_single_kernel<true>, ts::SMEM_ALLOC);
     if (attr_err != cudaSuccess) return attr_err;
     TcParams p;
     p.S = g.S;

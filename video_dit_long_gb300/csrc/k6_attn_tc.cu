@@ -38,8 +38,6 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
-#include <mutex>
-
 #include "k6_attn_common.cuh"
 #include "k6_device.cuh"
 #include "k6_internal.h"
@@ -452,40 +450,6 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
 
 // ------------------------------------------------------------------- host
 
-static PFN_cuTensorMapEncodeTiled_v12000 get_encode(const char **why) {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    if (!fn && why) *why = "cuTensorMapEncodeTiled is not available from the driver";
-    return fn;
-}
-
-// Tensor map over a BSHD bf16 tensor [B][rows][H][128]: box = 64 dims x 1 head
-// x 128 rows x 1 batch, 128-byte swizzle, zero fill out of bounds.
-static bool make_map(CUtensorMap *m, const void *base, long rows, int H, int B, const char **why) {
-    auto encode = get_encode(why);
-    if (!encode) return false;
-    cuuint64_t dims[4] = {(cuuint64_t)tc::D, (cuuint64_t)H, (cuuint64_t)rows, (cuuint64_t)B};
-    cuuint64_t strides[3] = {(cuuint64_t)tc::D * 2, (cuuint64_t)H * tc::D * 2, (cuuint64_t)rows * H * tc::D * 2};
-    cuuint32_t box[4] = {64, 1, (cuuint32_t)tc::BM, 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) {
-        if (why) *why = "cuTensorMapEncodeTiled rejected a tensor";
-        return false;
-    }
-    return true;
-}
-
 cudaError_t launch_attn_tc(const Geom &g, const void *q, const void *k, const void *v, const void *jk,
                            const void *jv, int n_chunks, void *out, float *lse, const AttnTcOptions &opt,
                            cudaStream_t st, const char **why) {
@@ -495,20 +459,14 @@ cudaError_t launch_attn_tc(const Geom &g, const void *q, const void *k, const vo
     // an empty segment never issues loads; give its maps a valid stand-in
     const void *kk = has_video ? k : jk, *vv = has_video ? v : jv;
     const long kv_rows = has_video ? g.Nv : g.Nj;
-    if (!make_map(&mq, q, g.Sq, g.H, g.B, why) || !make_map(&mk, kk, kv_rows, g.H, g.B, why) ||
-        !make_map(&mv, vv, kv_rows, g.H, g.B, why) ||
-        !make_map(&mjk, has_joint ? jk : kk, has_joint ? g.Nj : kv_rows, g.H, g.B, why) ||
-        !make_map(&mjv, has_joint ? jv : vv, has_joint ? g.Nj : kv_rows, g.H, g.B, why))
+    // the tile copies move 2-byte elements; fp16 q/k travel through the same maps
+    if (!make_bshd_map(&mq, q, g.Sq, g.H, g.B, false, why) || !make_bshd_map(&mk, kk, kv_rows, g.H, g.B, false, why) ||
+        !make_bshd_map(&mv, vv, kv_rows, g.H, g.B, false, why) ||
+        !make_bshd_map(&mjk, has_joint ? jk : kk, has_joint ? g.Nj : kv_rows, g.H, g.B, false, why) ||
+        !make_bshd_map(&mjv, has_joint ? jv : vv, has_joint ? g.Nj : kv_rows, g.H, g.B, false, why))
         return cudaErrorInvalidValue;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        tc::SMEM_ALLOC);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            tc::SMEM_ALLOC);
-    });
+    cudaError_t attr_err = set_max_dynamic_smem((const void *)attn_tc_kernel<false>, tc::SMEM_ALLOC);
+    if (attr_err == cudaSuccess) attr_err = set_max_dynamic_smem((const void *)attn_tc_kernel<true>, tc::SMEM_ALLOC);
     if (attr_err != cudaSuccess) return attr_err;
     TcParams p;
     p.S = g.S;

@@ -2,6 +2,7 @@
 // libk6attn (launchers, geometry, rotary table layout).  Not part of the ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -36,6 +37,21 @@ RopeLayout rope_layout(const Geom &g);
 // Error reporting of the host side (thread-local message).
 k6attn_status set_error(k6attn_status s, const char *fmt, ...);
 k6attn_status cuda_check(cudaError_t e, const char *what);
+
+// A handle is usable only while its own device is current (its tables and
+// error word live there): INVALID_ARG otherwise, and for a null handle.
+k6attn_status check_handle(const char *fn, k6attn_t h);
+
+// ---- host helpers shared by the launchers (k6_host.cu) ----
+
+// Unique id of the calling thread's current CUDA context; 0 when none is current.
+unsigned long long current_context_id();
+// Tensor map over a BSHD tensor [B][rows][H][128] of 2-byte elements: box = 64
+// dims x 1 head x 128 rows x 1 batch, 128-byte swizzle, zero fill out of bounds.
+bool make_bshd_map(CUtensorMap *m, const void *base, long rows, int H, int B, bool f16, const char **why);
+// Opt `func` in to `bytes` of dynamic shared memory in the current context
+// (once per kernel and context).
+cudaError_t set_max_dynamic_smem(const void *func, int bytes);
 
 // ---- launchers (return cudaSuccess or the launch error) ----
 

@@ -13,6 +13,7 @@
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <vector>
 
 #include "k6attn.h"
 #include "k6_internal.h"
@@ -25,27 +26,38 @@ namespace k6 {
 static __device__ __align__(256) unsigned char g_static_scratch[K6ATTN_STATIC_SCRATCH_BYTES];
 
 namespace {
-constexpr int kMaxDevices = 64;
+struct ScratchAddr {
+    unsigned long long ctx;  // unique id of the CUDA context the address belongs to
+    void *ptr;
+};
 std::mutex g_scratch_mu;
-void *g_scratch_addr[kMaxDevices];  // device address of g_static_scratch, per device (set once)
+std::vector<ScratchAddr> g_scratch_addr;  // one entry per context that has made a call
 }  // namespace
 
-// Set-up, once per device, with that device current: look up the device
-// address of the static array.  Allocates nothing.
+// Set-up, once per CUDA context, with that context current: look up the device
+// address of the static array.  Allocates nothing.  The address is cached per
+// context, not per device ordinal: cudaDeviceReset replaces a device's primary
+// context, the module (and the array) is loaded anew in the next one, and the
+// old address would be stale there.
 static k6attn_status static_scratch_address(void **out) {
-    int dev = 0;
-    k6attn_status s = cuda_check(cudaGetDevice(&dev), "forward_static_scratch: current device");
-    if (s != K6ATTN_OK) return s;
-    if (dev < 0 || dev >= kMaxDevices)
-        return set_error(K6ATTN_ERR_UNSUPPORTED, "forward_static_scratch: device %d beyond %d", dev, kMaxDevices);
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
-        s = cuda_check(cudaGetSymbolAddress(&p, g_static_scratch), "forward_static_scratch: scratch address");
-        if (s != K6ATTN_OK) return s;
-        g_scratch_addr[dev] = p;
+    unsigned long long id = current_context_id();
+    if (id) {
+        std::lock_guard<std::mutex> lock(g_scratch_mu);
+        for (const ScratchAddr &e : g_scratch_addr)
+            if (e.ctx == id) {
+                *out = e.ptr;
+                return K6ATTN_OK;
+            }
     }
-    *out = g_scratch_addr[dev];
+    void *p = nullptr;
+    k6attn_status s = cuda_check(cudaGetSymbolAddress(&p, g_static_scratch), "forward_static_scratch: scratch address");
+    if (s != K6ATTN_OK) return s;
+    id = current_context_id();  // the lookup above made the device's context current if none was
+    if (id) {
+        std::lock_guard<std::mutex> lock(g_scratch_mu);
+        g_scratch_addr.push_back({id, p});
+    }
+    *out = p;
     return K6ATTN_OK;
 }
 
@@ -56,7 +68,8 @@ extern "C" k6attn_status k6attn_forward_static_scratch(k6attn_t h, const void *q
                                                        const void *rope_tables, int n_chunks, void *out, float *lse,
                                                        void *stream) {
     using namespace k6;
-    if (!h) return set_error(K6ATTN_ERR_INVALID_ARG, "forward_static_scratch: null handle");
+    k6attn_status hs = check_handle("forward_static_scratch", h);
+    if (hs != K6ATTN_OK) return hs;
     if (n_chunks < 1) return set_error(K6ATTN_ERR_INVALID_ARG, "forward_static_scratch: n_chunks must be >= 1");
     const size_t need = k6attn_workspace_bytes(h, n_chunks, rope_tables != nullptr);
     if (need > (size_t)K6ATTN_STATIC_SCRATCH_BYTES)
