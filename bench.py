@@ -1,15 +1,17 @@
 #!/usr/bin/env python
 """Throughput of the joint-sequence attention path on one GB300.
 
-One step = the whole hot path over one batch of synthetic input, each row a
-separate C-ABI call with CUDA events between them:
-  rotary on q/k/joint_k (sequence layout, full head rows, into fp16 copies) ->
-  seq->head relayout of q, k, joint_k (fp16), v, joint_v (the Ulysses layout
-  change, 8-way, done on one GPU) -> attention over n K/V chunks (fp32
-  partials + LSE) -> LSE merge -> head->seq relayout of the output.
+One step = the whole hot path over one batch of synthetic input
+(video_dit_long_gb300.step.UlyssesStep), each row a C-ABI call with CUDA
+events between them:
+  k6attn_rope_split_heads (rotary on q/k/joint_k into fp16 and the 8-way
+  seq->head relayout of q, k, joint_k, v, joint_v, one pass) ->
+  k6attn_attention_chunk_groups (attention over n K/V chunks on the head
+  layout, each CTA's chunk group merged in the kernel: n/group fp32 partials
+  + LSE) -> k6attn_lse_merge_heads (LSE merge written to the sequence layout).
 The headline metric is attention TFLOP/s (4*B*H*S^2*d per step) over the whole
 step; the attention kernel alone gives the roofline fraction against the
-measured dense-bf16 peak.
+measured dense-bf16 peak (burst: it runs inside a step of tens of ms).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--config pro|long|lite|image] [--chunks n] [--no-secondary]
@@ -147,7 +149,8 @@ class Clocks:
 
 class Path(UlyssesStep):
     """The benchmarked step (`UlyssesStep.step`) plus the end-to-end loop from
-    pinned host buffers and the constant-max variant on the same buffers."""
+    pinned host buffers, and the secondary rows on the same buffers: the merge
+    of one partial per chunk and the constant-max variant."""
 
     E2E_BUFS = 3  # input and output buffer sets of the end-to-end loop (uploads run two steps ahead)
 
@@ -156,36 +159,55 @@ class Path(UlyssesStep):
         torch = self.torch
         bf = torch.bfloat16
         self.host = {k: torch.from_numpy(v.view(np.int16)).view(bf).pin_memory() for k, v in x.items()}
-        self.e2e_head = {k: torch.empty_like(self.seq[k]) for k in self.seq}
         self.e2e_in = [{k: torch.empty_like(self.seq[k]) for k in self.seq} for _ in range(self.E2E_BUFS)]
-        self.e2e_out = [{"out_h": torch.empty_like(self.out_h), "lse": torch.empty_like(self.lse),
-                         "out": torch.empty_like(self.out)} for _ in range(self.E2E_BUFS)]
+        self.e2e_out = [{"out": torch.empty_like(self.out), "lse": torch.empty_like(self.lse)}
+                        for _ in range(self.E2E_BUFS)]
         self.h2d_stream = torch.cuda.Stream()
         self.d2h_stream = torch.cuda.Stream()
-        self.ws = torch.empty(self.h.workspace_bytes(n_chunks, True), dtype=torch.uint8, device="cuda")
         self.out_host = torch.empty(self.out.shape, dtype=bf).pin_memory()
         self.lse_host = torch.empty(self.lse.shape, dtype=torch.float32).pin_memory()
+
+    def chunk_partials(self):
+        """One fp32 partial per chunk (the workload's n) on the head layout, from
+        k6attn_attention_chunks, for the secondary rows."""
+        torch, w, hd = self.torch, self.w, self.head
+        if not hasattr(self, "pc_o"):
+            f32 = torch.float32
+            self.pc_o = torch.empty((self.n, self.P * w.B, w.S, self.Hl, w.d), dtype=f32, device="cuda")
+            self.pc_lse = torch.empty((self.n, self.P * w.B, self.Hl, w.S), dtype=f32, device="cuda")
+            self.out2 = torch.empty_like(self.out)
+            self.lse2 = torch.empty_like(self.lse)
+            jk, jv = (hd["jk"], hd["jv"]) if w.Nj else (None, None)
+            self.h.attention_chunks(hd["q"], hd["k"], hd["v"], jk, jv, self.n, self.pc_o, self.pc_lse,
+                                    qk_dtype=K.F16)
+        return self.pc_o, self.pc_lse
+
+    def merge_per_chunk(self):
+        """The LSE merge of one partial per chunk (n of them) into the sequence layout."""
+        po, pl = self.chunk_partials()
+        self.hs.lse_merge_heads(po, pl, self.n, self.P, self.out2, self.lse2)
 
     def const_max_step(self):
         """Constant-max variant of the attention + merge rows on the head-layout buffers
         that step() filled: row bounds, bounded attention over the chunks, merge."""
         w, hd = self.w, self.head
+        po, pl = self.chunk_partials()
         if not hasattr(self, "bounds"):
             self.bounds = self.torch.empty(self.h.row_bounds_bytes() // 4, dtype=self.torch.float32, device="cuda")
         jk, jv = (hd["jk"], hd["jv"]) if w.Nj else (None, None)
         self.h.row_bounds(hd["q"], hd["k"], jk, self.bounds, qk_dtype=K.F16)
-        self.h.attention_chunks_bounded(hd["q"], hd["k"], hd["v"], jk, jv, self.bounds, self.n, self.part_o,
-                                        self.part_lse, qk_dtype=K.F16)
-        self.h.lse_merge(self.part_o, self.part_lse, self.n, self.out_h, self.lse)
+        self.h.attention_chunks_bounded(hd["q"], hd["k"], hd["v"], jk, jv, self.bounds, self.n, po, pl,
+                                        qk_dtype=K.F16)
+        self.hs.lse_merge_heads(po, pl, self.n, self.P, self.out2, self.lse2)
 
     def e2e_run(self, steps):
-        """Public API from pinned host buffers, `steps` steps: per step the H2D copy of its
-        inputs, relayout, k6attn_forward (rotary + chunks + merge), relayout back and the
-        D2H copy of out and lse.  Uploads and downloads run on their own streams (one per
-        direction, so a slow download never holds up an upload), uploads two steps ahead
-        of the compute with three input and output buffer sets, as a serving loop would
-        run it; every copy is inside the timed region."""
-        torch, w = self.torch, self.w
+        """The step through the public API from pinned host buffers, `steps` steps: per
+        step the H2D copy of its inputs, the three calls of the step and the D2H copy of
+        out and lse.  Uploads and downloads run on their own streams (one per direction,
+        so a slow download never holds up an upload), uploads two steps ahead of the
+        compute with three input and output buffer sets, as a serving loop would run it;
+        every copy is inside the timed region."""
+        torch = self.torch
         nb = self.E2E_BUFS
         comp = torch.cuda.current_stream()
         up, down = self.h2d_stream, self.d2h_stream
@@ -212,15 +234,9 @@ class Path(UlyssesStep):
             b = step % nb
             buf, ob = self.e2e_in[b], self.e2e_out[b]
             comp.wait_event(ev_in[b])
-            self.relayout_in(buf, self.e2e_head)
-            ev_used[b].record(comp)
-            hd = self.e2e_head
-            jk, jv = (hd["jk"], hd["jv"]) if w.Nj else (None, None)
             comp.wait_event(ev_read[b])  # this output buffer's previous contents have left the device
-            self.h.forward(hd["q"], hd["k"], hd["v"], jk, jv, ob["out_h"], ob["lse"], rope=True, n_chunks=self.n,
-                           workspace=self.ws)
-            K.seq2head_relayout(ob["out_h"], ob["out"], w.B, w.S, w.H, w.d, self.P, 1)
-            ev_out[b].record(comp)
+            # the prologue is the only reader of the inputs: release them after it
+            self.run(buf, ob["out"], ob["lse"], ev=[None, ev_used[b], None, ev_out[b]])
             with torch.cuda.stream(down):
                 down.wait_event(ev_out[b])
                 self.out_host.copy_(ob["out"], non_blocking=True)
@@ -273,14 +289,29 @@ def whole_job_rate(work_per_rank: float, world: int, seconds_max: float) -> floa
     return work_per_rank * world / seconds_max
 
 
-def measure(w, n_chunks, P, steps, warmup, dist_on, with_e2e=True, clocks=True):
+def time_calls(fn, steps, warmup=2):
+    """Mean device time (ms) of `fn` over `steps` back-to-back calls on the current stream."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def measure(w, n_chunks, P, steps, warmup, dist_on, with_e2e=True, clocks=True, step_only=False):
     import torch
     x = inputs.make_inputs(w)
     path = Path(w, n_chunks, P, x)
     for _ in range(warmup):
         path.step()
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    nev = len(path.intervals) + 1
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist_on)
     clk = Clocks(gpu_index())
@@ -292,22 +323,18 @@ def measure(w, n_chunks, P, steps, warmup, dist_on, with_e2e=True, clocks=True):
         barrier(dist_on)
     total_ms = max_over_ranks(t0.elapsed_time(t1), dist_on)
     path.sync()
-    per = np.array([[evs[s][i].elapsed_time(evs[s][i + 1]) for i in range(5)] for s in range(steps)])
-    res = {"total_ms": total_ms, "per_kernel_ms": per.mean(axis=0).tolist(),
-           "clocks": clk.summary() if clocks else None, "launches": path.launches_per_step * steps}
-    if with_e2e:
+    per = np.array([[evs[s][i].elapsed_time(evs[s][i + 1]) for i in range(nev - 1)] for s in range(steps)])
+    res = {"total_ms": total_ms, "per_kernel_ms": dict(zip(path.intervals, per.mean(axis=0).tolist())),
+           "clocks": clk.summary() if clocks else None, "launches": path.launches_per_step * steps,
+           "group": path.group, "parts": path.parts}
+    # the LSE merge of one partial per chunk (the workload's n), into the sequence layout
+    if not step_only:
+        res["merge_per_chunk_ms"] = time_calls(path.merge_per_chunk, steps)
+        path.sync()
+    if with_e2e and not step_only:
         # the constant-max variant of attention + merge on the same buffers
-        for _ in range(2):
-            path.const_max_step()
-        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        c0.record()
-        for _ in range(steps):
-            path.const_max_step()
-        c1.record()
-        torch.cuda.synchronize()
-        path.h.sync()
-        res["const_max_ms"] = c0.elapsed_time(c1) / steps
-    if with_e2e:
+        res["const_max_ms"] = time_calls(path.const_max_step, steps)
+        path.sync()
         path.e2e_run(max(1, warmup))
         torch.cuda.synchronize()
         barrier(dist_on)
@@ -319,7 +346,7 @@ def measure(w, n_chunks, P, steps, warmup, dist_on, with_e2e=True, clocks=True):
         res["e2e_ms"] = max_over_ranks(e0.elapsed_time(e1), dist_on)
         res["h2d"] = path.h2d_bytes()
         res["d2h"] = path.d2h_bytes()
-        path.h.sync()
+        path.sync()
     del path
     torch.cuda.empty_cache()
     return res, x
@@ -333,10 +360,13 @@ class _Null:
         pass
 
 
-def measure_cross(w, steps, warmup, n_chunks=8):
-    """Audio queries (the workload's joint tokens) over the full visual sequence, K/V in n chunks."""
+def measure_cross(w, steps, warmup, n_chunks=8, Sq=None):
+    """Audio queries (the workload's joint tokens, or the first Sq of them) over the
+    full visual sequence, K/V in n chunks (k6attn_cross_forward: attention with the
+    library's chunk groups, then the merge of the group partials)."""
     import torch
-    B, H, d, Sq, Sk = w.B, w.H, w.d, w.Nj, w.Nv
+    B, H, d, Sk = w.B, w.H, w.d, w.Nv
+    Sq = w.Nj if Sq is None else Sq
 
     def dev(tid, rows, std):
         return torch.from_numpy(inputs.tensor(42, tid, (B, rows, H, d), "bf16", std).view(np.int16)).view(
@@ -359,9 +389,10 @@ def measure_cross(w, steps, warmup, n_chunks=8):
     h.sync()
     ms = e0.elapsed_time(e1) / steps
     flops = 4.0 * B * H * Sq * Sk * d
+    kernel = "attn_tc_single_kernel" if Sq <= 128 else "attn_tc_kernel"
     return {"workload": f"{Sq} audio queries over {Sk} video keys (B={B}, H={H}, d={d}), {n_chunks} K/V chunks",
             "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_call": round(ms, 4),
-            "launches_per_call": 2}
+            "kernel": kernel, "flops_counted": "4*B*H*Sq*Sk*d on the real query rows"}
 
 
 def measure_backward(w, x, steps, warmup):
@@ -427,9 +458,17 @@ def measure_backward(w, x, steps, warmup):
              "ms_per_call": round(ms, 3), "launches_per_call": 3}, fwd)
 
 
-def merge_bytes(w, n, P):
+def merge_bytes(w, n):
+    """Algorithmic bytes of the LSE merge of n partials: n fp32 partial outputs and
+    LSEs read, the bf16 output and fp32 LSE written."""
     rows = w.B * w.S * w.H
     return n * (rows * w.d * 4 + rows * 4) + rows * w.d * 2 + rows * 4
+
+
+def prologue_bytes(w):
+    """Algorithmic bytes of the fused rotary + head split: q, k, joint_k, v, joint_v
+    read (bf16) and written (fp16 / bf16) once each."""
+    return 2 * (w.S + 2 * w.Nv + 2 * w.Nj) * w.H * w.d * 2
 
 
 def cpu_sample(w, x, rows_count, seed=7):
@@ -460,37 +499,36 @@ def workload_args(args):
 def run_ours(args, rank, world, dist_on):
     w, n, P = workload_args(args)
     pk = peaks()
-    res, x = measure(w, n, P, args.steps, args.warmup, dist_on)
+    res, x = measure(w, n, P, args.steps, args.warmup, dist_on, step_only=args.step_only)
     flops = w.flops()
     ms = res["total_ms"] / args.steps
     value = whole_job_rate(flops, world, res["total_ms"] / args.steps * 1e-3) / 1e12
-    k_ms = res["per_kernel_ms"]  # rope, relayout_in, attention, merge, relayout_out
-    attn_tflops = flops / (k_ms[2] * 1e-3) / 1e12
+    k_ms = res["per_kernel_ms"]
+    attn_tflops = flops / (k_ms["attention_chunk_groups"] * 1e-3) / 1e12
     # The attention kernel is timed with CUDA events inside a step of a few tens of
     # ms and a timed region of about a second: a burst, so the burst peak is its
     # denominator; the sustained (seconds-long, power-capped) figure is kept beside it.
     peak_b, peak_s = pk["bf16_tflops"], pk["bf16_tflops_sustained"]
     tag = "of measured" if pk["source"] == "measured" else "of fallback"
-    io = {k: w.H * w.d * 2 * r for k, r in {"q": w.S, "k": w.Nv, "v": w.Nv, "jk": w.Nj, "jv": w.Nj}.items()}
-    relayout_in_bytes = 2 * sum(io.values())
-    rope_bytes = 2 * (io["q"] + io["k"] + io["jk"])
-    mb = merge_bytes(w, n, P)
-    relayout_out_bytes = 2 * io["q"]
     hbm = pk["hbm_gbs"]
 
     def gbs(b, t_ms):
         return b / (t_ms * 1e-3) / 1e9
 
+    def hbm_rec(nbytes, t_ms):
+        return {"ms": round(t_ms, 4), "bytes": nbytes, "GB/s": round(gbs(nbytes, t_ms), 1),
+                "frac": round(gbs(nbytes, t_ms) / hbm, 4)}
+
     kernels = {
-        "rope_qk": {"ms": k_ms[0], "GB/s": gbs(rope_bytes, k_ms[0]), "frac": gbs(rope_bytes, k_ms[0]) / hbm},
-        "relayout_seq2head_qkv": {"ms": k_ms[1], "GB/s": gbs(relayout_in_bytes, k_ms[1]),
-                                  "frac": gbs(relayout_in_bytes, k_ms[1]) / hbm},
-        "attention_chunks": {"ms": k_ms[2], "TFLOP/s": attn_tflops, "frac": attn_tflops / peak_b,
-                             "frac_sustained": attn_tflops / peak_s},
-        "lse_merge": {"ms": k_ms[3], "GB/s": gbs(mb, k_ms[3]), "frac": gbs(mb, k_ms[3]) / hbm},
-        "relayout_head2seq_out": {"ms": k_ms[4], "GB/s": gbs(relayout_out_bytes, k_ms[4]),
-                                  "frac": gbs(relayout_out_bytes, k_ms[4]) / hbm},
+        "rope_split_heads": hbm_rec(prologue_bytes(w), k_ms["rope_split_heads"]),
+        "attention_chunk_groups": {"ms": round(k_ms["attention_chunk_groups"], 4), "TFLOP/s": round(attn_tflops, 2),
+                                   "frac": round(attn_tflops / peak_b, 4),
+                                   "frac_sustained": round(attn_tflops / peak_s, 4),
+                                   "chunks": n, "chunks_per_cta": res["group"], "partials": res["parts"]},
+        "lse_merge_heads": hbm_rec(merge_bytes(w, res["parts"]), k_ms["lse_merge_heads"]),
     }
+    if "merge_per_chunk_ms" in res:  # secondary: the merge of one partial per chunk (not part of the step)
+        kernels["lse_merge_per_chunk"] = hbm_rec(merge_bytes(w, n), res["merge_per_chunk_ms"])
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
@@ -512,14 +550,15 @@ def run_ours(args, rank, world, dist_on):
         line["e2e"] = {"value": round(flops * world / (res["e2e_ms"] / args.steps * 1e-3) / 1e12, 2),
                        "unit": "TFLOP/s", "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
                        "ms_per_step": round(res["e2e_ms"] / args.steps, 4)}
-    if args.secondary:
+    if args.secondary and not args.step_only:
         w2 = configs.WORKLOADS["long"]
         n2, P2 = w2.chunks[-1], w2.relayout_P[-1]
         steps2 = max(3, args.steps // 5)
         r2, _ = measure(w2, n2, P2, steps2, max(3, args.warmup), dist_on, with_e2e=False, clocks=True)
         f2 = w2.flops()
         t2 = r2["total_ms"] / steps2
-        a2 = f2 / (r2["per_kernel_ms"][2] * 1e-3) / 1e12
+        k2 = r2["per_kernel_ms"]
+        a2 = f2 / (k2["attention_chunk_groups"] * 1e-3) / 1e12
         line["long_video"] = {"workload": f"{w2.name}: {w2.note}", "n_chunks": n2, "relayout_P": P2,
                               "steps": steps2, "value": round(f2 * world / (t2 * 1e-3) / 1e12, 2),
                               "unit": "TFLOP/s", "ms_per_step": round(t2, 3),
@@ -529,24 +568,34 @@ def run_ours(args, rank, world, dist_on):
                                            "frac_sustained": round(a2 / peak_s, 4),
                                            "traffic": traffic_record("attn_tc_kernel", w2.name),
                                            "kernel": "attn_tc_kernel", "algorithmic_flops_per_launch": f2},
-                              "merge_GB/s": round(gbs(merge_bytes(w2, n2, P2), r2["per_kernel_ms"][3]), 1),
-                              "merge_frac": round(gbs(merge_bytes(w2, n2, P2), r2["per_kernel_ms"][3]) / hbm, 4),
+                              "kernels": {
+                                  "rope_split_heads": hbm_rec(prologue_bytes(w2), k2["rope_split_heads"]),
+                                  "attention_chunk_groups": {"ms": round(k2["attention_chunk_groups"], 3),
+                                                             "chunks_per_cta": r2["group"],
+                                                             "partials": r2["parts"]},
+                                  "lse_merge_heads": hbm_rec(merge_bytes(w2, r2["parts"]), k2["lse_merge_heads"]),
+                                  "lse_merge_per_chunk": hbm_rec(merge_bytes(w2, n2), r2["merge_per_chunk_ms"])},
                               "clocks": r2["clocks"]}
     if "const_max_ms" in res:
         line["const_max"] = {"what": "row bounds + bounded attention (no running max, no rescale) + merge",
                               "ms": round(res["const_max_ms"], 3),
                               "TFLOP/s": round(flops / (res["const_max_ms"] * 1e-3) / 1e12, 2),
-                              "standard_attention_plus_merge_ms": round(k_ms[2] + k_ms[3], 3)}
-    if args.secondary:
+                              "per_chunk_partials": n,
+                              "step_attention_plus_merge_ms": round(k_ms["attention_chunk_groups"] +
+                                                                    k_ms["lse_merge_heads"], 3)}
+    if args.secondary and not args.step_only:
         line["cross_attention"] = measure_cross(w, max(5, args.steps // 2), args.warmup)
         line["cross_attention"]["frac"] = round(line["cross_attention"]["value"] / peak_b, 4)
+        # a short query range (one 128-row tile: the single-tile kernel)
+        line["cross_attention_short"] = measure_cross(w, max(10, args.steps), args.warmup, Sq=100)
+        line["cross_attention_short"]["frac"] = round(line["cross_attention_short"]["value"] / peak_b, 4)
         bwd, fwd1 = measure_backward(w, x, max(3, args.steps // 10), max(3, args.warmup // 2))
         for rec in (bwd, fwd1):
             rec["frac"] = round(rec["value"] / peak_b, 4)
             rec["frac_sustained"] = round(rec["value"] / peak_s, 4)
         line["attention_n1"] = fwd1
         line["backward"] = bwd
-    if rank == 0 and world == 1 and not args.no_cpu:
+    if rank == 0 and world == 1 and not args.no_cpu and not args.step_only:
         dt, fl, thr = cpu_sample(w, x, args.cpu_rows)
         line["cpu_baseline"] = {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
                                 "sample": f"{args.cpu_rows} query rows x {w.H} heads x all {w.S} keys of "
@@ -581,6 +630,25 @@ def run_reference(args, rank, world):
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_only(args):
+    """One measurement alone, for profiling (the capture's kernel is the only heavy one)."""
+    w, n, P = workload_args(args)
+    if args.only == "step":
+        res, _ = measure(w, n, P, args.steps, args.warmup, False, step_only=True)
+        return {"only": "step", "workload": w.name, "n_chunks": n, "ms_per_step": res["total_ms"] / args.steps,
+                "per_kernel_ms": res["per_kernel_ms"], "chunks_per_cta": res["group"], "partials": res["parts"]}
+    if args.only == "merge_per_chunk":
+        res, _ = measure(w, n, P, args.steps, args.warmup, False, clocks=False)
+        return {"only": "merge_per_chunk", "workload": w.name, "n_chunks": n, "ms": res["merge_per_chunk_ms"]}
+    if args.only in ("cross", "cross_short"):
+        r = measure_cross(w, args.steps, args.warmup, Sq=None if args.only == "cross" else 100)
+        return dict(r, only=args.only)
+    if args.only == "backward":
+        bwd, fwd = measure_backward(w, inputs.make_inputs(w), args.steps, args.warmup)
+        return {"only": "backward", "backward": bwd, "attention_n1": fwd}
+    raise ValueError(args.only)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -591,6 +659,10 @@ def main():
     ap.add_argument("--chunks", type=int, default=0)
     ap.add_argument("--no-secondary", dest="secondary", action="store_false")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--step-only", action="store_true",
+                    help="time the step alone (no secondary rows, end-to-end loop or CPU baseline)")
+    ap.add_argument("--only", choices=["step", "merge_per_chunk", "cross", "cross_short", "backward"],
+                    help="run one measurement alone and print it (for profiling captures)")
     ap.add_argument("--cpu-rows", type=int, default=1536)
     ap.add_argument("--ref-rows", type=int, default=256)
     args = ap.parse_args()
@@ -608,7 +680,7 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         dist.init_process_group("nccl")
-    line = run_ours(args, rank, world, dist_on)
+    line = run_only(args) if args.only else run_ours(args, rank, world, dist_on)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist_on:

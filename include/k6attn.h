@@ -120,6 +120,8 @@ size_t k6attn_rope_tables_bytes(k6attn_t h);
  * (with_rope = 1) or without the rotated copies of q/k/joint_k:
  *   rotated copies  (B*Sq*H*d + B*Nv*H*d + B*Nj*H*d) * elem   if with_rope
  *   partial outputs n * B*Sq*H*d * 4 + n * B*H*Sq * 4          if n_chunks > 1
+ *   (room for one partial per chunk; with chunk groups only the first
+ *   n_chunks / k6attn_chunk_group(h, n_chunks) are written)
  * (each region rounded up to 256 bytes).  0 when neither applies. */
 size_t k6attn_workspace_bytes(k6attn_t h, int n_chunks, int with_rope);
 
@@ -176,8 +178,10 @@ k6attn_status k6attn_norm_rope_qk(k6attn_t h, const void *q, const void *k, cons
  *  n_chunks K/V chunks: chunk c covers keys [c*Sk/n, (c+1)*Sk/n) of
  *           concat(k, joint_k); Sk % n_chunks must be 0 ([CP] "Sequence
  *           Length Constraints").  n_chunks == 1 writes out/lse directly;
- *           n_chunks > 1 writes per-chunk fp32 partials [n][B][Sq][H][d] and
- *           [n][B][H][Sq] into the workspace and merges them (k6attn_lse_merge).
+ *           otherwise the chunks run in groups of k6attn_chunk_group(h,
+ *           n_chunks), each merged inside the kernel, and the n_chunks / group
+ *           fp32 partials (workspace) are merged by the k6attn_lse_merge
+ *           kernel (none when n_chunks / group == 1).
  *  out      [B][Sq][H][d], same element type as q.  Must not alias any input.
  *  lse      fp32 [B][H][Sq] (may be NULL: not written).
  *  workspace, workspace_bytes  caller-owned device scratch of at least
@@ -204,6 +208,77 @@ k6attn_status k6attn_forward(k6attn_t h, const void *q, const void *k, const voi
 k6attn_status k6attn_attention_chunks(k6attn_t h, const void *q, const void *k, const void *v, const void *joint_k,
                                       const void *joint_v, k6attn_dtype qk_dtype, int n_chunks, void *out, float *lse,
                                       void *stream);
+
+/*
+ * Chunk groups: the attention step over n_chunks K/V chunks in which each
+ * group of `group` consecutive chunks (group divides n_chunks) is merged
+ * inside the kernel, so that it leaves n_chunks / group partials instead of
+ * n_chunks ([CP] "Ring attention (current implementation)": the chunks'
+ * partials combine through their log-sum-exp, and that combine is
+ * associative).  Within a group the merge happens in tensor memory: the row
+ * maximum, row sum and unnormalised output of the chunks so far carry into the
+ * next chunk, whose tiles rescale them exactly as the tiles of one chunk do;
+ * the groups are then combined by k6attn_lse_merge / k6attn_lse_merge_heads.
+ *  group == 1 is k6attn_attention_chunks.  group > 1 needs a BF16 handle.
+ *  n_chunks / group == 1: out is [B][Sq][H][d] (handle type) and lse fp32
+ *           [B][H][Sq] (may be NULL) -- the attention of the whole sequence.
+ *  n_chunks / group > 1: out is fp32 [n_chunks/group][B][Sq][H][d], lse fp32
+ *           [n_chunks/group][B][H][Sq] (required); partial g covers chunks
+ *           [g*group, (g+1)*group).
+ * Other arguments as in k6attn_attention_chunks.
+ *
+ * k6attn_chunk_group: the group the library itself uses for n_chunks chunks of
+ * this handle's problem on the current device (k6attn_forward and
+ * k6attn_cross_forward use it): the largest divisor of n_chunks up to 4 that
+ * still leaves at least four waves of CTAs, 1 for F32 handles; 0 for a null
+ * handle or n_chunks < 1.
+ */
+int k6attn_chunk_group(k6attn_t h, int n_chunks);
+k6attn_status k6attn_attention_chunk_groups(k6attn_t h, const void *q, const void *k, const void *v,
+                                            const void *joint_k, const void *joint_v, k6attn_dtype qk_dtype,
+                                            int n_chunks, int group, void *out, float *lse, void *stream);
+
+/*
+ * The Ulysses prologue of one attention layer, one pass over HBM: rotary
+ * embeddings of q, k and joint_k (as k6attn_rope_qk) and the
+ * sequence->head relayout of q, k, joint_k, v and joint_v ([CP]
+ * "Self-Attention with Context Parallelism": rotary on the local tokens before
+ * attention; [USP] `_ft_c_input_all_to_all`; [CP] "Comparison with Other CP
+ * Strategies").  BF16 handles (d = 128); h describes the full problem
+ * (B, H heads).  P divides H; with Hl = H / P, for each tensor x of R rows
+ * per batch (R = Sq for q, Nv for k and v, Nj for joint_k and joint_v):
+ *   x_out[p][b][n][hh][e] = rot(x[b][n][p*Hl + hh][e])   (q, k, joint_k)
+ *   x_out[p][b][n][hh][e] =     x[b][n][p*Hl + hh][e]    (v, joint_v, bit copy)
+ * i.e. each output is [P][B][R][Hl][d]: the input of a handle with batch P*B
+ * and Hl heads.  For B == 1 this equals k6attn_rope_qk into copies followed by
+ * k6attn_seq2head_relayout of each tensor (bit for bit).
+ *  qk_out_dtype  BF16 or F16: the type of q_out, k_out, joint_k_out (v_out and
+ *           joint_v_out are bf16).  F16: a rotated value that is not finite in
+ *           fp16 sets K6ATTN_ERR_RANGE (at k6attn_sync).
+ *  joint_* may be NULL when Nj == 0.  Outputs must not overlap any input or
+ *  one another.
+ */
+k6attn_status k6attn_rope_split_heads(k6attn_t h, const void *q, const void *k, const void *v, const void *joint_k,
+                                      const void *joint_v, const void *rope_tables, int P, k6attn_dtype qk_out_dtype,
+                                      void *q_out, void *k_out, void *v_out, void *joint_k_out, void *joint_v_out,
+                                      void *stream);
+
+/*
+ * The Ulysses epilogue: the log-sum-exp merge of partials computed on the
+ * head-partitioned layout, written straight to the sequence layout ([CP]
+ * "Ring attention (current implementation)"; [USP]
+ * `_ft_c_output_all_to_all`).  h describes the full problem (B, H heads);
+ * P divides H and Hl = H / P.
+ *  part_o   fp32 [n_parts][P*B][Sq][Hl][d], part_lse fp32 [n_parts][P*B][Hl][Sq]:
+ *           partials of the handle with batch P*B and Hl heads (as written by
+ *           k6attn_attention_chunks or k6attn_attention_chunk_groups on
+ *           inputs from k6attn_rope_split_heads).
+ *  out      [B][Sq][H][d] in the handle's type, lse fp32 [B][H][Sq] (may be
+ *           NULL): head p*Hl + hh of batch b holds the merge of problem
+ *           p*B + b, head hh.  P == 1 is k6attn_lse_merge.
+ */
+k6attn_status k6attn_lse_merge_heads(k6attn_t h, const float *part_o, const float *part_lse, int n_parts, int P,
+                                     void *out, float *lse, void *stream);
 
 /*
  * Backward pass of the joint attention (the pages describe inference only;

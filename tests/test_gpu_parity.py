@@ -195,7 +195,9 @@ def test_split_calls_equal_forward():
 
 
 @pytest.mark.parametrize("dtype,n,B,S,H,d", [("bf16", 8, 1, 1000, 4, 128), ("f32", 4, 2, 130, 3, 64),
-                                             ("bf16", 16, 1, 257, 2, 128)])
+                                             ("bf16", 16, 1, 257, 2, 128), ("bf16", 1, 1, 77, 2, 128),
+                                             ("bf16", 2, 1, 1000, 4, 128), ("f32", 3, 2, 130, 3, 128),
+                                             ("bf16", 4, 2, 257, 2, 128), ("bf16", 40, 1, 33, 2, 128)])
 def test_lse_merge_matches_oracle(dtype, n, B, S, H, d):
     w = Workload("m", B, H, d, dtype, (1, 1, S), 0, (d, 0, 0), 0, 1.0, 1.0, (n,))
     h = K().Handle.for_workload(w)

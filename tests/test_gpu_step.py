@@ -3,9 +3,10 @@ sequence of C-ABI calls `bench.py` times) against the fp64 oracle.
 
 The step runs the Ulysses layout on one GPU ("Context Parallelism in vLLM
 Omni Neuron", "Comparison with Other CP Strategies"; xDiT PR #586, USP
-dispatch listing): rotary into fp16 copies on the sequence layout, the
-seq->head relayout, attention over the K/V chunks on the head-partitioned
-layout, the LSE merge and the head->seq relayout.  Each piece has its own
+dispatch listing): rotary into fp16 fused with the seq->head relayout,
+attention over the K/V chunks on the head-partitioned layout with each CTA's
+chunk group merged in the kernel, and the LSE merge of the group partials
+written back to the sequence layout.  Each piece has its own
 parity test; this one checks the chain the headline number is measured on, at
 the full workload sizes, on 1024 sampled query rows x all heads x all keys.
 """
@@ -44,7 +45,7 @@ def test_benchmarked_step_matches_oracle(name, n):
     rows = inputs.sample_rows(w.S, w.Nv, w.S // n, count=1024)
     idx = torch.from_numpy(rows).cuda()
     out = to_host(st.out.index_select(1, idx))
-    lse = st.lse_bhs().index_select(2, idx).cpu().numpy().astype(np.float64)
+    lse = st.lse.index_select(2, idx).cpu().numpy().astype(np.float64)
     del st
     torch.cuda.empty_cache()
     ref, ref_lse = oracle_sampled(w, x, rows)
@@ -58,7 +59,7 @@ def test_step_on_a_small_workload_matches_oracle():
     x = inputs.make_inputs(w)
     st = run_step(w, 2, 8, x)
     out = to_host(st.out)
-    lse = st.lse_bhs().cpu().numpy().astype(np.float64)
+    lse = st.lse.cpu().numpy().astype(np.float64)
     rows = np.arange(w.S)
     ref, ref_lse = oracle_sampled(w, x, rows)
     compare(out, ref, lse, ref_lse, "bf16")

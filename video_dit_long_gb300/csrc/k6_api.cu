@@ -77,11 +77,14 @@ static WsLayout ws_layout(const Geom &g, int n, bool rope) {
 
 // The attention kernels on rotated inputs: n_chunks == 1 writes out/lse,
 // n_chunks > 1 writes fp32 partials into out/lse (see k6attn_attention_chunks).
+// With group > 0 and merge, each CTA's `group` consecutive chunks leave one
+// partial (n_chunks / group partials; the output itself when that is 1).
 static k6attn_status run_attention(k6attn_handle *h, const Geom &g, const void *q, const void *k, const void *v,
                                    const void *jk, const void *jv, bool qk_f16, int n_chunks, void *out, float *lse,
-                                   cudaStream_t st, const float *row_bound = nullptr) {
+                                   cudaStream_t st, const float *row_bound = nullptr, int group = 0,
+                                   bool merge = false) {
     if (g.elem == 2) {
-        AttnTcOptions opt{h->wait_limit_ns, h->err, h->strict_order, qk_f16 ? 1 : 0, row_bound};
+        AttnTcOptions opt{h->wait_limit_ns, h->err, h->strict_order, qk_f16 ? 1 : 0, row_bound, group, merge ? 1 : 0};
         const char *why = nullptr;
         // a query range of one 128-row tile runs the single-tile kernel
         cudaError_t e = (g.Sq <= 128 ? launch_attn_tc_single : launch_attn_tc)(g, q, k, v, jk, jv, n_chunks, out, lse,
@@ -98,6 +101,28 @@ static k6attn_status run_attention(k6attn_handle *h, const Geom &g, const void *
                                       static_cast<const float *>(jv), n_chunks, static_cast<float *>(out), o_stride,
                                       lse, l_stride, st),
                       "fp32 attention launch");
+}
+
+// Chunks per CTA, and so partials per chunk count, for problem g: bf16 handles
+// merge each CTA's chunk group in the kernel; the fp32 kernel writes one
+// partial per chunk.
+static int group_for(const Geom &g, int n_chunks) { return g.elem == 2 ? chunk_group(g, n_chunks) : 1; }
+
+// Attention over n_chunks K/V chunks, then the log-sum-exp merge of what is
+// left: n_chunks / group partials (k6attn_forward, k6attn_cross_forward).
+// part_o / part_lse are workspace regions sized for n_chunks partials.
+static k6attn_status attention_and_merge(k6attn_handle *h, const Geom &g, const void *q, const void *k, const void *v,
+                                         const void *jk, const void *jv, bool qk_f16, int n_chunks, void *out,
+                                         float *lse, char *part_o, char *part_lse, cudaStream_t st, const char *fn) {
+    const int group = group_for(g, n_chunks);
+    const int parts = n_chunks / group;
+    if (parts == 1) return run_attention(h, g, q, k, v, jk, jv, qk_f16, n_chunks, out, lse, st, nullptr, group, true);
+    float *po = reinterpret_cast<float *>(part_o), *pl = reinterpret_cast<float *>(part_lse);
+    k6attn_status s = run_attention(h, g, q, k, v, jk, jv, qk_f16, n_chunks, po, pl, st, nullptr, group, true);
+    if (s != K6ATTN_OK) return s;
+    const cudaError_t e = launch_lse_merge(g, parts, po, pl, out, lse, st);
+    if (e != cudaSuccess) return set_error(K6ATTN_ERR_CUDA, "%s: merge launch: %s", fn, cudaGetErrorString(e));
+    return K6ATTN_OK;
 }
 
 // Checks shared by the two attention entry points.
@@ -426,12 +451,8 @@ k6attn_status k6attn_forward(k6attn_t h, const void *q, const void *k, const voi
         qa = qr, ka = kr, jka = jkr;
     }
     const bool qk_f16 = rope && g.dtype == K6ATTN_BF16;
-    if (n_chunks == 1) return run_attention(h, g, qa, ka, v, jka, joint_v, qk_f16, 1, out, lse, st);
-    float *part_o = reinterpret_cast<float *>(ws + L.part_o);
-    float *part_lse = reinterpret_cast<float *>(ws + L.part_lse);
-    s = run_attention(h, g, qa, ka, v, jka, joint_v, qk_f16, n_chunks, part_o, part_lse, st);
-    if (s != K6ATTN_OK) return s;
-    return cuda_check(launch_lse_merge(g, n_chunks, part_o, part_lse, out, lse, st), "forward: merge launch");
+    return attention_and_merge(h, g, qa, ka, v, jka, joint_v, qk_f16, n_chunks, out, lse, ws + L.part_o,
+                               ws + L.part_lse, st, "forward");
 }
 
 k6attn_status k6attn_attention_chunks(k6attn_t h, const void *q, const void *k, const void *v, const void *joint_k,
@@ -455,6 +476,106 @@ k6attn_status k6attn_attention_chunks(k6attn_t h, const void *q, const void *k, 
     if (s != K6ATTN_OK) return s;
     return run_attention(h, g, q, k, v, joint_k, joint_v, qk_dtype == K6ATTN_F16, n_chunks, out, lse,
                          static_cast<cudaStream_t>(stream));
+}
+
+int k6attn_chunk_group(k6attn_t h, int n_chunks) {
+    if (!h || n_chunks < 1) return 0;
+    return group_for(h->g, n_chunks);
+}
+
+k6attn_status k6attn_attention_chunk_groups(k6attn_t h, const void *q, const void *k, const void *v,
+                                            const void *joint_k, const void *joint_v, k6attn_dtype qk_dtype,
+                                            int n_chunks, int group, void *out, float *lse, void *stream) {
+    g_msg[0] = 0;
+    {
+        k6attn_status hs = check_handle("attention_chunk_groups", h);
+        if (hs != K6ATTN_OK) return hs;
+    }
+    const Geom &g = h->g;
+    if (group < 1 || n_chunks < 1 || n_chunks % group)
+        return set_error(K6ATTN_ERR_INVALID_ARG, "attention_chunk_groups: group %d must divide n_chunks %d", group,
+                         n_chunks);
+    if (group > 1 && g.elem != 2)
+        return set_error(K6ATTN_ERR_UNSUPPORTED, "attention_chunk_groups: chunk groups need a bf16 handle");
+    const int parts = n_chunks / group;
+    if (parts > 1 && !lse)
+        return set_error(K6ATTN_ERR_INVALID_ARG, "attention_chunk_groups: partial lse is required when "
+                                                 "n_chunks / group > 1");
+    if (qk_dtype != g.dtype && !(g.dtype == K6ATTN_BF16 && qk_dtype == K6ATTN_F16))
+        return set_error(K6ATTN_ERR_INVALID_ARG, "attention_chunk_groups: q/k type %d not allowed for this handle",
+                         (int)qk_dtype);
+    const size_t ob = (size_t)parts * g.B * g.S * g.H * g.d * (parts > 1 ? 4 : g.elem);
+    const size_t lb = (size_t)parts * g.B * g.H * g.S * 4;
+    k6attn_status s = check_inputs("attention_chunk_groups", g, q, k, v, joint_k, joint_v, n_chunks, out, ob, lse, lb);
+    if (s != K6ATTN_OK) return s;
+    return run_attention(h, g, q, k, v, joint_k, joint_v, qk_dtype == K6ATTN_F16, n_chunks, out, lse,
+                         static_cast<cudaStream_t>(stream), nullptr, group, true);
+}
+
+k6attn_status k6attn_rope_split_heads(k6attn_t h, const void *q, const void *k, const void *v, const void *joint_k,
+                                      const void *joint_v, const void *rope_tables, int P, k6attn_dtype qk_out_dtype,
+                                      void *q_out, void *k_out, void *v_out, void *joint_k_out, void *joint_v_out,
+                                      void *stream) {
+    g_msg[0] = 0;
+    {
+        k6attn_status hs = check_handle("rope_split_heads", h);
+        if (hs != K6ATTN_OK) return hs;
+    }
+    const Geom &g = h->g;
+    if (g.dtype != K6ATTN_BF16)
+        return set_error(K6ATTN_ERR_UNSUPPORTED, "rope_split_heads: needs a bf16 handle (d = 128)");
+    if (qk_out_dtype != K6ATTN_BF16 && qk_out_dtype != K6ATTN_F16)
+        return set_error(K6ATTN_ERR_INVALID_ARG, "rope_split_heads: rotated q/k type must be BF16 or F16");
+    if (P < 1 || g.H % P)
+        return set_error(K6ATTN_ERR_INVALID_ARG, "rope_split_heads: %d heads are not divisible by %d", g.H, P);
+    if (!q || !k || !v || !q_out || !k_out || !v_out || (!rope_tables && h->table_bytes))
+        return set_error(K6ATTN_ERR_INVALID_ARG, "rope_split_heads: null tensor or table pointer");
+    if (g.Nj > 0 && (!joint_k || !joint_v || !joint_k_out || !joint_v_out))
+        return set_error(K6ATTN_ERR_INVALID_ARG, "rope_split_heads: %ld joint tokens but a joint pointer is null",
+                         g.Nj);
+    const void *src[5] = {q, k, joint_k, v, joint_v};
+    void *dst[5] = {q_out, k_out, joint_k_out, v_out, joint_v_out};
+    const size_t row = (size_t)g.H * g.d * 2;
+    const size_t nb[5] = {g.B * g.S * row, g.B * g.Nv * row, g.B * g.Nj * row, g.B * g.Nv * row, g.B * g.Nj * row};
+    for (int a = 0; a < 5; a++) {
+        if (!aligned16(src[a]) || !aligned16(dst[a]))
+            return set_error(K6ATTN_ERR_INVALID_ARG, "rope_split_heads: pointers must be 16-byte aligned");
+        for (int b = 0; b < 5; b++) {
+            if (overlap(dst[a], nb[a], src[b], nb[b]))
+                return set_error(K6ATTN_ERR_INVALID_ARG, "rope_split_heads: an output overlaps an input");
+            if (a != b && overlap(dst[a], nb[a], dst[b], nb[b]))
+                return set_error(K6ATTN_ERR_INVALID_ARG, "rope_split_heads: outputs overlap");
+        }
+    }
+    if (!aligned16(rope_tables))
+        return set_error(K6ATTN_ERR_INVALID_ARG, "rope_split_heads: rotary tables must be 16-byte aligned");
+    return cuda_check(launch_rope_split(g, static_cast<const float2 *>(rope_tables), src, dst, P, qk_out_dtype, h->err,
+                                        static_cast<cudaStream_t>(stream)),
+                      "rope_split_heads launch");
+}
+
+k6attn_status k6attn_lse_merge_heads(k6attn_t h, const float *part_o, const float *part_lse, int n_parts, int P,
+                                     void *out, float *lse, void *stream) {
+    g_msg[0] = 0;
+    {
+        k6attn_status hs = check_handle("lse_merge_heads", h);
+        if (hs != K6ATTN_OK) return hs;
+    }
+    const Geom &g = h->g;
+    if (!part_o || !part_lse || !out) return set_error(K6ATTN_ERR_INVALID_ARG, "lse_merge_heads: null pointer");
+    if (n_parts < 1) return set_error(K6ATTN_ERR_INVALID_ARG, "lse_merge_heads: n_parts must be >= 1");
+    if (P < 1 || g.H % P)
+        return set_error(K6ATTN_ERR_INVALID_ARG, "lse_merge_heads: %d heads are not divisible by %d", g.H, P);
+    if (!aligned16(part_o) || !aligned16(out) || (reinterpret_cast<uintptr_t>(part_lse) & 3) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3))
+        return set_error(K6ATTN_ERR_INVALID_ARG, "lse_merge_heads: partials/out must be 16-byte aligned, lse 4-byte");
+    const size_t po = (size_t)n_parts * g.B * g.S * g.H * g.d * 4, pl = (size_t)n_parts * g.B * g.H * g.S * 4;
+    const size_t ob = (size_t)g.B * g.S * g.H * g.d * g.elem, lb = (size_t)g.B * g.H * g.S * 4;
+    if (overlap(out, ob, part_o, po) || overlap(out, ob, part_lse, pl) || overlap(lse, lb, part_o, po) ||
+        overlap(lse, lb, part_lse, pl) || overlap(out, ob, lse, lb))
+        return set_error(K6ATTN_ERR_INVALID_ARG, "lse_merge_heads: outputs overlap the partials");
+    return cuda_check(launch_lse_merge(g, n_parts, part_o, part_lse, out, lse, static_cast<cudaStream_t>(stream), P),
+                      "lse_merge_heads launch");
 }
 
 size_t k6attn_backward_workspace_bytes(k6attn_t h) {
@@ -557,11 +678,8 @@ k6attn_status k6attn_cross_forward(k6attn_t h, const void *q, long Sq, const voi
         overlap(workspace, L.total, lse, lb))
         return set_error(K6ATTN_ERR_INVALID_ARG, "cross_forward: workspace overlaps a tensor");
     char *ws = static_cast<char *>(workspace);
-    float *part_o = reinterpret_cast<float *>(ws + L.part_o);
-    float *part_lse = reinterpret_cast<float *>(ws + L.part_lse);
-    s = run_attention(h, g, q, k, v, nullptr, nullptr, false, n_chunks, part_o, part_lse, st);
-    if (s != K6ATTN_OK) return s;
-    return cuda_check(launch_lse_merge(g, n_chunks, part_o, part_lse, out, lse, st), "cross_forward: merge launch");
+    return attention_and_merge(h, g, q, k, v, nullptr, nullptr, false, n_chunks, out, lse, ws + L.part_o,
+                               ws + L.part_lse, st, "cross_forward");
 }
 
 k6attn_status k6attn_seq2head_relayout(const void *src, void *dst, int B, long S, int H, int d, int elem_bytes,

@@ -36,6 +36,7 @@ struct TcParams {
     uint32_t idesc_qk;                        // instruction descriptor of Q.K^T (bf16 or fp16 operands)
     long units;                               // B * H * n_chunks * q_pairs work units
     int group;                                // chunks per CTA, sharing one load of Q (divides n_chunks)
+    int merge;                                // 1: a CTA's group of chunks leaves one partial (index c / group)
     const float *row_bound;                   // constant-max softmax: bound per query row [B][H][Sq], or null
 };
 

@@ -18,7 +18,10 @@
 //     the same TMEM lanes); the halves meet in shared memory behind a named
 //     barrier of those two warps (row max once per tile, row sum once per unit);
 //   - loads K/V in the order K_0 K_1 V_0 K_2 V_1 K_3 ..., so that the tiles of
-//     block j go into the ring slots that block j-2 frees.
+//     block j go into the ring slots that block j-2 frees;
+//   - with p.merge, merges a CTA's group of chunks into one partial in tensor
+//     memory, as the two-tile kernel does: (m, l, O) carry from one chunk into
+//     the next and only the group's last chunk runs the epilogue.
 // Measured on GB300 (100 audio queries over 51,840 keys, 24 heads, 8 chunks):
 // 0.154 ms against 0.198 ms for the two-tile kernel on the same input.
 // All mbarrier waits are bounded (globaltimer); a wait that runs out records
@@ -204,6 +207,8 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
             bool ok = true;
             for (long u = u0; u < u1 && ok; u++, uc++) {
                 const int T = chunk_tiles(p, decode_unit(p, u).c).T;
+                const bool carry = p.merge && uc > 0;      // O accumulates over the previous chunks
+                const bool last = !p.merge || u + 1 == u1;  // this chunk's O goes to the epilogue
                 ok = uc > 0 || mbar_wait(q_full, 0, w);
                 for (int t = 0; t < 2 && t < T && ok; t++) {
                     const uint32_t kidx = kv_idx + t;
@@ -226,7 +231,7 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
                         break;
                     tc_fence_after();
                     if (with_s && started && !(ok = strict_wait())) break;
-                    issue_block(with_s, (n + 2) % NSBUF, kidx % NSTAGE, n % NSBUF, vidx % NSTAGE, j > 0);
+                    issue_block(with_s, (n + 2) % NSBUF, kidx % NSTAGE, n % NSBUF, vidx % NSTAGE, carry || j > 0);
                     started = true;
                     tc_commit(&pv_done[n & 1]);
                     if (with_s) {
@@ -234,7 +239,7 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
                         tc_commit(&kv_empty[kidx % NSTAGE]);
                     }
                     tc_commit(&kv_empty[vidx % NSTAGE]);
-                    if (j + 1 == T) tc_commit(o_final);
+                    if (j + 1 == T && last) tc_commit(o_final);
                 }
                 kv_idx += 2 * T;
                 tile += T;
@@ -257,13 +262,16 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
         float *xsum = xmax + 2 * 2 * BM;                           // [unit parity][half][row]
         const uint32_t pair_bar = 1 + warp % 4;                    // warps w and w + 4
         const float sl2 = p.scale_log2;
-        uint32_t tile = 0, uc = 0;
+        uint32_t tile = 0, uc = 0, n_epi = 0;
         bool ok = true;
+        float m_run = -INFINITY, l_run = 0.f;
         for (long u = u0; u < u1; u++, uc++) {
             const Unit un = decode_unit(p, u);
             const TileRange tr = chunk_tiles(p, un.c);
             const int T = tr.T;
-            float m_run = -INFINITY, l_run = 0.f;
+            const bool carry = p.merge && uc > 0;      // (m, l, O) of the previous chunks carry over
+            const bool last = !p.merge || u + 1 == u1;
+            if (!carry) m_run = -INFINITY, l_run = 0.f;
             if constexpr (BOUNDED) {
                 const long grow = (long)un.q0 + r;
                 m_run = grow < p.Sq ? p.row_bound[((long)un.b * p.H + un.h) * p.Sq + grow] * 1.4426950408889634f
@@ -309,7 +317,7 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
                     named_barrier_sync(pair_bar, 64);
                     const float mt = fmaxf(mx, xm[(hf ^ 1) * BM + r]) * sl2;
                     bool need = false;
-                    if (j == 0) m_run = mt;
+                    if (j == 0 && !carry) m_run = mt;
                     else need = mt > m_run + tc::RESCALE_THRESHOLD;
                     if (__any_sync(0xffffffffu, need)) {
                         rescale = true;
@@ -339,10 +347,10 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
                         }
                     }
                     tmem_st_cols<KP / 2>(tS, pk);  // P over the first KP/2 columns of this half's S
-                    // Every P.V(n-1) is waited for exactly once, here (a unit's last in its
+                    // Every P.V(n-1) is waited for exactly once, here (a partial's last in its
                     // epilogue), which keeps pv_done[(n-1) % 2] within one phase of the wait:
                     // before P(n) is published when O is to be rescaled, else after.
-                    const bool wait_pv = j > 0;
+                    const bool wait_pv = j > 0 || carry;
                     if (wait_pv && rescale) {
                         ok = mbar_wait(&pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, w);
                         tc_fence_after();
@@ -368,12 +376,18 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
                     l_run += (a0 + a1) + (b0 + b1);
                 }
             }
+            if (!last) {  // the group's partial is written after its last chunk
+                tile += T;
+                continue;
+            }
             // epilogue: this half's columns of O / l, with l summed over both halves
             if (ok) {
                 const uint32_t nl = tile + T - 1;
-                ok = mbar_wait(o_final, uc & 1, w) && mbar_wait(&pv_done[nl & 1], (nl >> 1) & 1, w);
+                ok = mbar_wait(o_final, n_epi & 1, w) && mbar_wait(&pv_done[nl & 1], (nl >> 1) & 1, w);
             }
-            float *xs = xsum + (uc & 1) * (2 * BM);
+            float *xs = xsum + (n_epi & 1) * (2 * BM);
+            n_epi++;
+            const long pc = p.merge ? un.c / p.group : un.c;  // index of the partial written
             xs[hf * BM + r] = l_run;
             named_barrier_sync(pair_bar, 64);
             const float l_tot = l_run + xs[(hf ^ 1) * BM + r];
@@ -394,7 +408,7 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
                     if (live) {
                         if (p.out_f32) {
                             // streaming stores: the partials are read once, by the merge
-                            float *dst = static_cast<float *>(p.out) + (long long)un.c * p.o_stride + obase + cc * 32;
+                            float *dst = static_cast<float *>(p.out) + (long long)pc * p.o_stride + obase + cc * 32;
 #pragma unroll
                             for (int k = 0; k < 32; k += 4)
                                 __stcs(reinterpret_cast<float4 *>(dst + k),
@@ -415,7 +429,7 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
                     }
                 }
                 if (live && p.lse && hf == 0)
-                    p.lse[(long long)un.c * p.l_stride + ((long)un.b * p.H + un.h) * p.Sq + grow] =
+                    p.lse[(long long)pc * p.l_stride + ((long)un.b * p.H + un.h) * p.Sq + grow] =
                         (m_run + log2f(l_tot)) * 0.69314718055994531f;
             }
             tile += T;
@@ -465,7 +479,6 @@ cudaError_t launch_attn_tc_single(const Geom &g, const void *q, const void *k, c
     p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)g.d));
     p.out = out;
     p.lse = lse;
-    p.out_f32 = n_chunks > 1;
     p.o_stride = (long long)g.B * g.Sq * g.H * g.d;
     p.l_stride = (long long)g.B * g.H * g.Sq;
     p.wait_limit_ns = opt.wait_limit_ns;
@@ -479,16 +492,14 @@ cudaError_t launch_attn_tc_single(const Geom &g, const void *q, const void *k, c
         if (why) *why = "too many work units (batch x heads x chunks must stay below 2^31)";
         return cudaErrorInvalidValue;
     }
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     // chunks per CTA (sharing one load of Q): as in the two-tile kernel
-    p.group = 1;
-    for (int gsz = 4; gsz > 1; gsz--)
-        if (n_chunks % gsz == 0 && p.units / gsz >= 4L * sms) {
-            p.group = gsz;
-            break;
-        }
+    p.group = opt.group > 0 ? opt.group : chunk_group(g, n_chunks);
+    if (n_chunks % p.group) {
+        if (why) *why = "the chunk group must divide the chunk count";
+        return cudaErrorInvalidValue;
+    }
+    p.merge = opt.merge && p.group > 1;
+    p.out_f32 = (p.merge ? n_chunks / p.group : n_chunks) > 1;
     p.row_bound = opt.row_bound;
     const long grid = p.units / p.group;
     if (opt.row_bound)

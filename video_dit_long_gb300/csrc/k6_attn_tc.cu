@@ -68,6 +68,13 @@ constexpr int TMEM_COLS = 512;
 // the K/V ring, the barrier phases and tensor memory carry over from one chunk
 // to the next, so the next chunk's first Q.K^T overlaps the previous chunk's
 // last P.V and epilogue.
+// MERGE (p.merge): the CTA's consecutive chunks leave one partial instead of
+// one each.  Their log-sum-exp merge is done in tensor memory as it goes: the
+// row max, row sum and unnormalised O of the chunks so far carry into the next
+// chunk, whose tiles rescale them exactly as later tiles of one chunk do
+// (combining (m_a, l_a, O_a) with (m_b, l_b, O_b) under m = max(m_a, m_b) is
+// the merge out = sum_c exp(LSE_c - LSE) O_c with LSE = m + ln l).  Only the
+// group's last chunk runs the epilogue.
 // BOUNDED: constant-max softmax.  Each row's running max is replaced by the
 // precomputed bound p.row_bound (>= every logit of the row), so the softmax
 // takes no row maximum and never rescales O; a row whose every term
@@ -208,6 +215,8 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
             for (long u = u0; u < u1 && ok; u++, uc++) {
                 const Unit un = decode_unit(p, u);
                 const int T = chunk_tiles(p, un.c).T;
+                const bool carry = p.merge && uc > 0;      // O accumulates over the previous chunks
+                const bool last = !p.merge || u + 1 == u1;  // this chunk's O goes to the epilogue
                 ok = (uc > 0 || mbar_wait(q_full, 0, w)) &&
                      mbar_wait(&kv_full[kv_idx % NSTAGE], (kv_idx / NSTAGE) & 1, w);
                 if (!ok) break;
@@ -232,17 +241,17 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                         for (int q = 0; q < P_PARTS; q++) {
                             if (!mbar_wait(&p_part[i * P_PARTS + q], ph, w)) return false;
                             tc_fence_after();
-                            issue_pv(i, vs, j > 0 || q > 0, q * MMA_PER_PART, (q + 1) * MMA_PER_PART);
+                            issue_pv(i, vs, carry || j > 0 || q > 0, q * MMA_PER_PART, (q + 1) * MMA_PER_PART);
                         }
                         return true;
                     };
                     if (!(ok = mbar_wait(&kv_full[vs], (vidx / NSTAGE) & 1, w) && pv_parts(0))) break;
                     started = true;
                     if (!more) {
-                        tc_commit(&o_final[0]);
+                        if (last) tc_commit(&o_final[0]);
                         if (!(ok = pv_parts(1))) break;
                         tc_commit(&kv_empty[vs]);
-                        tc_commit(&o_final[1]);
+                        if (last) tc_commit(&o_final[1]);
                         continue;
                     }
                     if (!(ok = strict_wait(0))) break;
@@ -260,7 +269,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                                 tc_fence_after();
                             }
                             mma_ts(tmem + 2 * BN + D, tmem + BN + kk * 8, vb + ((uint64_t)(kk * 16 * 128) >> 4),
-                                   idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);  // P1.V(j)
+                                   idesc_pv, (carry || j > 0 || kk > 0) ? 1u : 0u);  // P1.V(j)
                         }
                     }
                     if (!ok) break;
@@ -288,14 +297,17 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
         const uint32_t tS = lane_base + i * BN;
         const uint32_t tO = lane_base + 2 * BN + i * D;
         const float sl2 = p.scale_log2;
-        uint32_t tile = 0, uc = 0;
+        uint32_t tile = 0, uc = 0, n_epi = 0;
         bool ok = true;
+        float m_run = -INFINITY, l_run = 0.f;
         const long u0 = (long)blockIdx.x * p.group, u1 = u0 + p.group;
         for (long u = u0; u < u1 && ok; u++, uc++) {
             const Unit un = decode_unit(p, u);
             const TileRange tr = chunk_tiles(p, un.c);
             const int T = tr.T;
-            float m_run = -INFINITY, l_run = 0.f;
+            const bool carry = p.merge && uc > 0;      // (m, l, O) of the previous chunks carry over
+            const bool last = !p.merge || u + 1 == u1;
+            if (!carry) m_run = -INFINITY, l_run = 0.f;
             const long grow_u = (long)un.q0 + i * BM + r;
             if constexpr (BOUNDED)
                 m_run = grow_u < p.Sq ? p.row_bound[((long)un.b * p.H + un.h) * p.Sq + grow_u] * 1.4426950408889634f
@@ -334,7 +346,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                 const float mx = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]));
                 const float mt = mx * sl2;
                 bool need = false;
-                if (j == 0) m_run = mt;
+                if (j == 0 && !carry) m_run = mt;
                 else need = mt > m_run + RESCALE_THRESHOLD;
                 if (__any_sync(0xffffffffu, need)) {
                     // O_i holds P.V of tiles < j (S_i(j) was committed after it); it is
@@ -390,10 +402,16 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                 }
                 l_run += sum;
             }
-            if (!ok || !mbar_wait(&o_final[i], uc & 1, w)) {
+            if (!last) {  // the group's partial is written after its last chunk
+                tile += T;
+                continue;
+            }
+            if (!ok || !mbar_wait(&o_final[i], n_epi & 1, w)) {
                 ok = false;
                 break;
             }
+            n_epi++;
+            const long pc = p.merge ? un.c / p.group : un.c;  // index of the partial written
             // epilogue: O_i / l to the output (or fp32 partial), LSE; the next
             // unit's first P.V into O_i waits for this warpgroup's next P
             tc_fence_after();
@@ -411,7 +429,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                 tmem_ld_wait();
                 if (live) {
                     if (p.out_f32) {
-                        float *dst = static_cast<float *>(p.out) + (long long)un.c * p.o_stride + obase + cc * 32;
+                        float *dst = static_cast<float *>(p.out) + (long long)pc * p.o_stride + obase + cc * 32;
 #pragma unroll
                         for (int k = 0; k < 32; k += 4)
                             // streaming stores: the partials are read once, by the merge, and should
@@ -434,7 +452,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                 }
             }
             if (live && p.lse)
-                p.lse[(long long)un.c * p.l_stride + ((long)un.b * p.H + un.h) * p.Sq + grow] =
+                p.lse[(long long)pc * p.l_stride + ((long)un.b * p.H + un.h) * p.Sq + grow] =
                     (m_run + log2f(l_run)) * 0.69314718055994531f;
             tile += T;
         }
@@ -479,7 +497,6 @@ cudaError_t launch_attn_tc(const Geom &g, const void *q, const void *k, const vo
     p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)g.d));
     p.out = out;
     p.lse = lse;
-    p.out_f32 = n_chunks > 1;
     p.o_stride = (long long)g.B * g.Sq * g.H * g.d;
     p.l_stride = (long long)g.B * g.H * g.Sq;
     p.wait_limit_ns = opt.wait_limit_ns;
@@ -494,18 +511,15 @@ cudaError_t launch_attn_tc(const Geom &g, const void *q, const void *k, const vo
         if (why) *why = "too many work units (batch x heads x chunks x query-tile pairs must stay below 2^31)";
         return cudaErrorInvalidValue;
     }
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    // chunks per CTA (sharing one load of Q): the largest divisor of n_chunks up
-    // to 4 that still leaves at least four waves of CTAs; short query ranges
-    // (cross-attention from a few hundred audio rows) keep one chunk per CTA
-    p.group = 1;
-    for (int gsz = 4; gsz > 1; gsz--)
-        if (n_chunks % gsz == 0 && p.units / gsz >= 4L * sms) {
-            p.group = gsz;
-            break;
-        }
+    // chunks per CTA (sharing one load of Q): the caller's group, else the
+    // library's choice (chunk_group); with merge the group leaves one partial
+    p.group = opt.group > 0 ? opt.group : chunk_group(g, n_chunks);
+    if (n_chunks % p.group) {
+        if (why) *why = "the chunk group must divide the chunk count";
+        return cudaErrorInvalidValue;
+    }
+    p.merge = opt.merge && p.group > 1;
+    p.out_f32 = (p.merge ? n_chunks / p.group : n_chunks) > 1;
     // One CTA per Q tile pair and chunk group: the block scheduler hands each
     // freed SM the next CTA, which keeps the CTAs in flight (and their K/V in
     // L2) in a tight window; measured faster than a static persistent

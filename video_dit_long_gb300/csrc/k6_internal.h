@@ -73,8 +73,16 @@ cudaError_t launch_rope_qk(const Geom &g, const float2 *tables, const void *src_
                            void *dst_k, const void *src_jk, void *dst_jk, k6attn_dtype out_dtype, int *err,
                            cudaStream_t st, const QkNorm *norm = nullptr);
 
+// Merge of n partials of problem g (P = 1), or of the P*B problems of g.H/P
+// heads of a P-way head split of g, written to g's sequence layout.
+// Rotary of q/k/joint_k (into qk_out: BF16 or F16) and the P-way
+// sequence->head split of q, k, joint_k, v, joint_v (index order) of a bf16
+// d = 128 problem g: dst[t] is [P][B][rows_t][H/P][128].
+cudaError_t launch_rope_split(const Geom &g, const float2 *tables, const void *const src[5], void *const dst[5],
+                              int P, k6attn_dtype qk_out, int *err, cudaStream_t st);
+
 cudaError_t launch_lse_merge(const Geom &g, int n, const float *part_o, const float *part_lse, void *out, float *lse,
-                             cudaStream_t st);
+                             cudaStream_t st, int P = 1);
 
 cudaError_t launch_relayout(const void *src, void *dst, int B, long S, int H, int d, int elem_bytes, int P,
                             int direction, cudaStream_t st);
@@ -94,7 +102,14 @@ struct AttnTcOptions {
     int strict_order;        // 1: wait for P.V to finish before reusing its TMEM
     int qk_f16;              // 1: q/k/joint_k are fp16 (Q.K^T in fp16), else bf16
     const float *row_bound = nullptr;  // constant-max softmax bounds [B][H][Sq] (natural-log units), or null
+    int group = 0;           // chunks per CTA (divides n_chunks); 0: the library's choice, chunk_group()
+    int merge = 0;           // 1: each CTA's group of chunks leaves one partial (n_chunks / group partials)
 };
+
+// Chunks per CTA the library picks for n_chunks K/V chunks of problem g on the
+// current device: the largest divisor of n_chunks up to 4 that still leaves at
+// least four waves of CTAs (short query ranges keep one chunk per CTA).
+int chunk_group(const Geom &g, int n_chunks);
 
 // Constant-max bounds: bound[(b*H + h)*Sq + s] = |q| * max|k| / sqrt(d);
 // bound must hold B*H*Sq + B*H floats (the tail is the key-norm maximum).

@@ -331,20 +331,105 @@ __global__ void __launch_bounds__(256) rope_short_kernel(RopeArgs a, const float
     if (bad) atomicCAS(a.err, DEV_OK, DEV_RANGE);
 }
 
-cudaError_t launch_rope_qk(const Geom &g, const float2 *tables, const void *src_q, void *dst_q, const void *src_k,
-                           void *dst_k, const void *src_jk, void *dst_jk, k6attn_dtype out_dtype, int *err,
-                           cudaStream_t st, const QkNorm *norm) {
+// ------------------------------------------------ rotary + head split, fused
+//
+// The Ulysses prologue of one attention layer in one pass: rotary embeddings of
+// q, k and joint_k and the sequence->head relayout of q, k, joint_k, v and
+// joint_v ("Context Parallelism in vLLM Omni Neuron", "Self-Attention with
+// Context Parallelism": rotary on the local tokens before attention; xDiT PR
+// #586, USP dispatch listing, `_ft_c_input_all_to_all`).  Source rows are
+// BSHD bf16 token rows of H*128 elements (H*16 16-byte vectors); vector v of
+// a row belongs to head v/16, i.e. to head group p = v/(16*Hl), and lands in
+//   dst[p][b][n][v - 16*Hl*p]   (16-byte vectors; layout [P][B][rows][Hl][128]).
+// One warp per row: every load of the row is issued before its first store
+// (the outputs never alias the inputs), 12 vectors per lane for H = 24.  The
+// lane's 16-byte vectors always hold the same 4 pairs of their heads (16
+// vectors per head divide 32), so their cos/sin are read once per row.
+struct SplitArgs {
+    RopeArgs r;              // rotary tables and positions (tensors 0..2 = q, k, joint_k)
+    const void *src[5];      // q, k, joint_k, v, joint_v
+    void *dst[5];
+    long count[5];           // rows per tensor: B*S, B*Nv, B*Nj, B*Nv, B*Nj
+    long seq[5];             // rows per batch of each tensor
+    int B, P, Hl;
+};
+
+template <typename TQK>
+__global__ void __launch_bounds__(256) rope_split_kernel(SplitArgs a, const float2 *__restrict__ tab) {
+    constexpr int kU = 12;                        // vectors per lane in flight
+    const int vpt = a.r.H * 16;                   // 16-byte vectors per row
+    const int vpp = a.Hl * 16;                    // vectors per head group
+    const long total = a.count[0] + a.count[1] + a.count[2] + a.count[3] + a.count[4];
+    const int lane = threadIdx.x & 31;
+    const long warp0 = (blockIdx.x * (long)blockDim.x + threadIdx.x) >> 5;
+    const long nwarps = ((long)gridDim.x * blockDim.x) >> 5;
+    const int pair0 = (lane & 15) * 4;
+    bool bad = false;
+    for (long row = warp0; row < total; row += nwarps) {
+        int which = 0;
+        long local = row;
+        while (which < 4 && local >= a.count[which]) {
+            local -= a.count[which];
+            which++;
+        }
+        const bool rot = which < 3;
+        float2 cs[4] = {make_float2(1.f, 0.f), make_float2(1.f, 0.f), make_float2(1.f, 0.f), make_float2(1.f, 0.f)};
+        if (rot) {
+            // the row's position: token_pos walks q, k, joint_k in that order
+            long tok = local;
+            for (int t = 0; t < which; t++) tok += a.r.tokens[t];
+            const TokenPos tp = token_pos(a.r, tok);
+#pragma unroll
+            for (int k = 0; k < 4; k++) cs[k] = rope_cs(a.r, tab, pair0 + k, tp.t, tp.h, tp.w, tp.j);
+        }
+        const long seq = a.seq[which];
+        const long b = local / seq, n = local - b * seq;
+        const uint4 *src = static_cast<const uint4 *>(a.src[which]) + local * vpt;
+        uint4 *dst = static_cast<uint4 *>(a.dst[which]);
+        for (int base = 0; base < vpt; base += 32 * kU) {
+            uint4 x[kU];
+#pragma unroll
+            for (int u = 0; u < kU; u++) {
+                const int v = base + 32 * u + lane;
+                if (v < vpt) x[u] = __ldcs(src + v);
+            }
+#pragma unroll
+            for (int u = 0; u < kU; u++) {
+                const int v = base + 32 * u + lane;
+                if (v >= vpt) continue;
+                const int p = v / vpp;
+                uint4 *to = dst + (((long)p * a.B + b) * seq + n) * vpp + (v - p * vpp);
+                if (!rot) {
+                    __stcs(to, x[u]);
+                    continue;
+                }
+                float f[8];
+                const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&x[u]);
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    const float2 e = __bfloat1622float2(h2[k]);
+                    f[2 * k] = e.x * cs[k].x - e.y * cs[k].y;
+                    f[2 * k + 1] = e.x * cs[k].y + e.y * cs[k].x;
+                }
+                if constexpr (std::is_same<TQK, __half>::value) {
+#pragma unroll
+                    for (int k = 0; k < 8; k++) bad |= !(fabsf(f[k]) < 65520.f);  // a finite half
+                }
+                uint4 y;
+                Vec<TQK>::store(&y, f);
+                __stcs(to, y);
+            }
+        }
+    }
+    if (bad) atomicCAS(a.r.err, DEV_OK, DEV_RANGE);
+}
+
+// Rotary arguments of problem g: tensors q [B][S], k [B][Nv], joint_k [B][Nj]
+// (rows of H*d), their destinations, tables and positions.
+static RopeArgs rope_args(const Geom &g, const void *src_q, void *dst_q, const void *src_k, void *dst_k,
+                          const void *src_jk, void *dst_jk, int *err) {
     RopeArgs a;
     a.err = err;
-    const bool use_norm = norm != nullptr;
-    a.eps = use_norm ? norm->eps : 0.f;
-    for (int t = 0; t < 3; t++) a.norm_w[t][0] = a.norm_w[t][1] = nullptr;
-    if (use_norm) {
-        a.norm_w[0][0] = norm->q_w;
-        a.norm_w[0][1] = norm->jq_w ? norm->jq_w : norm->q_w;
-        a.norm_w[1][0] = a.norm_w[1][1] = norm->k_w;
-        a.norm_w[2][0] = a.norm_w[2][1] = norm->jk_w ? norm->jk_w : norm->k_w;
-    }
     a.src[0] = src_q, a.dst[0] = dst_q;
     a.src[1] = src_k, a.dst[1] = dst_k;
     a.src[2] = src_jk, a.dst[2] = dst_jk;
@@ -361,6 +446,56 @@ cudaError_t launch_rope_qk(const Geom &g, const float2 *tables, const void *src_
     RopeLayout L = rope_layout(g);
     for (int t = 0; t < 4; t++) a.off[t] = L.off[t];
     for (int t = 0; t < 3; t++) a.half[t] = g.axis_dim[t] / 2;
+    for (int t = 0; t < 3; t++) a.norm_w[t][0] = a.norm_w[t][1] = nullptr;
+    a.eps = 0.f;
+    return a;
+}
+
+cudaError_t launch_rope_split(const Geom &g, const float2 *tables, const void *const src[5], void *const dst[5],
+                              int P, k6attn_dtype qk_out, int *err, cudaStream_t st) {
+    SplitArgs a;
+    a.r = rope_args(g, src[0], nullptr, src[1], nullptr, src[2], nullptr, err);
+    const long cnt[5] = {(long)g.B * g.S, (long)g.B * g.Nv, (long)g.B * g.Nj, (long)g.B * g.Nv, (long)g.B * g.Nj};
+    const long seq[5] = {g.S, g.Nv, g.Nj, g.Nv, g.Nj};
+    long total = 0;
+    for (int t = 0; t < 5; t++) {
+        a.src[t] = src[t];
+        a.dst[t] = dst[t];
+        a.count[t] = cnt[t];
+        a.seq[t] = seq[t] > 0 ? seq[t] : 1;
+        total += cnt[t];
+    }
+    a.B = g.B, a.P = P, a.Hl = g.H / P;
+    if (total == 0) return cudaSuccess;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    auto launch = [&](auto kernel) {
+        int per_sm = 1;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0);
+        long blocks = (total + 7) / 8;  // one row per warp
+        const long wave = (long)sms * (per_sm > 0 ? per_sm : 1);
+        if (blocks > wave) blocks = wave;
+        kernel<<<(unsigned)blocks, 256, 0, st>>>(a, tables);
+    };
+    if (qk_out == K6ATTN_F16) launch(rope_split_kernel<__half>);
+    else launch(rope_split_kernel<__nv_bfloat16>);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rope_qk(const Geom &g, const float2 *tables, const void *src_q, void *dst_q, const void *src_k,
+                           void *dst_k, const void *src_jk, void *dst_jk, k6attn_dtype out_dtype, int *err,
+                           cudaStream_t st, const QkNorm *norm) {
+    RopeArgs a = rope_args(g, src_q, dst_q, src_k, dst_k, src_jk, dst_jk, err);
+    const bool use_norm = norm != nullptr;
+    a.eps = use_norm ? norm->eps : 0.f;
+    for (int t = 0; t < 3; t++) a.norm_w[t][0] = a.norm_w[t][1] = nullptr;
+    if (use_norm) {
+        a.norm_w[0][0] = norm->q_w;
+        a.norm_w[0][1] = norm->jq_w ? norm->jq_w : norm->q_w;
+        a.norm_w[1][0] = a.norm_w[1][1] = norm->k_w;
+        a.norm_w[2][0] = a.norm_w[2][1] = norm->jk_w ? norm->jk_w : norm->k_w;
+    }
     long total = a.tokens[0] + a.tokens[1] + a.tokens[2];
     if (total == 0) return cudaSuccess;
     int dev = 0, sms = 148;

@@ -23,7 +23,9 @@ SYMBOLS = ["k6attn_create", "k6attn_destroy", "k6attn_rope_tables", "k6attn_rope
            "k6attn_seq2head_relayout", "k6attn_sync", "k6attn_set_option", "k6attn_status_string",
            "k6attn_last_error", "k6attn_forward_static_scratch", "k6attn_cross_workspace_bytes",
            "k6attn_cross_forward", "k6attn_norm_rope_qk", "k6attn_row_bounds_bytes", "k6attn_row_bounds",
-           "k6attn_attention_chunks_bounded", "k6attn_backward_workspace_bytes", "k6attn_backward"]
+           "k6attn_attention_chunks_bounded", "k6attn_backward_workspace_bytes", "k6attn_backward",
+           "k6attn_chunk_group", "k6attn_attention_chunk_groups", "k6attn_rope_split_heads",
+           "k6attn_lse_merge_heads"]
 
 
 class K6Error(RuntimeError):
@@ -83,6 +85,11 @@ def load(build_if_missing: bool = True):
     L.k6attn_backward_workspace_bytes.restype = Z
     L.k6attn_backward.argtypes = [P, P, P, P, P, P, I, P, P, P, P, P, P, P, P, P, Z, P]
     L.k6attn_lse_merge.argtypes = [P, P, P, I, P, P, P]
+    L.k6attn_chunk_group.argtypes = [P, I]
+    L.k6attn_chunk_group.restype = I
+    L.k6attn_attention_chunk_groups.argtypes = [P, P, P, P, P, P, I, I, I, P, P, P]
+    L.k6attn_rope_split_heads.argtypes = [P, P, P, P, P, P, P, I, I, P, P, P, P, P, P]
+    L.k6attn_lse_merge_heads.argtypes = [P, P, P, I, I, P, P, P]
     L.k6attn_seq2head_relayout.argtypes = [P, P, I, ctypes.c_long, I, I, I, I, I, P]
     L.k6attn_sync.argtypes = [P, P]
     L.k6attn_set_option.argtypes = [P, I, ctypes.c_longlong]
@@ -92,7 +99,8 @@ def load(build_if_missing: bool = True):
     L.k6attn_last_error.restype = ctypes.c_char_p
     for name in ("k6attn_create", "k6attn_rope_qk", "k6attn_forward", "k6attn_forward_static_scratch",
                  "k6attn_attention_chunks", "k6attn_lse_merge", "k6attn_cross_forward", "k6attn_norm_rope_qk",
-                 "k6attn_row_bounds", "k6attn_attention_chunks_bounded",
+                 "k6attn_row_bounds", "k6attn_attention_chunks_bounded", "k6attn_attention_chunk_groups",
+                 "k6attn_rope_split_heads", "k6attn_lse_merge_heads",
                  "k6attn_seq2head_relayout", "k6attn_sync", "k6attn_set_option"):
         getattr(L, name).restype = I
     _lib = L
@@ -204,6 +212,30 @@ class Handle:
         qd = self._desc.dtype if qk_dtype is None else qk_dtype
         _check(load().k6attn_attention_chunks(self.h, _ptr(q), _ptr(k), _ptr(v), _ptr(joint_k), _ptr(joint_v),
                                               int(qd), int(n_chunks), _ptr(out), _ptr(lse), _stream(stream)))
+
+    def chunk_group(self, n_chunks: int) -> int:
+        return load().k6attn_chunk_group(self.h, int(n_chunks))
+
+    def attention_chunk_groups(self, q, k, v, joint_k, joint_v, n_chunks, group, out, lse=None, qk_dtype=None,
+                               stream=None):
+        """Attention over n_chunks chunks, each group of `group` merged in the kernel (n_chunks/group partials)."""
+        qd = self._desc.dtype if qk_dtype is None else qk_dtype
+        _check(load().k6attn_attention_chunk_groups(self.h, _ptr(q), _ptr(k), _ptr(v), _ptr(joint_k), _ptr(joint_v),
+                                                    int(qd), int(n_chunks), int(group), _ptr(out), _ptr(lse),
+                                                    _stream(stream)))
+
+    def rope_split_heads(self, q, k, v, joint_k, joint_v, P, q_out, k_out, v_out, joint_k_out=None,
+                         joint_v_out=None, *, qk_out_dtype=F16, tables=None, stream=None):
+        """Rotary of q/k/joint_k and the P-way seq->head split of all five tensors, one launch."""
+        tab = ctypes.c_void_p(self.rope_tables() if tables is None else tables)
+        _check(load().k6attn_rope_split_heads(self.h, _ptr(q), _ptr(k), _ptr(v), _ptr(joint_k), _ptr(joint_v), tab,
+                                              int(P), int(qk_out_dtype), _ptr(q_out), _ptr(k_out), _ptr(v_out),
+                                              _ptr(joint_k_out), _ptr(joint_v_out), _stream(stream)))
+
+    def lse_merge_heads(self, part_o, part_lse, n_parts, P, out, lse=None, stream=None):
+        """Merge of head-partitioned partials, written to the sequence layout [B][S][H][d]."""
+        _check(load().k6attn_lse_merge_heads(self.h, _ptr(part_o), _ptr(part_lse), int(n_parts), int(P), _ptr(out),
+                                             _ptr(lse), _stream(stream)))
 
     def backward_workspace_bytes(self) -> int:
         return load().k6attn_backward_workspace_bytes(self.h)

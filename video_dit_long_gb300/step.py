@@ -5,15 +5,18 @@ pages give it ("Context Parallelism in vLLM Omni Neuron", "Self-Attention
 with Context Parallelism": rotary on the local tokens, then attention;
 "Comparison with Other CP Strategies" and xDiT PR #586, USP dispatch listing:
 an all-to-all from the sequence-partitioned to the head-partitioned layout
-before attention and back after it):
+before attention and back after it; "Ring attention (current
+implementation)": attention per K/V chunk, partials merged by their
+log-sum-exp):
 
-  1. rotary embeddings of q, k and joint_k on the sequence layout (full head
-     rows), into fp16 copies;
-  2. seq->head relayout (P-way) of the rotated q, k, joint_k and of v, joint_v;
-  3. attention over n K/V chunks on the head-partitioned layout (P*B
-     independent problems of H/P heads), fp32 partials and their LSE;
-  4. LSE merge of the partials (head layout);
-  5. head->seq relayout of the output.
+  1. k6attn_rope_split_heads: rotary embeddings of q, k, joint_k (into fp16)
+     and the P-way seq->head relayout of q, k, joint_k, v, joint_v, one pass;
+  2. k6attn_attention_chunk_groups: attention over the n K/V chunks on the
+     head-partitioned layout (P*B independent problems of H/P heads); each
+     CTA's group of consecutive chunks is merged in the kernel, leaving
+     n / group fp32 partials and their LSE;
+  3. k6attn_lse_merge_heads: the LSE merge of those partials, written straight
+     back to the sequence layout [B][S][H][d] (the head->seq relayout).
 
 This module only holds the buffers and sequences the calls (marshalling); all
 arithmetic runs in the library's kernels.  The benchmark times `step()`, and
@@ -29,74 +32,66 @@ from . import k6attn as K
 class UlyssesStep:
     """Device buffers and handles for one workload; `step()` runs the path once."""
 
+    # rows of the hot path as timed by step(ev): names of the intervals between its events
+    intervals = ("rope_split_heads", "attention_chunk_groups", "lse_merge_heads")
+
     def __init__(self, w, n_chunks: int, P: int, x: dict):
         import torch
         self.torch = torch
         self.w, self.n, self.P = w, n_chunks, P
-        B, S, H, d, Nj = w.B, w.S, w.H, w.d, w.Nj
-        if H % P or S % P or w.Nv % P or Nj % P:
-            raise ValueError(f"{P}-way relayout needs H, S, Nv and Nj divisible by {P}")
+        B, S, H, d, Nv, Nj = w.B, w.S, w.H, w.d, w.Nv, w.Nj
+        if H % P:
+            raise ValueError(f"{H} heads are not divisible by {P}")
+        if n_chunks < 2 or S % n_chunks:
+            raise ValueError(f"the step merges chunk partials: n_chunks must be >= 2 and divide {S}")
         self.Hl = H // P
-        bf, f16 = torch.bfloat16, torch.float16
+        bf, f16, f32 = torch.bfloat16, torch.float16, torch.float32
 
         def dev(a):
             return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(bf).cuda()
 
         self.seq = {k: dev(v) for k, v in x.items()}
-        self.rows = {"q": S, "k": w.Nv, "v": w.Nv, "jk": Nj, "jv": Nj}
-        # rotary on the sequence-partitioned tensors (full head rows), into fp16 copies
+        # the full problem (B, H heads): rotary tables, prologue and epilogue
         self.hs = K.Handle(B, H, d, "bf16", w.grid, Nj, w.axis_dim, w.theta, w.joint_rope)
-        self.rot = {k: torch.empty(self.seq[k].shape, dtype=f16, device="cuda") for k in ("q", "k", "jk")}
-        # head-partitioned copies: rotated q/k/joint_k (fp16), v/joint_v (bf16)
-        self.head = {k: torch.empty_like(self.rot[k]) for k in ("q", "k", "jk")}
-        self.head.update({k: torch.empty_like(self.seq[k]) for k in ("v", "jv")})
         # attention runs on the head-partitioned layout: P*B independent problems of H/P heads
         self.h = K.Handle(P * B, self.Hl, d, "bf16", w.grid, Nj, w.axis_dim, w.theta, w.joint_rope)
-        self.part_o = torch.empty((n_chunks, P * B, S, self.Hl, d), dtype=torch.float32, device="cuda")
-        self.part_lse = torch.empty((n_chunks, P * B, self.Hl, S), dtype=torch.float32, device="cuda")
-        self.out_h = torch.empty((P * B, S, self.Hl, d), dtype=bf, device="cuda")
-        self.lse = torch.empty((P * B, self.Hl, S), dtype=torch.float32, device="cuda")
+        rows = {"q": S, "k": Nv, "v": Nv, "jk": Nj, "jv": Nj}
+        self.head = {k: torch.empty((P * B, r, self.Hl, d), dtype=f16 if k in ("q", "k", "jk") else bf,
+                                    device="cuda") for k, r in rows.items()}
+        # chunks per CTA: the library's choice, kept below n so that the merge has partials to combine
+        g = self.h.chunk_group(n_chunks)
+        while n_chunks // g < 2:
+            g = max(c for c in range(1, g) if n_chunks % c == 0)
+        self.group, self.parts = g, n_chunks // g
+        self.part_o = torch.empty((self.parts, P * B, S, self.Hl, d), dtype=f32, device="cuda")
+        self.part_lse = torch.empty((self.parts, P * B, self.Hl, S), dtype=f32, device="cuda")
         self.out = torch.empty((B, S, H, d), dtype=bf, device="cuda")
-        self.launches_per_step = 1 + sum(1 for r in self.rows.values() if r) + 1 + 1 + 1
-        # rows of the hot path as timed by step(ev): names of the intervals between its events
-        self.intervals = ("rope_qk", "relayout_seq2head_qkv", "attention_chunks", "lse_merge",
-                          "relayout_head2seq_out")
+        self.lse = torch.empty((B, H, S), dtype=f32, device="cuda")
+        self.launches_per_step = 3
 
-    def relayout_in(self, src: dict, dst: dict):
-        w = self.w
-        for name in ("q", "k", "v", "jk", "jv"):
-            if self.rows[name]:
-                K.seq2head_relayout(src[name], dst[name], w.B, self.rows[name], w.H, w.d, self.P, 0)
+    def run(self, seq: dict, out, lse, ev=None):
+        """One pass of the path from the sequence-layout inputs `seq` into out [B][S][H][d]
+        and lse [B][H][S]; `ev` (4 CUDA events, or None in place of one) brackets its rows."""
+        w, hd = self.w, self.head
+        j = w.Nj > 0
+
+        def mark(i):
+            if ev and ev[i] is not None:
+                ev[i].record()
+
+        mark(0)
+        self.hs.rope_split_heads(seq["q"], seq["k"], seq["v"], seq["jk"] if j else None, seq["jv"] if j else None,
+                                 self.P, hd["q"], hd["k"], hd["v"], hd["jk"] if j else None,
+                                 hd["jv"] if j else None, qk_out_dtype=K.F16)
+        mark(1)
+        self.h.attention_chunk_groups(hd["q"], hd["k"], hd["v"], hd["jk"] if j else None, hd["jv"] if j else None,
+                                      self.n, self.group, self.part_o, self.part_lse, qk_dtype=K.F16)
+        mark(2)
+        self.hs.lse_merge_heads(self.part_o, self.part_lse, self.parts, self.P, out, lse)
+        mark(3)
 
     def step(self, ev=None):
-        """One pass of the path; `ev` (6 CUDA events) brackets its rows."""
-        w, hd, rt = self.w, self.head, self.rot
-        if ev:
-            ev[0].record()
-        self.hs.rope_qk(self.seq["q"], self.seq["k"], self.seq["jk"] if w.Nj else None, q_out=rt["q"],
-                        k_out=rt["k"], joint_k_out=rt["jk"] if w.Nj else None, out_dtype=K.F16)
-        if ev:
-            ev[1].record()
-        self.relayout_in({"q": rt["q"], "k": rt["k"], "jk": rt["jk"], "v": self.seq["v"], "jv": self.seq["jv"]},
-                         hd)
-        if ev:
-            ev[2].record()
-        jk, jv = (hd["jk"], hd["jv"]) if w.Nj else (None, None)
-        self.h.attention_chunks(hd["q"], hd["k"], hd["v"], jk, jv, self.n, self.part_o, self.part_lse,
-                                qk_dtype=K.F16)
-        if ev:
-            ev[3].record()
-        self.h.lse_merge(self.part_o, self.part_lse, self.n, self.out_h, self.lse)
-        if ev:
-            ev[4].record()
-        K.seq2head_relayout(self.out_h, self.out, w.B, w.S, w.H, w.d, self.P, 1)
-        if ev:
-            ev[5].record()
-
-    def lse_bhs(self):
-        """The step's LSE as [B][H][S] (the merge leaves it in the head layout [P][B][H/P][S])."""
-        w = self.w
-        return self.lse.view(self.P, w.B, self.Hl, w.S).permute(1, 0, 2, 3).reshape(w.B, w.H, w.S)
+        self.run(self.seq, self.out, self.lse, ev)
 
     def sync(self):
         self.hs.sync()
