@@ -90,7 +90,7 @@ def traffic_record(kernel: str, workload: str):
         for line in f:
             parts = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
             if (parts.get("kernel") == kernel and parts.get("workload") == workload
-                    and parts.get("source_sha256") == sha):
+                    and parts.get("source_sha256") == sha):  # workload = <name>_n<chunks>
                 return float(parts["dram_bytes_per_launch"])
     return None
 
@@ -538,7 +538,7 @@ def run_ours(args, rank, world, dist_on):
         "config": bench_config(w, n, P),
         "roofline": {"bound": "tensor", "achieved": round(attn_tflops, 2), "peak": peak_b, "unit": "TFLOP/s",
                      "frac": round(attn_tflops / peak_b, 4), "frac_sustained": round(attn_tflops / peak_s, 4),
-                     "traffic": traffic_record("attn_tc_kernel", w.name), "kernel": "attn_tc_kernel",
+                     "traffic": traffic_record("attn_tc_kernel", f"{w.name}_n{n}"), "kernel": "attn_tc_kernel",
                      "peak_kind": f"bf16 burst, {tag}; frac_sustained against {peak_s}",
                      "algorithmic_flops_per_launch": flops},
         "kernels": kernels,
@@ -566,7 +566,7 @@ def run_ours(args, rank, world, dist_on):
                               "roofline": {"bound": "tensor", "achieved": round(a2, 2), "peak": peak_b,
                                            "unit": "TFLOP/s", "frac": round(a2 / peak_b, 4),
                                            "frac_sustained": round(a2 / peak_s, 4),
-                                           "traffic": traffic_record("attn_tc_kernel", w2.name),
+                                           "traffic": traffic_record("attn_tc_kernel", f"{w2.name}_n{n2}"),
                                            "kernel": "attn_tc_kernel", "algorithmic_flops_per_launch": f2},
                               "kernels": {
                                   "rope_split_heads": hbm_rec(prologue_bytes(w2), k2["rope_split_heads"]),

@@ -91,3 +91,31 @@ def test_single_tile_strict_mma_order_gives_identical_bits(n):
     a = run_cross(1, 2, 128, "bf16", 77, 2048, n, std=2.0, raw=True)
     b = run_cross(1, 2, 128, "bf16", 77, 2048, n, std=2.0, raw=True, strict=True)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_short_queries_split_into_sub_chunks_match_oracle():
+    # 100 audio queries over the Pro visual sequence in 8 chunks: with the full
+    # workspace the call runs each chunk as sub-chunks (the HBM-bound single-tile
+    # CTAs fill the last wave); with room for 8 partials only, unsplit.  Both
+    # equal the oracle, and each other within the bf16 bounds.
+    from video_dit_long_gb300 import k6attn as K
+    B, H, d, Sq, Sk, n = 1, 24, 128, 100, 51840, 8
+    q = inputs.tensor(42, 30, (B, Sq, H, d), "bf16", 0.5)
+    k = inputs.tensor(42, 31, (B, Sk, H, d), "bf16", 0.5)
+    v = inputs.tensor(42, 32, (B, Sk, H, d), "bf16")
+    h = K.Handle(B, H, d, "bf16", (1, 1, 1), 0, (d, 0, 0))
+    tq, tk, tv = (to_dev(a, "bf16") for a in (q, k, v))
+    ref, ref_lse = O.cross_attention(q, k, v)
+    full = h.cross_workspace_bytes(Sq, n)
+    unsplit = (n * B * Sq * H * d * 4 + 255) // 256 * 256 + (n * B * H * Sq * 4 + 255) // 256 * 256
+    assert full > unsplit
+    got = []
+    for nb in (full, unsplit):
+        out = torch.empty_like(tq)
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device="cuda")
+        ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+        h.cross_forward(tq, tk, tv, out, lse, n_chunks=n, workspace=ws)
+        h.sync()
+        got.append((to_host(out), lse.cpu().numpy().astype(np.float64)))
+        compare(got[-1][0], ref, got[-1][1], ref_lse, "bf16")
+    assert np.abs(got[0][0] - got[1][0]).max() <= 2e-2 and np.abs(got[0][1] - got[1][1]).max() <= 1e-3

@@ -40,16 +40,18 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(int n, long rows, long S
     const long step = (long)gridDim.x * blockDim.x / TPR;
     const int H = Hl * P;
     for (; r < rows; r += step) {
-        // r enumerates (problem, s, hh) in partial order [P*B][Sq][Hl]
-        const int hh = (int)(r % Hl);
-        const long t = r / Hl;
-        const long s = t % Sq;
-        const long pb = t / Sq;
-        const long li = (pb * Hl + hh) * Sq + s;            // partial LSE index
-        const long b = pb % B;
-        const int h = (int)(pb / B) * Hl + hh;               // head in the full layout
-        const long orow = (b * Sq + s) * H + h;              // output row [B][Sq][H]
-        const long lo = (b * H + h) * Sq + s;                // output LSE index [B][H][Sq]
+        // r enumerates (problem, s, hh) in partial order [P*B][Sq][Hl]; 32-bit
+        // index arithmetic (the host keeps B*Sq*H below 2^31)
+        const unsigned ru = (unsigned)r;
+        const unsigned hh = ru % (unsigned)Hl;
+        const unsigned t = ru / (unsigned)Hl;
+        const unsigned s = t % (unsigned)Sq;
+        const unsigned pb = t / (unsigned)Sq;
+        const long li = ((long)pb * Hl + hh) * Sq + s;      // partial LSE index
+        const unsigned b = pb % (unsigned)B;
+        const unsigned h = (pb / (unsigned)B) * Hl + hh;     // head in the full layout
+        const long orow = ((long)b * Sq + s) * H + h;        // output row [B][Sq][H]
+        const long lo = ((long)b * H + h) * Sq + s;          // output LSE index [B][H][Sq]
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         const float *po = part_o + r * D + sub * 4;
         float L;
@@ -126,13 +128,16 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(int n, long rows, long S
 
 // Few partials (N <= 4, d = 128): with one warp per row a lane would have only
 // N 16-byte loads in flight, too few to cover HBM latency.  Here a warp takes R
-// consecutive rows at a time (N * R = 8 loads of 16 bytes per lane, all issued
-// before any arithmetic), in partial order [P*B][Sq][Hl], so the partial
+// consecutive rows at a time (N * R = 8 loads of 16 bytes per lane for N >= 2,
+// 4 for N = 1, all issued before any arithmetic), in partial order
+// [P*B][Sq][Hl], so the partial
 // outputs stream through HBM in address order; the partial LSEs ([P*B][Hl][Sq],
 // a few MB) are read with a stride and served mostly from L2.  Each lane forms
 // the row's LSE from the N partial LSEs itself (warp-wide broadcast reads).
+// Index arithmetic is 32-bit: 64-bit divisions per row made the kernel
+// instruction-bound (measured: 60 % SM throughput at 52 % of DRAM bandwidth).
 template <typename OutT, int N, int R>
-__global__ void __launch_bounds__(256) lse_merge_few_kernel(long rows, long Sq, int Hl, int B, int P,
+__global__ void __launch_bounds__(256, 3) lse_merge_few_kernel(long rows, long Sq, int Hl, int B, int P,
                                                             const float *__restrict__ part_o,
                                                             const float *__restrict__ part_lse,
                                                             OutT *__restrict__ out, float *__restrict__ lse) {
@@ -148,19 +153,20 @@ __global__ void __launch_bounds__(256) lse_merge_few_kernel(long rows, long Sq, 
         long orow[R], lo[R];
 #pragma unroll
         for (int rr = 0; rr < R; rr++) {
-            const long r = r0 + rr < rows ? r0 + rr : rows - 1;  // a clamped row is computed, not stored
-            const int hh = (int)(r % Hl);
-            const long t = r / Hl;
-            const long s = t % Sq;
-            const long pb = t / Sq;
-            const long li = (pb * Hl + hh) * Sq + s;             // partial LSE [P*B][Hl][Sq]
-            const long b = pb % B;
-            const int h = (int)(pb / B) * Hl + hh;
-            orow[rr] = (b * Sq + s) * H + h;                     // output row [B][Sq][H]
-            lo[rr] = (b * H + h) * Sq + s;                       // output LSE [B][H][Sq]
+            // a clamped row is computed, not stored; 32-bit index arithmetic (B*Sq*H < 2^31)
+            const unsigned r = (unsigned)(r0 + rr < rows ? r0 + rr : rows - 1);
+            const unsigned hh = r % (unsigned)Hl;
+            const unsigned t = r / (unsigned)Hl;
+            const unsigned s = t % (unsigned)Sq;
+            const unsigned pb = t / (unsigned)Sq;
+            const long li = ((long)pb * Hl + hh) * Sq + s;       // partial LSE [P*B][Hl][Sq]
+            const unsigned b = pb % (unsigned)B;
+            const unsigned h = (pb / (unsigned)B) * Hl + hh;
+            orow[rr] = ((long)b * Sq + s) * H + h;               // output row [B][Sq][H]
+            lo[rr] = ((long)b * H + h) * Sq + s;                 // output LSE [B][H][Sq]
 #pragma unroll
             for (int c = 0; c < N; c++)
-                x[rr][c] = __ldcs(reinterpret_cast<const float4 *>(part_o + c * o_stride + r * D) + sub);
+                x[rr][c] = __ldcs(reinterpret_cast<const float4 *>(part_o + c * o_stride + (long)r * D) + sub);
 #pragma unroll
             for (int c = 0; c < N; c++) lc[rr][c] = __ldg(part_lse + c * l_stride + li);
         }
@@ -225,12 +231,12 @@ cudaError_t launch_lse_merge(const Geom &g, int n, const float *part_o, const fl
             kernel<<<nb, threads, 0, st>>>(rows, g.Sq, Hl, g.B, P, part_o, part_lse, o, lse);
         };
         if (g.elem == 2) {
-            if (n == 1) few(lse_merge_few_kernel<__nv_bfloat16, 1, 8>, ob, 8);
+            if (n == 1) few(lse_merge_few_kernel<__nv_bfloat16, 1, 4>, ob, 4);
             else if (n == 2) few(lse_merge_few_kernel<__nv_bfloat16, 2, 4>, ob, 4);
             else if (n == 3) few(lse_merge_few_kernel<__nv_bfloat16, 3, 2>, ob, 2);
             else few(lse_merge_few_kernel<__nv_bfloat16, 4, 2>, ob, 2);
         } else {
-            if (n == 1) few(lse_merge_few_kernel<float, 1, 8>, of, 8);
+            if (n == 1) few(lse_merge_few_kernel<float, 1, 4>, of, 4);
             else if (n == 2) few(lse_merge_few_kernel<float, 2, 4>, of, 4);
             else if (n == 3) few(lse_merge_few_kernel<float, 3, 2>, of, 2);
             else few(lse_merge_few_kernel<float, 4, 2>, of, 2);

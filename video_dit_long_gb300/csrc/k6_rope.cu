@@ -382,8 +382,8 @@ __global__ void __launch_bounds__(256) rope_split_kernel(SplitArgs a, const floa
 #pragma unroll
             for (int k = 0; k < 4; k++) cs[k] = rope_cs(a.r, tab, pair0 + k, tp.t, tp.h, tp.w, tp.j);
         }
-        const long seq = a.seq[which];
-        const long b = local / seq, n = local - b * seq;
+        const unsigned seq = (unsigned)a.seq[which];  // 32-bit: the host keeps B*S*H below 2^31
+        const unsigned b = (unsigned)local / seq, n = (unsigned)local - b * seq;
         const uint4 *src = static_cast<const uint4 *>(a.src[which]) + local * vpt;
         uint4 *dst = static_cast<uint4 *>(a.dst[which]);
         for (int base = 0; base < vpt; base += 32 * kU) {
@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(256) rope_split_kernel(SplitArgs a, const floa
                 const int v = base + 32 * u + lane;
                 if (v >= vpt) continue;
                 const int p = v / vpp;
-                uint4 *to = dst + (((long)p * a.B + b) * seq + n) * vpp + (v - p * vpp);
+                uint4 *to = dst + ((long)((unsigned)p * a.B + b) * seq + n) * vpp + (v - p * vpp);
                 if (!rot) {
                     __stcs(to, x[u]);
                     continue;
