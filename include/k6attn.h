@@ -367,11 +367,6 @@ k6attn_status k6attn_lse_merge(k6attn_t h, const float *part_o, const float *par
  * split into up to 4 sub-chunks, so that the few, HBM-bound CTAs fill the
  * GPU's last wave.  k6attn_cross_workspace_bytes allows for that; with a
  * smaller workspace (or none, for one chunk) the chunks run unsplit.
- * A query range whose last 256-row tile pair holds at most 128 rows (e.g.
- * 520 = 2 x 256 + 8) runs that last tile on a second stream owned by the
- * handle, forked from and joined back to `stream` with events: the call stays
- * ordered on `stream` as usual, but one handle's cross_forward calls must not
- * be issued from several host threads at once.
  */
 size_t k6attn_cross_workspace_bytes(k6attn_t h, long Sq, int n_chunks);
 k6attn_status k6attn_cross_forward(k6attn_t h, const void *q, long Sq, const void *k, const void *v, long Sk,

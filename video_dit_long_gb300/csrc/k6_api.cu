@@ -20,10 +20,6 @@ struct k6attn_handle {
     unsigned long long wait_limit_ns = 2000000000ull;
     int strict_order = 0;
     int device = 0;
-    // a second stream of the handle's device and the events that fork to it and
-    // join back: a mixed grid runs its single-tile CTAs there (see run_attention)
-    cudaStream_t side = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
 };
 
 namespace k6 {
@@ -81,44 +77,18 @@ static WsLayout ws_layout(const Geom &g, int n, bool rope) {
 
 // The attention kernels on rotated inputs: n_chunks == 1 writes out/lse,
 // n_chunks > 1 writes fp32 partials into out/lse (see k6attn_attention_chunks).
-// Mixed grids: a query range whose last 256-row tile pair holds at most 128
-// real rows (520 audio queries = two full pairs and 8 rows) would spend that
-// pair's second tile, and most of its first, on padding.  With tail_split the
-// full pairs run on the two-tile kernel and the last tile on the single-tile
-// kernel, on the handle's side stream so that both grids share the GPU; the
-// two kernels' code is unchanged, so grids without such a tail pay nothing.
-// Only for short ranges (at most TAIL_SPLIT_MAX_PAIRS pairs): beyond that the
-// padding is a negligible share.
-constexpr long TAIL_SPLIT_MAX_PAIRS = 16;
-
 // With group > 0 and merge, each CTA's `group` consecutive chunks leave one
 // partial (n_chunks / group partials; the output itself when that is 1).
 static k6attn_status run_attention(k6attn_handle *h, const Geom &g, const void *q, const void *k, const void *v,
                                    const void *jk, const void *jv, bool qk_f16, int n_chunks, void *out, float *lse,
                                    cudaStream_t st, const float *row_bound = nullptr, int group = 0,
-                                   bool merge = false, bool tail_split = false) {
+                                   bool merge = false) {
     if (g.elem == 2) {
         AttnTcOptions opt{h->wait_limit_ns, h->err, h->strict_order, qk_f16 ? 1 : 0, row_bound, group, merge ? 1 : 0};
         const char *why = nullptr;
-        const long pairs = (g.Sq + 255) / 256, tail = g.Sq - 256 * (pairs - 1);
-        cudaError_t e;
-        if (g.Sq <= 128) {  // a query range of one 128-row tile runs the single-tile kernel
-            e = launch_attn_tc_single(g, q, k, v, jk, jv, n_chunks, out, lse, opt, st, &why);
-        } else if (tail_split && tail <= 128 && pairs <= TAIL_SPLIT_MAX_PAIRS) {
-            if (opt.group <= 0) opt.group = chunk_group(g, n_chunks);  // both kernels number partials alike
-            AttnTcOptions full = opt, last = opt;
-            full.q_rows = 256 * (pairs - 1);
-            last.q_base = 256 * (pairs - 1);
-            last.q_rows = tail;
-            e = launch_attn_tc(g, q, k, v, jk, jv, n_chunks, out, lse, full, st, &why);
-            if (e == cudaSuccess) e = cudaEventRecord(h->fork, st);
-            if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side, h->fork, 0);
-            if (e == cudaSuccess) e = launch_attn_tc_single(g, q, k, v, jk, jv, n_chunks, out, lse, last, h->side, &why);
-            if (e == cudaSuccess) e = cudaEventRecord(h->join, h->side);
-            if (e == cudaSuccess) e = cudaStreamWaitEvent(st, h->join, 0);
-        } else {
-            e = launch_attn_tc(g, q, k, v, jk, jv, n_chunks, out, lse, opt, st, &why);
-        }
+        // a query range of one 128-row tile runs the single-tile kernel
+        cudaError_t e = (g.Sq <= 128 ? launch_attn_tc_single : launch_attn_tc)(g, q, k, v, jk, jv, n_chunks, out, lse,
+                                                                           opt, st, &why);
         if (e != cudaSuccess) {
             if (why) return set_error(K6ATTN_ERR_CUDA, "attention: %s", why);
             return cuda_check(e, "attention launch");
@@ -143,15 +113,12 @@ static int group_for(const Geom &g, int n_chunks) { return g.elem == 2 ? chunk_g
 // part_o / part_lse are workspace regions sized for n_chunks partials.
 static k6attn_status attention_and_merge(k6attn_handle *h, const Geom &g, const void *q, const void *k, const void *v,
                                          const void *jk, const void *jv, bool qk_f16, int n_chunks, void *out,
-                                         float *lse, char *part_o, char *part_lse, cudaStream_t st, const char *fn,
-                                         bool tail_split = false) {
+                                         float *lse, char *part_o, char *part_lse, cudaStream_t st, const char *fn) {
     const int group = group_for(g, n_chunks);
     const int parts = n_chunks / group;
-    if (parts == 1)
-        return run_attention(h, g, q, k, v, jk, jv, qk_f16, n_chunks, out, lse, st, nullptr, group, true, tail_split);
+    if (parts == 1) return run_attention(h, g, q, k, v, jk, jv, qk_f16, n_chunks, out, lse, st, nullptr, group, true);
     float *po = reinterpret_cast<float *>(part_o), *pl = reinterpret_cast<float *>(part_lse);
-    k6attn_status s =
-        run_attention(h, g, q, k, v, jk, jv, qk_f16, n_chunks, po, pl, st, nullptr, group, true, tail_split);
+    k6attn_status s = run_attention(h, g, q, k, v, jk, jv, qk_f16, n_chunks, po, pl, st, nullptr, group, true);
     if (s != K6ATTN_OK) return s;
     const cudaError_t e = launch_lse_merge(g, parts, po, pl, out, lse, st);
     if (e != cudaSuccess) return set_error(K6ATTN_ERR_CUDA, "%s: merge launch: %s", fn, cudaGetErrorString(e));
@@ -263,13 +230,7 @@ k6attn_status k6attn_create(const k6attn_desc *desc, k6attn_t *out) {
         st = cuda_check(cudaMalloc(&h->tables, h->table_bytes), "create: rotary tables");
     if (st == K6ATTN_OK) st = cuda_check(launch_rope_tables(g, d.theta, h->tables, 0), "create: rotary tables");
     if (st == K6ATTN_OK) st = cuda_check(cudaDeviceSynchronize(), "create: rotary tables");
-    if (st == K6ATTN_OK) st = cuda_check(cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking), "create: stream");
-    if (st == K6ATTN_OK) st = cuda_check(cudaEventCreateWithFlags(&h->fork, cudaEventDisableTiming), "create: event");
-    if (st == K6ATTN_OK) st = cuda_check(cudaEventCreateWithFlags(&h->join, cudaEventDisableTiming), "create: event");
     if (st != K6ATTN_OK) {
-        if (h->join) cudaEventDestroy(h->join);
-        if (h->fork) cudaEventDestroy(h->fork);
-        if (h->side) cudaStreamDestroy(h->side);
         cudaFree(h->tables);
         cudaFree(h->err);
         delete h;
@@ -286,9 +247,6 @@ void k6attn_destroy(k6attn_t h) {
     const bool other = cudaGetDevice(&cur) == cudaSuccess && cur != h->device;
     if (other) cudaSetDevice(h->device);
     cudaDeviceSynchronize();
-    cudaEventDestroy(h->join);
-    cudaEventDestroy(h->fork);
-    cudaStreamDestroy(h->side);
     cudaFree(h->tables);
     cudaFree(h->err);
     if (other) cudaSetDevice(cur);
@@ -739,7 +697,7 @@ k6attn_status k6attn_cross_forward(k6attn_t h, const void *q, long Sq, const voi
     int m = cross_split(g, n_chunks);
     if (m > 1 && (!workspace || workspace_bytes < ws_layout(g, n_chunks * m, false).total)) m = 1;
     const int n_int = n_chunks * m;
-    if (n_int == 1) return run_attention(h, g, q, k, v, nullptr, nullptr, false, 1, out, lse, st, nullptr, 0, false, true);
+    if (n_int == 1) return run_attention(h, g, q, k, v, nullptr, nullptr, false, 1, out, lse, st);
     const WsLayout L = ws_layout(g, n_int, false);
     if (!workspace || workspace_bytes < L.total)
         return set_error(K6ATTN_ERR_WORKSPACE, "cross_forward: workspace of %zu bytes needed, %zu given", L.total,
@@ -751,7 +709,7 @@ k6attn_status k6attn_cross_forward(k6attn_t h, const void *q, long Sq, const voi
         return set_error(K6ATTN_ERR_INVALID_ARG, "cross_forward: workspace overlaps a tensor");
     char *ws = static_cast<char *>(workspace);
     return attention_and_merge(h, g, q, k, v, nullptr, nullptr, false, n_int, out, lse, ws + L.part_o,
-                               ws + L.part_lse, st, "cross_forward", true);
+                               ws + L.part_lse, st, "cross_forward");
 }
 
 k6attn_status k6attn_seq2head_relayout(const void *src, void *dst, int B, long S, int H, int d, int elem_bytes,

@@ -37,7 +37,6 @@ struct TcParams {
     long units;                               // B * H * n_chunks * q_pairs work units
     int group;                                // chunks per CTA, sharing one load of Q (divides n_chunks)
     int merge;                                // 1: a CTA's group of chunks leaves one partial (index c / group)
-    int q_base;                               // first query row of this launch (q tiles start there)
     const float *row_bound;                   // constant-max softmax: bound per query row [B][H][Sq], or null
 };
 
@@ -96,7 +95,7 @@ __device__ __forceinline__ Unit decode_unit(const TcParams &p, long unit) {
     r.c = (int)(cg * p.group + g);
     r.h = (int)(u % (uint32_t)p.H);
     r.b = (int)(u / (uint32_t)p.H);
-    r.q0 = (int)qp * (tc::NQ * tc::BM) + p.q_base;
+    r.q0 = (int)qp * (tc::NQ * tc::BM);
     return r;
 }
 

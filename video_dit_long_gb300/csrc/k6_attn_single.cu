@@ -449,8 +449,7 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
 cudaError_t launch_attn_tc_single(const Geom &g, const void *q, const void *k, const void *v, const void *jk,
                                   const void *jv, int n_chunks, void *out, float *lse, const AttnTcOptions &opt,
                                   cudaStream_t st, const char **why) {
-    const long q_rows = opt.q_rows < 0 ? g.Sq - opt.q_base : opt.q_rows;
-    if (q_rows > tc::BM) {
+    if (g.Sq > tc::BM) {
         if (why) *why = "single-tile attention takes at most 128 query rows";
         return cudaErrorInvalidValue;
     }
@@ -476,8 +475,7 @@ cudaError_t launch_attn_tc_single(const Geom &g, const void *q, const void *k, c
     p.Nj = g.Nj;
     p.H = g.H;
     p.n_chunks = n_chunks;
-    p.q_base = (int)opt.q_base;
-    p.q_pairs = q_rows > 0 ? 1 : 0;  // one unit per (b, h, chunk): q0 = q_base
+    p.q_pairs = g.Sq > 0 ? 1 : 0;  // one unit per (b, h, chunk): q0 = 0
     p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)g.d));
     p.out = out;
     p.lse = lse;

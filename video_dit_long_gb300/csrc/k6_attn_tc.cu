@@ -493,9 +493,7 @@ cudaError_t launch_attn_tc(const Geom &g, const void *q, const void *k, const vo
     p.Nj = g.Nj;
     p.H = g.H;
     p.n_chunks = n_chunks;
-    const long q_rows = opt.q_rows < 0 ? g.Sq - opt.q_base : opt.q_rows;
-    p.q_base = (int)opt.q_base;
-    p.q_pairs = (int)((q_rows + tc::NQ * tc::BM - 1) / (tc::NQ * tc::BM));
+    p.q_pairs = (int)((g.Sq + tc::NQ * tc::BM - 1) / (tc::NQ * tc::BM));
     p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)g.d));
     p.out = out;
     p.lse = lse;

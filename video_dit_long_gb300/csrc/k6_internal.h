@@ -104,8 +104,6 @@ struct AttnTcOptions {
     const float *row_bound = nullptr;  // constant-max softmax bounds [B][H][Sq] (natural-log units), or null
     int group = 0;           // chunks per CTA (divides n_chunks); 0: the library's choice, chunk_group()
     int merge = 0;           // 1: each CTA's group of chunks leaves one partial (n_chunks / group partials)
-    long q_base = 0;         // this launch covers query rows [q_base, q_base + q_rows) of the g.Sq rows
-    long q_rows = -1;        // (-1: to the end); outputs keep their full [.][B][Sq][H][d] layout
 };
 
 // Chunks per CTA the library picks for n_chunks K/V chunks of problem g on the
