@@ -174,7 +174,7 @@ k6attn_status k6attn_norm_rope_qk(k6attn_t h, const void *q, const void *k, cons
  *           Otherwise rotated copies are written to the workspace first
  *           (k6attn_rope_qk math; fp16 copies for a BF16 handle, so a
  *           rotated value must be finite in fp16: K6ATTN_ERR_RANGE at
- *           k6attn_sync otherwise).
+ *           k6attn_sync otherwise; bf16 copies with K6ATTN_OPT_ROTATE_BF16).
  *  n_chunks K/V chunks: chunk c covers keys [c*Sk/n, (c+1)*Sk/n) of
  *           concat(k, joint_k); Sk % n_chunks must be 0 ([CP] "Sequence
  *           Length Constraints").  n_chunks == 1 writes out/lse directly;
@@ -442,8 +442,18 @@ k6attn_status k6attn_sync(k6attn_t h, void *stream);
  *      to finish reading P (which shares tensor memory with the next S tile)
  *      before issuing the next Q.K^T product; 0 (default): relies on the
  *      tensor pipe executing one thread's MMAs in issue order.
+ *  K6ATTN_OPT_ROTATE_BF16  1: k6attn_forward and k6attn_forward_static_scratch
+ *      keep the rotated q/k copies of a BF16 handle in bf16, whose range is
+ *      that of fp32, instead of fp16 (default 0).  fp16 copies add 8 times less
+ *      rounding error to the logits but fail (K6ATTN_ERR_RANGE) on a rotated
+ *      value beyond 65,504, which bf16 inputs can hold; this option accepts any
+ *      finite input at the cost of that extra rounding.
  * Returns K6ATTN_ERR_INVALID_ARG for an unknown option or a negative value. */
-typedef enum { K6ATTN_OPT_WAIT_LIMIT_NS = 0, K6ATTN_OPT_STRICT_MMA_ORDER = 1 } k6attn_option;
+typedef enum {
+    K6ATTN_OPT_WAIT_LIMIT_NS = 0,
+    K6ATTN_OPT_STRICT_MMA_ORDER = 1,
+    K6ATTN_OPT_ROTATE_BF16 = 2
+} k6attn_option;
 k6attn_status k6attn_set_option(k6attn_t h, k6attn_option opt, long long value);
 
 /* Static description of a status code, and the last error message of the

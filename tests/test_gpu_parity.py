@@ -315,3 +315,25 @@ def test_forward_argument_errors():
     with pytest.raises(k6.K6Error) as e:
         h.forward(q, k, v, None, None, out, n_chunks=1, rope=False)
     assert e.value.status == k6.ERR_INVALID_ARG
+
+
+def test_rotated_values_beyond_fp16_take_the_bf16_route():
+    """A query entry above 65,504 (exact in bf16, at grid position 0 where the
+    rotation is the identity, in dims whose key entries are all zero so that it
+    adds nothing to any logit): the forward's fp16 copies report ERR_RANGE;
+    with OPT_ROTATE_BF16 the copies stay bf16 and the result matches the
+    oracle within the bf16 bounds."""
+    w = Workload("wide", 1, 2, 128, "bf16", (3, 10, 20), 40, (32, 48, 48), 0, 0.5, 1.0, (2,))
+    x = inputs.make_inputs(w)
+    for name in ("k", "jk"):
+        x[name][:, :, 1, 6:8] = 0
+    x["q"][0, 0, 1, 6] = inputs.bf16_bits(np.array([66048.0], np.float32))[0]
+    k6 = K()
+    h = k6.Handle.for_workload(w)
+    with pytest.raises(k6.K6Error) as e:
+        run_forward(w, x, 2, handle=h)
+    assert e.value.status == k6.ERR_RANGE
+    h.set_option(k6.OPT_ROTATE_BF16, 1)
+    out, lse, _ = run_forward(w, x, 2, handle=h)
+    ref, ref_lse = oracle_forward(w, x)
+    compare(out, ref, lse, ref_lse, "bf16")

@@ -19,6 +19,7 @@ struct k6attn_handle {
     int *err = nullptr;                 // device error word
     unsigned long long wait_limit_ns = 2000000000ull;
     int strict_order = 0;
+    int rotate_bf16 = 0;                // forward: rotated copies in bf16 instead of fp16
     int device = 0;
 };
 
@@ -267,6 +268,7 @@ k6attn_status k6attn_set_option(k6attn_t h, k6attn_option opt, long long value) 
     switch (opt) {
         case K6ATTN_OPT_WAIT_LIMIT_NS: h->wait_limit_ns = (unsigned long long)value; return K6ATTN_OK;
         case K6ATTN_OPT_STRICT_MMA_ORDER: h->strict_order = value ? 1 : 0; return K6ATTN_OK;
+        case K6ATTN_OPT_ROTATE_BF16: h->rotate_bf16 = value ? 1 : 0; return K6ATTN_OK;
     }
     return set_error(K6ATTN_ERR_INVALID_ARG, "set_option: unknown option %d", (int)opt);
 }
@@ -444,13 +446,14 @@ k6attn_status k6attn_forward(k6attn_t h, const void *q, const void *k, const voi
     if (rope) {
         void *qr = ws + L.q_rot, *kr = ws + L.k_rot, *jkr = g.Nj ? ws + L.jk_rot : nullptr;
         // a bf16 handle keeps its rotated copies in fp16 (8x finer rounding of the logits' inputs)
+        // unless asked to keep bf16's range
         s = cuda_check(launch_rope_qk(g, static_cast<const float2 *>(rope_tables), q, qr, k, kr, joint_k, jkr,
-                                      g.dtype == K6ATTN_BF16 ? K6ATTN_F16 : g.dtype, h->err, st),
+                                      g.dtype == K6ATTN_BF16 && !h->rotate_bf16 ? K6ATTN_F16 : g.dtype, h->err, st),
                        "forward: rope launch");
         if (s != K6ATTN_OK) return s;
         qa = qr, ka = kr, jka = jkr;
     }
-    const bool qk_f16 = rope && g.dtype == K6ATTN_BF16;
+    const bool qk_f16 = rope && g.dtype == K6ATTN_BF16 && !h->rotate_bf16;
     return attention_and_merge(h, g, qa, ka, v, jka, joint_v, qk_f16, n_chunks, out, lse, ws + L.part_o,
                                ws + L.part_lse, st, "forward");
 }

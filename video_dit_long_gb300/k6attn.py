@@ -15,7 +15,7 @@ from . import build as _build
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_RANGE = range(7)
 BF16, F32, F16 = 0, 1, 2
-OPT_WAIT_LIMIT_NS, OPT_STRICT_MMA_ORDER = 0, 1
+OPT_WAIT_LIMIT_NS, OPT_STRICT_MMA_ORDER, OPT_ROTATE_BF16 = 0, 1, 2
 
 # every symbol the header declares
 SYMBOLS = ["k6attn_create", "k6attn_destroy", "k6attn_rope_tables", "k6attn_rope_tables_bytes",
