@@ -63,3 +63,15 @@ def test_step_on_a_small_workload_matches_oracle():
     rows = np.arange(w.S)
     ref, ref_lse = oracle_sampled(w, x, rows)
     compare(out, ref, lse, ref_lse, "bf16")
+
+
+def test_step_with_two_batches_matches_oracle():
+    """The chain with B = 2 (image workload: 2-D rotary, 256 text tokens; 8-way head split of 24
+    heads, 4 chunks in the library's groups), every row of both batches."""
+    w = configs.WORKLOADS["image"].with_batch(2)
+    x = inputs.make_inputs(w)
+    st = run_step(w, 4, 8, x)
+    out = to_host(st.out)
+    lse = st.lse.cpu().numpy().astype(np.float64)
+    ref, ref_lse = oracle_sampled(w, x, np.arange(w.S))
+    compare(out, ref, lse, ref_lse, "bf16")
