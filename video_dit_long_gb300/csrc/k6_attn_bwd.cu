@@ -374,14 +374,14 @@ __device__ __forceinline__ void p_half(float (&pr)[64], const uint32_t (&sv)[2][
     }
 }
 
-// dS^T = P (dP^T - D) over the 64 columns at taddr (16-column chunks; each chunk's
-// dS^T lands on columns already read), and P rounded to bf16 into this thread's
-// row of the swizzled P^T panel at prow.
-template <bool FULL>
+// dS^T = P (dP^T - D) over 16-query chunks [C0, C1) of the 64 columns at taddr
+// (each chunk's dS^T lands on columns already read), and P rounded to bf16 into
+// this thread's row of the swizzled P^T panel at prow.
+template <bool FULL, int C0, int C1>
 __device__ __forceinline__ void ds_half(const float (&pr)[64], const float2 *ldq, int nq, uint32_t taddr,
                                         uint32_t prow, int r, int ds_f16) {
 #pragma unroll
-    for (int c = 0; c < 4; c++) {
+    for (int c = C0; c < C1; c++) {
         uint32_t pv[16], ds[8], pk[8];
         tmem_ld16(taddr + 16 * c, pv);
         tmem_ld_wait();
@@ -411,21 +411,25 @@ __device__ __forceinline__ void ds_half(const float (&pr)[64], const float2 *ldq
 //
 // smem tiles: K 0, V 1, ring slot s: Q 2+2s, dO 3+2s; P^T 6.
 // barriers: stat_full, q_full[2], do_full[2], q_empty[2], do_empty[2], s_ready
-//           (S^T(i) done), consumed (256 arrivals: S^T(i) read), pds_ready (256
-//           arrivals: P^T(i) in shared memory, dS^T(i) in tensor memory), window
-//           (dV/dK(i-1) and dP^T(i) done), acc_done, drain.
+//           (S^T(i) done), consumed (256 arrivals: S^T(i) read), pds_ready[2] (256
+//           arrivals each: P^T(i) in shared memory and dS^T(i) in tensor memory for
+//           the first / last 32 queries of each half), window (dV/dK(i-1) and
+//           dP^T(i) done), acc_done, drain.
 // Q and dO slots are released separately: Q(i) once dK(i) is done, midway
 // through the window, so Q(i+2) is in flight while the window finishes.
 //
 // Per tile i the MMA thread issues S^T(i+1) as soon as the row pass has read
-// S^T(i), then, once P^T(i)/dS^T(i) are published, the window dK(i) | dV(i)
-// first half, then dP^T(i+1) | dV(i) second half (dP^T(i+1) overwrites dS^T(i),
+// S^T(i).  The row pass publishes P^T(i)/dS^T(i) in two parts (queries 0-31 and
+// 64-95, then 32-63 and 96-127: the first half of each warpgroup's columns), so
+// the window starts on the first part while the second is formed: dK(i) | dV(i)
+// over the first part's 4 K-steps, then over the second part's (dK) and two of
+// dV's, then dP^T(i+1) | the last two dV steps (dP^T(i+1) overwrites dS^T(i),
 // so it follows every dK(i) MMA).  The row pass of tile i+1 computes its P from
 // S^T(i+1) while that window runs, and only the dS / P^T stores wait for it.
 
 namespace dkvb {
 constexpr int STAT = 0, QFULL = 1, DOFULL = 3, QEMPTY = 5, DOEMPTY = 7, SREADY = 9, CONSUMED = 10, PDS = 11,
-              WIN = 12, ACC = 13, DRAIN = 14, NB = 15;
+              WIN = 13, ACC = 14, DRAIN = 15, NB = 16;  // PDS, PDS + 1: the two parts of a tile's P^T / dS^T
 }
 
 __global__ void __launch_bounds__(bw::THREADS, 1)
@@ -437,7 +441,7 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     using namespace dkvb;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int counts[NB] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 256, 256, 1, 1, 1};
+    const int counts[NB] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 256, 256, 256, 1, 1, 1};
     uint64_t *bar;
     volatile int *abort_flag;
     const uint32_t tmem = bw_setup<NB>(smem, counts, bar, abort_flag);
@@ -516,28 +520,40 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
                     for (int kk = 0; kk < D / 16; kk++) mma_kmajor(tS, dk0, slot(dring, t + 1, 0), p.idesc_qk, kk);
                     tc_commit(bar + SREADY);
                 }
-                // P^T(t) is in shared memory and dS^T(t) over dP^T(t)
+                // the first part of P^T(t) is in shared memory and of dS^T(t) over dP^T(t)
                 if (!(ok = mbar_wait(bar + PDS, t & 1, w))) break;
                 if (next && !(ok = wait_do(t + 1))) break;
                 tc_fence_after();
                 const uint32_t acc = t > 0 ? 1u : 0u;
+                // K-step kk covers queries 16 kk .. 16 kk + 15: the first part holds kk 0, 1, 4, 5
                 auto dv_step = [&](int kk) {  // dV += P^T dO
                     const uint64_t poff = (uint64_t)((kk >> 2) * PANEL + (kk & 3) * 32) >> 4;
                     mma_ss(tV, dp + poff, slot(dring_mn, t, 1) + (uint64_t)((kk * 16 * 128) >> 4), p.idesc_bf16_mn,
                            acc | (kk > 0 ? 1u : 0u));
                 };
-#pragma unroll
-                for (int kk = 0; kk < BM / 16; kk++) {  // dK += dS^T Q
+                auto dk_step = [&](int kk) {  // dK += dS^T Q
                     mma_ts(tK, tP + (kk >> 2) * 64 + (kk & 3) * 8,
                            slot(dring_mn, t, 0) + (uint64_t)((kk * 16 * 128) >> 4), p.idesc_ds_mn,
                            acc | (kk > 0 ? 1u : 0u));
-                    if (kk < 4) dv_step(kk);
+                };
+                constexpr int part0[4] = {0, 1, 4, 5}, part1[4] = {2, 3, 6, 7};
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    dk_step(part0[i]);
+                    dv_step(part0[i]);
+                }
+                if (!(ok = mbar_wait(bar + PDS + 1, t & 1, w))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    dk_step(part1[i]);
+                    if (i < 2) dv_step(part1[i]);
                 }
                 tc_commit(bar + QEMPTY + (t & 1));  // Q(t): S^T(t) and dK(t) done
 #pragma unroll
                 for (int kk = 0; kk < D / 16; kk++) {
                     if (next) mma_kmajor(tP, dv0, slot(dring, t + 1, 1), p.idesc_bf16, kk);  // dP^T(t+1)
-                    if (kk < 4) dv_step(4 + kk);
+                    if (kk < 2) dv_step(part1[2 + kk]);
                 }
                 tc_commit(bar + DOEMPTY + (t & 1));  // dO(t): dP^T(t) and dV(t) done
                 tc_commit(bar + WIN);
@@ -585,14 +601,23 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
                 break;
             }
             tc_fence_after();
+            // first part (queries 0-31 of this half), published before the second is formed
             if (nq == 64)
-                ds_half<true>(pr, ldq, 64, lb + 128 + 64 * g, prow, r, p.ds_f16);
+                ds_half<true, 0, 2>(pr, ldq, 64, lb + 128 + 64 * g, prow, r, p.ds_f16);
             else
-                ds_half<false>(pr, ldq, nq, lb + 128 + 64 * g, prow, r, p.ds_f16);
+                ds_half<false, 0, 2>(pr, ldq, nq, lb + 128 + 64 * g, prow, r, p.ds_f16);
             fence_proxy_async_smem();
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar + PDS);
+            if (nq == 64)
+                ds_half<true, 2, 4>(pr, ldq, 64, lb + 128 + 64 * g, prow, r, p.ds_f16);
+            else
+                ds_half<false, 2, 4>(pr, ldq, nq, lb + 128 + 64 * g, prow, r, p.ds_f16);
+            fence_proxy_async_smem();
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar + PDS + 1);
         }
         if (ok && mbar_wait(bar + ACC, 0, w)) {
             tc_fence_after();
