@@ -267,3 +267,27 @@ def test_chunk_group_argument_errors():
     with pytest.raises(k6.K6Error) as e:  # partial lse required
         h.attention_chunk_groups(d["q"], d["k"], d["v"], d["jk"], d["jv"], 4, 2, out, None)
     assert e.value.status == k6.ERR_INVALID_ARG
+
+
+def test_fused_calls_without_joint_tokens():
+    """No joint segment (Nj = 0): the prologue moves only q, k, v (null joint pointers), the chunk
+    groups run on video keys alone, and the merged step result equals the oracle."""
+    w = Workload("nojoint", 1, 4, 128, "bf16", (2, 10, 24), 0, (32, 48, 48), 0, 1.0, 1.0, (4,))  # S = 480
+    k6 = K()
+    x = inputs.make_inputs(w)
+    d = dev_inputs(w, x)
+    P = 2
+    hf = k6.Handle.for_workload(w)
+    hh = k6.Handle(P * w.B, w.H // P, w.d, "bf16", w.grid, 0, w.axis_dim)
+    sp = split_buffers(w, P, torch.float16)
+    hf.rope_split_heads(d["q"], d["k"], d["v"], None, None, P, sp["q"], sp["k"], sp["v"])
+    po = torch.empty((2, P * w.B, w.S, w.H // P, w.d), dtype=torch.float32, device="cuda")
+    pl = torch.empty((2, P * w.B, w.H // P, w.S), dtype=torch.float32, device="cuda")
+    hh.attention_chunk_groups(sp["q"], sp["k"], sp["v"], None, None, 4, 2, po, pl, qk_dtype=k6.F16)
+    out = torch.empty_like(d["q"])
+    lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device="cuda")
+    hf.lse_merge_heads(po, pl, 2, P, out, lse)
+    hf.sync()
+    hh.sync()
+    ref, ref_lse = O.attention(geom(w), x["q"], x["k"], x["v"])
+    compare(to_host(out), ref, lse.cpu().numpy().astype(np.float64), ref_lse, "bf16")
