@@ -329,6 +329,11 @@ k6attn_status k6attn_backward(k6attn_t h, const void *q, const void *k, const vo
  *   mathematics; a row whose every term underflows (a bound more than about
  *   87 above its largest logit) sets the error word (K6ATTN_ERR_RANGE at
  *   k6attn_sync) and gets a zero output.
+ * k6attn_attention_chunk_groups_bounded: the same with each CTA's group of
+ *   `group` consecutive chunks merged in the kernel (as
+ *   k6attn_attention_chunk_groups): n_chunks / group partials, or out/lse
+ *   directly when that is 1.  With one bound for every chunk, the merge inside
+ *   a group is a plain sum of the chunks' terms.
  */
 size_t k6attn_row_bounds_bytes(k6attn_t h);
 k6attn_status k6attn_row_bounds(k6attn_t h, const void *q, const void *k, const void *joint_k, k6attn_dtype qk_dtype,
@@ -337,6 +342,10 @@ k6attn_status k6attn_attention_chunks_bounded(k6attn_t h, const void *q, const v
                                               const void *joint_k, const void *joint_v, k6attn_dtype qk_dtype,
                                               const float *bounds, int n_chunks, void *out, float *lse,
                                               void *stream);
+k6attn_status k6attn_attention_chunk_groups_bounded(k6attn_t h, const void *q, const void *k, const void *v,
+                                                    const void *joint_k, const void *joint_v, k6attn_dtype qk_dtype,
+                                                    const float *bounds, int n_chunks, int group, void *out,
+                                                    float *lse, void *stream);
 
 /*
  * Log-sum-exp merge of per-chunk partials (ring attention's combine step,

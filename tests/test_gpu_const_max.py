@@ -29,7 +29,7 @@ def _need_gpu():
         pytest.skip("no CUDA device")
 
 
-def run_bounded(w, x, n, rope=True):
+def run_bounded(w, x, n, rope=True, group=0):
     from video_dit_long_gb300 import k6attn as K
     h = K.Handle.for_workload(w)
     q, k, v, jk, jv = (to_dev(x[nm], w.dtype) for nm in ("q", "k", "v", "jk", "jv"))
@@ -46,7 +46,16 @@ def run_bounded(w, x, n, rope=True):
     h.row_bounds(qo, ko, jo, bounds, qk_dtype=qd)
     out = torch.empty_like(q)
     lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device="cuda")
-    if n == 1:
+    if group:  # each CTA's group of chunks merged in the kernel
+        parts = n // group
+        if parts == 1:
+            h.attention_chunk_groups_bounded(qo, ko, v, jo, jv, bounds, n, group, out, lse, qk_dtype=qd)
+        else:
+            po = torch.empty((parts, w.B, w.S, w.H, w.d), dtype=torch.float32, device="cuda")
+            pl = torch.empty((parts, w.B, w.H, w.S), dtype=torch.float32, device="cuda")
+            h.attention_chunk_groups_bounded(qo, ko, v, jo, jv, bounds, n, group, po, pl, qk_dtype=qd)
+            h.lse_merge(po, pl, parts, out, lse)
+    elif n == 1:
         h.attention_chunks_bounded(qo, ko, v, jo, jv, bounds, 1, out, lse, qk_dtype=qd)
     else:
         po = torch.empty((n, w.B, w.S, w.H, w.d), dtype=torch.float32, device="cuda")
@@ -94,3 +103,15 @@ def test_loose_bound_underflow_is_reported():
         h.sync()
     assert e.value.status == K.ERR_RANGE
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("name,n,group", [("ragged", 4, 2), ("ragged", 4, 4), ("audio1d", 3, 3), ("one_tile", 3, 3)])
+def test_bounded_chunk_groups_match_oracle(name, n, group):
+    """Constant max with each CTA's chunk group merged in the kernel (the chunks' terms share one bound)."""
+    w = CASES[name]
+    x = inputs.make_inputs(w)
+    h, out, lse, _ = run_bounded(w, x, n, group=group)
+    h.sync()
+    ref, ref_lse = O.attention(geom(w), x["q"], x["k"], x["v"], x["jk"] if w.Nj else None,
+                               x["jv"] if w.Nj else None)
+    compare(to_host(out), ref, lse.cpu().numpy().astype(np.float64), ref_lse, "bf16")

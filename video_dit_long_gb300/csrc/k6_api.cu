@@ -388,6 +388,41 @@ k6attn_status k6attn_attention_chunks_bounded(k6attn_t h, const void *q, const v
                          static_cast<cudaStream_t>(stream), bounds);
 }
 
+k6attn_status k6attn_attention_chunk_groups_bounded(k6attn_t h, const void *q, const void *k, const void *v,
+                                                    const void *joint_k, const void *joint_v, k6attn_dtype qk_dtype,
+                                                    const float *bounds, int n_chunks, int group, void *out,
+                                                    float *lse, void *stream) {
+    g_msg[0] = 0;
+    {
+        k6attn_status hs = check_handle("attention_chunk_groups_bounded", h);
+        if (hs != K6ATTN_OK) return hs;
+    }
+    const Geom &g = h->g;
+    if (g.dtype != K6ATTN_BF16)
+        return set_error(K6ATTN_ERR_UNSUPPORTED, "attention_chunk_groups_bounded: the constant-max path is bf16 only");
+    if (!bounds || (reinterpret_cast<uintptr_t>(bounds) & 3))
+        return set_error(K6ATTN_ERR_INVALID_ARG, "attention_chunk_groups_bounded: null or misaligned bounds");
+    if (group < 1 || n_chunks < 1 || n_chunks % group)
+        return set_error(K6ATTN_ERR_INVALID_ARG, "attention_chunk_groups_bounded: group %d must divide n_chunks %d",
+                         group, n_chunks);
+    const int parts = n_chunks / group;
+    if (parts > 1 && !lse)
+        return set_error(K6ATTN_ERR_INVALID_ARG,
+                         "attention_chunk_groups_bounded: partial lse is required when n_chunks / group > 1");
+    if (qk_dtype != K6ATTN_BF16 && qk_dtype != K6ATTN_F16)
+        return set_error(K6ATTN_ERR_INVALID_ARG, "attention_chunk_groups_bounded: q/k type %d", (int)qk_dtype);
+    const size_t ob = (size_t)parts * g.B * g.Sq * g.H * g.d * (parts > 1 ? 4 : g.elem);
+    const size_t lb = (size_t)parts * g.B * g.H * g.Sq * 4;
+    k6attn_status s =
+        check_inputs("attention_chunk_groups_bounded", g, q, k, v, joint_k, joint_v, n_chunks, out, ob, lse, lb);
+    if (s != K6ATTN_OK) return s;
+    const size_t bb = k6attn_row_bounds_bytes(h);
+    if (overlap(bounds, bb, out, ob) || overlap(bounds, bb, lse, lb))
+        return set_error(K6ATTN_ERR_INVALID_ARG, "attention_chunk_groups_bounded: bounds overlap an output");
+    return run_attention(h, g, q, k, v, joint_k, joint_v, qk_dtype == K6ATTN_F16, n_chunks, out, lse,
+                         static_cast<cudaStream_t>(stream), bounds, group, true);
+}
+
 k6attn_status k6attn_lse_merge(k6attn_t h, const float *part_o, const float *part_lse, int n_chunks, void *out,
                                float *lse, void *stream) {
     g_msg[0] = 0;

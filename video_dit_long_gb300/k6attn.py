@@ -25,7 +25,7 @@ SYMBOLS = ["k6attn_create", "k6attn_destroy", "k6attn_rope_tables", "k6attn_rope
            "k6attn_cross_forward", "k6attn_norm_rope_qk", "k6attn_row_bounds_bytes", "k6attn_row_bounds",
            "k6attn_attention_chunks_bounded", "k6attn_backward_workspace_bytes", "k6attn_backward",
            "k6attn_chunk_group", "k6attn_attention_chunk_groups", "k6attn_rope_split_heads",
-           "k6attn_lse_merge_heads"]
+           "k6attn_lse_merge_heads", "k6attn_attention_chunk_groups_bounded"]
 
 
 class K6Error(RuntimeError):
@@ -90,6 +90,7 @@ def load(build_if_missing: bool = True):
     L.k6attn_attention_chunk_groups.argtypes = [P, P, P, P, P, P, I, I, I, P, P, P]
     L.k6attn_rope_split_heads.argtypes = [P, P, P, P, P, P, P, I, I, P, P, P, P, P, P]
     L.k6attn_lse_merge_heads.argtypes = [P, P, P, I, I, P, P, P]
+    L.k6attn_attention_chunk_groups_bounded.argtypes = [P, P, P, P, P, P, I, P, I, I, P, P, P]
     L.k6attn_seq2head_relayout.argtypes = [P, P, I, ctypes.c_long, I, I, I, I, I, P]
     L.k6attn_sync.argtypes = [P, P]
     L.k6attn_set_option.argtypes = [P, I, ctypes.c_longlong]
@@ -100,7 +101,7 @@ def load(build_if_missing: bool = True):
     for name in ("k6attn_create", "k6attn_rope_qk", "k6attn_forward", "k6attn_forward_static_scratch",
                  "k6attn_attention_chunks", "k6attn_lse_merge", "k6attn_cross_forward", "k6attn_norm_rope_qk",
                  "k6attn_row_bounds", "k6attn_attention_chunks_bounded", "k6attn_attention_chunk_groups",
-                 "k6attn_rope_split_heads", "k6attn_lse_merge_heads",
+                 "k6attn_rope_split_heads", "k6attn_lse_merge_heads", "k6attn_attention_chunk_groups_bounded",
                  "k6attn_seq2head_relayout", "k6attn_sync", "k6attn_set_option"):
         getattr(L, name).restype = I
     _lib = L
@@ -273,6 +274,13 @@ class Handle:
         _check(load().k6attn_attention_chunks_bounded(self.h, _ptr(q), _ptr(k), _ptr(v), _ptr(joint_k),
                                                       _ptr(joint_v), int(qd), _ptr(bounds), int(n_chunks), _ptr(out),
                                                       _ptr(lse), _stream(stream)))
+
+    def attention_chunk_groups_bounded(self, q, k, v, joint_k, joint_v, bounds, n_chunks, group, out, lse=None,
+                                       qk_dtype=None, stream=None):
+        qd = self._desc.dtype if qk_dtype is None else qk_dtype
+        _check(load().k6attn_attention_chunk_groups_bounded(self.h, _ptr(q), _ptr(k), _ptr(v), _ptr(joint_k),
+                                                            _ptr(joint_v), int(qd), _ptr(bounds), int(n_chunks),
+                                                            int(group), _ptr(out), _ptr(lse), _stream(stream)))
 
     def lse_merge(self, part_o, part_lse, n_chunks, out, lse=None, stream=None):
         _check(load().k6attn_lse_merge(self.h, _ptr(part_o), _ptr(part_lse), int(n_chunks), _ptr(out), _ptr(lse),
