@@ -370,6 +370,30 @@ class _Null:
         pass
 
 
+def measure_fp8(w, n_chunks, P, x, steps, warmup):
+    """The step in the FP8 mode (rotated q/k stored as e4m3, Q.K^T on 8-bit operands, P.V bf16)."""
+    import torch
+    st = UlyssesStep(w, n_chunks, P, x, qk="e4m3")
+    for _ in range(warmup):
+        st.step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for s in range(steps):
+        st.step(evs[s])
+    torch.cuda.synchronize()
+    st.sync()
+    per = np.array([[evs[s][i].elapsed_time(evs[s][i + 1]) for i in range(3)] for s in range(steps)]).mean(axis=0)
+    total = float(per.sum())
+    flops = w.flops()
+    del st
+    torch.cuda.empty_cache()
+    return {"what": f"{w.name}: the step with rotated q/k in e4m3 (Q.K^T on kind::f8f6f4, P.V bf16)",
+            "value": round(flops / (total * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(total, 4),
+            "attention_ms": round(float(per[1]), 4),
+            "attention_TFLOP/s": round(flops / (float(per[1]) * 1e-3) / 1e12, 2),
+            "parity": "tests/test_gpu_fp8.py (bf16 bounds on exact e4m3 inputs; relative L2 4e-2 at this workload)"}
+
+
 def measure_cross(w, steps, warmup, n_chunks=8, Sq=None):
     """Audio queries (the workload's joint tokens, or the first Sq of them) over the
     full visual sequence, K/V in n chunks (k6attn_cross_forward: attention with the
@@ -607,6 +631,8 @@ def run_ours(args, rank, world, dist_on):
             rec["frac_sustained"] = round(rec["value"] / peak_s, 4)
         line["attention_n1"] = fwd1
         line["backward"] = bwd
+        line["fp8_logits"] = measure_fp8(w, n, P, x, max(5, args.steps // 2), args.warmup)
+        line["fp8_logits"]["frac_of_bf16_peak"] = round(line["fp8_logits"]["attention_TFLOP/s"] / peak_b, 4)
     if rank == 0 and world == 1 and not args.no_cpu and not args.step_only:
         dt, fl, thr = cpu_sample(w, x, args.cpu_rows)
         line["cpu_baseline"] = {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
@@ -652,6 +678,8 @@ def run_only(args):
     if args.only == "merge_per_chunk":
         res, _ = measure(w, n, P, args.steps, args.warmup, False, clocks=False)
         return {"only": "merge_per_chunk", "workload": w.name, "n_chunks": n, "ms": res["merge_per_chunk_ms"]}
+    if args.only == "fp8":
+        return dict(measure_fp8(w, n, P, inputs.make_inputs(w), args.steps, args.warmup), only="fp8")
     if args.only in ("cross", "cross_short"):
         r = measure_cross(w, args.steps, args.warmup, Sq=None if args.only == "cross" else 100)
         return dict(r, only=args.only)
@@ -673,7 +701,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--step-only", action="store_true",
                     help="time the step alone (no secondary rows, end-to-end loop or CPU baseline)")
-    ap.add_argument("--only", choices=["step", "merge_per_chunk", "cross", "cross_short", "backward"],
+    ap.add_argument("--only", choices=["step", "merge_per_chunk", "cross", "cross_short", "backward", "fp8"],
                     help="run one measurement alone and print it (for profiling captures)")
     ap.add_argument("--cpu-rows", type=int, default=1536)
     ap.add_argument("--ref-rows", type=int, default=256)

@@ -69,8 +69,12 @@ typedef enum {
  * BF16 handle: rounding the rotated values to fp16 (11-bit significand)
  * instead of bf16 (8-bit) cuts the error they add to the logits 8-fold, at the
  * same tensor-core rate (Q.K^T runs fp16 x fp16, P.V bf16 x bf16, both with
- * fp32 accumulation). */
-typedef enum { K6ATTN_BF16 = 0, K6ATTN_F32 = 1, K6ATTN_F16 = 2 } k6attn_dtype;
+ * fp32 accumulation).  E4M3 (8-bit float, 3 mantissa bits, finite range
+ * +-448) is likewise only a type for rotated q/k/joint_k of a BF16 handle: the
+ * FP8 mode, where Q.K^T runs on e4m3 operands (kind::f8f6f4, half the tensor
+ * instructions of 16-bit operands) and P.V stays bf16; its error is that of
+ * rounding q and k to 3 mantissa bits (2^-4 relative), 16 times fp16's. */
+typedef enum { K6ATTN_BF16 = 0, K6ATTN_F32 = 1, K6ATTN_F16 = 2, K6ATTN_E4M3 = 3 } k6attn_dtype;
 
 /*
  * Problem descriptor, fixed at handle creation.
@@ -202,7 +206,10 @@ k6attn_status k6attn_forward(k6attn_t h, const void *q, const void *k, const voi
  *           [n_chunks][B][H][Sq] (required); combine them with
  *           k6attn_lse_merge.
  *  qk_dtype the type of q, k and joint_k: the handle's dtype, or F16 for a
- *           BF16 handle (v and joint_v always have the handle's dtype).
+ *           BF16 handle (v and joint_v always have the handle's dtype), or
+ *           E4M3 for a BF16 handle with more than 128 query rows
+ *           (K6ATTN_ERR_UNSUPPORTED otherwise): Q.K^T then runs on 8-bit
+ *           operands, P.V as before.
  * Inputs as in k6attn_forward; outputs must not alias them.
  */
 k6attn_status k6attn_attention_chunks(k6attn_t h, const void *q, const void *k, const void *v, const void *joint_k,
@@ -252,9 +259,10 @@ k6attn_status k6attn_attention_chunk_groups(k6attn_t h, const void *q, const voi
  * i.e. each output is [P][B][R][Hl][d]: the input of a handle with batch P*B
  * and Hl heads.  For B == 1 this equals k6attn_rope_qk into copies followed by
  * k6attn_seq2head_relayout of each tensor (bit for bit).
- *  qk_out_dtype  BF16 or F16: the type of q_out, k_out, joint_k_out (v_out and
- *           joint_v_out are bf16).  F16: a rotated value that is not finite in
- *           fp16 sets K6ATTN_ERR_RANGE (at k6attn_sync).
+ *  qk_out_dtype  BF16, F16 or E4M3: the type of q_out, k_out, joint_k_out
+ *           (v_out and joint_v_out are bf16).  F16: a rotated value that is
+ *           not finite in fp16 sets K6ATTN_ERR_RANGE (at k6attn_sync); E4M3: a
+ *           rotated value beyond +-448 is stored as +-448 and sets it too.
  *  joint_* may be NULL when Nj == 0.  Outputs must not overlap any input or
  *  one another.
  */

@@ -83,9 +83,10 @@ static WsLayout ws_layout(const Geom &g, int n, bool rope) {
 static k6attn_status run_attention(k6attn_handle *h, const Geom &g, const void *q, const void *k, const void *v,
                                    const void *jk, const void *jv, bool qk_f16, int n_chunks, void *out, float *lse,
                                    cudaStream_t st, const float *row_bound = nullptr, int group = 0,
-                                   bool merge = false) {
+                                   bool merge = false, bool qk8 = false) {
     if (g.elem == 2) {
-        AttnTcOptions opt{h->wait_limit_ns, h->err, h->strict_order, qk_f16 ? 1 : 0, row_bound, group, merge ? 1 : 0};
+        AttnTcOptions opt{h->wait_limit_ns, h->err,    h->strict_order, qk_f16 ? 1 : 0, row_bound,
+                          qk8 ? 1 : 0,      group,     merge ? 1 : 0};
         const char *why = nullptr;
         // a query range of one 128-row tile runs the single-tile kernel
         cudaError_t e = (g.Sq <= 128 ? launch_attn_tc_single : launch_attn_tc)(g, q, k, v, jk, jv, n_chunks, out, lse,
@@ -129,7 +130,7 @@ static k6attn_status attention_and_merge(k6attn_handle *h, const Geom &g, const 
 // Checks shared by the two attention entry points.
 static k6attn_status check_inputs(const char *fn, const Geom &g, const void *q, const void *k, const void *v,
                                   const void *jk, const void *jv, int n_chunks, const void *out, size_t out_bytes,
-                                  const float *lse, size_t lse_bytes) {
+                                  const float *lse, size_t lse_bytes, int qk_elem = 0) {
     if (!q || !k || !v || !out) return set_error(K6ATTN_ERR_INVALID_ARG, "%s: null q, k, v or out", fn);
     if (g.Nj > 0 && (!jk || !jv))
         return set_error(K6ATTN_ERR_INVALID_ARG, "%s: %ld joint tokens but joint_k/joint_v is null", fn, g.Nj);
@@ -142,14 +143,34 @@ static k6attn_status check_inputs(const char *fn, const Geom &g, const void *q, 
         if (!aligned16(p)) return set_error(K6ATTN_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", fn);
     if (reinterpret_cast<uintptr_t>(lse) & 3) return set_error(K6ATTN_ERR_INVALID_ARG, "%s: lse misaligned", fn);
     const size_t row = (size_t)g.H * g.d * g.elem;
-    const size_t qb = g.B * g.Sq * row, kvb = g.B * g.Nv * row, jb = g.B * g.Nj * row;
+    const size_t qkrow = (size_t)g.H * g.d * (qk_elem ? qk_elem : g.elem);  // q/k/joint_k may be narrower
+    const size_t qb = g.B * g.Sq * qkrow, kb = g.B * g.Nv * qkrow, jkb = g.B * g.Nj * qkrow;
+    const size_t vb = g.B * g.Nv * row, jvb = g.B * g.Nj * row;
     const void *ins[] = {q, k, v, jk, jv};
-    const size_t insz[] = {qb, kvb, kvb, jb, jb};
+    const size_t insz[] = {qb, kb, vb, jkb, jvb};
     for (int i = 0; i < 5; i++)
         if (overlap(out, out_bytes, ins[i], insz[i]) || overlap(lse, lse_bytes, ins[i], insz[i]))
             return set_error(K6ATTN_ERR_INVALID_ARG, "%s: out or lse overlaps an input", fn);
     if (overlap(out, out_bytes, lse, lse_bytes)) return set_error(K6ATTN_ERR_INVALID_ARG, "%s: out overlaps lse", fn);
     return K6ATTN_OK;
+}
+
+// The q/k type an attention call may take with this handle: the handle's own,
+// F16 for BF16 handles, and E4M3 for BF16 handles whose query range needs the
+// two-tile kernel (more than 128 rows).  Bytes per q/k element, or 0 (refused,
+// message set).
+static int qk_bytes(const char *fn, const Geom &g, k6attn_dtype qk) {
+    if (qk == g.dtype) return g.elem;
+    if (g.dtype == K6ATTN_BF16 && qk == K6ATTN_F16) return 2;
+    if (g.dtype == K6ATTN_BF16 && qk == K6ATTN_E4M3) {
+        if (g.Sq <= 128) {
+            set_error(K6ATTN_ERR_UNSUPPORTED, "%s: e4m3 q/k need a query range of more than 128 rows", fn);
+            return 0;
+        }
+        return 1;
+    }
+    set_error(K6ATTN_ERR_INVALID_ARG, "%s: q/k type %d not allowed for this handle", fn, (int)qk);
+    return 0;
 }
 
 k6attn_status check_handle(const char *fn, k6attn_t h) {
@@ -507,13 +528,12 @@ k6attn_status k6attn_attention_chunks(k6attn_t h, const void *q, const void *k, 
     const int n = n_chunks > 1 ? n_chunks : 1;
     const size_t ob = (size_t)n * g.B * g.S * g.H * g.d * (n_chunks > 1 ? 4 : g.elem);
     const size_t lb = (size_t)n * g.B * g.H * g.S * 4;
-    if (qk_dtype != g.dtype && !(g.dtype == K6ATTN_BF16 && qk_dtype == K6ATTN_F16))
-        return set_error(K6ATTN_ERR_INVALID_ARG, "attention_chunks: q/k type %d not allowed for this handle",
-                         (int)qk_dtype);
-    k6attn_status s = check_inputs("attention_chunks", g, q, k, v, joint_k, joint_v, n_chunks, out, ob, lse, lb);
+    const int qkb = qk_bytes("attention_chunks", g, qk_dtype);
+    if (!qkb) return g.dtype == K6ATTN_BF16 && qk_dtype == K6ATTN_E4M3 ? K6ATTN_ERR_UNSUPPORTED : K6ATTN_ERR_INVALID_ARG;
+    k6attn_status s = check_inputs("attention_chunks", g, q, k, v, joint_k, joint_v, n_chunks, out, ob, lse, lb, qkb);
     if (s != K6ATTN_OK) return s;
     return run_attention(h, g, q, k, v, joint_k, joint_v, qk_dtype == K6ATTN_F16, n_chunks, out, lse,
-                         static_cast<cudaStream_t>(stream));
+                         static_cast<cudaStream_t>(stream), nullptr, 0, false, qk_dtype == K6ATTN_E4M3);
 }
 
 int k6attn_chunk_group(k6attn_t h, int n_chunks) {
@@ -539,15 +559,15 @@ k6attn_status k6attn_attention_chunk_groups(k6attn_t h, const void *q, const voi
     if (parts > 1 && !lse)
         return set_error(K6ATTN_ERR_INVALID_ARG, "attention_chunk_groups: partial lse is required when "
                                                  "n_chunks / group > 1");
-    if (qk_dtype != g.dtype && !(g.dtype == K6ATTN_BF16 && qk_dtype == K6ATTN_F16))
-        return set_error(K6ATTN_ERR_INVALID_ARG, "attention_chunk_groups: q/k type %d not allowed for this handle",
-                         (int)qk_dtype);
+    const int qkb = qk_bytes("attention_chunk_groups", g, qk_dtype);
+    if (!qkb) return g.dtype == K6ATTN_BF16 && qk_dtype == K6ATTN_E4M3 ? K6ATTN_ERR_UNSUPPORTED : K6ATTN_ERR_INVALID_ARG;
     const size_t ob = (size_t)parts * g.B * g.S * g.H * g.d * (parts > 1 ? 4 : g.elem);
     const size_t lb = (size_t)parts * g.B * g.H * g.S * 4;
-    k6attn_status s = check_inputs("attention_chunk_groups", g, q, k, v, joint_k, joint_v, n_chunks, out, ob, lse, lb);
+    k6attn_status s =
+        check_inputs("attention_chunk_groups", g, q, k, v, joint_k, joint_v, n_chunks, out, ob, lse, lb, qkb);
     if (s != K6ATTN_OK) return s;
     return run_attention(h, g, q, k, v, joint_k, joint_v, qk_dtype == K6ATTN_F16, n_chunks, out, lse,
-                         static_cast<cudaStream_t>(stream), nullptr, group, true);
+                         static_cast<cudaStream_t>(stream), nullptr, group, true, qk_dtype == K6ATTN_E4M3);
 }
 
 k6attn_status k6attn_rope_split_heads(k6attn_t h, const void *q, const void *k, const void *v, const void *joint_k,
@@ -562,8 +582,8 @@ k6attn_status k6attn_rope_split_heads(k6attn_t h, const void *q, const void *k, 
     const Geom &g = h->g;
     if (g.dtype != K6ATTN_BF16)
         return set_error(K6ATTN_ERR_UNSUPPORTED, "rope_split_heads: needs a bf16 handle (d = 128)");
-    if (qk_out_dtype != K6ATTN_BF16 && qk_out_dtype != K6ATTN_F16)
-        return set_error(K6ATTN_ERR_INVALID_ARG, "rope_split_heads: rotated q/k type must be BF16 or F16");
+    if (qk_out_dtype != K6ATTN_BF16 && qk_out_dtype != K6ATTN_F16 && qk_out_dtype != K6ATTN_E4M3)
+        return set_error(K6ATTN_ERR_INVALID_ARG, "rope_split_heads: rotated q/k type must be BF16, F16 or E4M3");
     if (P < 1 || g.H % P)
         return set_error(K6ATTN_ERR_INVALID_ARG, "rope_split_heads: %d heads are not divisible by %d", g.H, P);
     if (!q || !k || !v || !q_out || !k_out || !v_out || (!rope_tables && h->table_bytes))
@@ -573,15 +593,17 @@ k6attn_status k6attn_rope_split_heads(k6attn_t h, const void *q, const void *k, 
                          g.Nj);
     const void *src[5] = {q, k, joint_k, v, joint_v};
     void *dst[5] = {q_out, k_out, joint_k_out, v_out, joint_v_out};
-    const size_t row = (size_t)g.H * g.d * 2;
+    const size_t row = (size_t)g.H * g.d * 2, orow = (size_t)g.H * g.d * (qk_out_dtype == K6ATTN_E4M3 ? 1 : 2);
     const size_t nb[5] = {g.B * g.S * row, g.B * g.Nv * row, g.B * g.Nj * row, g.B * g.Nv * row, g.B * g.Nj * row};
+    const size_t ob[5] = {g.B * g.S * orow, g.B * g.Nv * orow, g.B * g.Nj * orow, g.B * g.Nv * row,
+                          g.B * g.Nj * row};
     for (int a = 0; a < 5; a++) {
         if (!aligned16(src[a]) || !aligned16(dst[a]))
             return set_error(K6ATTN_ERR_INVALID_ARG, "rope_split_heads: pointers must be 16-byte aligned");
         for (int b = 0; b < 5; b++) {
-            if (overlap(dst[a], nb[a], src[b], nb[b]))
+            if (overlap(dst[a], ob[a], src[b], nb[b]))
                 return set_error(K6ATTN_ERR_INVALID_ARG, "rope_split_heads: an output overlaps an input");
-            if (a != b && overlap(dst[a], nb[a], dst[b], nb[b]))
+            if (a != b && overlap(dst[a], ob[a], dst[b], ob[b]))
                 return set_error(K6ATTN_ERR_INVALID_ARG, "rope_split_heads: outputs overlap");
         }
     }

@@ -79,7 +79,11 @@ constexpr int TMEM_COLS = 512;
 // precomputed bound p.row_bound (>= every logit of the row), so the softmax
 // takes no row maximum and never rescales O; a row whose every term
 // underflows (a bound far above the true maximum) is reported as DEV_RANGE.
-template <bool BOUNDED>
+// QK8: q/k/joint_k are e4m3.  Their tiles are 128 rows of 128 bytes (one
+// swizzle panel, 16 KB, in the first half of their 32 KB slots) and Q.K^T runs
+// as 4 kind::f8f6f4 MMAs of K = 32 per tile instead of 8 kind::f16 MMAs; P.V is
+// unchanged (bf16 P from tensor memory, bf16 V).
+template <bool BOUNDED, bool QK8>
 __global__ void __launch_bounds__(tc::THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_jk,
@@ -144,9 +148,9 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                 const Unit un = decode_unit(p, u);
                 const TileRange tr = chunk_tiles(p, un.c);
                 if (uc == 0) {  // the CTA's Q tile pair, once
-                    mbar_arrive_expect_tx(q_full, NQ * TILE);
+                    mbar_arrive_expect_tx(q_full, NQ * (QK8 ? PANEL : TILE));
                     for (int i = 0; i < NQ; i++)
-                        for (int half = 0; half < 2; half++)
+                        for (int half = 0; half < (QK8 ? 1 : 2); half++)
                             tma_load_4d(smem + SMEM_Q + i * TILE + half * PANEL, &tm_q, q_full, half * 64, un.h,
                                         un.q0 + i * BM, un.b);
                 }
@@ -160,10 +164,11 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                             break;
                         }
                         const CUtensorMap *tm = kv == 0 ? (map == 0 ? &tm_k : &tm_jk) : (map == 0 ? &tm_v : &tm_jv);
-                        mbar_arrive_expect_tx(&kv_full[slot], TILE);
+                        const bool one_panel = QK8 && kv == 0;  // an e4m3 K tile is one 16 KB panel
+                        mbar_arrive_expect_tx(&kv_full[slot], one_panel ? PANEL : TILE);
                         uint8_t *dst = smem + SMEM_KV + slot * TILE;
                         tma_load_4d(dst, tm, &kv_full[slot], 0, un.h, row, un.b);
-                        tma_load_4d(dst + PANEL, tm, &kv_full[slot], 64, un.h, row, un.b);
+                        if (!one_panel) tma_load_4d(dst + PANEL, tm, &kv_full[slot], 64, un.h, row, un.b);
                     }
                 }
             }
@@ -180,14 +185,22 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
             // (bits 0-13, 16-byte units) moves, so each issue is one 64-bit add.
             const uint64_t dq0 = smem_desc_sw128(sQ, 16, 1024);         // Q / K: K-major, SBO 1024
             const uint64_t dv0 = smem_desc_sw128(sKV, PANEL, 1024);     // V: MN-major, LBO = panel stride
+            // step kk of S_i = Q_i K^T: 16 (bf16/fp16) or 32 (e4m3) head dims, 32 bytes of each row
+            auto s_step = [&](uint32_t d_tmem, uint64_t qa, uint64_t kb, int kk) {
+                if constexpr (QK8) {
+                    const uint64_t off = (uint64_t)(kk * 32) >> 4;
+                    mma_ss_f8(d_tmem, qa + off, kb + off, idesc_qk, kk > 0);
+                } else {
+                    const uint64_t off = (uint64_t)((kk >> 2) * PANEL + (kk & 3) * 32) >> 4;
+                    mma_ss(d_tmem, qa + off, kb + off, idesc_qk, kk > 0);
+                }
+            };
+            constexpr int S_STEPS = QK8 ? D / 32 : D / 16;
             auto issue_s = [&](int i, uint32_t slot) {
                 const uint64_t qa = dq0 + ((uint64_t)(i * TILE) >> 4);
                 const uint64_t kb = dq0 + ((uint64_t)(SMEM_KV - SMEM_Q + slot * TILE) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; kk++) {
-                    const uint64_t off = (uint64_t)((kk >> 2) * PANEL + (kk & 3) * 32) >> 4;
-                    mma_ss(tmem + i * BN, qa + off, kb + off, idesc_qk, kk > 0);
-                }
+                for (int kk = 0; kk < S_STEPS; kk++) s_step(tmem + i * BN, qa, kb, kk);
             };
             // keys [16*k0, 16*k1) of P_i . V
             auto issue_pv = [&](int i, uint32_t slot, bool acc, int k0, int k1) {
@@ -262,8 +275,8 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                         const uint64_t vb = dv0 + ((uint64_t)(vs * TILE) >> 4);
 #pragma unroll
                         for (int kk = 0; kk < D / 16; kk++) {
-                            const uint64_t off = (uint64_t)((kk >> 2) * PANEL + (kk & 3) * 32) >> 4;
-                            mma_ss(tmem, dq0 + off, kb + off, idesc_qk, kk > 0);  // S0(j+1)
+                            // S0(j+1): one step per P.V step (16-bit q/k), or on every other one (e4m3)
+                            if (!QK8 || kk % 2 == 0) s_step(tmem, dq0, kb, QK8 ? kk / 2 : kk);
                             if (kk % MMA_PER_PART == 0) {
                                 if (!(ok = mbar_wait(&p_part[P_PARTS + kk / MMA_PER_PART], ph, w))) break;
                                 tc_fence_after();
@@ -477,14 +490,18 @@ cudaError_t launch_attn_tc(const Geom &g, const void *q, const void *k, const vo
     // an empty segment never issues loads; give its maps a valid stand-in
     const void *kk = has_video ? k : jk, *vv = has_video ? v : jv;
     const long kv_rows = has_video ? g.Nv : g.Nj;
-    // the tile copies move 2-byte elements; fp16 q/k travel through the same maps
-    if (!make_bshd_map(&mq, q, g.Sq, g.H, g.B, false, why) || !make_bshd_map(&mk, kk, kv_rows, g.H, g.B, false, why) ||
+    // the tile copies move 2-byte elements (fp16 q/k travel through the same maps), or 1-byte e4m3 q/k
+    const int qkb = opt.qk8 ? 1 : 2;
+    if (!make_bshd_map(&mq, q, g.Sq, g.H, g.B, false, why, qkb) ||
+        !make_bshd_map(&mk, kk, kv_rows, g.H, g.B, false, why, has_video ? qkb : 2) ||
         !make_bshd_map(&mv, vv, kv_rows, g.H, g.B, false, why) ||
-        !make_bshd_map(&mjk, has_joint ? jk : kk, has_joint ? g.Nj : kv_rows, g.H, g.B, false, why) ||
+        !make_bshd_map(&mjk, has_joint ? jk : kk, has_joint ? g.Nj : kv_rows, g.H, g.B, false, why,
+                       has_joint || has_video ? qkb : 2) ||
         !make_bshd_map(&mjv, has_joint ? jv : vv, has_joint ? g.Nj : kv_rows, g.H, g.B, false, why))
         return cudaErrorInvalidValue;
-    cudaError_t attr_err = set_max_dynamic_smem((const void *)attn_tc_kernel<false>, tc::SMEM_ALLOC);
-    if (attr_err == cudaSuccess) attr_err = set_max_dynamic_smem((const void *)attn_tc_kernel<true>, tc::SMEM_ALLOC);
+    auto kernel = opt.qk8 ? (opt.row_bound ? attn_tc_kernel<true, true> : attn_tc_kernel<false, true>)
+                          : (opt.row_bound ? attn_tc_kernel<true, false> : attn_tc_kernel<false, false>);
+    cudaError_t attr_err = set_max_dynamic_smem((const void *)kernel, tc::SMEM_ALLOC);
     if (attr_err != cudaSuccess) return attr_err;
     TcParams p;
     p.S = g.S;
@@ -502,9 +519,10 @@ cudaError_t launch_attn_tc(const Geom &g, const void *q, const void *k, const vo
     p.wait_limit_ns = opt.wait_limit_ns;
     p.err = opt.err;
     p.strict_order = opt.strict_order;
-    // Q.K^T operands: bf16 (A/B format 1) or fp16 (format 0); P.V stays bf16
-    p.idesc_qk = opt.qk_f16 ? (idesc_bf16_f32(tc::BM, tc::BN, false) & ~((7u << 7) | (7u << 10)))
-                            : idesc_bf16_f32(tc::BM, tc::BN, false);
+    // Q.K^T operands: bf16 (A/B format 1), fp16 (format 0) or e4m3 (kind::f8f6f4, format 0); P.V stays bf16
+    p.idesc_qk = opt.qk8      ? idesc_e4m3_f32(tc::BM, tc::BN)
+                 : opt.qk_f16 ? (idesc_bf16_f32(tc::BM, tc::BN, false) & ~((7u << 7) | (7u << 10)))
+                              : idesc_bf16_f32(tc::BM, tc::BN, false);
     p.units = (long)g.B * g.H * n_chunks * p.q_pairs;
     if (p.units == 0) return cudaSuccess;
     if (p.units >= (1L << 31)) {
@@ -526,10 +544,7 @@ cudaError_t launch_attn_tc(const Geom &g, const void *q, const void *k, const vo
     // round-robin over SMs.
     const long grid = p.units / p.group;
     p.row_bound = opt.row_bound;
-    if (opt.row_bound)
-        attn_tc_kernel<true><<<(unsigned)grid, tc::THREADS, tc::SMEM_ALLOC, st>>>(mq, mk, mv, mjk, mjv, p);
-    else
-        attn_tc_kernel<false><<<(unsigned)grid, tc::THREADS, tc::SMEM_ALLOC, st>>>(mq, mk, mv, mjk, mjv, p);
+    kernel<<<(unsigned)grid, tc::THREADS, tc::SMEM_ALLOC, st>>>(mq, mk, mv, mjk, mjv, p);
     return cudaGetLastError();
 }
 

@@ -58,18 +58,24 @@ unsigned long long current_context_id() {
     return id;
 }
 
-bool make_bshd_map(CUtensorMap *m, const void *base, long rows, int H, int B, bool f16, const char **why) {
+bool make_bshd_map(CUtensorMap *m, const void *base, long rows, int H, int B, bool f16, const char **why,
+                   int elem_bytes) {
     const DriverFns &f = driver();
     if (!f.encode) {
         if (why) *why = "cuTensorMapEncodeTiled is not available from the driver";
         return false;
     }
     constexpr int D = 128;
+    const cuuint64_t eb = (cuuint64_t)elem_bytes;
     cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows, (cuuint64_t)B};
-    cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)rows * H * D * 2};
-    cuuint32_t box[4] = {64, 1, 128, 1};
+    cuuint64_t strides[3] = {(cuuint64_t)D * eb, (cuuint64_t)H * D * eb, (cuuint64_t)rows * H * D * eb};
+    // one 128-byte row of the swizzle atom per box row: 64 2-byte or 128 1-byte elements
+    cuuint32_t box[4] = {elem_bytes == 1 ? 128u : 64u, 1, 128, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
-    if (f.encode(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+    const CUtensorMapDataType type = elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                     : f16          ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (f.encode(m, type, 4,
                  const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {

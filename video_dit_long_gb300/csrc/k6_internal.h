@@ -46,9 +46,11 @@ k6attn_status check_handle(const char *fn, k6attn_t h);
 
 // Unique id of the calling thread's current CUDA context; 0 when none is current.
 unsigned long long current_context_id();
-// Tensor map over a BSHD tensor [B][rows][H][128] of 2-byte elements: box = 64
-// dims x 1 head x 128 rows x 1 batch, 128-byte swizzle, zero fill out of bounds.
-bool make_bshd_map(CUtensorMap *m, const void *base, long rows, int H, int B, bool f16, const char **why);
+// Tensor map over a BSHD tensor [B][rows][H][128] of 2-byte elements (box = 64
+// dims x 1 head x 128 rows x 1 batch) or 1-byte elements (box = 128 dims x 1 x
+// 128 x 1): 128-byte box rows, 128-byte swizzle, zero fill out of bounds.
+bool make_bshd_map(CUtensorMap *m, const void *base, long rows, int H, int B, bool f16, const char **why,
+                   int elem_bytes = 2);
 // Opt `func` in to `bytes` of dynamic shared memory in the current context
 // (once per kernel and context).
 cudaError_t set_max_dynamic_smem(const void *func, int bytes);
@@ -75,7 +77,7 @@ cudaError_t launch_rope_qk(const Geom &g, const float2 *tables, const void *src_
 
 // Merge of n partials of problem g (P = 1), or of the P*B problems of g.H/P
 // heads of a P-way head split of g, written to g's sequence layout.
-// Rotary of q/k/joint_k (into qk_out: BF16 or F16) and the P-way
+// Rotary of q/k/joint_k (into qk_out: BF16, F16 or E4M3) and the P-way
 // sequence->head split of q, k, joint_k, v, joint_v (index order) of a bf16
 // d = 128 problem g: dst[t] is [P][B][rows_t][H/P][128].
 cudaError_t launch_rope_split(const Geom &g, const float2 *tables, const void *const src[5], void *const dst[5],
@@ -102,6 +104,7 @@ struct AttnTcOptions {
     int strict_order;        // 1: wait for P.V to finish before reusing its TMEM
     int qk_f16;              // 1: q/k/joint_k are fp16 (Q.K^T in fp16), else bf16
     const float *row_bound = nullptr;  // constant-max softmax bounds [B][H][Sq] (natural-log units), or null
+    int qk8 = 0;             // 1: q/k/joint_k are e4m3 (Q.K^T on kind::f8f6f4); two-tile kernel only
     int group = 0;           // chunks per CTA (divides n_chunks); 0: the library's choice, chunk_group()
     int merge = 0;           // 1: each CTA's group of chunks leaves one partial (n_chunks / group partials)
 };

@@ -16,6 +16,7 @@
 // per 8 bf16 (or 4 f32) elements; Q, K and joint K are rotated in one launch.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include <type_traits>
 
@@ -385,7 +386,7 @@ __global__ void __launch_bounds__(256) rope_split_kernel(SplitArgs a, const floa
         const unsigned seq = (unsigned)a.seq[which];  // 32-bit: the host keeps B*S*H below 2^31
         const unsigned b = (unsigned)local / seq, n = (unsigned)local - b * seq;
         const uint4 *src = static_cast<const uint4 *>(a.src[which]) + local * vpt;
-        uint4 *dst = static_cast<uint4 *>(a.dst[which]);
+        char *dst = static_cast<char *>(a.dst[which]);
         for (int base = 0; base < vpt; base += 32 * kU) {
             uint4 x[kU];
 #pragma unroll
@@ -398,9 +399,10 @@ __global__ void __launch_bounds__(256) rope_split_kernel(SplitArgs a, const floa
                 const int v = base + 32 * u + lane;
                 if (v >= vpt) continue;
                 const int p = v / vpp;
-                uint4 *to = dst + ((long)((unsigned)p * a.B + b) * seq + n) * vpp + (v - p * vpp);
+                // first element of the vector in the destination [P][B][rows][Hl][128]
+                const long e0 = ((long)((unsigned)p * a.B + b) * seq + n) * (vpp * 8) + (long)(v - p * vpp) * 8;
                 if (!rot) {
-                    __stcs(to, x[u]);
+                    __stcs(reinterpret_cast<uint4 *>(dst + e0 * 2), x[u]);
                     continue;
                 }
                 float f[8];
@@ -415,9 +417,25 @@ __global__ void __launch_bounds__(256) rope_split_kernel(SplitArgs a, const floa
 #pragma unroll
                     for (int k = 0; k < 8; k++) bad |= !(fabsf(f[k]) < 65520.f);  // a finite half
                 }
-                uint4 y;
-                Vec<TQK>::store(&y, f);
-                __stcs(to, y);
+                if constexpr (sizeof(TQK) == 1) {
+                    // e4m3, round to nearest even; beyond +-448 saturates and is reported
+                    uint32_t w[2];
+#pragma unroll
+                    for (int k = 0; k < 8; k++) bad |= !(fabsf(f[k]) <= 448.f);
+#pragma unroll
+                    for (int k = 0; k < 2; k++) {
+                        const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(f[4 * k], f[4 * k + 1]), __NV_SATFINITE,
+                                                                     __NV_E4M3);
+                        const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(f[4 * k + 2], f[4 * k + 3]),
+                                                                     __NV_SATFINITE, __NV_E4M3);
+                        w[k] = lo | (hi << 16);
+                    }
+                    __stcs(reinterpret_cast<uint2 *>(dst + e0), make_uint2(w[0], w[1]));
+                } else {
+                    uint4 y;
+                    Vec<TQK>::store(&y, f);
+                    __stcs(reinterpret_cast<uint4 *>(dst + e0 * 2), y);
+                }
             }
         }
     }
@@ -479,6 +497,7 @@ cudaError_t launch_rope_split(const Geom &g, const float2 *tables, const void *c
         kernel<<<(unsigned)blocks, 256, 0, st>>>(a, tables);
     };
     if (qk_out == K6ATTN_F16) launch(rope_split_kernel<__half>);
+    else if (qk_out == K6ATTN_E4M3) launch(rope_split_kernel<__nv_fp8_e4m3>);
     else launch(rope_split_kernel<__nv_bfloat16>);
     return cudaGetLastError();
 }

@@ -56,14 +56,46 @@ def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
     return (np.ascontiguousarray(bits, np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
+def _e4m3_value(code: int) -> float:
+    """Value of a non-negative e4m3 code (1 sign, 4 exponent bits of bias 7, 3 mantissa bits;
+    exponent 0 is subnormal, m * 2^-9; code 127 is NaN, there is no infinity)."""
+    e, m = (code >> 3) & 0xF, code & 7
+    if e == 0:
+        return m * 2.0**-9
+    return (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+_E4M3_POS = np.array([_e4m3_value(c) for c in range(127)], np.float64)  # codes 0..126, ascending; 448 = max
+
+
+def e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """Round to e4m3, nearest with ties to the even code, saturating at +-448; the bit patterns (uint8)."""
+    x = np.asarray(x, np.float64)
+    a = np.minimum(np.abs(x), 448.0)
+    i = np.clip(np.searchsorted(_E4M3_POS, a), 1, 126)
+    lo, hi = _E4M3_POS[i - 1], _E4M3_POS[i]
+    pick_hi = (hi - a < a - lo) | ((hi - a == a - lo) & (i % 2 == 0))
+    code = np.where(pick_hi, i, i - 1).astype(np.uint8)
+    return code | (np.signbit(x).astype(np.uint8) << 7)
+
+
+def e4m3_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of e4m3 bit patterns (no NaN codes expected) to float32."""
+    b = np.asarray(bits, np.uint8)
+    v = _E4M3_POS[np.minimum(b & 0x7F, 126)].astype(np.float32)
+    return np.where(b & 0x80, -v, v).astype(np.float32)
+
+
 def tensor(seed: int, tensor_id: int, shape, dtype: str, std: float = 1.0) -> np.ndarray:
-    """A seeded N(0, std^2) tensor stored as float32 or as bf16 bits (uint16)."""
+    """A seeded N(0, std^2) tensor stored as float32, as bf16 bits (uint16) or as e4m3 bits (uint8)."""
     n = int(np.prod(shape))
     x = normal_f32(seed, tensor_id, n, std)
     if dtype == "bf16":
         return bf16_bits(x).reshape(shape)
     if dtype == "f32":
         return x.reshape(shape)
+    if dtype == "e4m3":
+        return e4m3_bits(x).reshape(shape)
     raise ValueError(dtype)
 
 

@@ -14,7 +14,7 @@ import os
 from . import build as _build
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_RANGE = range(7)
-BF16, F32, F16 = 0, 1, 2
+BF16, F32, F16, E4M3 = 0, 1, 2, 3
 OPT_WAIT_LIMIT_NS, OPT_STRICT_MMA_ORDER, OPT_ROTATE_BF16 = 0, 1, 2
 
 # every symbol the header declares

@@ -35,7 +35,9 @@ class UlyssesStep:
     # rows of the hot path as timed by step(ev): names of the intervals between its events
     intervals = ("rope_split_heads", "attention_chunk_groups", "lse_merge_heads")
 
-    def __init__(self, w, n_chunks: int, P: int, x: dict):
+    def __init__(self, w, n_chunks: int, P: int, x: dict, qk: str = "f16"):
+        """qk: the type of the rotated q/k copies, "f16" (the default path) or "e4m3" (the FP8 mode:
+        Q.K^T on 8-bit operands)."""
         import torch
         self.torch = torch
         self.w, self.n, self.P = w, n_chunks, P
@@ -56,7 +58,11 @@ class UlyssesStep:
         # attention runs on the head-partitioned layout: P*B independent problems of H/P heads
         self.h = K.Handle(P * B, self.Hl, d, "bf16", w.grid, Nj, w.axis_dim, w.theta, w.joint_rope)
         rows = {"q": S, "k": Nv, "v": Nv, "jk": Nj, "jv": Nj}
-        self.head = {k: torch.empty((P * B, r, self.Hl, d), dtype=f16 if k in ("q", "k", "jk") else bf,
+        if qk not in ("f16", "e4m3"):
+            raise ValueError(qk)
+        self.qk_code = K.F16 if qk == "f16" else K.E4M3
+        qk_t = f16 if qk == "f16" else torch.uint8
+        self.head = {k: torch.empty((P * B, r, self.Hl, d), dtype=qk_t if k in ("q", "k", "jk") else bf,
                                     device="cuda") for k, r in rows.items()}
         # chunks per CTA: the library's choice, kept below n so that the merge has partials to combine
         g = self.h.chunk_group(n_chunks)
@@ -82,10 +88,10 @@ class UlyssesStep:
         mark(0)
         self.hs.rope_split_heads(seq["q"], seq["k"], seq["v"], seq["jk"] if j else None, seq["jv"] if j else None,
                                  self.P, hd["q"], hd["k"], hd["v"], hd["jk"] if j else None,
-                                 hd["jv"] if j else None, qk_out_dtype=K.F16)
+                                 hd["jv"] if j else None, qk_out_dtype=self.qk_code)
         mark(1)
         self.h.attention_chunk_groups(hd["q"], hd["k"], hd["v"], hd["jk"] if j else None, hd["jv"] if j else None,
-                                      self.n, self.group, self.part_o, self.part_lse, qk_dtype=K.F16)
+                                      self.n, self.group, self.part_o, self.part_lse, qk_dtype=self.qk_code)
         mark(2)
         self.hs.lse_merge_heads(self.part_o, self.part_lse, self.parts, self.P, out, lse)
         mark(3)
