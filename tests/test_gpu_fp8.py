@@ -165,3 +165,24 @@ def test_fp8_step_on_the_pro_workload():
     print("fp8 pro: vs quantised oracle", m, "vs exact oracle: rel-L2", rel, "max-abs", float(np.abs(out - ref).max()),
           "lse", float(np.abs(lse - ref_lse).max()))
     assert rel <= FP8_REL_L2
+
+
+def test_e4m3_saturation_is_reported():
+    """A rotated value beyond +-448 is stored as +-448 and reported as ERR_RANGE at sync (at grid position 0
+    the rotation is the identity, so the input value itself is the rotated one)."""
+    w = CASES["ragged"]
+    k6 = K()
+    x = inputs.make_inputs(w)
+    x["q"][0, 0, 1, 5] = inputs.bf16_bits(np.array([600.0], np.float32))[0]
+    d = {n: to_dev(x[n], "bf16") for n in ("q", "k", "v", "jk", "jv")}
+    h = k6.Handle.for_workload(w)
+    rows = {"q": w.S, "k": w.Nv, "v": w.Nv, "jk": w.Nj, "jv": w.Nj}
+    out = {n: torch.empty((w.B, r, w.H, w.d), dtype=torch.uint8 if n in ("q", "k", "jk") else torch.bfloat16,
+                          device="cuda") for n, r in rows.items()}
+    h.rope_split_heads(d["q"], d["k"], d["v"], d["jk"], d["jv"], 1, out["q"], out["k"], out["v"], out["jk"],
+                       out["jv"], qk_out_dtype=k6.E4M3)
+    with pytest.raises(k6.K6Error) as e:
+        h.sync()
+    assert e.value.status == k6.ERR_RANGE
+    assert inputs.e4m3_to_f32(out["q"][0, 0, 1, 5].cpu().numpy()) == 448.0
+    h.sync()  # the error word was cleared
