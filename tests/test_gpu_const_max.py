@@ -115,3 +115,34 @@ def test_bounded_chunk_groups_match_oracle(name, n, group):
     ref, ref_lse = O.attention(geom(w), x["q"], x["k"], x["v"], x["jk"] if w.Nj else None,
                                x["jv"] if w.Nj else None)
     compare(to_host(out), ref, lse.cpu().numpy().astype(np.float64), ref_lse, "bf16")
+
+
+@pytest.mark.slow
+def test_bounded_step_on_the_pro_workload_matches_oracle():
+    """The constant-max variant as the benchmark times it: row bounds, bounded attention over the 8 chunks in
+    the step's chunk groups on the head layout, merge into the sequence layout; 1024 sampled query rows x all
+    heads x all keys of the Pro workload against the oracle."""
+    from video_dit_long_gb300 import k6attn as K
+    from video_dit_long_gb300.step import UlyssesStep
+    from .helpers import oracle_sampled
+    w = configs.WORKLOADS["pro"]
+    x = inputs.make_inputs(w)
+    st = UlyssesStep(w, 8, 8, x)
+    st.step()
+    hd = st.head
+    bounds = torch.empty(st.h.row_bounds_bytes() // 4, dtype=torch.float32, device="cuda")
+    st.h.row_bounds(hd["q"], hd["k"], hd["jk"], bounds, qk_dtype=K.F16)
+    st.h.attention_chunk_groups_bounded(hd["q"], hd["k"], hd["v"], hd["jk"], hd["jv"], bounds, 8, st.group,
+                                        st.part_o, st.part_lse, qk_dtype=K.F16)
+    out = torch.empty_like(st.out)
+    lse = torch.empty_like(st.lse)
+    st.hs.lse_merge_heads(st.part_o, st.part_lse, st.parts, 8, out, lse)
+    st.sync()
+    rows = inputs.sample_rows(w.S, w.Nv, w.S // 8, count=1024)
+    idx = torch.from_numpy(rows).cuda()
+    got = to_host(out.index_select(1, idx))
+    got_lse = lse.index_select(2, idx).cpu().numpy().astype(np.float64)
+    del st
+    torch.cuda.empty_cache()
+    ref, ref_lse = oracle_sampled(w, x, rows)
+    print(compare(got, ref, got_lse, ref_lse, "bf16"))
