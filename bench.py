@@ -182,6 +182,34 @@ class Path(UlyssesStep):
                                     qk_dtype=K.F16)
         return self.pc_o, self.pc_lse
 
+    def standalone_rows(self, steps):
+        """The unfused a1 and a4 rows alone, each one launch on the Pro buffers: rotary of q/k/joint_k into
+        fp16 copies (sequence layout), the seq->head relayout of q, k, v, joint_k, joint_v (bf16) and the
+        head->seq relayout of one output-sized tensor.  Returns ms per call of each."""
+        torch, w, P = self.torch, self.w, self.P
+        rows = {"q": w.S, "k": w.Nv, "v": w.Nv, "jk": w.Nj, "jv": w.Nj}
+        rot = {n: torch.empty(self.seq[n].shape, dtype=torch.float16, device="cuda") for n in ("q", "k", "jk")}
+        head = {n: torch.empty_like(self.seq[n]) for n in rows}
+        j = w.Nj > 0
+
+        def rope():
+            self.hs.rope_qk(self.seq["q"], self.seq["k"], self.seq["jk"] if j else None, q_out=rot["q"],
+                            k_out=rot["k"], joint_k_out=rot["jk"] if j else None, out_dtype=K.F16)
+
+        def relayout_in():
+            for n, r in rows.items():
+                if r:
+                    K.seq2head_relayout(self.seq[n], head[n], w.B, r, w.H, w.d, P, 0)
+
+        def relayout_out():  # an output-sized bf16 tensor, head -> seq (into the fp16 buffer of the same size)
+            K.seq2head_relayout(head["q"], rot["q"], w.B, w.S, w.H, w.d, P, 1)
+
+        res = {"rope_qk": time_calls(rope, steps), "relayout_seq2head_qkv": time_calls(relayout_in, steps),
+               "relayout_head2seq_out": time_calls(relayout_out, steps)}
+        self.hs.sync()
+        del rot, head
+        return res
+
     def merge_per_chunk(self):
         """The LSE merge of one partial per chunk (n of them) into the sequence layout."""
         po, pl = self.chunk_partials()
@@ -339,6 +367,7 @@ def measure(w, n_chunks, P, steps, warmup, dist_on, with_e2e=True, clocks=True, 
     # the LSE merge of one partial per chunk (the workload's n), into the sequence layout
     if not step_only:
         res["merge_per_chunk_ms"] = time_calls(path.merge_per_chunk, steps)
+        res["standalone_ms"] = path.standalone_rows(steps)
         path.sync()
     if with_e2e and not step_only:
         # the constant-max variant of attention + merge on the same buffers
@@ -563,6 +592,12 @@ def run_ours(args, rank, world, dist_on):
     }
     if "merge_per_chunk_ms" in res:  # secondary: the merge of one partial per chunk (not part of the step)
         kernels["lse_merge_per_chunk"] = hbm_rec(merge_bytes(w, n), res["merge_per_chunk_ms"])
+    if "standalone_ms" in res:  # secondary: the unfused a1 and a4 rows, each alone
+        sa = res["standalone_ms"]
+        qkj = (w.S + w.Nv + w.Nj) * w.H * w.d * 2
+        kernels["standalone_rope_qk"] = hbm_rec(2 * qkj, sa["rope_qk"])
+        kernels["standalone_relayout_seq2head_qkv"] = hbm_rec(prologue_bytes(w), sa["relayout_seq2head_qkv"])
+        kernels["standalone_relayout_head2seq_out"] = hbm_rec(2 * w.S * w.H * w.d * 2, sa["relayout_head2seq_out"])
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
