@@ -88,9 +88,11 @@ static k6attn_status run_attention(k6attn_handle *h, const Geom &g, const void *
         AttnTcOptions opt{h->wait_limit_ns, h->err,    h->strict_order, qk_f16 ? 1 : 0, row_bound,
                           qk8 ? 1 : 0,      group,     merge ? 1 : 0};
         const char *why = nullptr;
-        // a query range of one 128-row tile runs the single-tile kernel
-        cudaError_t e = (g.Sq <= 128 ? launch_attn_tc_single : launch_attn_tc)(g, q, k, v, jk, jv, n_chunks, out, lse,
-                                                                           opt, st, &why);
+        // 16-bit q/k run the single-tile kernel (one 128-row Q tile per CTA, faster at
+        // every query length measured); e4m3 q/k the two-tile kernel, which has the
+        // 8-bit Q.K^T path
+        cudaError_t e = (qk8 ? launch_attn_tc : launch_attn_tc_single)(g, q, k, v, jk, jv, n_chunks, out, lse, opt,
+                                                                       st, &why);
         if (e != cudaSuccess) {
             if (why) return set_error(K6ATTN_ERR_CUDA, "attention: %s", why);
             return cuda_check(e, "attention launch");

@@ -24,7 +24,8 @@ constexpr unsigned long long DRAIN_NS = 1000000000ull;
 struct TcParams {
     long S, Nv, Nj;                           // keys (video then joint)
     long Sq;                                  // query rows
-    int H, n_chunks, q_pairs;
+    int H, n_chunks, q_pairs;                 // q_pairs: query units per (b, h), of unit_rows rows
+    int unit_rows;                            // query rows per work unit: NQ * BM (two-tile kernel) or BM
     float scale_log2;                         // log2(e) / sqrt(d)
     void *out;                                // bf16 [B][S][H][d] or fp32 partials
     float *lse;
@@ -74,10 +75,10 @@ __device__ __forceinline__ TileRange chunk_tiles(const TcParams &p, int c) {
     return t;
 }
 
-// Work unit u -> (b, h, chunk group, query-tile pair, chunk within the group),
+// Work unit u -> (b, h, chunk group, query unit, chunk within the group),
 // the chunk within the group fastest: CTA x owns units [x*group, (x+1)*group),
-// one Q tile pair over `group` consecutive chunks.  Across CTAs the query-tile
-// pair varies fastest, so the CTAs running at the same time walk through the
+// one query unit (a Q tile pair, or one Q tile) over `group` consecutive
+// chunks.  Across CTAs the query unit varies fastest, so the CTAs running at the same time walk through the
 // same chunks and share their K/V in L2.
 struct Unit {
     int b, h, c, q0;
@@ -95,7 +96,7 @@ __device__ __forceinline__ Unit decode_unit(const TcParams &p, long unit) {
     r.c = (int)(cg * p.group + g);
     r.h = (int)(u % (uint32_t)p.H);
     r.b = (int)(u / (uint32_t)p.H);
-    r.q0 = (int)qp * (tc::NQ * tc::BM);
+    r.q0 = (int)qp * p.unit_rows;
     return r;
 }
 

@@ -1,29 +1,28 @@
-// k6_attn_single.cu -- the bf16 tensor-core attention of k6_attn_tc.cu for a
-// query range of at most one 128-row tile: cross-attention from a short text
-// or audio segment, or a self-attention call of at most 128 tokens.
+// k6_attn_single.cu -- the bf16 tensor-core attention of k6_attn_tc.cu with one
+// 128-row Q tile per CTA.  It runs query ranges of at most one tile
+// (cross-attention from a short text or audio segment, self-attention calls of
+// at most 128 tokens), where the two-tile kernel would spend half its MMAs on
+// padding rows, and it takes longer ranges too (one CTA per Q tile).
 //
 // Same result as attn_tc_kernel (per K/V chunk: O_c = softmax(Q K^T / sqrt(d)) V
 // and its log-sum-exp, non-causal, K/V = video keys then joint tokens), same
-// launch parameters, work units and outputs.  With one Q tile per CTA the
-// two-tile kernel would leave half its tensor-core work on padding rows and,
-// with no second tile to interleave, run one dependent MMA chain at a time.
-// This kernel instead:
+// launch parameters, work units (of one Q tile) and outputs.  This kernel:
 //   - keeps S in three tensor-memory buffers (S(n) in buffer n % 3; O in the
-//     last 128 columns), so that MMA block j issues S(j+2) = Q K_{j+2}^T and
-//     P(j).V_j interleaved MMA by MMA (two independent accumulator chains)
-//     while the softmax works on S(j+1);
+//     last 128 columns), so that S(n+1) and S(n+2) can be computed while the
+//     softmax works on S(n);
+//   - issues MMAs from two threads on different sub-partitions, Q.K^T from one
+//     and P.V from the other, with S(n) waiting only for the P.V of tile n-3
+//     whose P its buffer held;
 //   - splits each row's softmax between the two softmax warpgroups: warpgroup
 //     hf owns keys [64 hf, 64 hf + 64) of every S tile and columns
 //     [64 hf, 64 hf + 64) of O, for the same 128 rows (warps w and w + 4 reach
 //     the same TMEM lanes); the halves meet in shared memory behind a named
 //     barrier of those two warps (row max once per tile, row sum once per unit);
-//   - loads K/V in the order K_0 K_1 V_0 K_2 V_1 K_3 ..., so that the tiles of
-//     block j go into the ring slots that block j-2 frees;
+//   - loads K/V in the order K_0 K_1 V_0 K_2 V_1 K_3 ..., so that K runs two
+//     tiles ahead of V in the ring;
 //   - with p.merge, merges a CTA's group of chunks into one partial in tensor
 //     memory, as the two-tile kernel does: (m, l, O) carry from one chunk into
 //     the next and only the group's last chunk runs the epilogue.
-// Measured on GB300 (100 audio queries over 51,840 keys, 24 heads, 8 chunks):
-// 0.154 ms against 0.198 ms for the two-tile kernel on the same input.
 // All mbarrier waits are bounded (globaltimer); a wait that runs out records
 // the error, and every warp still passes the same named barriers and leaves in
 // order, letting copies and MMAs in flight land before tensor memory is freed.
@@ -46,14 +45,17 @@ using tc::PANEL;
 using tc::TILE;
 constexpr int NSTAGE = 4;                     // K/V tile slots
 constexpr int NSBUF = 3;                      // S buffers in tensor memory
-constexpr int KP = BN / 2;                    // keys per softmax warpgroup
 constexpr int SMEM_Q = 0;
 constexpr int SMEM_KV = TILE;
 constexpr int SMEM_BAR = SMEM_KV + NSTAGE * TILE;
-// q_full, kv_full/empty, s_full, p_part [tile parity][half], o_final, o_step, drain, pv_done [tile parity]
-constexpr int NBAR = 1 + 2 * NSTAGE + NSBUF + 4 + 1 + 1 + 1 + 2;
+constexpr int P_PARTS = 2;                    // P of a tile is published in this many parts
+constexpr int KP = BN / P_PARTS;              // keys per part
+// q_full, kv_full/empty, s_full, p_part [S buffer][part], o_final, drain, pv_buf [S buffer],
+// m_ready [tile parity][warp], epi [warp], epi_done [warp]
+constexpr int NBAR = 1 + 2 * NSTAGE + NSBUF + NSBUF * P_PARTS + 1 + 1 + NSBUF + 8 + 4 + 4;
 constexpr int SMEM_XCH = (SMEM_BAR + NBAR * 8 + 16 + 15) & ~15;  // + TMEM address word and abort flag
-constexpr int SMEM_TOTAL = SMEM_XCH + 2 * (2 * 2 * BM) * 4;      // row maxima, row sums: [parity][half][row]
+// running row max [row]; epilogue exchange [unit parity][warpgroup][row] of (l, m)
+constexpr int SMEM_TOTAL = SMEM_XCH + (BM + 2 * 2 * 2 * BM) * 4;
 constexpr int SMEM_ALLOC = SMEM_TOTAL + 1024;                   // room to align the base to 1024 bytes
 constexpr int THREADS = 384;                  // softmax halves 0 and 1, producer/MMA/spare
 // Register split (launch: 384 x 168 = 64512): 2*128*184 + 128*136 = 64512.
@@ -76,12 +78,19 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
     uint64_t *kv_full = q_full + 1;
     uint64_t *kv_empty = kv_full + NSTAGE;
     uint64_t *s_full = kv_empty + NSTAGE;  // [NSBUF]
-    uint64_t *p_part = s_full + NSBUF;     // [tile parity][half], 128 arrivals each
-    uint64_t *o_final = p_part + 4;
-    uint64_t *o_step = o_final + 1;
-    uint64_t *drain = o_step + 1;
-    uint64_t *pv_done = drain + 1;         // [tile parity]: P.V of tile n done
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(pv_done + 2);
+    // [S buffer][part], 128 arrivals each.  Indexed by buffer, not by tile parity:
+    // P(n+3), the next completion of the same barrier, needs S(n+3), which waits
+    // for P(n).V, so the P.V thread can never miss a phase.  (By parity, P(n+2)
+    // could complete the barrier a second time while that thread still waits for
+    // a slow V(n) tile.)
+    uint64_t *p_part = s_full + NSBUF;
+    uint64_t *o_final = p_part + NSBUF * P_PARTS;
+    uint64_t *drain = o_final + 1;
+    uint64_t *pv_buf = drain + 1;          // [S buffer]: P.V of the tile in that buffer done
+    uint64_t *m_ready = pv_buf + NSBUF;    // [tile parity][warp % 4]: row max after tile n published
+    uint64_t *epi = m_ready + 8;           // [warp % 4]: both warps of a row pair posted (l, m)
+    uint64_t *epi_done = epi + 4;          // [warp % 4]: both warps of a row pair have read O
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(epi_done + 4);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -93,12 +102,15 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
             mbar_init(&kv_empty[s], 1);
         }
         for (int b = 0; b < NSBUF; b++) mbar_init(&s_full[b], 1);
-        for (int q = 0; q < 4; q++) mbar_init(&p_part[q], BM);
+        for (int q = 0; q < NSBUF * P_PARTS; q++) mbar_init(&p_part[q], BM);
         mbar_init(o_final, 1);
-        mbar_init(o_step, 1);
-        mbar_init(drain, 1);
-        mbar_init(&pv_done[0], 1);
-        mbar_init(&pv_done[1], 1);
+        mbar_init(drain, 2);  // one commit per MMA issuer
+        for (int b = 0; b < NSBUF; b++) mbar_init(&pv_buf[b], 1);
+        for (int q = 0; q < 8; q++) mbar_init(&m_ready[q], 32);
+        for (int q = 0; q < 4; q++) {
+            mbar_init(&epi[q], 64);
+            mbar_init(&epi_done[q], 64);
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -156,166 +168,165 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
             if (uc > 0) mbar_drain(q_full, 0, tc::DRAIN_NS);
             for (uint32_t idx = kv_idx > NSTAGE ? kv_idx - NSTAGE : 0; idx < kv_idx; idx++)
                 mbar_drain(&kv_full[idx % NSTAGE], (idx / NSTAGE) & 1, tc::DRAIN_NS);
-        } else if (warp == 9 && lane == 0) {
-            // --------------------------------------------------- MMA issuer
-            // K/V tile n counts over the CTA's units.  A unit starts with S(0) and
-            // S(1); block j then waits for both halves of P(j) and issues S(j+2) and
-            // P(j).V interleaved MMA by MMA.  S(j+2) overwrites the P of tile j-1,
-            // whose P.V was issued before it (the tensor pipe runs one thread's
-            // MMAs in order; the strict option waits for them instead).
-            // pv_done[n % 2] follows the P.V of tile n.
+        } else if ((warp == 9 || warp == 10) && lane == 0) {
+            // ------------------------------------------------- MMA issuers
+            // Warp 9 issues every S(n) = Q K_n^T, warp 10 every O += P(n).V_n: one
+            // issuing thread would share its sub-partition's issue slots with two
+            // softmax warps and feed the tensor pipe too slowly.  K/V tile n counts
+            // over the CTA's units.  S(n) goes into buffer n % 3, which held P(n-3):
+            // it waits for pv_buf[n % 3], committed after the P.V of tile n-3, so
+            // it never overwrites a P still to be read.  P(n).V waits for the
+            // parts of P(n); pv_buf[n % 3] follows it.
             const uint32_t idesc_qk = p.idesc_qk;
             const uint32_t idesc_pv = idesc_bf16_f32(BM, D, true);
             const uint32_t sQ = smem_u32(smem + SMEM_Q), sKV = smem_u32(smem + SMEM_KV);
             const uint64_t dq0 = smem_desc_sw128(sQ, 16, 1024);      // Q / K: K-major, SBO 1024
             const uint64_t dv0 = smem_desc_sw128(sKV, PANEL, 1024);  // V: MN-major, LBO = panel stride
-            auto k_desc = [&](uint32_t slot) { return dq0 + ((uint64_t)(SMEM_KV - SMEM_Q + slot * TILE) >> 4); };
-            auto issue_s = [&](int sb, uint32_t kslot) {
-                const uint64_t kb = k_desc(kslot);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; kk++) {
-                    const uint64_t off = (uint64_t)((kk >> 2) * PANEL + (kk & 3) * 32) >> 4;
-                    mma_ss(tmem + sb * BN, dq0 + off, kb + off, idesc_qk, kk > 0);
-                }
-            };
-            // S(sb) <- Q K^T (if with_s) interleaved with O += P(pb) V; P half q (keys
-            // [KP q, KP q + KP)) sits over the first KP/2 columns of that half's S columns
-            auto issue_block = [&](bool with_s, int sb, uint32_t kslot, int pb, uint32_t vslot, bool acc) {
-                const uint64_t kb = k_desc(kslot);
-                const uint64_t vb = dv0 + ((uint64_t)(vslot * TILE) >> 4);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; kk++) {
-                    const uint64_t off = (uint64_t)((kk >> 2) * PANEL + (kk & 3) * 32) >> 4;
-                    if (with_s) mma_ss(tmem + sb * BN, dq0 + off, kb + off, idesc_qk, kk > 0);
-                    const int q = kk / (BN / 16 / 2);
-                    mma_ts(tmem + O_COL, tmem + pb * BN + q * KP + (kk - q * (BN / 16 / 2)) * 8,
-                           vb + ((uint64_t)(kk * 16 * 128) >> 4), idesc_pv, (acc || kk > 0) ? 1u : 0u);
-                }
-            };
-            uint32_t step_phase = 0;
-            auto strict_wait = [&]() -> bool {
-                if (!p.strict_order) return true;
-                tc_commit(o_step);
-                const bool done = mbar_wait(o_step, step_phase, w);
-                step_phase ^= 1;
-                return done;
-            };
-            uint32_t kv_idx = 0;   // K/V loads consumed before this unit
-            uint32_t tile = 0;     // K/V tiles of earlier units
+            uint32_t kv_idx = 0;  // K/V loads consumed before this unit
+            uint32_t tile = 0;    // K/V tiles of earlier units
             uint32_t uc = 0;
-            bool started = false;  // any P.V issued yet (the strict hazard exists from then on)
             bool ok = true;
-            for (long u = u0; u < u1 && ok; u++, uc++) {
-                const int T = chunk_tiles(p, decode_unit(p, u).c).T;
-                const bool carry = p.merge && uc > 0;      // O accumulates over the previous chunks
-                const bool last = !p.merge || u + 1 == u1;  // this chunk's O goes to the epilogue
-                ok = uc > 0 || mbar_wait(q_full, 0, w);
-                for (int t = 0; t < 2 && t < T && ok; t++) {
-                    const uint32_t kidx = kv_idx + t;
-                    if (!(ok = mbar_wait(&kv_full[kidx % NSTAGE], (kidx / NSTAGE) & 1, w))) break;
-                    tc_fence_after();
-                    if (started && !(ok = strict_wait())) break;
-                    issue_s((tile + t) % NSBUF, kidx % NSTAGE);
-                    tc_commit(&s_full[(tile + t) % NSBUF]);
-                    tc_commit(&kv_empty[kidx % NSTAGE]);
-                }
-                for (int j = 0; j < T && ok; j++) {
-                    const uint32_t n = tile + j;
-                    const uint32_t vidx = kv_idx + (j + 2 < T ? j + 2 : T) + j;  // V(j)
-                    const uint32_t kidx = kv_idx + 2 * j + 3;                      // K(j+2)
-                    const bool with_s = j + 2 < T;
-                    if (with_s && !(ok = mbar_wait(&kv_full[kidx % NSTAGE], (kidx / NSTAGE) & 1, w))) break;
-                    if (!(ok = mbar_wait(&kv_full[vidx % NSTAGE], (vidx / NSTAGE) & 1, w) &&
-                               mbar_wait(&p_part[(n & 1) * 2], (n >> 1) & 1, w) &&
-                               mbar_wait(&p_part[(n & 1) * 2 + 1], (n >> 1) & 1, w)))
-                        break;
-                    tc_fence_after();
-                    if (with_s && started && !(ok = strict_wait())) break;
-                    issue_block(with_s, (n + 2) % NSBUF, kidx % NSTAGE, n % NSBUF, vidx % NSTAGE, carry || j > 0);
-                    started = true;
-                    tc_commit(&pv_done[n & 1]);
-                    if (with_s) {
-                        tc_commit(&s_full[(n + 2) % NSBUF]);
+            if (warp == 9) {
+                for (long u = u0; u < u1 && ok; u++, uc++) {
+                    const int T = chunk_tiles(p, decode_unit(p, u).c).T;
+                    ok = uc > 0 || mbar_wait(q_full, 0, w);
+                    for (int t = 0; t < T && ok; t++) {
+                        const uint32_t n = tile + t;
+                        // loads run K_0 K_1 V_0 K_2 V_1 K_3 ...: K_t is load 2t - 1 of the unit for t >= 2
+                        const uint32_t kidx = kv_idx + (t < 2 ? t : 2 * t - 1);
+                        if (!(ok = mbar_wait(&kv_full[kidx % NSTAGE], (kidx / NSTAGE) & 1, w))) break;
+                        if (n >= NSBUF && !(ok = mbar_wait(&pv_buf[n % NSBUF], (n / NSBUF - 1) & 1, w))) break;
+                        tc_fence_after();
+                        const uint64_t kb = dq0 + ((uint64_t)(SMEM_KV - SMEM_Q + (kidx % NSTAGE) * TILE) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; kk++) {
+                            const uint64_t off = (uint64_t)((kk >> 2) * PANEL + (kk & 3) * 32) >> 4;
+                            mma_ss(tmem + (n % NSBUF) * BN, dq0 + off, kb + off, idesc_qk, kk > 0);
+                        }
+                        tc_commit(&s_full[n % NSBUF]);
                         tc_commit(&kv_empty[kidx % NSTAGE]);
                     }
-                    tc_commit(&kv_empty[vidx % NSTAGE]);
-                    if (j + 1 == T && last) tc_commit(o_final);
+                    kv_idx += 2 * T;
+                    tile += T;
                 }
-                kv_idx += 2 * T;
-                tile += T;
+            } else {
+                for (long u = u0; u < u1 && ok; u++, uc++) {
+                    const int T = chunk_tiles(p, decode_unit(p, u).c).T;
+                    const bool carry = p.merge && uc > 0;      // O accumulates over the previous chunks
+                    const bool last = !p.merge || u + 1 == u1;  // this chunk's O goes to the epilogue
+                    for (int j = 0; j < T && ok; j++) {
+                        const uint32_t n = tile + j;
+                        const uint32_t vidx = kv_idx + (j + 2 < T ? j + 2 : T) + j;  // V_j
+                        if (!(ok = mbar_wait(&kv_full[vidx % NSTAGE], (vidx / NSTAGE) & 1, w))) break;
+                        // P(n) (bf16, keys in order) sits over the first BN/2 columns of its buffer;
+                        // each part's P.V starts as soon as the softmax has published that part
+                        const uint64_t vb = dv0 + ((uint64_t)((vidx % NSTAGE) * TILE) >> 4);
+                        const uint32_t pb = tmem + (n % NSBUF) * BN;
+                        for (int q = 0; q < P_PARTS && ok; q++) {
+                            if (!(ok = mbar_wait(&p_part[(n % NSBUF) * P_PARTS + q], (n / NSBUF) & 1, w))) break;
+                            tc_fence_after();
+#pragma unroll
+                            for (int kk = q * (KP / 16); kk < (q + 1) * (KP / 16); kk++)
+                                mma_ts(tmem + O_COL, pb + kk * 8, vb + ((uint64_t)(kk * 16 * 128) >> 4), idesc_pv,
+                                       (carry || j > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        if (!ok) break;
+                        tc_commit(&pv_buf[n % NSBUF]);
+                        tc_commit(&kv_empty[vidx % NSTAGE]);
+                        if (j + 1 == T && last) tc_commit(o_final);
+                    }
+                    kv_idx += 2 * T;
+                    tile += T;
+                }
             }
             // every MMA issued so far must complete before tensor memory is freed
+            // (the drain barrier counts one commit per issuer)
             tc_commit(drain);
             mbar_drain(drain, 0, tc::DRAIN_NS);
         }
         __syncwarp();
     } else {
         regs_increase<REGS_SOFTMAX>();
-        // ------------------------------------------- softmax / epilogue (half hf)
-        // Both warps of a pair pass the same named barriers whatever happens, also
-        // after a wait has given up, so that neither is left waiting at one.
-        const int hf = warp / 4;
+        // ------------------------------------ softmax / epilogue (warpgroup hf)
+        // Warpgroup hf takes the K/V tiles n with n % 2 == hf, whole rows (thread =
+        // row = TMEM lane; warps w and w + 4 reach the same lanes), so that each
+        // group has two tiles' time for one tile's softmax.  The groups share the
+        // row's running max: tile n's owner waits for the max after tile n-1
+        // (m_ready), takes the new max, posts it and only then computes P(n).  The
+        // max moves, and O is rescaled in tensor memory, only when the tile max
+        // exceeds it by 2^8 (a lazy rescale: the same stale max scales numerator
+        // and denominator).  Each group keeps the row sum of its own tiles,
+        // expressed in the max it last saw; the epilogue combines the two.
+        const int hf = warp / 4, wq = warp % 4;
         const int r = threadIdx.x % BM;
-        const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp % 4)) << 16);
-        const uint32_t tO = lane_base + O_COL + hf * (D / 2);
-        float *xmax = reinterpret_cast<float *>(smem + SMEM_XCH);  // [tile parity][half][row]
-        float *xsum = xmax + 2 * 2 * BM;                           // [unit parity][half][row]
-        const uint32_t pair_bar = 1 + warp % 4;                    // warps w and w + 4
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * wq) << 16);
+        const uint32_t tO = lane_base + O_COL;
+        float *xm = reinterpret_cast<float *>(smem + SMEM_XCH);  // [row]: max after the latest tile
+        float *xe = xm + BM;                                      // [unit parity][group][row][l, m]
         const float sl2 = p.scale_log2;
         uint32_t tile = 0, uc = 0, n_epi = 0;
         bool ok = true;
-        float m_run = -INFINITY, l_run = 0.f;
-        for (long u = u0; u < u1; u++, uc++) {
+        float m_run = -INFINITY;  // the row max in force after the latest tile of this unit
+        float m_own = -INFINITY;  // the max l_own is expressed in
+        float l_own = 0.f;        // row sum over this group's tiles
+        for (long u = u0; u < u1 && ok; u++, uc++) {
             const Unit un = decode_unit(p, u);
             const TileRange tr = chunk_tiles(p, un.c);
             const int T = tr.T;
             const bool carry = p.merge && uc > 0;      // (m, l, O) of the previous chunks carry over
             const bool last = !p.merge || u + 1 == u1;
-            if (!carry) m_run = -INFINITY, l_run = 0.f;
+            if (!carry) m_run = -INFINITY, m_own = -INFINITY, l_own = 0.f;
             if constexpr (BOUNDED) {
                 const long grow = (long)un.q0 + r;
                 m_run = grow < p.Sq ? p.row_bound[((long)un.b * p.H + un.h) * p.Sq + grow] * 1.4426950408889634f
                                     : 0.f;
+                m_own = m_run;
             }
             for (int j = 0; j < T; j++) {
+                const uint32_t n = tile + j;
+                if ((int)(n & 1) != hf) continue;  // the other group's tile
                 int map, row, valid;
                 tr.at(j, map, row, valid);
-                const uint32_t n = tile + j;
-                const uint32_t tS = lane_base + (n % NSBUF) * BN + hf * KP;  // this half's keys of S(n)
-                const int vh = valid - hf * KP;  // valid keys in this half (warp-uniform)
-                // this half's S, 32 columns at a time, keys past the segment at -inf
-                auto load_s = [&](int c2, uint32_t (&x)[32]) {
-                    tmem_ld32(tS + c2 * 32, x);
-                    tmem_ld_wait();
-                    if (vh < (c2 + 1) * 32) {
-#pragma unroll
-                        for (int k = 0; k < 32; k++)
-                            if (c2 * 32 + k >= vh) x[k] = 0xff800000u;
-                    }
-                };
-                float mx = -INFINITY;
-                if (ok && (ok = mbar_wait(&s_full[n % NSBUF], (n / NSBUF) & 1, w))) {
-                    tc_fence_after();
-                    if constexpr (!BOUNDED) {
-#pragma unroll
-                        for (int c2 = 0; c2 < 2; c2++) {
-                            uint32_t x[32];
-                            load_s(c2, x);
-                            float m = fmax3(__uint_as_float(x[0]), __uint_as_float(x[1]), __uint_as_float(x[2]));
-#pragma unroll
-                            for (int k = 3; k < 31; k += 2)
-                                m = fmax3(m, __uint_as_float(x[k]), __uint_as_float(x[k + 1]));
-                            mx = fmaxf(mx, fmaxf(m, __uint_as_float(x[31])));
+                const uint32_t tS = lane_base + (n % NSBUF) * BN;
+                if (!mbar_wait(&s_full[n % NSBUF], (n / NSBUF) & 1, w)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if constexpr (!BOUNDED) {
+                    // the max after tile n-1 (posted by the other group early in its
+                    // tile), every phase waited in turn
+                    if (n > 0) {
+                        if (!mbar_wait(&m_ready[((n - 1) & 1) * 4 + wq], ((n - 1) >> 1) & 1, w)) {
+                            ok = false;
+                            break;
                         }
+                        if (j > 0 || carry) m_run = xm[r];
                     }
                 }
-                bool rescale = false;  // warp-uniform, and the same in both halves of a row
+                uint32_t s[BN];
+#pragma unroll
+                for (int cc = 0; cc < BN / 32; cc++)
+                    tmem_ld32(tS + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[cc * 32]));
+                tmem_ld_wait();
+                if (valid < BN) {  // ragged tile end (warp-uniform): keys past the segment get -inf
+#pragma unroll
+                    for (int k = 0; k < BN; k++)
+                        if (k >= valid) s[k] = 0xff800000u;
+                }
+                bool rescale = false;  // warp-uniform
                 float alpha = 1.f;
                 if constexpr (!BOUNDED) {
-                    float *xm = xmax + (n & 1) * (2 * BM);
-                    xm[hf * BM + r] = mx;
-                    named_barrier_sync(pair_bar, 64);
-                    const float mt = fmaxf(mx, xm[(hf ^ 1) * BM + r]) * sl2;
+                    float mc[4];
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; c4++) {
+                        const uint32_t *x = &s[c4 * 32];
+                        float m = fmax3(__uint_as_float(x[0]), __uint_as_float(x[1]), __uint_as_float(x[2]));
+#pragma unroll
+                        for (int k = 3; k < 31; k += 2) m = fmax3(m, __uint_as_float(x[k]), __uint_as_float(x[k + 1]));
+                        mc[c4] = fmaxf(m, __uint_as_float(x[31]));
+                    }
+                    const float mt = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3])) * sl2;
                     bool need = false;
                     if (j == 0 && !carry) m_run = mt;
                     else need = mt > m_run + tc::RESCALE_THRESHOLD;
@@ -324,40 +335,43 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
                         if (need) {
                             alpha = ex2(m_run - mt);
                             m_run = mt;
-                            l_run *= alpha;
                         }
+                    }
+                    xm[r] = m_run;
+                    mbar_arrive(&m_ready[(n & 1) * 4 + wq]);
+                    if (m_own != m_run) {
+                        l_own = l_own > 0.f ? l_own * ex2(m_own - m_run) : 0.f;
+                        m_own = m_run;
                     }
                 }
-                if (ok) {
-                    const uint64_t scale2 = f2(sl2, sl2), negm2 = f2(-m_run, -m_run);
-                    uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+                // p = 2^(s * scale*log2e - m): packed FMA, then the SFU; row sum on
+                // packed adds.  P is published in parts so that P.V can start on
+                // the first keys while the rest is computed.
+                const uint64_t scale2 = f2(sl2, sl2), negm2 = f2(-m_run, -m_run);
+                uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+                for (int q = 0; q < P_PARTS; q++) {
                     uint32_t pk[KP / 2];
 #pragma unroll
-                    for (int c2 = 0; c2 < 2; c2++) {  // S read again: fewer registers live across the exchange
-                        uint32_t x[32];
-                        load_s(c2, x);
-#pragma unroll
-                        for (int k = 0; k < 32; k += 2) {
-                            float a, b2;
-                            f2_split(ffma2(f2(__uint_as_float(x[k]), __uint_as_float(x[k + 1])), scale2, negm2), a,
-                                     b2);
-                            const float p0 = ex2(a), p1 = ex2(b2);
-                            pk[c2 * 16 + k / 2] = pack_bf16x2(p0, p1);
-                            acc[(k / 2) & 3] = fadd2(acc[(k / 2) & 3], f2(p0, p1));
+                    for (int k = 0; k < KP; k += 2) {
+                        const int kk = q * KP + k;
+                        float a, b2;
+                        f2_split(ffma2(f2(__uint_as_float(s[kk]), __uint_as_float(s[kk + 1])), scale2, negm2), a,
+                                 b2);
+                        const float p0 = ex2(a), p1 = ex2(b2);
+                        pk[k / 2] = pack_bf16x2(p0, p1);
+                        acc[(k / 2) & 3] = fadd2(acc[(k / 2) & 3], f2(p0, p1));
+                    }
+                    tmem_st_cols<KP / 2>(tS + q * (KP / 2), pk);
+                    if (!BOUNDED && q == 0 && rescale) {
+                        // O holds P.V of tiles < n once P(n-1).V is done; rescale it before P(n).V
+                        if (!mbar_wait(&pv_buf[(n - 1) % NSBUF], ((n - 1) / NSBUF) & 1, w)) {
+                            ok = false;
+                            break;
                         }
-                    }
-                    tmem_st_cols<KP / 2>(tS, pk);  // P over the first KP/2 columns of this half's S
-                    // Every P.V(n-1) is waited for exactly once, here (a partial's last in its
-                    // epilogue), which keeps pv_done[(n-1) % 2] within one phase of the wait:
-                    // before P(n) is published when O is to be rescaled, else after.
-                    const bool wait_pv = j > 0 || carry;
-                    if (wait_pv && rescale) {
-                        ok = mbar_wait(&pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, w);
                         tc_fence_after();
-                    }
-                    if (!BOUNDED && rescale && ok) {
 #pragma unroll
-                        for (int cc = 0; cc < D / 64; cc++) {
+                        for (int cc = 0; cc < D / 32; cc++) {
                             uint32_t o[32];
                             tmem_ld32(tO + cc * 32, o);
                             tmem_ld_wait();
@@ -368,70 +382,84 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
                     }
                     tmem_st_wait();
                     tc_fence_before();
-                    mbar_arrive(&p_part[(n & 1) * 2 + hf]);
-                    if (wait_pv && !rescale) ok = mbar_wait(&pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, w);
-                    float a0, a1, b0, b1;
-                    f2_split(fadd2(acc[0], acc[1]), a0, a1);
-                    f2_split(fadd2(acc[2], acc[3]), b0, b1);
-                    l_run += (a0 + a1) + (b0 + b1);
+                    mbar_arrive(&p_part[(n % NSBUF) * P_PARTS + q]);
                 }
+                if (!ok) break;
+                float a0, a1, b0, b1;
+                f2_split(fadd2(acc[0], acc[1]), a0, a1);
+                f2_split(fadd2(acc[2], acc[3]), b0, b1);
+                l_own += (a0 + a1) + (b0 + b1);
             }
+            if (!ok) break;
             if (!last) {  // the group's partial is written after its last chunk
                 tile += T;
                 continue;
             }
-            // epilogue: this half's columns of O / l, with l summed over both halves
-            if (ok) {
-                const uint32_t nl = tile + T - 1;
-                ok = mbar_wait(o_final, n_epi & 1, w) && mbar_wait(&pv_done[nl & 1], (nl >> 1) & 1, w);
+            // epilogue: the two groups combine their row sums, each writes half of O's
+            // columns; both have read O before either publishes the next unit's P
+            if (!mbar_wait(o_final, n_epi & 1, w)) {
+                ok = false;
+                break;
             }
-            float *xs = xsum + (n_epi & 1) * (2 * BM);
-            n_epi++;
+            float *xs = xe + (n_epi & 1) * (2 * BM * 2);
+            xs[(hf * BM + r) * 2] = l_own;
+            xs[(hf * BM + r) * 2 + 1] = m_own;
+            mbar_arrive(&epi[wq]);
+            if (!mbar_wait(&epi[wq], n_epi & 1, w)) {
+                ok = false;
+                break;
+            }
+            const float l_oth = xs[((hf ^ 1) * BM + r) * 2], m_oth = xs[((hf ^ 1) * BM + r) * 2 + 1];
+            const float m_fin = fmaxf(m_own, m_oth);  // the max O is expressed in
+            const float l_tot = (l_own > 0.f ? l_own * ex2(m_own - m_fin) : 0.f) +
+                                (l_oth > 0.f ? l_oth * ex2(m_oth - m_fin) : 0.f);
             const long pc = p.merge ? un.c / p.group : un.c;  // index of the partial written
-            xs[hf * BM + r] = l_run;
-            named_barrier_sync(pair_bar, 64);
-            const float l_tot = l_run + xs[(hf ^ 1) * BM + r];
             const long grow = (long)un.q0 + r;
             const bool live = grow < p.Sq;
-            if (ok) {
-                tc_fence_after();
-                if constexpr (BOUNDED) {
-                    if (live && !(l_tot > 0.f)) atomicCAS(p.err, DEV_OK, DEV_RANGE);  // all terms underflowed
-                }
-                const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
-                const long obase = (((long)un.b * p.Sq + (live ? grow : 0)) * p.H + un.h) * D + hf * (D / 2);
+            tc_fence_after();
+            if constexpr (BOUNDED) {
+                if (live && !(l_tot > 0.f)) atomicCAS(p.err, DEV_OK, DEV_RANGE);  // all terms underflowed
+            }
+            const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+            const long obase = (((long)un.b * p.Sq + (live ? grow : 0)) * p.H + un.h) * D + hf * (D / 2);
 #pragma unroll
-                for (int cc = 0; cc < D / 64; cc++) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + cc * 32, o);
-                    tmem_ld_wait();
-                    if (live) {
-                        if (p.out_f32) {
-                            // streaming stores: the partials are read once, by the merge
-                            float *dst = static_cast<float *>(p.out) + (long long)pc * p.o_stride + obase + cc * 32;
+            for (int cc = 0; cc < D / 64; cc++) {
+                uint32_t o[32];
+                tmem_ld32(tO + hf * (D / 2) + cc * 32, o);
+                tmem_ld_wait();
+                if (live) {
+                    if (p.out_f32) {
+                        // streaming stores: the partials are read once, by the merge
+                        float *dst = static_cast<float *>(p.out) + (long long)pc * p.o_stride + obase + cc * 32;
 #pragma unroll
-                            for (int k = 0; k < 32; k += 4)
-                                __stcs(reinterpret_cast<float4 *>(dst + k),
-                                       make_float4(__uint_as_float(o[k]) * inv, __uint_as_float(o[k + 1]) * inv,
-                                                   __uint_as_float(o[k + 2]) * inv, __uint_as_float(o[k + 3]) * inv));
-                        } else {
-                            __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.out) + obase + cc * 32;
+                        for (int k = 0; k < 32; k += 4)
+                            __stcs(reinterpret_cast<float4 *>(dst + k),
+                                   make_float4(__uint_as_float(o[k]) * inv, __uint_as_float(o[k + 1]) * inv,
+                                               __uint_as_float(o[k + 2]) * inv, __uint_as_float(o[k + 3]) * inv));
+                    } else {
+                        __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.out) + obase + cc * 32;
 #pragma unroll
-                            for (int k = 0; k < 32; k += 8) {
-                                uint4 v;
-                                v.x = pack_bf16x2(__uint_as_float(o[k]) * inv, __uint_as_float(o[k + 1]) * inv);
-                                v.y = pack_bf16x2(__uint_as_float(o[k + 2]) * inv, __uint_as_float(o[k + 3]) * inv);
-                                v.z = pack_bf16x2(__uint_as_float(o[k + 4]) * inv, __uint_as_float(o[k + 5]) * inv);
-                                v.w = pack_bf16x2(__uint_as_float(o[k + 6]) * inv, __uint_as_float(o[k + 7]) * inv);
-                                *reinterpret_cast<uint4 *>(dst + k) = v;
-                            }
+                        for (int k = 0; k < 32; k += 8) {
+                            uint4 v;
+                            v.x = pack_bf16x2(__uint_as_float(o[k]) * inv, __uint_as_float(o[k + 1]) * inv);
+                            v.y = pack_bf16x2(__uint_as_float(o[k + 2]) * inv, __uint_as_float(o[k + 3]) * inv);
+                            v.z = pack_bf16x2(__uint_as_float(o[k + 4]) * inv, __uint_as_float(o[k + 5]) * inv);
+                            v.w = pack_bf16x2(__uint_as_float(o[k + 6]) * inv, __uint_as_float(o[k + 7]) * inv);
+                            *reinterpret_cast<uint4 *>(dst + k) = v;
                         }
                     }
                 }
-                if (live && p.lse && hf == 0)
-                    p.lse[(long long)pc * p.l_stride + ((long)un.b * p.H + un.h) * p.Sq + grow] =
-                        (m_run + log2f(l_tot)) * 0.69314718055994531f;
             }
+            if (live && p.lse && hf == 0)
+                p.lse[(long long)pc * p.l_stride + ((long)un.b * p.H + un.h) * p.Sq + grow] =
+                    (m_fin + log2f(l_tot)) * 0.69314718055994531f;
+            tc_fence_before();
+            mbar_arrive(&epi_done[wq]);
+            if (!mbar_wait(&epi_done[wq], n_epi & 1, w)) {
+                ok = false;
+                break;
+            }
+            n_epi++;
             tile += T;
         }
     }
@@ -449,10 +477,6 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
 cudaError_t launch_attn_tc_single(const Geom &g, const void *q, const void *k, const void *v, const void *jk,
                                   const void *jv, int n_chunks, void *out, float *lse, const AttnTcOptions &opt,
                                   cudaStream_t st, const char **why) {
-    if (g.Sq > tc::BM) {
-        if (why) *why = "single-tile attention takes at most 128 query rows";
-        return cudaErrorInvalidValue;
-    }
     CUtensorMap mq, mk, mv, mjk, mjv;
     const bool has_joint = g.Nj > 0;
     const bool has_video = g.Nv > 0;
@@ -475,7 +499,8 @@ cudaError_t launch_attn_tc_single(const Geom &g, const void *q, const void *k, c
     p.Nj = g.Nj;
     p.H = g.H;
     p.n_chunks = n_chunks;
-    p.q_pairs = g.Sq > 0 ? 1 : 0;  // one unit per (b, h, chunk): q0 = 0
+    p.unit_rows = tc::BM;  // one Q tile per unit
+    p.q_pairs = (int)((g.Sq + tc::BM - 1) / tc::BM);
     p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)g.d));
     p.out = out;
     p.lse = lse;

@@ -17,12 +17,13 @@
 //               gives registers to the two softmax warpgroups): Q0/Q1 (2 x 128 rows) once, then K_j, V_j tiles of
 //               128 keys x 128 dims through a 4-slot ring (32 KB per tile, two
 //               128-byte-swizzled 64-dim panels per tile).
-//   warp 9      MMA issuer (one thread): S_i = Q_i K_j^T (SS, K-major) into
-//               TMEM, then O_i += P_i V_j with P_i read from TMEM (TS) and V
-//               MN-major from shared memory.  Order per K/V tile:
-//               PV0(j), then S0(j+1) and PV1(j) interleaved MMA by MMA (two
-//               independent accumulator chains), then S1(j+1); each softmax
-//               group has the other group's work to hide behind.
+//   warps 9, 10 MMA issuers, one thread each, for Q tile 0 and Q tile 1:
+//               S_i = Q_i K_j^T (SS, K-major) into TMEM, then O_i += P_i V_j
+//               with P_i read from TMEM (TS) and V MN-major from shared
+//               memory.  Each thread issues its tile's chain in order,
+//               P_i.V(j) then S_i(j+1); the tensor pipe interleaves the two
+//               chains, so each softmax group has the other tile's MMAs to
+//               hide behind.
 //   warps 0-3   softmax of Q tile 0, warps 4-7 of Q tile 1: one thread per
 //               query row (its TMEM lane); online softmax in base 2 with the
 //               scale folded in; the running max is only moved (and O
@@ -109,7 +110,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
         mbar_init(q_full, 1);
         for (int s = 0; s < NSTAGE; s++) {
             mbar_init(&kv_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
+            mbar_init(&kv_empty[s], NQ);  // released by both Q tiles' issuers
         }
         for (int i = 0; i < NQ; i++) {
             mbar_init(&s_full[i], 1);
@@ -117,7 +118,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
             mbar_init(&o_final[i], 1);
             mbar_init(&o_step[i], 1);
         }
-        mbar_init(drain, 1);
+        mbar_init(drain, NQ);  // one commit per MMA issuer
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -176,47 +177,59 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
             if (uc > 0) mbar_drain(q_full, 0, DRAIN_NS);
             for (uint32_t idx = kv_idx > NSTAGE ? kv_idx - NSTAGE : 0; idx < kv_idx; idx++)
                 mbar_drain(&kv_full[idx % NSTAGE], (idx / NSTAGE) & 1, DRAIN_NS);
-        } else if (warp == 9 && lane == 0) {
-            // --------------------------------------------------- MMA issuer
+        } else if ((warp == 9 || warp == 10) && lane == 0) {
+            // -------------------------------------------------- MMA issuers
+            // One issuing thread per Q tile, on two different SM sub-partitions.
+            // Each sub-partition also runs two softmax warps, whose issue slots
+            // a single issuing thread would share: it then issues an MMA about
+            // every 90 cycles against the 64 the tensor pipe takes for one, and
+            // the pipe starves.  Two issuers keep it fed.  Tile i's S_i and P_i.V
+            // form one accumulator chain issued by one thread in order, so the
+            // two threads never have to be ordered against each other; a K or V
+            // slot is read by both tiles and is released by both (kv_empty
+            // counts two arrivals).
+            const int i = warp - 9;  // the Q tile this thread issues for
             const uint32_t idesc_qk = p.idesc_qk;
             const uint32_t idesc_pv = idesc_bf16_f32(BM, D, true);
-            const uint32_t sQ = smem_u32(smem + SMEM_Q), sKV = smem_u32(smem + SMEM_KV);
+            const uint32_t sQ = smem_u32(smem + SMEM_Q);
             // Descriptors are built once; per MMA only the start-address field
             // (bits 0-13, 16-byte units) moves, so each issue is one 64-bit add.
-            const uint64_t dq0 = smem_desc_sw128(sQ, 16, 1024);         // Q / K: K-major, SBO 1024
-            const uint64_t dv0 = smem_desc_sw128(sKV, PANEL, 1024);     // V: MN-major, LBO = panel stride
-            // step kk of S_i = Q_i K^T: 16 (bf16/fp16) or 32 (e4m3) head dims, 32 bytes of each row
-            auto s_step = [&](uint32_t d_tmem, uint64_t qa, uint64_t kb, int kk) {
+            const uint64_t dq0 = smem_desc_sw128(sQ, 16, 1024);                       // Q / K: K-major, SBO 1024
+            const uint64_t dv0 = smem_desc_sw128(smem_u32(smem + SMEM_KV), PANEL, 1024);  // V: MN-major, LBO = panel
+            const uint64_t qa = dq0 + ((uint64_t)(i * TILE) >> 4);
+            const uint32_t tS = tmem + i * BN, tO = tmem + 2 * BN + i * D;
+            // S_i = Q_i K^T from the K tile in `slot`: steps of 16 (bf16/fp16) or 32 (e4m3) head dims
+            auto issue_s = [&](uint32_t slot) {
+                const uint64_t kb = dq0 + ((uint64_t)(SMEM_KV - SMEM_Q + slot * TILE) >> 4);
                 if constexpr (QK8) {
-                    const uint64_t off = (uint64_t)(kk * 32) >> 4;
-                    mma_ss_f8(d_tmem, qa + off, kb + off, idesc_qk, kk > 0);
+#pragma unroll
+                    for (int kk = 0; kk < D / 32; kk++) {
+                        const uint64_t off = (uint64_t)(kk * 32) >> 4;
+                        mma_ss_f8(tS, qa + off, kb + off, idesc_qk, kk > 0);
+                    }
                 } else {
-                    const uint64_t off = (uint64_t)((kk >> 2) * PANEL + (kk & 3) * 32) >> 4;
-                    mma_ss(d_tmem, qa + off, kb + off, idesc_qk, kk > 0);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; kk++) {
+                        const uint64_t off = (uint64_t)((kk >> 2) * PANEL + (kk & 3) * 32) >> 4;
+                        mma_ss(tS, qa + off, kb + off, idesc_qk, kk > 0);
+                    }
                 }
             };
-            constexpr int S_STEPS = QK8 ? D / 32 : D / 16;
-            auto issue_s = [&](int i, uint32_t slot) {
-                const uint64_t qa = dq0 + ((uint64_t)(i * TILE) >> 4);
-                const uint64_t kb = dq0 + ((uint64_t)(SMEM_KV - SMEM_Q + slot * TILE) >> 4);
-#pragma unroll
-                for (int kk = 0; kk < S_STEPS; kk++) s_step(tmem + i * BN, qa, kb, kk);
-            };
-            // keys [16*k0, 16*k1) of P_i . V
-            auto issue_pv = [&](int i, uint32_t slot, bool acc, int k0, int k1) {
+            // keys [16*k0, 16*k1) of O_i += P_i . V from the V tile in `slot`
+            auto issue_pv = [&](uint32_t slot, bool acc, int k0, int k1) {
                 const uint64_t vb = dv0 + ((uint64_t)(slot * TILE) >> 4);
 #pragma unroll
                 for (int kk = k0; kk < k1; kk++)
-                    mma_ts(tmem + 2 * BN + i * D, tmem + i * BN + kk * 8, vb + ((uint64_t)(kk * 16 * 128) >> 4),
-                           idesc_pv, (acc || kk > 0) ? 1u : 0u);
+                    mma_ts(tO, tS + kk * 8, vb + ((uint64_t)(kk * 16 * 128) >> 4), idesc_pv,
+                           (acc || kk > 0) ? 1u : 0u);
             };
-            uint32_t step_phase[2] = {0, 0};
+            uint32_t step_phase = 0;
             // P_i lives in S_i's columns: in strict mode let the P.V that read it finish before S_i is rewritten
-            auto strict_wait = [&](int i) -> bool {
+            auto strict_wait = [&]() -> bool {
                 if (!p.strict_order) return true;
                 tc_commit(&o_step[i]);
-                const bool done = mbar_wait(&o_step[i], step_phase[i], w);
-                step_phase[i] ^= 1;
+                const bool done = mbar_wait(&o_step[i], step_phase, w);
+                step_phase ^= 1;
                 return done;
             };
             uint32_t kv_idx = 0;  // K/V tiles consumed (K_j, V_j alternate)
@@ -234,69 +247,39 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                      mbar_wait(&kv_full[kv_idx % NSTAGE], (kv_idx / NSTAGE) & 1, w);
                 if (!ok) break;
                 tc_fence_after();
-                for (int i = 0; i < NQ && ok; i++) {
-                    if (started && !(ok = strict_wait(i))) break;
-                    issue_s(i, kv_idx % NSTAGE);
-                    tc_commit(&s_full[i]);
-                }
-                if (!ok) break;
+                if (started && !(ok = strict_wait())) break;
+                issue_s(kv_idx % NSTAGE);
+                tc_commit(&s_full[i]);
                 tc_commit(&kv_empty[kv_idx % NSTAGE]);
-                // Per K/V tile j: P0.V(j); then S0(j+1) interleaved MMA by MMA with
-                // P1.V(j), two independent accumulator chains for the tensor pipe;
-                // then S1(j+1).  S_i(j+1) always follows P_i.V(j), whose P it overwrites.
+                // Per K/V tile j: P_i.V(j), part by part as the softmax publishes
+                // P_i, then S_i(j+1), which overwrites P_i(j) and so follows it.
                 for (int j = 0; j < T && ok; j++) {
                     const uint32_t vidx = kv_idx + 2 * j + 1, kidx = vidx + 1;
                     const uint32_t vs = vidx % NSTAGE, ks = kidx % NSTAGE;
-                    const bool more = j + 1 < T;
                     const uint32_t ph = (tile + j) & 1;
-                    // P_i.V(j), part by part as the softmax publishes P
-                    auto pv_parts = [&](int i) -> bool {
-                        for (int q = 0; q < P_PARTS; q++) {
-                            if (!mbar_wait(&p_part[i * P_PARTS + q], ph, w)) return false;
-                            tc_fence_after();
-                            issue_pv(i, vs, carry || j > 0 || q > 0, q * MMA_PER_PART, (q + 1) * MMA_PER_PART);
-                        }
-                        return true;
-                    };
-                    if (!(ok = mbar_wait(&kv_full[vs], (vidx / NSTAGE) & 1, w) && pv_parts(0))) break;
-                    started = true;
-                    if (!more) {
-                        if (last) tc_commit(&o_final[0]);
-                        if (!(ok = pv_parts(1))) break;
-                        tc_commit(&kv_empty[vs]);
-                        if (last) tc_commit(&o_final[1]);
-                        continue;
-                    }
-                    if (!(ok = strict_wait(0))) break;
-                    if (!(ok = mbar_wait(&kv_full[ks], (kidx / NSTAGE) & 1, w))) break;
-                    tc_fence_after();
-                    {
-                        const uint64_t kb = dq0 + ((uint64_t)(SMEM_KV - SMEM_Q + ks * TILE) >> 4);
-                        const uint64_t vb = dv0 + ((uint64_t)(vs * TILE) >> 4);
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; kk++) {
-                            // S0(j+1): one step per P.V step (16-bit q/k), or on every other one (e4m3)
-                            if (!QK8 || kk % 2 == 0) s_step(tmem, dq0, kb, QK8 ? kk / 2 : kk);
-                            if (kk % MMA_PER_PART == 0) {
-                                if (!(ok = mbar_wait(&p_part[P_PARTS + kk / MMA_PER_PART], ph, w))) break;
-                                tc_fence_after();
-                            }
-                            mma_ts(tmem + 2 * BN + D, tmem + BN + kk * 8, vb + ((uint64_t)(kk * 16 * 128) >> 4),
-                                   idesc_pv, (carry || j > 0 || kk > 0) ? 1u : 0u);  // P1.V(j)
-                        }
+                    if (!(ok = mbar_wait(&kv_full[vs], (vidx / NSTAGE) & 1, w))) break;
+                    for (int q = 0; q < P_PARTS && ok; q++) {
+                        if (!(ok = mbar_wait(&p_part[i * P_PARTS + q], ph, w))) break;
+                        tc_fence_after();
+                        issue_pv(vs, carry || j > 0 || q > 0, q * MMA_PER_PART, (q + 1) * MMA_PER_PART);
                     }
                     if (!ok) break;
-                    tc_commit(&s_full[0]);
+                    started = true;
+                    if (last && j + 1 == T) tc_commit(&o_final[i]);
                     tc_commit(&kv_empty[vs]);
-                    if (!(ok = strict_wait(1))) break;
-                    issue_s(1, ks);
-                    tc_commit(&s_full[1]);
+                    if (j + 1 == T) continue;
+                    if (!(ok = strict_wait())) break;
+                    if (!(ok = mbar_wait(&kv_full[ks], (kidx / NSTAGE) & 1, w))) break;
+                    tc_fence_after();
+                    issue_s(ks);
+                    tc_commit(&s_full[i]);
                     tc_commit(&kv_empty[ks]);
                 }
                 kv_idx += 2 * T;
                 tile += T;
             }
             // every MMA issued so far must complete before tensor memory is freed
+            // (the drain barrier counts one arrival per issuer)
             tc_commit(drain);
             mbar_drain(drain, 0, DRAIN_NS);
         }
@@ -510,7 +493,8 @@ cudaError_t launch_attn_tc(const Geom &g, const void *q, const void *k, const vo
     p.Nj = g.Nj;
     p.H = g.H;
     p.n_chunks = n_chunks;
-    p.q_pairs = (int)((g.Sq + tc::NQ * tc::BM - 1) / (tc::NQ * tc::BM));
+    p.unit_rows = tc::NQ * tc::BM;
+    p.q_pairs = (int)((g.Sq + p.unit_rows - 1) / p.unit_rows);
     p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)g.d));
     p.out = out;
     p.lse = lse;

@@ -108,9 +108,9 @@ int chunk_group(const Geom &g, int n_chunks) {
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    // CTAs per chunk and (batch, head): one per 256-row Q tile pair, or one for
-    // a query range of a single tile (the single-tile kernel)
-    const long q_units = g.Sq <= 128 ? 1 : (g.Sq + 255) / 256;
+    // CTAs per chunk and (batch, head): one per 128-row Q tile (the single-tile
+    // kernel, which runs 16-bit q/k)
+    const long q_units = (g.Sq + 127) / 128;
     const long units = (long)g.B * g.H * n_chunks * q_units;
     for (int gsz = 4; gsz > 1; gsz--)
         if (n_chunks % gsz == 0 && units / gsz >= 4L * sms) return gsz;
