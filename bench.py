@@ -65,8 +65,11 @@ def peaks():
 # the sources each profiled kernel is built from: a traffic record counts only
 # while these files are unchanged since the ncu capture
 KERNEL_SOURCES = {
+    "attn_tc_single_kernel": ("k6_attn_single.cu", "k6_attn_common.cuh", "k6_device.cuh"),
     "attn_tc_kernel": ("k6_attn_tc.cu", "k6_attn_common.cuh", "k6_device.cuh"),
 }
+# the attention kernel of the step (bf16/fp16 q/k); e4m3 q/k run attn_tc_kernel
+STEP_KERNEL = "attn_tc_single_kernel"
 
 
 def source_digest(kernel: str) -> str:
@@ -419,7 +422,7 @@ def measure_fp8(w, n_chunks, P, x, steps, warmup):
     return {"what": f"{w.name}: the step with rotated q/k in e4m3 (Q.K^T on kind::f8f6f4, P.V bf16)",
             "value": round(flops / (total * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(total, 4),
             "attention_ms": round(float(per[1]), 4),
-            "attention_TFLOP/s": round(flops / (float(per[1]) * 1e-3) / 1e12, 2),
+            "attention_TFLOP/s": round(flops / (float(per[1]) * 1e-3) / 1e12, 2), "kernel": "attn_tc_kernel",
             "parity": "tests/test_gpu_fp8.py (bf16 bounds on exact e4m3 inputs; relative L2 4e-2 at this workload)"}
 
 
@@ -452,7 +455,7 @@ def measure_cross(w, steps, warmup, n_chunks=8, Sq=None):
     h.sync()
     ms = e0.elapsed_time(e1) / steps
     flops = 4.0 * B * H * Sq * Sk * d
-    kernel = "attn_tc_single_kernel" if Sq <= 128 else "attn_tc_kernel"
+    kernel = STEP_KERNEL
     return {"workload": f"{Sq} audio queries over {Sk} video keys (B={B}, H={H}, d={d}), {n_chunks} K/V chunks",
             "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_call": round(ms, 4),
             "kernel": kernel, "flops_counted": "4*B*H*Sq*Sk*d on the real query rows"}
@@ -607,7 +610,7 @@ def run_ours(args, rank, world, dist_on):
         "config": bench_config(w, n, P),
         "roofline": {"bound": "tensor", "achieved": round(attn_tflops, 2), "peak": peak_b, "unit": "TFLOP/s",
                      "frac": round(attn_tflops / peak_b, 4), "frac_sustained": round(attn_tflops / peak_s, 4),
-                     "traffic": traffic_record("attn_tc_kernel", f"{w.name}_n{n}"), "kernel": "attn_tc_kernel",
+                     "traffic": traffic_record(STEP_KERNEL, f"{w.name}_n{n}"), "kernel": STEP_KERNEL,
                      "peak_kind": f"bf16 burst, {tag}; frac_sustained against {peak_s}",
                      "algorithmic_flops_per_launch": flops},
         "kernels": kernels,
@@ -635,8 +638,8 @@ def run_ours(args, rank, world, dist_on):
                               "roofline": {"bound": "tensor", "achieved": round(a2, 2), "peak": peak_b,
                                            "unit": "TFLOP/s", "frac": round(a2 / peak_b, 4),
                                            "frac_sustained": round(a2 / peak_s, 4),
-                                           "traffic": traffic_record("attn_tc_kernel", f"{w2.name}_n{n2}"),
-                                           "kernel": "attn_tc_kernel", "algorithmic_flops_per_launch": f2},
+                                           "traffic": traffic_record(STEP_KERNEL, f"{w2.name}_n{n2}"),
+                                           "kernel": STEP_KERNEL, "algorithmic_flops_per_launch": f2},
                               "kernels": {
                                   "rope_split_heads": hbm_rec(prologue_bytes(w2), k2["rope_split_heads"]),
                                   "attention_chunk_groups": {"ms": round(k2["attention_chunk_groups"], 3),

@@ -43,7 +43,7 @@ using tc::BN;
 using tc::D;
 using tc::PANEL;
 using tc::TILE;
-constexpr int NSTAGE = 4;                     // K/V tile slots
+constexpr int NSTAGE = 5;                     // K/V tile slots (four leave V(n+1) too little time to arrive)
 constexpr int NSBUF = 3;                      // S buffers in tensor memory
 constexpr int SMEM_Q = 0;
 constexpr int SMEM_KV = TILE;
