@@ -66,9 +66,8 @@ def peaks():
 # while these files are unchanged since the ncu capture
 KERNEL_SOURCES = {
     "attn_tc_single_kernel": ("k6_attn_single.cu", "k6_attn_common.cuh", "k6_device.cuh"),
-    "attn_tc_kernel": ("k6_attn_tc.cu", "k6_attn_common.cuh", "k6_device.cuh"),
 }
-# the attention kernel of the step (bf16/fp16 q/k); e4m3 q/k run attn_tc_kernel
+# the attention kernel of the step (and of every other attention line)
 STEP_KERNEL = "attn_tc_single_kernel"
 
 
@@ -422,7 +421,7 @@ def measure_fp8(w, n_chunks, P, x, steps, warmup):
     return {"what": f"{w.name}: the step with rotated q/k in e4m3 (Q.K^T on kind::f8f6f4, P.V bf16)",
             "value": round(flops / (total * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(total, 4),
             "attention_ms": round(float(per[1]), 4),
-            "attention_TFLOP/s": round(flops / (float(per[1]) * 1e-3) / 1e12, 2), "kernel": "attn_tc_kernel",
+            "attention_TFLOP/s": round(flops / (float(per[1]) * 1e-3) / 1e12, 2), "kernel": STEP_KERNEL,
             "parity": "tests/test_gpu_fp8.py (bf16 bounds on exact e4m3 inputs; relative L2 4e-2 at this workload)"}
 
 

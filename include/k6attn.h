@@ -207,9 +207,8 @@ k6attn_status k6attn_forward(k6attn_t h, const void *q, const void *k, const voi
  *           k6attn_lse_merge.
  *  qk_dtype the type of q, k and joint_k: the handle's dtype, or F16 for a
  *           BF16 handle (v and joint_v always have the handle's dtype), or
- *           E4M3 for a BF16 handle with more than 128 query rows
- *           (K6ATTN_ERR_UNSUPPORTED otherwise): Q.K^T then runs on 8-bit
- *           operands, P.V as before.
+ *           E4M3 for a BF16 handle: Q.K^T then runs on 8-bit operands, P.V
+ *           as before.
  * Inputs as in k6attn_forward; outputs must not alias them.
  */
 k6attn_status k6attn_attention_chunks(k6attn_t h, const void *q, const void *k, const void *v, const void *joint_k,
@@ -455,10 +454,10 @@ k6attn_status k6attn_sync(k6attn_t h, void *stream);
  *      device-side wait of this handle's kernels (default 2e9).  0 makes every
  *      wait give up at once, which tests use to exercise the timeout path
  *      without hanging the GPU.
- *  K6ATTN_OPT_STRICT_MMA_ORDER  1: the bf16 kernel waits for each P.V product
- *      to finish reading P (which shares tensor memory with the next S tile)
- *      before issuing the next Q.K^T product; 0 (default): relies on the
- *      tensor pipe executing one thread's MMAs in issue order.
+ *  K6ATTN_OPT_STRICT_MMA_ORDER  accepted (0 or 1) and without effect: the
+ *      bf16 kernel always waits for a P.V product to finish reading P before a
+ *      Q.K^T product rewrites the tensor memory that holds it, so results do
+ *      not depend on the order in which the tensor pipe runs MMAs.
  *  K6ATTN_OPT_ROTATE_BF16  1: k6attn_forward and k6attn_forward_static_scratch
  *      keep the rotated q/k copies of a BF16 handle in bf16, whose range is
  *      that of fp32, instead of fp16 (default 0).  fp16 copies add 8 times less

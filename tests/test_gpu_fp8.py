@@ -44,8 +44,10 @@ CASES = {
     "ragged": Workload("ragged", 1, 4, 128, "bf16", (3, 10, 20), 40, (32, 48, 48), 0, 1.0, 1.0, (4,)),
     # B = 2, S = 288
     "batch2": Workload("batch2", 2, 2, 128, "bf16", (2, 8, 16), 32, (32, 48, 48), 0, 1.0, 1.0, (3,)),
-    # S = 130: the smallest query range of the two-tile kernel, one row past a tile
+    # S = 130: one row past a Q tile
     "s130": Workload("s130", 1, 3, 128, "bf16", (1, 10, 12), 10, (32, 48, 48), 0, 1.0, 1.0, (2,)),
+    # S = 63: a query range shorter than one Q tile
+    "short": Workload("short", 1, 2, 128, "bf16", (1, 7, 9), 0, (32, 48, 48), 0, 1.0, 1.0, (1,)),
 }
 
 
@@ -66,7 +68,8 @@ def dev8(a):
 
 
 @pytest.mark.parametrize("name,n,group", [("ragged", 1, 1), ("ragged", 4, 1), ("ragged", 4, 2), ("ragged", 8, 4),
-                                          ("batch2", 3, 3), ("batch2", 2, 1), ("s130", 2, 2)])
+                                          ("batch2", 3, 3), ("batch2", 2, 1), ("s130", 2, 2), ("short", 1, 1),
+                                          ("short", 3, 1)])
 @pytest.mark.parametrize("std", [1.0, 3.0])
 def test_attention_on_exact_e4m3_inputs_matches_oracle(name, n, group, std):
     w = CASES[name]
@@ -88,19 +91,6 @@ def test_attention_on_exact_e4m3_inputs_matches_oracle(name, n, group, std):
     h.sync()
     ref, ref_lse = O.attention(geom(w), f32["q"], f32["k"], f32["v"], f32["jk"], f32["jv"], rope=False)
     compare(to_host(out), ref, lse.cpu().numpy().astype(np.float64), ref_lse, "bf16")
-
-
-def test_e4m3_needs_the_two_tile_kernel():
-    w = Workload("short", 1, 2, 128, "bf16", (1, 7, 9), 0, (32, 48, 48), 0, 1.0, 1.0, (1,))  # 63 rows
-    k6 = K()
-    raw, _ = e4m3_inputs(w)
-    h = k6.Handle.for_workload(w)
-    q, k = dev8(raw["q"]), dev8(raw["k"])
-    v = to_dev(raw["v"], "bf16")
-    out = torch.empty((w.B, w.S, w.H, w.d), dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(k6.K6Error) as e:
-        h.attention_chunks(q, k, v, None, None, 1, out, qk_dtype=k6.E4M3)
-    assert e.value.status == k6.ERR_UNSUPPORTED
 
 
 @pytest.mark.parametrize("name,P", [("lite", 8), ("ragged", 2)])

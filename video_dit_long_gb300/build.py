@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libk6attn.so")
 
-SOURCES = ["k6_api.cu", "k6_host.cu", "k6_rope.cu", "k6_merge.cu", "k6_relayout.cu", "k6_attn_f32.cu", "k6_attn_tc.cu", "k6_attn_single.cu", "k6_noalloc.cu", "k6_bounds.cu", "k6_attn_bwd.cu"]
+SOURCES = ["k6_api.cu", "k6_host.cu", "k6_rope.cu", "k6_merge.cu", "k6_relayout.cu", "k6_attn_f32.cu", "k6_attn_single.cu", "k6_noalloc.cu", "k6_bounds.cu", "k6_attn_bwd.cu"]
 HEADERS = ["k6_device.cuh", "k6_internal.h", "k6_attn_common.cuh"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")

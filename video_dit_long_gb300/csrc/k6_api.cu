@@ -88,11 +88,8 @@ static k6attn_status run_attention(k6attn_handle *h, const Geom &g, const void *
         AttnTcOptions opt{h->wait_limit_ns, h->err,    h->strict_order, qk_f16 ? 1 : 0, row_bound,
                           qk8 ? 1 : 0,      group,     merge ? 1 : 0};
         const char *why = nullptr;
-        // 16-bit q/k run the single-tile kernel (one 128-row Q tile per CTA, faster at
-        // every query length measured); e4m3 q/k the two-tile kernel, which has the
-        // 8-bit Q.K^T path
-        cudaError_t e = (qk8 ? launch_attn_tc : launch_attn_tc_single)(g, q, k, v, jk, jv, n_chunks, out, lse, opt,
-                                                                       st, &why);
+        // the single-tile kernel (one 128-row Q tile per CTA), for bf16, fp16 and e4m3 q/k
+        cudaError_t e = launch_attn_tc_single(g, q, k, v, jk, jv, n_chunks, out, lse, opt, st, &why);
         if (e != cudaSuccess) {
             if (why) return set_error(K6ATTN_ERR_CUDA, "attention: %s", why);
             return cuda_check(e, "attention launch");
@@ -158,19 +155,12 @@ static k6attn_status check_inputs(const char *fn, const Geom &g, const void *q, 
 }
 
 // The q/k type an attention call may take with this handle: the handle's own,
-// F16 for BF16 handles, and E4M3 for BF16 handles whose query range needs the
-// two-tile kernel (more than 128 rows).  Bytes per q/k element, or 0 (refused,
+// and F16 or E4M3 for BF16 handles.  Bytes per q/k element, or 0 (refused,
 // message set).
 static int qk_bytes(const char *fn, const Geom &g, k6attn_dtype qk) {
     if (qk == g.dtype) return g.elem;
     if (g.dtype == K6ATTN_BF16 && qk == K6ATTN_F16) return 2;
-    if (g.dtype == K6ATTN_BF16 && qk == K6ATTN_E4M3) {
-        if (g.Sq <= 128) {
-            set_error(K6ATTN_ERR_UNSUPPORTED, "%s: e4m3 q/k need a query range of more than 128 rows", fn);
-            return 0;
-        }
-        return 1;
-    }
+    if (g.dtype == K6ATTN_BF16 && qk == K6ATTN_E4M3) return 1;
     set_error(K6ATTN_ERR_INVALID_ARG, "%s: q/k type %d not allowed for this handle", fn, (int)qk);
     return 0;
 }
@@ -531,7 +521,7 @@ k6attn_status k6attn_attention_chunks(k6attn_t h, const void *q, const void *k, 
     const size_t ob = (size_t)n * g.B * g.S * g.H * g.d * (n_chunks > 1 ? 4 : g.elem);
     const size_t lb = (size_t)n * g.B * g.H * g.S * 4;
     const int qkb = qk_bytes("attention_chunks", g, qk_dtype);
-    if (!qkb) return g.dtype == K6ATTN_BF16 && qk_dtype == K6ATTN_E4M3 ? K6ATTN_ERR_UNSUPPORTED : K6ATTN_ERR_INVALID_ARG;
+    if (!qkb) return K6ATTN_ERR_INVALID_ARG;
     k6attn_status s = check_inputs("attention_chunks", g, q, k, v, joint_k, joint_v, n_chunks, out, ob, lse, lb, qkb);
     if (s != K6ATTN_OK) return s;
     return run_attention(h, g, q, k, v, joint_k, joint_v, qk_dtype == K6ATTN_F16, n_chunks, out, lse,
@@ -562,7 +552,7 @@ k6attn_status k6attn_attention_chunk_groups(k6attn_t h, const void *q, const voi
         return set_error(K6ATTN_ERR_INVALID_ARG, "attention_chunk_groups: partial lse is required when "
                                                  "n_chunks / group > 1");
     const int qkb = qk_bytes("attention_chunk_groups", g, qk_dtype);
-    if (!qkb) return g.dtype == K6ATTN_BF16 && qk_dtype == K6ATTN_E4M3 ? K6ATTN_ERR_UNSUPPORTED : K6ATTN_ERR_INVALID_ARG;
+    if (!qkb) return K6ATTN_ERR_INVALID_ARG;
     const size_t ob = (size_t)parts * g.B * g.S * g.H * g.d * (parts > 1 ? 4 : g.elem);
     const size_t lb = (size_t)parts * g.B * g.H * g.S * 4;
     k6attn_status s =

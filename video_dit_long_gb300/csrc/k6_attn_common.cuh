@@ -14,7 +14,6 @@ namespace tc {
 constexpr int D = 128;
 constexpr int BM = 128;                       // query rows per Q tile
 constexpr int BN = 128;                       // keys per K/V tile
-constexpr int NQ = 2;                         // Q tiles per CTA
 constexpr int PANEL = BM * 64 * 2;            // one 128-row x 64-dim bf16 panel: 16 KB
 constexpr int TILE = 2 * PANEL;               // 32 KB
 constexpr float RESCALE_THRESHOLD = 8.0f;     // log2 units: rescale when the max grows past 2^8
@@ -24,8 +23,7 @@ constexpr unsigned long long DRAIN_NS = 1000000000ull;
 struct TcParams {
     long S, Nv, Nj;                           // keys (video then joint)
     long Sq;                                  // query rows
-    int H, n_chunks, q_pairs;                 // q_pairs: query units per (b, h), of unit_rows rows
-    int unit_rows;                            // query rows per work unit: NQ * BM (two-tile kernel) or BM
+    int H, n_chunks, q_tiles;                 // q_tiles: 128-row query tiles per (b, h)
     float scale_log2;                         // log2(e) / sqrt(d)
     void *out;                                // bf16 [B][S][H][d] or fp32 partials
     float *lse;
@@ -35,7 +33,7 @@ struct TcParams {
     int *err;
     int strict_order;
     uint32_t idesc_qk;                        // instruction descriptor of Q.K^T (bf16 or fp16 operands)
-    long units;                               // B * H * n_chunks * q_pairs work units
+    long units;                               // B * H * n_chunks * q_tiles work units
     int group;                                // chunks per CTA, sharing one load of Q (divides n_chunks)
     int merge;                                // 1: a CTA's group of chunks leaves one partial (index c / group)
     const float *row_bound;                   // constant-max softmax: bound per query row [B][H][Sq], or null
@@ -75,10 +73,10 @@ __device__ __forceinline__ TileRange chunk_tiles(const TcParams &p, int c) {
     return t;
 }
 
-// Work unit u -> (b, h, chunk group, query unit, chunk within the group),
+// Work unit u -> (b, h, chunk group, query tile, chunk within the group),
 // the chunk within the group fastest: CTA x owns units [x*group, (x+1)*group),
-// one query unit (a Q tile pair, or one Q tile) over `group` consecutive
-// chunks.  Across CTAs the query unit varies fastest, so the CTAs running at the same time walk through the
+// one Q tile over `group` consecutive chunks.  Across CTAs the query tile
+// varies fastest, so the CTAs running at the same time walk through the
 // same chunks and share their K/V in L2.
 struct Unit {
     int b, h, c, q0;
@@ -88,15 +86,15 @@ __device__ __forceinline__ Unit decode_unit(const TcParams &p, long unit) {
     uint32_t u = (uint32_t)unit;
     const uint32_t g = u % (uint32_t)p.group;
     u /= (uint32_t)p.group;
-    const uint32_t qp = u % (uint32_t)p.q_pairs;
-    u /= (uint32_t)p.q_pairs;
+    const uint32_t qp = u % (uint32_t)p.q_tiles;
+    u /= (uint32_t)p.q_tiles;
     const uint32_t groups = (uint32_t)(p.n_chunks / p.group);
     const uint32_t cg = u % groups;
     u /= groups;
     r.c = (int)(cg * p.group + g);
     r.h = (int)(u % (uint32_t)p.H);
     r.b = (int)(u / (uint32_t)p.H);
-    r.q0 = (int)qp * p.unit_rows;
+    r.q0 = (int)qp * tc::BM;
     return r;
 }
 

@@ -1,31 +1,45 @@
-// k6_attn_single.cu -- the bf16 tensor-core attention of k6_attn_tc.cu with one
-// 128-row Q tile per CTA.  It runs query ranges of at most one tile
-// (cross-attention from a short text or audio segment, self-attention calls of
-// at most 128 tokens), where the two-tile kernel would spend half its MMAs on
-// padding rows, and it takes longer ranges too (one CTA per Q tile).
+// k6_attn_single.cu -- joint-sequence attention on the 5th-generation tensor
+// cores of sm_103a (tcgen05 MMA into tensor memory, TMA tile loads), one
+// 128-row Q tile per CTA.
 //
-// Same result as attn_tc_kernel (per K/V chunk: O_c = softmax(Q K^T / sqrt(d)) V
-// and its log-sum-exp, non-causal, K/V = video keys then joint tokens), same
-// launch parameters, work units (of one Q tile) and outputs.  This kernel:
-//   - keeps S in three tensor-memory buffers (S(n) in buffer n % 3; O in the
-//     last 128 columns), so that S(n+1) and S(n+2) can be computed while the
-//     softmax works on S(n);
-//   - issues MMAs from two threads on different sub-partitions, Q.K^T from one
-//     and P.V from the other, with S(n) waiting only for the P.V of tile n-3
-//     whose P its buffer held;
-//   - splits each row's softmax between the two softmax warpgroups: warpgroup
-//     hf owns keys [64 hf, 64 hf + 64) of every S tile and columns
-//     [64 hf, 64 hf + 64) of O, for the same 128 rows (warps w and w + 4 reach
-//     the same TMEM lanes); the halves meet in shared memory behind a named
-//     barrier of those two warps (row max once per tile, row sum once per unit);
-//   - loads K/V in the order K_0 K_1 V_0 K_2 V_1 K_3 ..., so that K runs two
-//     tiles ahead of V in the ring;
-//   - with p.merge, merges a CTA's group of chunks into one partial in tensor
-//     memory, as the two-tile kernel does: (m, l, O) carry from one chunk into
-//     the next and only the group's last chunk runs the epilogue.
+// What it computes: for one K/V chunk c of the joint sequence (video keys
+// followed by the text/audio "joint tensors", xDiT PR #586 "How?"), every
+// query row i gets
+//   O_c[i] = sum_j softmax_j(q_i . k_j / sqrt(d)) v_j,  LSE_c[i] = log sum_j exp(q_i . k_j / sqrt(d)),
+// full and non-causal ("Context Parallelism in vLLM Omni Neuron",
+// "Self-Attention with Context Parallelism": local Q x full K/V; "Ring
+// attention (current implementation)": one K/V chunk per ring step, partials
+// combined through their log-sum-exp).  With one chunk (or one chunk group
+// merged in the kernel) the normalised output is written as bf16; otherwise
+// fp32 partials and LSE go to the caller's workspace for the merge kernel.
+// q/k/joint_k are bf16, fp16 or e4m3 (QK8); v/joint_v bf16.
+//
+// How (one CTA per work unit = 128 query rows of one (batch, head), over a
+// group of consecutive chunks):
+//   warp 8      TMA producer: the Q tile once, then K_j and V_j tiles of 128
+//               keys x 128 dims through a 5-slot ring of 32 KB slots (two
+//               128-byte-swizzled 64-dim panels; an e4m3 tile is one panel),
+//               in the order K_0 K_1 V_0 K_2 V_1 K_3 ..., so that K runs two
+//               tiles ahead of V.
+//   warp 9      one thread issues every S(n) = Q K_n^T (SS, both K-major) into
+//               tensor-memory buffer n % 3; the buffer held P(n-3), so S(n)
+//               waits for the P.V of tile n-3 (pv_buf).
+//   warp 10     one thread issues every O += P(n) V_n (P from tensor memory,
+//               V MN-major from shared memory), part by part as the softmax
+//               publishes P(n).  Two issuing threads on different SM
+//               sub-partitions: one would share its sub-partition's issue
+//               slots with two softmax warps and feed the tensor pipe too
+//               slowly.
+//   warps 0-7   two softmax warpgroups on alternate K/V tiles (whole rows, one
+//               thread per row = TMEM lane), passing the running row max from
+//               tile to tile; both run the epilogue, each writing half of O.
+//   Tensor memory (512 columns): S buffers 0-2 (128 columns each), O.
+//   With p.merge a CTA's group of chunks leaves one partial: (m, l, O) carry
+//   from one chunk into the next and only the group's last chunk runs the
+//   epilogue.
 // All mbarrier waits are bounded (globaltimer); a wait that runs out records
-// the error, and every warp still passes the same named barriers and leaves in
-// order, letting copies and MMAs in flight land before tensor memory is freed.
+// the error, sets the CTA's abort flag, and every warp leaves in order,
+// letting copies and MMAs in flight land before tensor memory is freed.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -65,7 +79,11 @@ constexpr int TMEM_COLS = 512;
 constexpr int O_COL = NSBUF * BN;             // O accumulator columns [384, 512)
 }  // namespace ts
 
-template <bool BOUNDED>
+// QK8: q/k/joint_k are e4m3.  Their tiles are 128 rows of 128 bytes (one
+// swizzle panel, 16 KB, in the first half of their 32 KB slots) and Q.K^T runs as
+// 4 kind::f8f6f4 MMAs of K = 32 per tile instead of 8 kind::f16 MMAs; P.V is
+// unchanged (bf16 P from tensor memory, bf16 V).
+template <bool BOUNDED, bool QK8>
 __global__ void __launch_bounds__(ts::THREADS, 1)
     attn_tc_single_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_jk,
@@ -141,8 +159,8 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
                 const Unit un = decode_unit(p, u);
                 const TileRange tr = chunk_tiles(p, un.c);
                 if (uc == 0) {  // the CTA's Q tile, once
-                    mbar_arrive_expect_tx(q_full, TILE);
-                    for (int half = 0; half < 2; half++)
+                    mbar_arrive_expect_tx(q_full, QK8 ? PANEL : TILE);
+                    for (int half = 0; half < (QK8 ? 1 : 2); half++)
                         tma_load_4d(smem + SMEM_Q + half * PANEL, &tm_q, q_full, half * 64, un.h, un.q0, un.b);
                 }
                 auto load = [&](int kv, int j) -> bool {  // kv 0: K_j, 1: V_j
@@ -151,10 +169,11 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
                     const uint32_t slot = kv_idx % NSTAGE;
                     if (!mbar_wait(&kv_empty[slot], ((kv_idx / NSTAGE) & 1) ^ 1, w)) return false;
                     const CUtensorMap *tm = kv == 0 ? (map == 0 ? &tm_k : &tm_jk) : (map == 0 ? &tm_v : &tm_jv);
-                    mbar_arrive_expect_tx(&kv_full[slot], TILE);
+                    const bool one_panel = QK8 && kv == 0;  // an e4m3 K tile is one 16 KB panel
+                    mbar_arrive_expect_tx(&kv_full[slot], one_panel ? PANEL : TILE);
                     uint8_t *dst = smem + SMEM_KV + slot * TILE;
                     tma_load_4d(dst, tm, &kv_full[slot], 0, un.h, row, un.b);
-                    tma_load_4d(dst + PANEL, tm, &kv_full[slot], 64, un.h, row, un.b);
+                    if (!one_panel) tma_load_4d(dst + PANEL, tm, &kv_full[slot], 64, un.h, row, un.b);
                     kv_idx++;
                     return true;
                 };
@@ -198,10 +217,18 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
                         if (n >= NSBUF && !(ok = mbar_wait(&pv_buf[n % NSBUF], (n / NSBUF - 1) & 1, w))) break;
                         tc_fence_after();
                         const uint64_t kb = dq0 + ((uint64_t)(SMEM_KV - SMEM_Q + (kidx % NSTAGE) * TILE) >> 4);
+                        if constexpr (QK8) {  // 32 head dims (32 bytes of each row) per MMA
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; kk++) {
-                            const uint64_t off = (uint64_t)((kk >> 2) * PANEL + (kk & 3) * 32) >> 4;
-                            mma_ss(tmem + (n % NSBUF) * BN, dq0 + off, kb + off, idesc_qk, kk > 0);
+                            for (int kk = 0; kk < D / 32; kk++) {
+                                const uint64_t off = (uint64_t)(kk * 32) >> 4;
+                                mma_ss_f8(tmem + (n % NSBUF) * BN, dq0 + off, kb + off, idesc_qk, kk > 0);
+                            }
+                        } else {  // 16 head dims per MMA, 4 per 64-dim panel
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; kk++) {
+                                const uint64_t off = (uint64_t)((kk >> 2) * PANEL + (kk & 3) * 32) >> 4;
+                                mma_ss(tmem + (n % NSBUF) * BN, dq0 + off, kb + off, idesc_qk, kk > 0);
+                            }
                         }
                         tc_commit(&s_full[n % NSBUF]);
                         tc_commit(&kv_empty[kidx % NSTAGE]);
@@ -483,14 +510,18 @@ cudaError_t launch_attn_tc_single(const Geom &g, const void *q, const void *k, c
     // an empty segment never issues loads; give its maps a valid stand-in
     const void *kk = has_video ? k : jk, *vv = has_video ? v : jv;
     const long kv_rows = has_video ? g.Nv : g.Nj;
-    if (!make_bshd_map(&mq, q, g.Sq, g.H, g.B, false, why) || !make_bshd_map(&mk, kk, kv_rows, g.H, g.B, false, why) ||
+    // the tile copies move 2-byte elements (fp16 q/k travel through the same maps), or 1-byte e4m3 q/k
+    const int qkb = opt.qk8 ? 1 : 2;
+    if (!make_bshd_map(&mq, q, g.Sq, g.H, g.B, false, why, qkb) ||
+        !make_bshd_map(&mk, kk, kv_rows, g.H, g.B, false, why, has_video ? qkb : 2) ||
         !make_bshd_map(&mv, vv, kv_rows, g.H, g.B, false, why) ||
-        !make_bshd_map(&mjk, has_joint ? jk : kk, has_joint ? g.Nj : kv_rows, g.H, g.B, false, why) ||
+        !make_bshd_map(&mjk, has_joint ? jk : kk, has_joint ? g.Nj : kv_rows, g.H, g.B, false, why,
+                       has_joint || has_video ? qkb : 2) ||
         !make_bshd_map(&mjv, has_joint ? jv : vv, has_joint ? g.Nj : kv_rows, g.H, g.B, false, why))
         return cudaErrorInvalidValue;
-    cudaError_t attr_err = set_max_dynamic_smem((const void *)attn_tc_single_kernel<false>, ts::SMEM_ALLOC);
-    if (attr_err == cudaSuccess)
-        attr_err = set_max_dynamic_smem((const void *)attn_tc_single_kernel<true>, ts::SMEM_ALLOC);
+    auto kernel = opt.qk8 ? (opt.row_bound ? attn_tc_single_kernel<true, true> : attn_tc_single_kernel<false, true>)
+                          : (opt.row_bound ? attn_tc_single_kernel<true, false> : attn_tc_single_kernel<false, false>);
+    cudaError_t attr_err = set_max_dynamic_smem((const void *)kernel, ts::SMEM_ALLOC);
     if (attr_err != cudaSuccess) return attr_err;
     TcParams p;
     p.S = g.S;
@@ -499,8 +530,7 @@ cudaError_t launch_attn_tc_single(const Geom &g, const void *q, const void *k, c
     p.Nj = g.Nj;
     p.H = g.H;
     p.n_chunks = n_chunks;
-    p.unit_rows = tc::BM;  // one Q tile per unit
-    p.q_pairs = (int)((g.Sq + tc::BM - 1) / tc::BM);
+    p.q_tiles = (int)((g.Sq + tc::BM - 1) / tc::BM);
     p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)g.d));
     p.out = out;
     p.lse = lse;
@@ -509,15 +539,18 @@ cudaError_t launch_attn_tc_single(const Geom &g, const void *q, const void *k, c
     p.wait_limit_ns = opt.wait_limit_ns;
     p.err = opt.err;
     p.strict_order = opt.strict_order;
-    p.idesc_qk = opt.qk_f16 ? (idesc_bf16_f32(tc::BM, tc::BN, false) & ~((7u << 7) | (7u << 10)))
-                            : idesc_bf16_f32(tc::BM, tc::BN, false);
-    p.units = (long)g.B * g.H * n_chunks * p.q_pairs;
+    // Q.K^T operands: bf16 (A/B format 1), fp16 (format 0) or e4m3 (kind::f8f6f4, format 0); P.V stays bf16
+    p.idesc_qk = opt.qk8      ? idesc_e4m3_f32(tc::BM, tc::BN)
+                 : opt.qk_f16 ? (idesc_bf16_f32(tc::BM, tc::BN, false) & ~((7u << 7) | (7u << 10)))
+                              : idesc_bf16_f32(tc::BM, tc::BN, false);
+    p.units = (long)g.B * g.H * n_chunks * p.q_tiles;
     if (p.units == 0) return cudaSuccess;
     if (p.units >= (1L << 31)) {
         if (why) *why = "too many work units (batch x heads x chunks must stay below 2^31)";
         return cudaErrorInvalidValue;
     }
-    // chunks per CTA (sharing one load of Q): as in the two-tile kernel
+    // chunks per CTA (sharing one load of Q): the caller's group, else the
+    // library's choice (chunk_group); with merge the group leaves one partial
     p.group = opt.group > 0 ? opt.group : chunk_group(g, n_chunks);
     if (n_chunks % p.group) {
         if (why) *why = "the chunk group must divide the chunk count";
@@ -527,10 +560,7 @@ cudaError_t launch_attn_tc_single(const Geom &g, const void *q, const void *k, c
     p.out_f32 = (p.merge ? n_chunks / p.group : n_chunks) > 1;
     p.row_bound = opt.row_bound;
     const long grid = p.units / p.group;
-    if (opt.row_bound)
-        attn_tc_single_kernel<true><<<(unsigned)grid, ts::THREADS, ts::SMEM_ALLOC, st>>>(mq, mk, mv, mjk, mjv, p);
-    else
-        attn_tc_single_kernel<false><<<(unsigned)grid, ts::THREADS, ts::SMEM_ALLOC, st>>>(mq, mk, mv, mjk, mjv, p);
+    kernel<<<(unsigned)grid, ts::THREADS, ts::SMEM_ALLOC, st>>>(mq, mk, mv, mjk, mjv, p);
     return cudaGetLastError();
 }
 

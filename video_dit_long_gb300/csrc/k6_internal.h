@@ -101,10 +101,10 @@ cudaError_t launch_attn_f32(const Geom &g, const float *q, const float *k, const
 struct AttnTcOptions {
     unsigned long long wait_limit_ns;
     int *err;
-    int strict_order;        // 1: wait for P.V to finish before reusing its TMEM
+    int strict_order;        // accepted; the kernel already waits for P.V before reusing its TMEM
     int qk_f16;              // 1: q/k/joint_k are fp16 (Q.K^T in fp16), else bf16
     const float *row_bound = nullptr;  // constant-max softmax bounds [B][H][Sq] (natural-log units), or null
-    int qk8 = 0;             // 1: q/k/joint_k are e4m3 (Q.K^T on kind::f8f6f4); two-tile kernel only
+    int qk8 = 0;             // 1: q/k/joint_k are e4m3 (Q.K^T on kind::f8f6f4)
     int group = 0;           // chunks per CTA (divides n_chunks); 0: the library's choice, chunk_group()
     int merge = 0;           // 1: each CTA's group of chunks leaves one partial (n_chunks / group partials)
 };
@@ -118,10 +118,7 @@ int chunk_group(const Geom &g, int n_chunks);
 // bound must hold B*H*Sq + B*H floats (the tail is the key-norm maximum).
 cudaError_t launch_row_bounds(const Geom &g, k6attn_dtype qk_dtype, const void *q, const void *k, const void *jk,
                               float *bound, cudaStream_t st);
-cudaError_t launch_attn_tc(const Geom &g, const void *q, const void *k, const void *v, const void *jk,
-                           const void *jv, int n_chunks, void *out, float *lse, const AttnTcOptions &opt,
-                           cudaStream_t st, const char **why);
-// The same attention for at most 128 query rows (one Q tile per CTA).
+// One CTA per 128-row Q tile and group of chunks (k6_attn_single.cu).
 cudaError_t launch_attn_tc_single(const Geom &g, const void *q, const void *k, const void *v, const void *jk,
                                   const void *jv, int n_chunks, void *out, float *lse, const AttnTcOptions &opt,
                                   cudaStream_t st, const char **why);
