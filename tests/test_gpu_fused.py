@@ -206,6 +206,40 @@ def test_chunk_groups_match_oracle(name, n, group):
     compare(to_host(merged), ref, mlse.cpu().numpy().astype(np.float64), ref_lse, "bf16")
 
 
+def test_per_chunk_partials_of_multi_chunk_ctas_match_oracle():
+    """k6attn_attention_chunks at a size where the library gives each CTA
+    several chunks (here 2) but still writes one partial per chunk: every
+    CTA runs an epilogue per chunk and starts the next chunk afresh.  Sampled
+    rows of three chunks' partials against the oracle's attention over that
+    chunk's keys, and the merge of all eight against all keys."""
+    k6 = K()
+    w = Workload("groups", 1, 8, 128, "bf16", (4, 32, 32), 96, (32, 48, 48), 0, 1.0, 1.0, (8,))  # S = 4,192
+    n = 8
+    x = inputs.make_inputs(w)
+    d = dev_inputs(w, x)
+    h = k6.Handle.for_workload(w)
+    assert h.chunk_group(n) >= 2  # the path under test: several chunks per CTA
+    rot = {nm: torch.empty(d[nm].shape, dtype=torch.float16, device="cuda") for nm in ("q", "k", "jk")}
+    h.rope_qk(d["q"], d["k"], d["jk"], q_out=rot["q"], k_out=rot["k"], joint_k_out=rot["jk"], out_dtype=k6.F16)
+    po = torch.empty((n, w.B, w.S, w.H, w.d), dtype=torch.float32, device="cuda")
+    pl = torch.empty((n, w.B, w.H, w.S), dtype=torch.float32, device="cuda")
+    h.attention_chunks(rot["q"], rot["k"], d["v"], rot["jk"], d["jv"], n, po, pl, qk_dtype=k6.F16)
+    merged = torch.empty((w.B, w.S, w.H, w.d), dtype=torch.bfloat16, device="cuda")
+    mlse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device="cuda")
+    h.lse_merge(po, pl, n, merged, mlse)
+    h.sync()
+    g = geom(w)
+    L = w.S // n
+    rows = inputs.sample_rows(w.S, w.Nv, L, count=256)
+    for c in (0, 3, 7):  # chunk 7 holds the joint keys
+        ref, ref_lse = O.attention(g, x["q"], x["k"], x["v"], x["jk"], x["jv"], kv_range=(c * L, (c + 1) * L),
+                                   rows=rows)
+        got, got_lse = to_host(po[c])[:, rows], pl[c].cpu().numpy().astype(np.float64)[:, :, rows]
+        compare(got, ref, got_lse, ref_lse, "bf16")
+    ref, ref_lse = O.attention(g, x["q"], x["k"], x["v"], x["jk"], x["jv"], rows=rows)
+    compare(to_host(merged)[:, rows], ref, mlse.cpu().numpy().astype(np.float64)[:, :, rows], ref_lse, "bf16")
+
+
 def test_chunk_groups_peaked_rescale_across_chunks():
     """Q, K x 4 with pre-rotated inputs: the running max moves (and O is rescaled)
     at chunk boundaries inside a group, not only between tiles of one chunk."""
