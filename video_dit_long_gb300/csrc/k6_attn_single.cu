@@ -23,7 +23,10 @@
 //               tiles ahead of V.
 //   warp 9      one thread issues every S(n) = Q K_n^T (SS, both K-major) into
 //               tensor-memory buffer n % 3; the buffer held P(n-3), so S(n)
-//               waits for the P.V of tile n-3 (pv_buf).
+//               waits for the P.V of tile n-3 (pv_buf), and having seen it
+//               done, frees V(n-3)'s ring slot (the softmax group that sees
+//               S(n) done frees K(n)'s), so the issuing threads spend no
+//               commits on the ring.
 //   warp 10     one thread issues every O += P(n) V_n (P from tensor memory,
 //               V MN-major from shared memory), part by part as the softmax
 //               publishes P(n).  Two issuing threads on different SM
@@ -206,15 +209,23 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
             uint32_t uc = 0;
             bool ok = true;
             if (warp == 9) {
+                // This thread also frees V(n-3)'s ring slot: it waits for that tile's P.V
+                // anyway (pv_buf) before S(n), so the P.V thread needs no commit for it.
+                uint32_t vslot[4] = {0, 0, 0, 0};  // ring slot of V(m) at m % 4
                 for (long u = u0; u < u1 && ok; u++, uc++) {
                     const int T = chunk_tiles(p, decode_unit(p, u).c).T;
                     ok = uc > 0 || mbar_wait(q_full, 0, w);
                     for (int t = 0; t < T && ok; t++) {
                         const uint32_t n = tile + t;
-                        // loads run K_0 K_1 V_0 K_2 V_1 K_3 ...: K_t is load 2t - 1 of the unit for t >= 2
+                        // loads run K_0 K_1 V_0 K_2 V_1 K_3 ...: K_t is load 2t - 1 of the unit for t >= 2,
+                        // V_t load min(t + 2, T) + t
                         const uint32_t kidx = kv_idx + (t < 2 ? t : 2 * t - 1);
+                        vslot[n % 4] = (kv_idx + (t + 2 < T ? t + 2 : T) + t) % NSTAGE;
+                        if (n >= NSBUF) {  // before waiting for K(n): that load may need this slot
+                            if (!(ok = mbar_wait(&pv_buf[n % NSBUF], (n / NSBUF - 1) & 1, w))) break;
+                            mbar_arrive(&kv_empty[vslot[(n - NSBUF) % 4]]);  // V(n-3) read by its P.V
+                        }
                         if (!(ok = mbar_wait(&kv_full[kidx % NSTAGE], (kidx / NSTAGE) & 1, w))) break;
-                        if (n >= NSBUF && !(ok = mbar_wait(&pv_buf[n % NSBUF], (n / NSBUF - 1) & 1, w))) break;
                         tc_fence_after();
                         const uint64_t kb = dq0 + ((uint64_t)(SMEM_KV - SMEM_Q + (kidx % NSTAGE) * TILE) >> 4);
                         if constexpr (QK8) {  // 32 head dims (32 bytes of each row) per MMA
@@ -230,8 +241,7 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
                                 mma_ss(tmem + (n % NSBUF) * BN, dq0 + off, kb + off, idesc_qk, kk > 0);
                             }
                         }
-                        tc_commit(&s_full[n % NSBUF]);
-                        tc_commit(&kv_empty[kidx % NSTAGE]);
+                        tc_commit(&s_full[n % NSBUF]);  // K(n)'s slot is freed by the softmax, which sees S(n)
                     }
                     kv_idx += 2 * T;
                     tile += T;
@@ -259,7 +269,6 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
                         }
                         if (!ok) break;
                         tc_commit(&pv_buf[n % NSBUF]);
-                        tc_commit(&kv_empty[vidx % NSTAGE]);
                         if (j + 1 == T && last) tc_commit(o_final);
                     }
                     kv_idx += 2 * T;
@@ -292,6 +301,7 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
         float *xe = xm + BM;                                      // [unit parity][group][row][l, m]
         const float sl2 = p.scale_log2;
         uint32_t tile = 0, uc = 0, n_epi = 0;
+        uint32_t kv_idx = 0;      // K/V loads of earlier units
         bool ok = true;
         float m_run = -INFINITY;  // the row max in force after the latest tile of this unit
         float m_own = -INFINITY;  // the max l_own is expressed in
@@ -320,6 +330,8 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
                     break;
                 }
                 tc_fence_after();
+                // S(n) is complete: K(n)'s ring slot (load 2j - 1 of the unit, j for j < 2) is free
+                if (r == 0) mbar_arrive(&kv_empty[(kv_idx + (j < 2 ? j : 2 * j - 1)) % NSTAGE]);
                 if constexpr (!BOUNDED) {
                     // the max after tile n-1 (posted by the other group early in its
                     // tile), every phase waited in turn
@@ -420,6 +432,7 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
             if (!ok) break;
             if (!last) {  // the group's partial is written after its last chunk
                 tile += T;
+                kv_idx += 2 * T;
                 continue;
             }
             // epilogue: the two groups combine their row sums, each writes half of O's
@@ -488,6 +501,7 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
             }
             n_epi++;
             tile += T;
+            kv_idx += 2 * T;
         }
     }
 
