@@ -1,0 +1,169 @@
+"""Host-side model of the attention kernel's K/V ring (k6_attn_single.cu).
+
+The kernel's producer loads a unit's K/V tiles in the order K_0 K_1, then V_j
+followed by K_{j+2}, into a 5-slot ring; the Q.K^T thread consumes the K tiles,
+the P.V thread the V tiles.  A slot is freed by an mbarrier arrival: K(n)'s by
+the softmax group that sees S(n) done, V(n)'s by the Q.K^T thread once it has
+seen P(n).V done (before it issues S(n+3)).  Each slot's kv_full barrier is
+tested by phase parity only, so a wait for a slot's load is unambiguous only if
+the slot's previous load has already landed when the wait starts.
+
+This model writes each thread's waits in the kernel's program order as a
+dependency graph and checks, for every sequence of up to three chunks of 1-7
+tiles and a few long ones:
+- the load-index formulas (k_load, v_load) agree with the producer's order;
+- every load the producer issues finds its slot freed by someone;
+- the graph has no cycle (no thread waits on itself);
+- no wait can match an earlier phase of its slot.
+A lead of 3 (K_0 K_1 K_2 V_0 K_3 ...) with the same wait order is shown to
+break the last condition, which is why the kernel keeps a lead of 2.
+"""
+import collections
+import itertools
+import sys
+
+NSTAGE, NSBUF = 5, 3
+
+
+def k_load(t, T, A):
+    return t if t < A else 2 * t - A + 1
+
+
+def v_load(j, T, A):
+    lead = min(A, T)
+    more = max(T - A, 0)
+    return lead + j + min(j, more)
+
+
+def producer_order(Ts, A):
+    loads, tile = [], 0
+    for T in Ts:
+        loads += [("K", tile + t) for t in range(min(A, T))]
+        for j in range(T):
+            loads.append(("V", tile + j))
+            if j + A < T:
+                loads.append(("K", tile + j + A))
+        tile += T
+    return loads, tile
+
+
+def model(Ts, A):
+    """Dependency graph of the kernel's waits: node -> set of nodes it waits for."""
+    loads, N = producer_order(Ts, A)
+    idx = {l: i for i, l in enumerate(loads)}
+    deps = collections.defaultdict(set)
+
+    def dep(a, b):
+        deps[a].add(b)
+
+    release = {idx[("K", n)]: ("wake", n) for n in range(N)}
+    release.update({idx[("V", m)]: ("S_release", m + NSBUF) for m in range(N - NSBUF)})
+    consumer = {}
+    for i in range(len(loads)):
+        if i:
+            dep(("load", i), ("load", i - 1))        # the producer issues loads in order
+        if i >= NSTAGE:
+            assert i - NSTAGE in release, ("a load needs a slot nobody frees", Ts, i)
+            dep(("load", i), release[i - NSTAGE])
+        dep(("landed", i), ("load", i))
+    for n in range(N):
+        consumer[idx[("K", n)]] = ("S", n)
+        consumer[idx[("V", n)]] = ("PV", n)
+        # Q.K^T thread, in order: wait P(n-3).V, free V(n-3); wait K(n); issue S(n)
+        if n:
+            dep(("S_release", n), ("S", n - 1))
+        if n >= NSBUF:
+            dep(("S_release", n), ("PV_done", n - NSBUF))
+        dep(("wait_K", n), ("S_release", n))
+        dep(("S", n), ("wait_K", n))
+        dep(("S", n), ("landed", idx[("K", n)]))
+        # softmax: tile n after S(n), the max of tile n-1, and its group's previous tile
+        dep(("wake", n), ("S", n))
+        if n:
+            dep(("wake", n), ("wake", n - 1))
+        if n >= 2:
+            dep(("wake", n), ("P", n - 2))
+        dep(("P", n), ("wake", n))
+        # P.V thread, in order: wait V(n), then the parts of P(n); issue P(n).V
+        if n:
+            dep(("wait_V", n), ("PV", n - 1))
+        dep(("PV", n), ("wait_V", n))
+        dep(("PV", n), ("landed", idx[("V", n)]))
+        dep(("PV", n), ("P", n))
+        dep(("PV_done", n), ("PV", n))
+    return loads, idx, deps, consumer, N
+
+
+def ancestors(deps, root):
+    seen, stack = set(), [root]
+    while stack:
+        for y in deps.get(stack.pop(), ()):
+            if y not in seen:
+                seen.add(y)
+                stack.append(y)
+    return seen
+
+
+def acyclic(deps):
+    sys.setrecursionlimit(max(10000, sys.getrecursionlimit()))
+    state = {}
+
+    def visit(x):
+        st = state.get(x)
+        if st == 1:
+            return False
+        if st == 2:
+            return True
+        state[x] = 1
+        ok = all(visit(y) for y in deps.get(x, ()))
+        state[x] = 2
+        return ok
+
+    nodes = set(deps) | {b for v in deps.values() for b in v}
+    return all(visit(x) for x in nodes)
+
+
+def aliasing(Ts, A):
+    """The first wait that could match an earlier phase of its slot, or None."""
+    loads, idx, deps, consumer, N = model(Ts, A)
+    for i, (kind, n) in enumerate(loads):
+        if i < NSTAGE:
+            continue
+        wait = ("wait_K" if kind == "K" else "wait_V", n)
+        if consumer[i - NSTAGE] not in ancestors(deps, wait):
+            return loads[i], loads[i - NSTAGE]
+    return None
+
+
+CASES = [list(Ts) for k in range(1, 4) for Ts in itertools.product(range(1, 8), repeat=k)] + \
+    [[17], [51, 51], [52, 51, 51, 52]]
+
+
+def test_load_index_formulas_match_the_producer_order():
+    for T in range(1, 80):
+        loads, _ = producer_order([T], 2)
+        for t in range(T):
+            assert loads[k_load(t, T, 2)] == ("K", t)
+            assert loads[v_load(t, T, 2)] == ("V", t)
+        # the closed forms in the kernel for a lead of 2
+        for t in range(T):
+            assert k_load(t, T, 2) == (t if t < 2 else 2 * t - 1)
+            assert v_load(t, T, 2) == (t + 2 if t + 2 < T else T) + t
+
+
+def test_every_slot_is_freed_and_no_wait_cycles():
+    for Ts in CASES:
+        _, _, deps, _, _ = model(Ts, 2)   # model() asserts that every needed slot is freed
+        assert acyclic(deps), Ts
+
+
+def test_no_wait_can_match_an_earlier_phase():
+    for Ts in CASES:
+        assert aliasing(Ts, 2) is None, Ts
+
+
+def test_a_lead_of_three_would_alias():
+    # with K three tiles ahead, the P.V thread could wait for V(n) while K(n)
+    # (the slot's previous load) is still in flight
+    found = aliasing([5], 3)
+    assert found == (("V", 2), ("K", 2))

@@ -61,6 +61,15 @@ using tc::D;
 using tc::PANEL;
 using tc::TILE;
 constexpr int NSTAGE = 5;                     // K/V tile slots (four leave V(n+1) too little time to arrive)
+// K_t is loaded before V_{t-KAHEAD} (see k_load, v_load).  A ring slot holds K
+// and V tiles in turn and its kv_full barrier is tested by phase parity only,
+// so a consumer may wait for a load only once the slot's previous load has
+// landed, or the wait could match that earlier phase.  With KAHEAD = 2 the
+// slot before V(n) held K(n-1), which has landed when P(n-1).V is issued, and
+// the slot before K(n) held V(n-4), landed once P(n-3).V is done: the waits
+// below come in that order.  (A lead of 3 would let the P.V thread reach V(n)
+// while K(n) is still in flight; checked on a model of the waits.)
+constexpr int KAHEAD = 2;
 constexpr int NSBUF = 3;                      // S buffers in tensor memory
 constexpr int SMEM_Q = 0;
 constexpr int SMEM_KV = TILE;
@@ -81,6 +90,19 @@ constexpr int REGS_CONTROL = 136;
 constexpr int TMEM_COLS = 512;
 constexpr int O_COL = NSBUF * BN;             // O accumulator columns [384, 512)
 }  // namespace ts
+
+// Load order of a unit of T K/V tiles: K_0 .. K_{A-1}, then V_j followed by
+// K_{j+A} (while j + A < T), A = KAHEAD: K runs A tiles ahead of V.  The
+// index of each tile's load within the unit:
+__device__ __forceinline__ uint32_t k_load(int t, int T) {
+    (void)T;
+    return t < ts::KAHEAD ? t : 2 * t - ts::KAHEAD + 1;
+}
+__device__ __forceinline__ uint32_t v_load(int j, int T) {
+    const int lead = T < ts::KAHEAD ? T : ts::KAHEAD;      // K loads before V_0
+    const int more = T > ts::KAHEAD ? T - ts::KAHEAD : 0;  // K loads that follow a V
+    return lead + j + (j < more ? j : more);
+}
 
 // QK8: q/k/joint_k are e4m3.  Their tiles are 128 rows of 128 bytes (one
 // swizzle panel, 16 KB, in the first half of their 32 KB slots) and Q.K^T runs as
@@ -180,11 +202,10 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
                     kv_idx++;
                     return true;
                 };
-                // K_0 K_1, then V_j K_{j+2}: load kv_idx + t holds K_t for t < 2, then
-                // V_j is load kv_idx + min(j + 2, T) + j and K_t (t >= 2) load kv_idx + 2t - 1
+                // K_0 .. K_{A-1}, then V_j K_{j+A}: the order k_load / v_load describe
                 const int T = tr.T;
-                for (int t = 0; t < 2 && t < T && ok; t++) ok = load(0, t);
-                for (int j = 0; j < T && ok; j++) ok = load(1, j) && (j + 2 >= T || load(0, j + 2));
+                for (int t = 0; t < KAHEAD && t < T && ok; t++) ok = load(0, t);
+                for (int j = 0; j < T && ok; j++) ok = load(1, j) && (j + KAHEAD >= T || load(0, j + KAHEAD));
             }
             // let every copy issued into shared memory land before the CTA can exit
             if (uc > 0) mbar_drain(q_full, 0, tc::DRAIN_NS);
@@ -217,11 +238,9 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
                     ok = uc > 0 || mbar_wait(q_full, 0, w);
                     for (int t = 0; t < T && ok; t++) {
                         const uint32_t n = tile + t;
-                        // loads run K_0 K_1 V_0 K_2 V_1 K_3 ...: K_t is load 2t - 1 of the unit for t >= 2,
-                        // V_t load min(t + 2, T) + t
-                        const uint32_t kidx = kv_idx + (t < 2 ? t : 2 * t - 1);
-                        vslot[n % 4] = (kv_idx + (t + 2 < T ? t + 2 : T) + t) % NSTAGE;
-                        if (n >= NSBUF) {  // before waiting for K(n): that load may need this slot
+                        const uint32_t kidx = kv_idx + k_load(t, T);
+                        vslot[n % 4] = (kv_idx + v_load(t, T)) % NSTAGE;
+                        if (n >= NSBUF) {  // before waiting for K(n): the slot before K(n) held V(n-4)
                             if (!(ok = mbar_wait(&pv_buf[n % NSBUF], (n / NSBUF - 1) & 1, w))) break;
                             mbar_arrive(&kv_empty[vslot[(n - NSBUF) % 4]]);  // V(n-3) read by its P.V
                         }
@@ -253,7 +272,8 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
                     const bool last = !p.merge || u + 1 == u1;  // this chunk's O goes to the epilogue
                     for (int j = 0; j < T && ok; j++) {
                         const uint32_t n = tile + j;
-                        const uint32_t vidx = kv_idx + (j + 2 < T ? j + 2 : T) + j;  // V_j
+                        const uint32_t vidx = kv_idx + v_load(j, T);  // V_j
+                        // the slot's previous load, K(n-1), has landed: P(n-1).V was issued
                         if (!(ok = mbar_wait(&kv_full[vidx % NSTAGE], (vidx / NSTAGE) & 1, w))) break;
                         // P(n) (bf16, keys in order) sits over the first BN/2 columns of its buffer;
                         // each part's P.V starts as soon as the softmax has published that part
@@ -330,8 +350,8 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                // S(n) is complete: K(n)'s ring slot (load 2j - 1 of the unit, j for j < 2) is free
-                if (r == 0) mbar_arrive(&kv_empty[(kv_idx + (j < 2 ? j : 2 * j - 1)) % NSTAGE]);
+                // S(n) is complete: K(n)'s ring slot is free
+                if (r == 0) mbar_arrive(&kv_empty[(kv_idx + k_load(j, T)) % NSTAGE]);
                 if constexpr (!BOUNDED) {
                     // the max after tile n-1 (posted by the other group early in its
                     // tile), every phase waited in turn
