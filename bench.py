@@ -711,7 +711,8 @@ def run_only(args):
     if args.only == "step":
         res, _ = measure(w, n, P, args.steps, args.warmup, False, step_only=True)
         return {"only": "step", "workload": w.name, "n_chunks": n, "ms_per_step": res["total_ms"] / args.steps,
-                "per_kernel_ms": res["per_kernel_ms"], "chunks_per_cta": res["group"], "partials": res["parts"]}
+                "per_kernel_ms": res["per_kernel_ms"], "chunks_per_cta": res["group"], "partials": res["parts"],
+                "clocks": res["clocks"]}
     if args.only == "merge_per_chunk":
         res, _ = measure(w, n, P, args.steps, args.warmup, False, clocks=False)
         return {"only": "merge_per_chunk", "workload": w.name, "n_chunks": n, "ms": res["merge_per_chunk_ms"]}

@@ -170,20 +170,25 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
 
     if (warp >= 8) {
         regs_decrease<REGS_CONTROL>();
-        if (warp == 8 && lane == 0) {
+        if (warp == 8) {
             // -------------------------------------------------- TMA producer
-            prefetch_tmap(&tm_q);
-            prefetch_tmap(&tm_k);
-            prefetch_tmap(&tm_v);
-            prefetch_tmap(&tm_jk);
-            prefetch_tmap(&tm_jv);
+            // The whole warp runs the loop and waits; one elected lane arms the
+            // barriers and issues the copies.
+            const bool leader = elect_one();
+            if (leader) {
+                prefetch_tmap(&tm_q);
+                prefetch_tmap(&tm_k);
+                prefetch_tmap(&tm_v);
+                prefetch_tmap(&tm_jk);
+                prefetch_tmap(&tm_jv);
+            }
             uint32_t kv_idx = 0;  // K/V tile loads issued so far
             uint32_t uc = 0;      // units started by this CTA
             bool ok = true;
             for (long u = u0; u < u1 && ok; u++, uc++) {
                 const Unit un = decode_unit(p, u);
                 const TileRange tr = chunk_tiles(p, un.c);
-                if (uc == 0) {  // the CTA's Q tile, once
+                if (uc == 0 && leader) {  // the CTA's Q tile, once
                     mbar_arrive_expect_tx(q_full, QK8 ? PANEL : TILE);
                     for (int half = 0; half < (QK8 ? 1 : 2); half++)
                         tma_load_4d(smem + SMEM_Q + half * PANEL, &tm_q, q_full, half * 64, un.h, un.q0, un.b);
@@ -192,13 +197,15 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
                     int map, row, valid;
                     tr.at(j, map, row, valid);
                     const uint32_t slot = kv_idx % NSTAGE;
-                    if (!mbar_wait(&kv_empty[slot], ((kv_idx / NSTAGE) & 1) ^ 1, w)) return false;
+                    if (!mbar_wait_w(&kv_empty[slot], ((kv_idx / NSTAGE) & 1) ^ 1, w)) return false;
                     const CUtensorMap *tm = kv == 0 ? (map == 0 ? &tm_k : &tm_jk) : (map == 0 ? &tm_v : &tm_jv);
                     const bool one_panel = QK8 && kv == 0;  // an e4m3 K tile is one 16 KB panel
-                    mbar_arrive_expect_tx(&kv_full[slot], one_panel ? PANEL : TILE);
-                    uint8_t *dst = smem + SMEM_KV + slot * TILE;
-                    tma_load_4d(dst, tm, &kv_full[slot], 0, un.h, row, un.b);
-                    if (!one_panel) tma_load_4d(dst + PANEL, tm, &kv_full[slot], 64, un.h, row, un.b);
+                    if (leader) {
+                        mbar_arrive_expect_tx(&kv_full[slot], one_panel ? PANEL : TILE);
+                        uint8_t *dst = smem + SMEM_KV + slot * TILE;
+                        tma_load_4d(dst, tm, &kv_full[slot], 0, un.h, row, un.b);
+                        if (!one_panel) tma_load_4d(dst + PANEL, tm, &kv_full[slot], 64, un.h, row, un.b);
+                    }
                     kv_idx++;
                     return true;
                 };
@@ -211,11 +218,13 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
             if (uc > 0) mbar_drain(q_full, 0, tc::DRAIN_NS);
             for (uint32_t idx = kv_idx > NSTAGE ? kv_idx - NSTAGE : 0; idx < kv_idx; idx++)
                 mbar_drain(&kv_full[idx % NSTAGE], (idx / NSTAGE) & 1, tc::DRAIN_NS);
-        } else if ((warp == 9 || warp == 10) && lane == 0) {
+        } else if (warp == 9 || warp == 10) {
             // ------------------------------------------------- MMA issuers
             // Warp 9 issues every S(n) = Q K_n^T, warp 10 every O += P(n).V_n: one
-            // issuing thread would share its sub-partition's issue slots with two
-            // softmax warps and feed the tensor pipe too slowly.  K/V tile n counts
+            // issuer would share its sub-partition's issue slots with two softmax
+            // warps and feed the tensor pipe too slowly.  Each issuer is a whole,
+            // converged warp: all lanes wait and compute descriptors, one elected
+            // lane issues the MMAs and commits (the _w forms).  K/V tile n counts
             // over the CTA's units.  S(n) goes into buffer n % 3, which held P(n-3):
             // it waits for pv_buf[n % 3], committed after the P.V of tile n-3, so
             // it never overwrites a P still to be read.  P(n).V waits for the
@@ -230,37 +239,37 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
             uint32_t uc = 0;
             bool ok = true;
             if (warp == 9) {
-                // This thread also frees V(n-3)'s ring slot: it waits for that tile's P.V
+                // This warp also frees V(n-3)'s ring slot: it waits for that tile's P.V
                 // anyway (pv_buf) before S(n), so the P.V thread needs no commit for it.
                 uint32_t vslot[4] = {0, 0, 0, 0};  // ring slot of V(m) at m % 4
                 for (long u = u0; u < u1 && ok; u++, uc++) {
                     const int T = chunk_tiles(p, decode_unit(p, u).c).T;
-                    ok = uc > 0 || mbar_wait(q_full, 0, w);
+                    ok = uc > 0 || mbar_wait_w(q_full, 0, w);
                     for (int t = 0; t < T && ok; t++) {
                         const uint32_t n = tile + t;
                         const uint32_t kidx = kv_idx + k_load(t, T);
                         vslot[n % 4] = (kv_idx + v_load(t, T)) % NSTAGE;
                         if (n >= NSBUF) {  // before waiting for K(n): the slot before K(n) held V(n-4)
-                            if (!(ok = mbar_wait(&pv_buf[n % NSBUF], (n / NSBUF - 1) & 1, w))) break;
-                            mbar_arrive(&kv_empty[vslot[(n - NSBUF) % 4]]);  // V(n-3) read by its P.V
+                            if (!(ok = mbar_wait_w(&pv_buf[n % NSBUF], (n / NSBUF - 1) & 1, w))) break;
+                            if (lane == 0) mbar_arrive(&kv_empty[vslot[(n - NSBUF) % 4]]);  // V(n-3) read by its P.V
                         }
-                        if (!(ok = mbar_wait(&kv_full[kidx % NSTAGE], (kidx / NSTAGE) & 1, w))) break;
+                        if (!(ok = mbar_wait_w(&kv_full[kidx % NSTAGE], (kidx / NSTAGE) & 1, w))) break;
                         tc_fence_after();
                         const uint64_t kb = dq0 + ((uint64_t)(SMEM_KV - SMEM_Q + (kidx % NSTAGE) * TILE) >> 4);
                         if constexpr (QK8) {  // 32 head dims (32 bytes of each row) per MMA
 #pragma unroll
                             for (int kk = 0; kk < D / 32; kk++) {
                                 const uint64_t off = (uint64_t)(kk * 32) >> 4;
-                                mma_ss_f8(tmem + (n % NSBUF) * BN, dq0 + off, kb + off, idesc_qk, kk > 0);
+                                mma_ss_f8_w(tmem + (n % NSBUF) * BN, dq0 + off, kb + off, idesc_qk, kk > 0);
                             }
                         } else {  // 16 head dims per MMA, 4 per 64-dim panel
 #pragma unroll
                             for (int kk = 0; kk < D / 16; kk++) {
                                 const uint64_t off = (uint64_t)((kk >> 2) * PANEL + (kk & 3) * 32) >> 4;
-                                mma_ss(tmem + (n % NSBUF) * BN, dq0 + off, kb + off, idesc_qk, kk > 0);
+                                mma_ss_w(tmem + (n % NSBUF) * BN, dq0 + off, kb + off, idesc_qk, kk > 0);
                             }
                         }
-                        tc_commit(&s_full[n % NSBUF]);  // K(n)'s slot is freed by the softmax, which sees S(n)
+                        tc_commit_w(&s_full[n % NSBUF]);  // K(n)'s slot is freed by the softmax, which sees S(n)
                     }
                     kv_idx += 2 * T;
                     tile += T;
@@ -274,22 +283,22 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
                         const uint32_t n = tile + j;
                         const uint32_t vidx = kv_idx + v_load(j, T);  // V_j
                         // the slot's previous load, K(n-1), has landed: P(n-1).V was issued
-                        if (!(ok = mbar_wait(&kv_full[vidx % NSTAGE], (vidx / NSTAGE) & 1, w))) break;
+                        if (!(ok = mbar_wait_w(&kv_full[vidx % NSTAGE], (vidx / NSTAGE) & 1, w))) break;
                         // P(n) (bf16, keys in order) sits over the first BN/2 columns of its buffer;
                         // each part's P.V starts as soon as the softmax has published that part
                         const uint64_t vb = dv0 + ((uint64_t)((vidx % NSTAGE) * TILE) >> 4);
                         const uint32_t pb = tmem + (n % NSBUF) * BN;
                         for (int q = 0; q < P_PARTS && ok; q++) {
-                            if (!(ok = mbar_wait(&p_part[(n % NSBUF) * P_PARTS + q], (n / NSBUF) & 1, w))) break;
+                            if (!(ok = mbar_wait_w(&p_part[(n % NSBUF) * P_PARTS + q], (n / NSBUF) & 1, w))) break;
                             tc_fence_after();
 #pragma unroll
                             for (int kk = q * (KP / 16); kk < (q + 1) * (KP / 16); kk++)
-                                mma_ts(tmem + O_COL, pb + kk * 8, vb + ((uint64_t)(kk * 16 * 128) >> 4), idesc_pv,
+                                mma_ts_w(tmem + O_COL, pb + kk * 8, vb + ((uint64_t)(kk * 16 * 128) >> 4), idesc_pv,
                                        (carry || j > 0 || kk > 0) ? 1u : 0u);
                         }
                         if (!ok) break;
-                        tc_commit(&pv_buf[n % NSBUF]);
-                        if (j + 1 == T && last) tc_commit(o_final);
+                        tc_commit_w(&pv_buf[n % NSBUF]);
+                        if (j + 1 == T && last) tc_commit_w(o_final);
                     }
                     kv_idx += 2 * T;
                     tile += T;
@@ -297,7 +306,7 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
             }
             // every MMA issued so far must complete before tensor memory is freed
             // (the drain barrier counts one commit per issuer)
-            tc_commit(drain);
+            tc_commit_w(drain);
             mbar_drain(drain, 0, tc::DRAIN_NS);
         }
         __syncwarp();

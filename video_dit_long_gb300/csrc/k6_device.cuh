@@ -61,21 +61,45 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking probe of the same phase (try_wait may suspend the thread for a
+// hardware-defined while before it answers; test_wait answers at once).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase of `bar` with the given parity to complete.  Gives up
 // (returns false) when another warp of the CTA has aborted, or after
-// w.limit_ns, in which case it records DEV_TIMEOUT and aborts the CTA.
+// w.limit_ns, in which case it records DEV_TIMEOUT and aborts the CTA.  The
+// first probe does not block and the limit is checked before every blocking
+// one, so a limit of 0 makes a wait whose phase is not already complete give
+// up at once.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const WaitCtx &w) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_test_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
         if (*w.abort) return false;
         if (global_ns() - t0 >= w.limit_ns) {
             *w.abort = 1;
             atomicCAS(w.err, DEV_OK, DEV_TIMEOUT);
             return false;
         }
+        if (mbar_try_wait(bar, parity)) return true;
     }
+}
+
+// Warp-uniform form, for code that all 32 lanes of a warp run together: every
+// lane polls, and the warp goes on only if every lane saw the phase complete,
+// so its lanes never part ways on the timeout path.
+__device__ __forceinline__ bool mbar_wait_w(uint64_t *bar, uint32_t parity, const WaitCtx &w) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, w));
 }
 
 // Same, with a fixed deadline and no abort check: used on the way out to let
@@ -193,6 +217,61 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
                  : "memory");
+}
+
+// Warp-wide forms of the issuing instructions above: the whole (converged) warp
+// executes them and elect.sync picks the one lane that issues.  Election is
+// deterministic for a given member mask, so MMAs and the commit that tracks
+// them come from the same thread.  Keeping the issuing warp converged lets
+// the compiler hold descriptors and addresses as warp-uniform values; a lone
+// lane sharing its sub-partition with busy warps issues measurably slower.
+__device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b32 rx;\n\t"
+        "elect.sync rx|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ss_f8_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b32 rx;\n\t"
+        "elect.sync rx|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b32 rx;\n\t"
+        "elect.sync rx|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// True in the one lane elect.sync picks from a converged warp (the same lane
+// every time for the full mask).
+__device__ __forceinline__ bool elect_one() {
+    uint32_t e;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 rx;\n\t"
+        "elect.sync rx|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(e));
+    return e != 0;
+}
+__device__ __forceinline__ void tc_commit_w(uint64_t *bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t.reg .b32 rx;\n\t"
+        "elect.sync rx|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+        : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread (lane) gets its row.
