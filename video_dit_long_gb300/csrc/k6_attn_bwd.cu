@@ -188,10 +188,11 @@ __device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *m, ui
     tma_load_4d(dst + bw::PANEL, m, bar, 64, h, row, b);
 }
 
-// Step kk of a K-major SS MMA chain over d = 128 (both operands 128-byte swizzled).
+// Step kk of a K-major SS MMA chain over d = 128 (both operands 128-byte swizzled),
+// issued by the elected lane of the converged calling warp.
 __device__ __forceinline__ void mma_kmajor(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, int kk) {
     const uint64_t off = (uint64_t)((kk >> 2) * bw::PANEL + (kk & 3) * 32) >> 4;
-    mma_ss(d, a + off, b + off, idesc, kk > 0);
+    mma_ss_w(d, a + off, b + off, idesc, kk > 0);
 }
 
 // Epilogue: 64 fp32 columns of this thread's TMEM lane, times `scale`, to dst.
@@ -244,23 +245,32 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     const int T = p.kv_tiles_v + p.kv_tiles_j;
     uint8_t *sQ = smem, *sDO = smem + TILE, *sK = smem + 2 * TILE, *sV = smem + 5 * TILE;
 
+    // The control warps run whole and converged: every lane waits (a warp-uniform
+    // vote), one elected lane arms barriers, issues copies, MMAs and commits.
     if (warp == 8) {
-        if (lane == 0) {
-            mbar_arrive_expect_tx(bar + STAT, 2 * TILE);
-            load_tile(sQ, &tm_q, bar + STAT, h, q0, b);
-            load_tile(sDO, &tm_do, bar + STAT, h, q0, b);
+        {
+            const bool leader = elect_one();
+            if (leader) {
+                mbar_arrive_expect_tx(bar + STAT, 2 * TILE);
+                load_tile(sQ, &tm_q, bar + STAT, h, q0, b);
+                load_tile(sDO, &tm_do, bar + STAT, h, q0, b);
+            }
             int nk = 0, nv = 0;  // K and V tiles issued
             for (int t = 0; t < T; t++) {
                 const int ks = t % 3, vs = t & 1;
                 int map, row;
                 kv_tile(p, t, map, row);
-                if (!mbar_wait(bar + KEMPTY + ks, ((t / 3) & 1) ^ 1, w)) break;
-                mbar_arrive_expect_tx(bar + KFULL + ks, TILE);
-                load_tile(sK + ks * TILE, map ? &tm_jk : &tm_k, bar + KFULL + ks, h, row, b);
+                if (!mbar_wait_w(bar + KEMPTY + ks, ((t / 3) & 1) ^ 1, w)) break;
+                if (leader) {
+                    mbar_arrive_expect_tx(bar + KFULL + ks, TILE);
+                    load_tile(sK + ks * TILE, map ? &tm_jk : &tm_k, bar + KFULL + ks, h, row, b);
+                }
                 nk++;
-                if (!mbar_wait(bar + VEMPTY + vs, ((t >> 1) & 1) ^ 1, w)) break;
-                mbar_arrive_expect_tx(bar + VFULL + vs, TILE);
-                load_tile(sV + vs * TILE, map ? &tm_jv : &tm_v, bar + VFULL + vs, h, row, b);
+                if (!mbar_wait_w(bar + VEMPTY + vs, ((t >> 1) & 1) ^ 1, w)) break;
+                if (leader) {
+                    mbar_arrive_expect_tx(bar + VFULL + vs, TILE);
+                    load_tile(sV + vs * TILE, map ? &tm_jv : &tm_v, bar + VFULL + vs, h, row, b);
+                }
                 nv++;
             }
             // let copies in flight land before the CTA exits
@@ -270,7 +280,7 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
         }
         __syncwarp();
     } else if (warp == 9) {
-        if (lane == 0) {
+        {
             const uint32_t tS = tmem, tP = tmem + 128, tA = tmem + 256, tDS = tmem + 384;
             const uint64_t dq_ = smem_desc_sw128(smem_u32(sQ), 16, 1024);
             const uint64_t ddo = smem_desc_sw128(smem_u32(sDO), 16, 1024);
@@ -281,8 +291,8 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
             // V slot and publish S/dP (each commit also covers every earlier MMA).
             auto issue_sdp = [&](int t) -> bool {
                 const int ks = t % 3, vs = t & 1;
-                if (!mbar_wait(bar + KFULL + ks, (t / 3) & 1, w)) return false;
-                if (!mbar_wait(bar + VFULL + vs, (t >> 1) & 1, w)) return false;
+                if (!mbar_wait_w(bar + KFULL + ks, (t / 3) & 1, w)) return false;
+                if (!mbar_wait_w(bar + VFULL + vs, (t >> 1) & 1, w)) return false;
                 tc_fence_after();
                 const uint64_t kd = dk0 + (uint64_t)((ks * TILE) >> 4), vd = dv0 + (uint64_t)((vs * TILE) >> 4);
 #pragma unroll
@@ -290,26 +300,26 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
                     mma_kmajor(tS, dq_, kd, p.idesc_qk, kk);
                     mma_kmajor(tP, ddo, vd, p.idesc_bf16, kk);
                 }
-                tc_commit(bar + VEMPTY + vs);
-                tc_commit(bar + SFULL);
+                tc_commit_w(bar + VEMPTY + vs);
+                tc_commit_w(bar + SFULL);
                 return true;
             };
-            bool ok = mbar_wait(bar + STAT, 0, w) && T > 0 && issue_sdp(0);
+            bool ok = mbar_wait_w(bar + STAT, 0, w) && T > 0 && issue_sdp(0);
             for (int t = 0; t < T && ok; t++) {
                 // the row pass has read S(t)/dP(t) and written dS(t) to buffer t & 1
-                if (!(ok = mbar_wait(bar + DSFULL, t & 1, w))) break;
+                if (!(ok = mbar_wait_w(bar + DSFULL, t & 1, w))) break;
                 tc_fence_after();
                 if (t + 1 < T && !(ok = issue_sdp(t + 1))) break;
                 const uint64_t kmn = dkmn + (uint64_t)(((t % 3) * TILE) >> 4);
                 const uint32_t ads = tDS + (t & 1) * 64;
 #pragma unroll
                 for (int kk = 0; kk < BM / 16; kk++)
-                    mma_ts(tA, ads + kk * 8, kmn + (uint64_t)((kk * 16 * 128) >> 4), p.idesc_ds_mn,
+                    mma_ts_w(tA, ads + kk * 8, kmn + (uint64_t)((kk * 16 * 128) >> 4), p.idesc_ds_mn,
                            (t > 0 || kk > 0) ? 1u : 0u);  // dQ += dS K
-                tc_commit(bar + KEMPTY + t % 3);
+                tc_commit_w(bar + KEMPTY + t % 3);
             }
-            if (ok) tc_commit(bar + ACC);
-            tc_commit(bar + DRAIN);
+            if (ok) tc_commit_w(bar + ACC);
+            tc_commit_w(bar + DRAIN);
             mbar_drain(bar + DRAIN, 0, DRAIN_NS);
         }
         __syncwarp();
@@ -456,22 +466,31 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     const int T = p.q_tiles;
     uint8_t *sK = smem, *sV = smem + TILE, *sRing = smem + 2 * TILE, *sP = smem + 6 * TILE;
 
+    // The control warps run whole and converged: every lane waits (a warp-uniform
+    // vote), one elected lane arms barriers, issues copies, MMAs and commits.
     if (warp == 8) {
-        if (lane == 0) {
-            mbar_arrive_expect_tx(bar + STAT, 2 * TILE);
-            load_tile(sK, map ? &tm_jk : &tm_k, bar + STAT, h, krow, b);
-            load_tile(sV, map ? &tm_jv : &tm_v, bar + STAT, h, krow, b);
+        {
+            const bool leader = elect_one();
+            if (leader) {
+                mbar_arrive_expect_tx(bar + STAT, 2 * TILE);
+                load_tile(sK, map ? &tm_jk : &tm_k, bar + STAT, h, krow, b);
+                load_tile(sV, map ? &tm_jv : &tm_v, bar + STAT, h, krow, b);
+            }
             int nq = 0, ndo = 0;  // Q and dO tiles issued
             for (int t = 0; t < T; t++) {
                 const int s = t & 1;
                 const uint32_t par = ((t >> 1) & 1) ^ 1;
-                if (!mbar_wait(bar + QEMPTY + s, par, w)) break;
-                mbar_arrive_expect_tx(bar + QFULL + s, TILE);
-                load_tile(sRing + 2 * s * TILE, &tm_q, bar + QFULL + s, h, t * BM, b);
+                if (!mbar_wait_w(bar + QEMPTY + s, par, w)) break;
+                if (leader) {
+                    mbar_arrive_expect_tx(bar + QFULL + s, TILE);
+                    load_tile(sRing + 2 * s * TILE, &tm_q, bar + QFULL + s, h, t * BM, b);
+                }
                 nq++;
-                if (!mbar_wait(bar + DOEMPTY + s, par, w)) break;
-                mbar_arrive_expect_tx(bar + DOFULL + s, TILE);
-                load_tile(sRing + (2 * s + 1) * TILE, &tm_do, bar + DOFULL + s, h, t * BM, b);
+                if (!mbar_wait_w(bar + DOEMPTY + s, par, w)) break;
+                if (leader) {
+                    mbar_arrive_expect_tx(bar + DOFULL + s, TILE);
+                    load_tile(sRing + (2 * s + 1) * TILE, &tm_do, bar + DOFULL + s, h, t * BM, b);
+                }
                 ndo++;
             }
             mbar_drain(bar + STAT, 0, DRAIN_NS);
@@ -481,7 +500,7 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
         }
         __syncwarp();
     } else if (warp == 9) {
-        if (lane == 0) {
+        {
             const uint32_t tS = tmem, tP = tmem + 128, tV = tmem + 256, tK = tmem + 384;
             const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
             const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), 16, 1024);
@@ -492,25 +511,25 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
             auto slot = [&](uint64_t base, int t, int which) {
                 return base + (uint64_t)(((2 * (t & 1) + which) * TILE) >> 4);
             };
-            auto wait_q = [&](int t) { return mbar_wait(bar + QFULL + (t & 1), (t >> 1) & 1, w); };
-            auto wait_do = [&](int t) { return mbar_wait(bar + DOFULL + (t & 1), (t >> 1) & 1, w); };
-            bool ok = mbar_wait(bar + STAT, 0, w) && T > 0 && wait_q(0);
+            auto wait_q = [&](int t) { return mbar_wait_w(bar + QFULL + (t & 1), (t >> 1) & 1, w); };
+            auto wait_do = [&](int t) { return mbar_wait_w(bar + DOFULL + (t & 1), (t >> 1) & 1, w); };
+            bool ok = mbar_wait_w(bar + STAT, 0, w) && T > 0 && wait_q(0);
             if (ok) {
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; kk++) mma_kmajor(tS, dk0, slot(dring, 0, 0), p.idesc_qk, kk);  // S^T = K Q^T
-                tc_commit(bar + SREADY);
+                tc_commit_w(bar + SREADY);
                 ok = wait_do(0);
             }
             if (ok) {
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; kk++) mma_kmajor(tP, dv0, slot(dring, 0, 1), p.idesc_bf16, kk);  // dP^T = V dO^T
-                tc_commit(bar + WIN);
+                tc_commit_w(bar + WIN);
             }
             for (int t = 0; t < T && ok; t++) {
                 // the row pass has read S^T(t): S^T(t+1) may overwrite its columns
-                if (!(ok = mbar_wait(bar + CONSUMED, t & 1, w))) break;
+                if (!(ok = mbar_wait_w(bar + CONSUMED, t & 1, w))) break;
                 tc_fence_after();
                 const bool next = t + 1 < T;
                 if (next) {
@@ -518,21 +537,21 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < D / 16; kk++) mma_kmajor(tS, dk0, slot(dring, t + 1, 0), p.idesc_qk, kk);
-                    tc_commit(bar + SREADY);
+                    tc_commit_w(bar + SREADY);
                 }
                 // the first part of P^T(t) is in shared memory and of dS^T(t) over dP^T(t)
-                if (!(ok = mbar_wait(bar + PDS, t & 1, w))) break;
+                if (!(ok = mbar_wait_w(bar + PDS, t & 1, w))) break;
                 if (next && !(ok = wait_do(t + 1))) break;
                 tc_fence_after();
                 const uint32_t acc = t > 0 ? 1u : 0u;
                 // K-step kk covers queries 16 kk .. 16 kk + 15: the first part holds kk 0, 1, 4, 5
                 auto dv_step = [&](int kk) {  // dV += P^T dO
                     const uint64_t poff = (uint64_t)((kk >> 2) * PANEL + (kk & 3) * 32) >> 4;
-                    mma_ss(tV, dp + poff, slot(dring_mn, t, 1) + (uint64_t)((kk * 16 * 128) >> 4), p.idesc_bf16_mn,
+                    mma_ss_w(tV, dp + poff, slot(dring_mn, t, 1) + (uint64_t)((kk * 16 * 128) >> 4), p.idesc_bf16_mn,
                            acc | (kk > 0 ? 1u : 0u));
                 };
                 auto dk_step = [&](int kk) {  // dK += dS^T Q
-                    mma_ts(tK, tP + (kk >> 2) * 64 + (kk & 3) * 8,
+                    mma_ts_w(tK, tP + (kk >> 2) * 64 + (kk & 3) * 8,
                            slot(dring_mn, t, 0) + (uint64_t)((kk * 16 * 128) >> 4), p.idesc_ds_mn,
                            acc | (kk > 0 ? 1u : 0u));
                 };
@@ -542,24 +561,24 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
                     dk_step(part0[i]);
                     dv_step(part0[i]);
                 }
-                if (!(ok = mbar_wait(bar + PDS + 1, t & 1, w))) break;
+                if (!(ok = mbar_wait_w(bar + PDS + 1, t & 1, w))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int i = 0; i < 4; i++) {
                     dk_step(part1[i]);
                     if (i < 2) dv_step(part1[i]);
                 }
-                tc_commit(bar + QEMPTY + (t & 1));  // Q(t): S^T(t) and dK(t) done
+                tc_commit_w(bar + QEMPTY + (t & 1));  // Q(t): S^T(t) and dK(t) done
 #pragma unroll
                 for (int kk = 0; kk < D / 16; kk++) {
                     if (next) mma_kmajor(tP, dv0, slot(dring, t + 1, 1), p.idesc_bf16, kk);  // dP^T(t+1)
                     if (kk < 2) dv_step(part1[2 + kk]);
                 }
-                tc_commit(bar + DOEMPTY + (t & 1));  // dO(t): dP^T(t) and dV(t) done
-                tc_commit(bar + WIN);
+                tc_commit_w(bar + DOEMPTY + (t & 1));  // dO(t): dP^T(t) and dV(t) done
+                tc_commit_w(bar + WIN);
             }
-            if (ok) tc_commit(bar + ACC);
-            tc_commit(bar + DRAIN);
+            if (ok) tc_commit_w(bar + ACC);
+            tc_commit_w(bar + DRAIN);
             mbar_drain(bar + DRAIN, 0, DRAIN_NS);
         }
         __syncwarp();
