@@ -446,7 +446,10 @@ k6attn_status k6attn_forward_static_scratch(k6attn_t h, const void *q, const voi
  * K6ATTN_ERR_TIMEOUT if any kernel of this handle gave up on a wait,
  * K6ATTN_ERR_RANGE if a rotation into fp16 overflowed or a constant-max row
  * underflowed,
- * K6ATTN_ERR_CUDA on an asynchronous CUDA error, else K6ATTN_OK. */
+ * K6ATTN_ERR_CUDA on an asynchronous CUDA error, or if the device placed
+ * the attention kernel's dynamic shared memory off a 1024-byte boundary (the
+ * kernel then computes nothing; its tiles need that alignment and its 227 KB
+ * plan leaves no room to realign), else K6ATTN_OK. */
 k6attn_status k6attn_sync(k6attn_t h, void *stream);
 
 /* Handle options.

@@ -1,9 +1,9 @@
 """Host-side model of the attention kernel's K/V ring (k6_attn_single.cu).
 
 The kernel's producer loads a unit's K/V tiles in the order K_0 K_1, then V_j
-followed by K_{j+2}, into a 5-slot ring; the Q.K^T thread consumes the K tiles,
-the P.V thread the V tiles.  A slot is freed by an mbarrier arrival: K(n)'s by
-the softmax group that sees S(n) done, V(n)'s by the Q.K^T thread once it has
+followed by K_{j+2}, into a 6-slot ring; the Q.K^T warp consumes the K tiles,
+the P.V warp the V tiles.  A slot is freed by an mbarrier arrival: K(n)'s by
+the softmax group that sees S(n) done, V(n)'s by the Q.K^T warp once it has
 seen P(n).V done (before it issues S(n+3)).  Each slot's kv_full barrier is
 tested by phase parity only, so a wait for a slot's load is unambiguous only if
 the slot's previous load has already landed when the wait starts.
@@ -15,14 +15,15 @@ tiles and a few long ones:
 - every load the producer issues finds its slot freed by someone;
 - the graph has no cycle (no thread waits on itself);
 - no wait can match an earlier phase of its slot.
-A lead of 3 (K_0 K_1 K_2 V_0 K_3 ...) with the same wait order is shown to
-break the last condition, which is why the kernel keeps a lead of 2.
+With six slots every slot holds one kind of tile, and a lead of 2 or 3 passes.
+The kernel's earlier 5-slot ring, where K and V take turns in a slot, passes
+with a lead of 2 only: a lead of 3 is shown to break the last condition.
 """
 import collections
 import itertools
 import sys
 
-NSTAGE, NSBUF = 5, 3
+NSTAGE, NSBUF = 6, 3   # the kernel's ring slots and S buffers
 
 
 def k_load(t, T, A):
@@ -47,7 +48,7 @@ def producer_order(Ts, A):
     return loads, tile
 
 
-def model(Ts, A):
+def model(Ts, A, nstage=NSTAGE):
     """Dependency graph of the kernel's waits: node -> set of nodes it waits for."""
     loads, N = producer_order(Ts, A)
     idx = {l: i for i, l in enumerate(loads)}
@@ -62,9 +63,9 @@ def model(Ts, A):
     for i in range(len(loads)):
         if i:
             dep(("load", i), ("load", i - 1))        # the producer issues loads in order
-        if i >= NSTAGE:
-            assert i - NSTAGE in release, ("a load needs a slot nobody frees", Ts, i)
-            dep(("load", i), release[i - NSTAGE])
+        if i >= nstage:
+            assert i - nstage in release, ("a load needs a slot nobody frees", Ts, i)
+            dep(("load", i), release[i - nstage])
         dep(("landed", i), ("load", i))
     for n in range(N):
         consumer[idx[("K", n)]] = ("S", n)
@@ -123,15 +124,15 @@ def acyclic(deps):
     return all(visit(x) for x in nodes)
 
 
-def aliasing(Ts, A):
+def aliasing(Ts, A, nstage=NSTAGE):
     """The first wait that could match an earlier phase of its slot, or None."""
-    loads, idx, deps, consumer, N = model(Ts, A)
+    loads, idx, deps, consumer, N = model(Ts, A, nstage)
     for i, (kind, n) in enumerate(loads):
-        if i < NSTAGE:
+        if i < nstage:
             continue
         wait = ("wait_K" if kind == "K" else "wait_V", n)
-        if consumer[i - NSTAGE] not in ancestors(deps, wait):
-            return loads[i], loads[i - NSTAGE]
+        if consumer[i - nstage] not in ancestors(deps, wait):
+            return loads[i], loads[i - nstage]
     return None
 
 
@@ -153,17 +154,33 @@ def test_load_index_formulas_match_the_producer_order():
 
 def test_every_slot_is_freed_and_no_wait_cycles():
     for Ts in CASES:
-        _, _, deps, _, _ = model(Ts, 2)   # model() asserts that every needed slot is freed
-        assert acyclic(deps), Ts
+        for A in (2, 3):
+            _, _, deps, _, _ = model(Ts, A)   # model() asserts that every needed slot is freed
+            assert acyclic(deps), (Ts, A)
 
 
 def test_no_wait_can_match_an_earlier_phase():
     for Ts in CASES:
-        assert aliasing(Ts, 2) is None, Ts
+        for A in (2, 3):
+            assert aliasing(Ts, A) is None, (Ts, A)
 
 
-def test_a_lead_of_three_would_alias():
-    # with K three tiles ahead, the P.V thread could wait for V(n) while K(n)
-    # (the slot's previous load) is still in flight
-    found = aliasing([5], 3)
+def test_with_six_slots_a_steady_state_slot_holds_one_kind():
+    # inside a unit, loads 2 .. 2T-3 alternate V and K, so there a slot's load
+    # and the load six before it are the same kind: K(n) follows K(n-3), V(n)
+    # follows V(n-3).  (The first two loads and a unit's tail, where only V
+    # loads remain, shift the pattern; the checks above cover those.)
+    for T in range(3, 40):
+        loads, _ = producer_order([T], 2)
+        for i in range(2 + NSTAGE, 2 * T - 2):
+            assert loads[i][0] == loads[i - NSTAGE][0], (T, i)
+            assert loads[i][1] == loads[i - NSTAGE][1] + 3, (T, i)
+
+
+def test_five_slots_alias_with_a_lead_of_three():
+    # the earlier 5-slot ring: with K three tiles ahead, the P.V warp could wait
+    # for V(n) while K(n) (the slot's previous load) is still in flight
+    for Ts in CASES:
+        assert aliasing(Ts, 2, nstage=5) is None, Ts
+    found = aliasing([5], 3, nstage=5)
     assert found == (("V", 2), ("K", 2))

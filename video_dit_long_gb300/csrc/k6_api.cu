@@ -799,6 +799,8 @@ k6attn_status k6attn_sync(k6attn_t h, void *stream) {
     if (word) {
         cudaMemset(h->err, 0, sizeof(int));
         if (word == DEV_RANGE) return set_error(K6ATTN_ERR_RANGE, "a rotated q/k value does not fit fp16");
+        if (word == DEV_LAYOUT)
+            return set_error(K6ATTN_ERR_CUDA, "the device placed the attention kernel's shared memory off a 1024-byte boundary");
         return set_error(K6ATTN_ERR_TIMEOUT, "a device-side wait gave up (code %d)", word);
     }
     return K6ATTN_OK;

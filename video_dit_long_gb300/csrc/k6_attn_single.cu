@@ -60,15 +60,21 @@ using tc::BN;
 using tc::D;
 using tc::PANEL;
 using tc::TILE;
-constexpr int NSTAGE = 5;                     // K/V tile slots (four leave V(n+1) too little time to arrive)
-// K_t is loaded before V_{t-KAHEAD} (see k_load, v_load).  A ring slot holds K
-// and V tiles in turn and its kv_full barrier is tested by phase parity only,
-// so a consumer may wait for a load only once the slot's previous load has
-// landed, or the wait could match that earlier phase.  With KAHEAD = 2 the
-// slot before V(n) held K(n-1), which has landed when P(n-1).V is issued, and
-// the slot before K(n) held V(n-4), landed once P(n-3).V is done: the waits
-// below come in that order.  (A lead of 3 would let the P.V thread reach V(n)
-// while K(n) is still in flight; checked on a model of the waits.)
+// K/V tile slots.  Inside a unit the loads alternate K and V, so with an even
+// count a slot keeps one kind there: K(n) reuses K(n-3)'s slot, freed once
+// S(n-3) is done, and V(n) reuses V(n-3)'s, freed once P(n-3).V is done.
+// (With five, K(n) took V(n-4)'s slot and could not load before P(n-4).V
+// finished.)
+constexpr int NSTAGE = 6;
+// K_t is loaded before V_{t-KAHEAD} (see k_load, v_load).  Each slot's kv_full
+// barrier is tested by phase parity only, so a consumer may wait for a load
+// only once the slot's previous load has landed, or the wait could match that
+// earlier phase.  In a unit's steady state the previous load of a slot is the
+// same kind, waited for by the same warp before; at unit starts and tails the
+// kinds shift, and a model of every warp's waits in program order checks that
+// the rule still holds there, for every sequence of up to three chunks of 1-7
+// tiles.  (With five slots the kinds alternate in a slot and a lead of 3
+// breaks the rule.)
 constexpr int KAHEAD = 2;
 constexpr int NSBUF = 3;                      // S buffers in tensor memory
 constexpr int SMEM_Q = 0;
@@ -80,9 +86,14 @@ constexpr int KP = BN / P_PARTS;              // keys per part
 // m_ready [tile parity][warp], epi [warp], epi_done [warp]
 constexpr int NBAR = 1 + 2 * NSTAGE + NSBUF + NSBUF * P_PARTS + 1 + 1 + NSBUF + 8 + 4 + 4;
 constexpr int SMEM_XCH = (SMEM_BAR + NBAR * 8 + 16 + 15) & ~15;  // + TMEM address word and abort flag
-// running row max [row]; epilogue exchange [unit parity][warpgroup][row] of (l, m)
-constexpr int SMEM_TOTAL = SMEM_XCH + (BM + 2 * 2 * 2 * BM) * 4;
-constexpr int SMEM_ALLOC = SMEM_TOTAL + 1024;                   // room to align the base to 1024 bytes
+// running row max [row]; epilogue exchange [warpgroup][row] of (l, m)
+constexpr int SMEM_TOTAL = SMEM_XCH + (BM + 2 * 2 * BM) * 4;
+// The tiles need a 1024-byte-aligned base (128-byte swizzle).  The dynamic
+// shared memory of a kernel without static shared memory starts there; the
+// kernel checks it and reports DEV_LAYOUT otherwise, as there is no room to
+// realign: six 32 KB slots and the Q tile leave 144 of the 227 KB.
+constexpr int SMEM_ALLOC = SMEM_TOTAL;
+static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory plan exceeds the per-CTA limit");
 constexpr int THREADS = 384;                  // softmax halves 0 and 1, producer/MMA/spare
 // Register split (launch: 384 x 168 = 64512): 2*128*184 + 128*136 = 64512.
 constexpr int REGS_SOFTMAX = 184;
@@ -114,8 +125,12 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
                           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_jk,
                           const __grid_constant__ CUtensorMap tm_jv, const TcParams p) {
     using namespace ts;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw;
+    if (smem_u32(smem) & 1023u) {  // the same for every thread: the CTA leaves before any barrier
+        if (threadIdx.x == 0) atomicCAS(p.err, DEV_OK, DEV_LAYOUT);
+        return;
+    }
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SMEM_BAR);
     uint64_t *q_full = bars;
     uint64_t *kv_full = q_full + 1;
@@ -327,7 +342,7 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
         const uint32_t lane_base = tmem + ((uint32_t)(32 * wq) << 16);
         const uint32_t tO = lane_base + O_COL;
         float *xm = reinterpret_cast<float *>(smem + SMEM_XCH);  // [row]: max after the latest tile
-        float *xe = xm + BM;                                      // [unit parity][group][row][l, m]
+        float *xe = xm + BM;                                      // [group][row][l, m]
         const float sl2 = p.scale_log2;
         uint32_t tile = 0, uc = 0, n_epi = 0;
         uint32_t kv_idx = 0;      // K/V loads of earlier units
@@ -470,7 +485,9 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
                 ok = false;
                 break;
             }
-            float *xs = xe + (n_epi & 1) * (2 * BM * 2);
+            // one buffer serves every unit: both groups have read it (epi_done) before either
+            // writes the next unit's (l, m)
+            float *xs = xe;
             xs[(hf * BM + r) * 2] = l_own;
             xs[(hf * BM + r) * 2 + 1] = m_own;
             mbar_arrive(&epi[wq]);

@@ -12,7 +12,7 @@
 namespace k6 {
 
 // Device error word codes (written with atomicCAS, first error wins).
-enum : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_RANGE = 2 };
+enum : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_RANGE = 2, DEV_LAYOUT = 3 };
 
 // Geometry of one joint attention problem, as the kernels see it.
 struct Geom {
