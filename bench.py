@@ -71,12 +71,43 @@ KERNEL_SOURCES = {
 STEP_KERNEL = "attn_tc_single_kernel"
 
 
-def source_digest(kernel: str) -> str:
+def strip_comments(src: str) -> str:
+    """C/C++ source without its comments (string and character literals kept
+    as they are), so that a comment edit leaves the digest of the code alone."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "".join(out)
+
+
+def source_digest(kernel: str, read=None) -> str:
+    """sha256 (first 16 hex digits) of the kernel's sources with comments,
+    blank lines and trailing blanks removed.  `read(name)` returns a file's
+    text (default: the working tree)."""
     csrc = os.path.join(ROOT, "video_dit_long_gb300", "csrc")
+    if read is None:
+        def read(name):
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                return f.read()
     digest = hashlib.sha256()
     for name in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(csrc, name), "rb") as f:
-            digest.update(f.read())
+        code = "\n".join(ln.rstrip() for ln in strip_comments(read(name)).splitlines() if ln.strip())
+        digest.update(code.encode("utf-8"))
     return digest.hexdigest()[:16]
 
 

@@ -17,22 +17,23 @@
 // How (one CTA per work unit = 128 query rows of one (batch, head), over a
 // group of consecutive chunks):
 //   warp 8      TMA producer: the Q tile once, then K_j and V_j tiles of 128
-//               keys x 128 dims through a 5-slot ring of 32 KB slots (two
+//               keys x 128 dims through a 6-slot ring of 32 KB slots (two
 //               128-byte-swizzled 64-dim panels; an e4m3 tile is one panel),
 //               in the order K_0 K_1 V_0 K_2 V_1 K_3 ..., so that K runs two
 //               tiles ahead of V.
-//   warp 9      one thread issues every S(n) = Q K_n^T (SS, both K-major) into
+//   warp 9      issues every S(n) = Q K_n^T (SS, both K-major) into
 //               tensor-memory buffer n % 3; the buffer held P(n-3), so S(n)
 //               waits for the P.V of tile n-3 (pv_buf), and having seen it
 //               done, frees V(n-3)'s ring slot (the softmax group that sees
-//               S(n) done frees K(n)'s), so the issuing threads spend no
-//               commits on the ring.
-//   warp 10     one thread issues every O += P(n) V_n (P from tensor memory,
-//               V MN-major from shared memory), part by part as the softmax
-//               publishes P(n).  Two issuing threads on different SM
-//               sub-partitions: one would share its sub-partition's issue
-//               slots with two softmax warps and feed the tensor pipe too
-//               slowly.
+//               S(n) done frees K(n)'s), so the issuers spend no commits on
+//               the ring.
+//   warp 10     issues every O += P(n) V_n (P from tensor memory, V MN-major
+//               from shared memory), part by part as the softmax publishes
+//               P(n).  Two issuers on different SM sub-partitions: one would
+//               share its sub-partition's issue slots with two softmax warps
+//               and feed the tensor pipe too slowly.
+//   Warps 8-10 run whole and converged: every lane waits (a warp-uniform
+//   vote), one lane picked by elect.sync issues each copy, MMA and commit.
 //   warps 0-7   two softmax warpgroups on alternate K/V tiles (whole rows, one
 //               thread per row = TMEM lane), passing the running row max from
 //               tile to tile; both run the epilogue, each writing half of O.
