@@ -40,6 +40,8 @@ SMALL = {
     "one_tile": Workload("one_tile", 1, 3, 128, "bf16", (1, 7, 9), 0, (32, 48, 48), 0, 1.0, 1.0, (1, 3)),
     "audio1d": Workload("audio1d", 2, 2, 128, "bf16", (2, 8, 16), 62, (32, 48, 48), 1, 1.0, 1.0, (1, 3)),
     "f32_d128": Workload("f32_d128", 1, 2, 128, "f32", (2, 6, 10), 8, (32, 48, 48), 0, 1.0, 1.0, (1, 4)),
+    # an even number of Q tiles (4, the last ragged): the attention runs in CTA pairs sharing K/V tiles
+    "pair4": Workload("pair4", 1, 2, 128, "bf16", (1, 20, 24), 20, (32, 48, 48), 0, 1.0, 1.0, (1, 2, 5)),
 }
 
 
@@ -230,14 +232,14 @@ def test_tiny_fp32_matches_oracle(n):
     check_full(configs.WORKLOADS["tiny"], n)
 
 
-@pytest.mark.parametrize("name", ["ragged", "one_tile", "audio1d", "f32_d128"])
+@pytest.mark.parametrize("name", ["ragged", "one_tile", "audio1d", "f32_d128", "pair4"])
 def test_small_workloads_match_oracle(name):
     w = SMALL[name]
     for n in w.chunks:
         check_full(w, n)
 
 
-@pytest.mark.parametrize("name", ["ragged", "audio1d"])
+@pytest.mark.parametrize("name", ["ragged", "audio1d", "pair4"])
 def test_peaked_attention_matches_oracle(name):
     # Q and K scaled x4 (logit std ~4-16): far from uniform attention; inputs
     # taken as already rotated so that no bf16 rounding of rotated Q/K enters
@@ -282,8 +284,11 @@ def test_long_video_sampled_rows(name, n):
     print(name, n, m)
 
 
-def test_timeout_path_reports_and_recovers():
-    w = SMALL["ragged"]
+@pytest.mark.parametrize("name", ["ragged", "pair4"])
+def test_timeout_path_reports_and_recovers(name):
+    # ragged: 5 Q tiles, one CTA per tile; pair4: 4 tiles in CTA pairs, whose
+    # way out waits for the partner's copies into each CTA before either leaves
+    w = SMALL[name]
     x = inputs.make_inputs(w)
     h = K().Handle.for_workload(w)
     h.set_option(K().OPT_WAIT_LIMIT_NS, 0)

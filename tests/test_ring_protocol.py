@@ -184,3 +184,28 @@ def test_five_slots_alias_with_a_lead_of_three():
         assert aliasing(Ts, 2, nstage=5) is None, Ts
     found = aliasing([5], 3, nstage=5)
     assert found == (("V", 2), ("K", 2))
+
+
+def pair_model(Ts, A, nstage=NSTAGE):
+    """Two CTAs of a cluster running the same units (the kernel's multicast
+    form): each loads one panel of every tile into both, so a load lands in a
+    CTA only once both CTAs issued their panels, and a slot is refilled only
+    once the consumers of both CTAs released it."""
+    loads, idx, deps, consumer, N = model(Ts, A, nstage)
+    pair = collections.defaultdict(set)
+    for node, ds in deps.items():
+        for cta in (0, 1):
+            for d in ds:
+                pair[(cta, node)].add((cta, d))
+    for i in range(len(loads)):
+        for cta in (0, 1):
+            pair[(cta, ("landed", i))].add((1 - cta, ("load", i)))    # the partner's panel
+            if i >= nstage:
+                release = next(iter(deps[("load", i)] - {("load", i - 1)}))
+                pair[(cta, ("load", i))].add((1 - cta, release))      # the partner's release
+    return pair
+
+
+def test_cluster_pair_has_no_wait_cycle():
+    for Ts in CASES:
+        assert acyclic(pair_model(Ts, 2)), Ts

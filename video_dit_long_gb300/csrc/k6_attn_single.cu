@@ -34,6 +34,8 @@
 //               and feed the tensor pipe too slowly.
 //   Warps 8-10 run whole and converged: every lane waits (a warp-uniform
 //   vote), one lane picked by elect.sync issues each copy, MMA and commit.
+//   With 16-bit q/k the CTAs run in clusters of two that share each K/V tile,
+//   every CTA loading one panel for both (CLUSTER, below).
 //   warps 0-7   two softmax warpgroups on alternate K/V tiles (whole rows, one
 //               thread per row = TMEM lane), passing the running row max from
 //               tile to tile; both run the epilogue, each writing half of O.
@@ -54,6 +56,11 @@
 #include "k6_internal.h"
 
 namespace k6 {
+
+// 1: 16-bit q/k attention runs in CTA pairs that multicast K/V tiles.
+#ifndef K6_KV_MULTICAST
+#define K6_KV_MULTICAST 1
+#endif
 
 namespace ts {
 using tc::BM;
@@ -83,16 +90,17 @@ constexpr int SMEM_KV = TILE;
 constexpr int SMEM_BAR = SMEM_KV + NSTAGE * TILE;
 constexpr int P_PARTS = 2;                    // P of a tile is published in this many parts
 constexpr int KP = BN / P_PARTS;              // keys per part
-// q_full, kv_full/empty, s_full, p_part [S buffer][part], o_final, drain, pv_buf [S buffer],
-// m_ready [tile parity][warp], epi [warp], epi_done [warp]
-constexpr int NBAR = 1 + 2 * NSTAGE + NSBUF + NSBUF * P_PARTS + 1 + 1 + NSBUF + 8 + 4 + 4;
-constexpr int SMEM_XCH = (SMEM_BAR + NBAR * 8 + 16 + 15) & ~15;  // + TMEM address word and abort flag
+// q_full, kv_full [source CTA][slot], kv_empty, s_full, p_part [S buffer][part], o_final, drain,
+// pv_buf [S buffer], m_ready [tile parity][warp], epi [warp], epi_done [warp]
+constexpr int NBAR = 1 + 3 * NSTAGE + NSBUF + NSBUF * P_PARTS + 1 + 1 + NSBUF + 8 + 4 + 4;
+// + TMEM address word, abort flag and the count of K/V loads this CTA issued
+constexpr int SMEM_XCH = (SMEM_BAR + NBAR * 8 + 16 + 15) & ~15;
 // running row max [row]; epilogue exchange [warpgroup][row] of (l, m)
 constexpr int SMEM_TOTAL = SMEM_XCH + (BM + 2 * 2 * BM) * 4;
 // The tiles need a 1024-byte-aligned base (128-byte swizzle).  The dynamic
 // shared memory of a kernel without static shared memory starts there; the
 // kernel checks it and reports DEV_LAYOUT otherwise, as there is no room to
-// realign: six 32 KB slots and the Q tile leave 144 of the 227 KB.
+// realign: six 32 KB slots and the Q tile leave 96 of the 227 KB.
 constexpr int SMEM_ALLOC = SMEM_TOTAL;
 static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory plan exceeds the per-CTA limit");
 constexpr int THREADS = 384;                  // softmax halves 0 and 1, producer/MMA/spare
@@ -120,12 +128,26 @@ __device__ __forceinline__ uint32_t v_load(int j, int T) {
 // swizzle panel, 16 KB, in the first half of their 32 KB slots) and Q.K^T runs as
 // 4 kind::f8f6f4 MMAs of K = 32 per tile instead of 8 kind::f16 MMAs; P.V is
 // unchanged (bf16 P from tensor memory, bf16 V).
-template <bool BOUNDED, bool QK8>
+//
+// CLUSTER (16-bit q/k): the grid runs in clusters of two CTAs that hold
+// consecutive Q tiles of the same (batch, head, chunk group), so they stream
+// the same K/V tiles.  Each CTA loads one 64-dim panel of every tile (CTA rank
+// r: panel r) and multicasts it to both, halving the K/V bytes read from L2.
+// kv_full is split by source CTA; each CTA's producer arms both of its own
+// barriers for a load when it issues its panel of it.  A slot is refilled only
+// when the consumers of both CTAs have released it (kv_empty counts one local
+// and one remote arrival).  On the way out, after a cluster barrier (no copy
+// or remote arrival is issued any more), each CTA waits for the last load of
+// every source in every slot to land, arming first a phase the partner sent
+// but this CTA never armed, and a second cluster barrier keeps both CTAs
+// resident until then.
+template <bool BOUNDED, bool QK8, bool CLUSTER>
 __global__ void __launch_bounds__(ts::THREADS, 1)
     attn_tc_single_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_jk,
                           const __grid_constant__ CUtensorMap tm_jv, const TcParams p) {
     using namespace ts;
+    static_assert(!(CLUSTER && QK8), "the cluster form multicasts the two 64-dim panels of 16-bit tiles");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw;
     if (smem_u32(smem) & 1023u) {  // the same for every thread: the CTA leaves before any barrier
@@ -134,8 +156,8 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
     }
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SMEM_BAR);
     uint64_t *q_full = bars;
-    uint64_t *kv_full = q_full + 1;
-    uint64_t *kv_empty = kv_full + NSTAGE;
+    uint64_t *kv_full = q_full + 1;        // [source CTA rank][slot]; rank 0 only without CLUSTER
+    uint64_t *kv_empty = kv_full + 2 * NSTAGE;
     uint64_t *s_full = kv_empty + NSTAGE;  // [NSBUF]
     // [S buffer][part], 128 arrivals each.  Indexed by buffer, not by tile parity:
     // P(n+3), the next completion of the same barrier, needs S(n+3), which waits
@@ -151,14 +173,17 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
     uint64_t *epi_done = epi + 4;          // [warp % 4]: both warps of a row pair have read O
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(epi_done + 4);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    uint32_t *issued = tmem_slot + 2;      // K/V loads this CTA issued (CLUSTER exit protocol)
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t crank = CLUSTER ? cluster_ctarank() : 0u;  // this CTA's rank in its cluster
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         for (int s = 0; s < NSTAGE; s++) {
             mbar_init(&kv_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
+            mbar_init(&kv_full[NSTAGE + s], 1);
+            mbar_init(&kv_empty[s], CLUSTER ? 2 : 1);  // with CLUSTER: this CTA's release and the partner's
         }
         for (int b = 0; b < NSBUF; b++) mbar_init(&s_full[b], 1);
         for (int q = 0; q < NSBUF * P_PARTS; q++) mbar_init(&p_part[q], BM);
@@ -171,6 +196,7 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
             mbar_init(&epi_done[q], 64);
         }
         *abort_flag = 0;
+        *issued = 0;
         fence_barrier_init();
     }
     if (warp == 9) {
@@ -178,7 +204,9 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    // with CLUSTER the partner's barriers must be initialised before any remote arrival or multicast
+    if constexpr (CLUSTER) cluster_sync();
+    else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const WaitCtx w{p.wait_limit_ns, p.err, abort_flag};
@@ -217,10 +245,20 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
                     const CUtensorMap *tm = kv == 0 ? (map == 0 ? &tm_k : &tm_jk) : (map == 0 ? &tm_v : &tm_jv);
                     const bool one_panel = QK8 && kv == 0;  // an e4m3 K tile is one 16 KB panel
                     if (leader) {
-                        mbar_arrive_expect_tx(&kv_full[slot], one_panel ? PANEL : TILE);
                         uint8_t *dst = smem + SMEM_KV + slot * TILE;
-                        tma_load_4d(dst, tm, &kv_full[slot], 0, un.h, row, un.b);
-                        if (!one_panel) tma_load_4d(dst + PANEL, tm, &kv_full[slot], 64, un.h, row, un.b);
+                        if constexpr (CLUSTER) {
+                            // arm this CTA's barriers for both panels of the load, then
+                            // send this CTA's panel to both CTAs
+                            uint64_t *bar = &kv_full[crank * NSTAGE + slot];
+                            mbar_arrive_expect_tx(&kv_full[slot], PANEL);
+                            mbar_arrive_expect_tx(&kv_full[NSTAGE + slot], PANEL);
+                            tma_load_4d_multicast(dst + crank * PANEL, tm, bar, (int)crank * 64, un.h, row, un.b,
+                                                  (uint16_t)0x3);
+                        } else {
+                            mbar_arrive_expect_tx(&kv_full[slot], one_panel ? PANEL : TILE);
+                            tma_load_4d(dst, tm, &kv_full[slot], 0, un.h, row, un.b);
+                            if (!one_panel) tma_load_4d(dst + PANEL, tm, &kv_full[slot], 64, un.h, row, un.b);
+                        }
                     }
                     kv_idx++;
                     return true;
@@ -231,9 +269,14 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
                 for (int j = 0; j < T && ok; j++) ok = load(1, j) && (j + KAHEAD >= T || load(0, j + KAHEAD));
             }
             // let every copy issued into shared memory land before the CTA can exit
+            // (with CLUSTER the K/V copies are waited for after the first cluster barrier)
             if (uc > 0) mbar_drain(q_full, 0, tc::DRAIN_NS);
-            for (uint32_t idx = kv_idx > NSTAGE ? kv_idx - NSTAGE : 0; idx < kv_idx; idx++)
-                mbar_drain(&kv_full[idx % NSTAGE], (idx / NSTAGE) & 1, tc::DRAIN_NS);
+            if constexpr (CLUSTER) {
+                if (leader) *issued = kv_idx;
+            } else {
+                for (uint32_t idx = kv_idx > NSTAGE ? kv_idx - NSTAGE : 0; idx < kv_idx; idx++)
+                    mbar_drain(&kv_full[idx % NSTAGE], (idx / NSTAGE) & 1, tc::DRAIN_NS);
+            }
         } else if (warp == 9 || warp == 10) {
             // ------------------------------------------------- MMA issuers
             // Warp 9 issues every S(n) = Q K_n^T, warp 10 every O += P(n).V_n: one
@@ -267,9 +310,15 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
                         vslot[n % 4] = (kv_idx + v_load(t, T)) % NSTAGE;
                         if (n >= NSBUF) {  // before waiting for K(n): the slot before K(n) held V(n-4)
                             if (!(ok = mbar_wait_w(&pv_buf[n % NSBUF], (n / NSBUF - 1) & 1, w))) break;
-                            if (lane == 0) mbar_arrive(&kv_empty[vslot[(n - NSBUF) % 4]]);  // V(n-3) read by its P.V
+                            if (lane == 0) {  // V(n-3) read by its P.V
+                                uint64_t *e = &kv_empty[vslot[(n - NSBUF) % 4]];
+                                mbar_arrive(e);
+                                if constexpr (CLUSTER) mbar_arrive_cluster(cluster_addr(e, crank ^ 1u));
+                            }
                         }
                         if (!(ok = mbar_wait_w(&kv_full[kidx % NSTAGE], (kidx / NSTAGE) & 1, w))) break;
+                        if constexpr (CLUSTER)  // the partner's panel
+                            if (!(ok = mbar_wait_w(&kv_full[NSTAGE + kidx % NSTAGE], (kidx / NSTAGE) & 1, w))) break;
                         tc_fence_after();
                         const uint64_t kb = dq0 + ((uint64_t)(SMEM_KV - SMEM_Q + (kidx % NSTAGE) * TILE) >> 4);
                         if constexpr (QK8) {  // 32 head dims (32 bytes of each row) per MMA
@@ -300,6 +349,8 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
                         const uint32_t vidx = kv_idx + v_load(j, T);  // V_j
                         // the slot's previous load, K(n-1), has landed: P(n-1).V was issued
                         if (!(ok = mbar_wait_w(&kv_full[vidx % NSTAGE], (vidx / NSTAGE) & 1, w))) break;
+                        if constexpr (CLUSTER)
+                            if (!(ok = mbar_wait_w(&kv_full[NSTAGE + vidx % NSTAGE], (vidx / NSTAGE) & 1, w))) break;
                         // P(n) (bf16, keys in order) sits over the first BN/2 columns of its buffer;
                         // each part's P.V starts as soon as the softmax has published that part
                         const uint64_t vb = dv0 + ((uint64_t)((vidx % NSTAGE) * TILE) >> 4);
@@ -376,7 +427,11 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
                 }
                 tc_fence_after();
                 // S(n) is complete: K(n)'s ring slot is free
-                if (r == 0) mbar_arrive(&kv_empty[(kv_idx + k_load(j, T)) % NSTAGE]);
+                if (r == 0) {
+                    uint64_t *e = &kv_empty[(kv_idx + k_load(j, T)) % NSTAGE];
+                    mbar_arrive(e);
+                    if constexpr (CLUSTER) mbar_arrive_cluster(cluster_addr(e, crank ^ 1u));
+                }
                 if constexpr (!BOUNDED) {
                     // the max after tile n-1 (posted by the other group early in its
                     // tile), every phase waited in turn
@@ -553,7 +608,33 @@ __global__ void __launch_bounds__(ts::THREADS, 1)
     }
 
     tc_fence_before();
-    __syncthreads();
+    if constexpr (CLUSTER) {
+        cluster_sync();  // neither CTA issues a copy or a remote arrival any more
+        if (warp == 8) {
+            // wait for the last load of each source CTA in each slot to land here
+            // (earlier loads of a slot landed before it could be refilled).  This
+            // CTA armed both panels of each load it issued; the partner, at most
+            // one load a slot ahead (it refills a slot only after this CTA's
+            // consumers released it), may have sent a panel this CTA never
+            // armed: arm that phase now, so that it completes when the bytes land.
+            const uint32_t mine = *issued, theirs = ld_cluster_u32(cluster_addr(issued, crank ^ 1u));
+            for (uint32_t s = lane; s < (uint32_t)NSTAGE; s += 32) {
+                if (mine > s) {
+                    const uint32_t last = s + NSTAGE * ((mine - 1 - s) / NSTAGE);
+                    mbar_drain(&kv_full[crank * NSTAGE + s], (last / NSTAGE) & 1, tc::DRAIN_NS);
+                }
+                if (theirs > s) {
+                    const uint32_t last = s + NSTAGE * ((theirs - 1 - s) / NSTAGE);
+                    uint64_t *bar = &kv_full[(crank ^ 1u) * NSTAGE + s];
+                    if (last >= mine) mbar_arrive_expect_tx(bar, PANEL);
+                    mbar_drain(bar, (last / NSTAGE) & 1, tc::DRAIN_NS);
+                }
+            }
+        }
+        cluster_sync();  // no CTA leaves while a copy may still land in it
+    } else {
+        __syncthreads();
+    }
     if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
@@ -580,8 +661,17 @@ cudaError_t launch_attn_tc_single(const Geom &g, const void *q, const void *k, c
                        has_joint || has_video ? qkb : 2) ||
         !make_bshd_map(&mjv, has_joint ? jv : vv, has_joint ? g.Nj : kv_rows, g.H, g.B, false, why))
         return cudaErrorInvalidValue;
-    auto kernel = opt.qk8 ? (opt.row_bound ? attn_tc_single_kernel<true, true> : attn_tc_single_kernel<false, true>)
-                          : (opt.row_bound ? attn_tc_single_kernel<true, false> : attn_tc_single_kernel<false, false>);
+    // Clusters of two CTAs share every K/V tile (16-bit q/k).  The pair holds Q
+    // tiles 2i and 2i+1, so an odd tile count gets one all-padding tile per
+    // (batch, head, chunk group), worth it only when there are enough tiles.
+    const long q_tiles = (g.Sq + tc::BM - 1) / tc::BM;
+    const bool cluster = K6_KV_MULTICAST && !opt.qk8 && (q_tiles % 2 == 0 || q_tiles >= 16);
+    auto kernel = opt.qk8   ? (opt.row_bound ? attn_tc_single_kernel<true, true, false>
+                                             : attn_tc_single_kernel<false, true, false>)
+                  : cluster ? (opt.row_bound ? attn_tc_single_kernel<true, false, true>
+                                             : attn_tc_single_kernel<false, false, true>)
+                            : (opt.row_bound ? attn_tc_single_kernel<true, false, false>
+                                             : attn_tc_single_kernel<false, false, false>);
     cudaError_t attr_err = set_max_dynamic_smem((const void *)kernel, ts::SMEM_ALLOC);
     if (attr_err != cudaSuccess) return attr_err;
     TcParams p;
@@ -591,7 +681,7 @@ cudaError_t launch_attn_tc_single(const Geom &g, const void *q, const void *k, c
     p.Nj = g.Nj;
     p.H = g.H;
     p.n_chunks = n_chunks;
-    p.q_tiles = (int)((g.Sq + tc::BM - 1) / tc::BM);
+    p.q_tiles = (int)(cluster ? (q_tiles + 1) / 2 * 2 : q_tiles);  // rows >= Sq are masked
     p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)g.d));
     p.out = out;
     p.lse = lse;
@@ -620,9 +710,24 @@ cudaError_t launch_attn_tc_single(const Geom &g, const void *q, const void *k, c
     p.merge = opt.merge && p.group > 1;
     p.out_f32 = (p.merge ? n_chunks / p.group : n_chunks) > 1;
     p.row_bound = opt.row_bound;
-    const long grid = p.units / p.group;
-    kernel<<<(unsigned)grid, ts::THREADS, ts::SMEM_ALLOC, st>>>(mq, mk, mv, mjk, mjv, p);
-    return cudaGetLastError();
+    const long grid = p.units / p.group;  // even with cluster: q_tiles is
+    if (!cluster) {
+        kernel<<<(unsigned)grid, ts::THREADS, ts::SMEM_ALLOC, st>>>(mq, mk, mv, mjk, mjv, p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(ts::THREADS);
+    cfg.dynamicSmemBytes = ts::SMEM_ALLOC;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, mq, mk, mv, mjk, mjv, p);
 }
 
 }  // namespace k6
