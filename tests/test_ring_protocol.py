@@ -186,11 +186,12 @@ def test_five_slots_alias_with_a_lead_of_three():
     assert found == (("V", 2), ("K", 2))
 
 
-def pair_model(Ts, A, nstage=NSTAGE):
+def pair_model(Ts, A, nstage=NSTAGE, remote_release=True):
     """Two CTAs of a cluster running the same units (the kernel's multicast
     form): each loads one panel of every tile into both, so a load lands in a
     CTA only once both CTAs issued their panels, and a slot is refilled only
-    once the consumers of both CTAs released it."""
+    once the consumers of both CTAs released it (remote_release=False drops the
+    partner's release, a mistake the checks below must catch)."""
     loads, idx, deps, consumer, N = model(Ts, A, nstage)
     pair = collections.defaultdict(set)
     for node, ds in deps.items():
@@ -200,12 +201,34 @@ def pair_model(Ts, A, nstage=NSTAGE):
     for i in range(len(loads)):
         for cta in (0, 1):
             pair[(cta, ("landed", i))].add((1 - cta, ("load", i)))    # the partner's panel
-            if i >= nstage:
+            if i >= nstage and remote_release:
                 release = next(iter(deps[("load", i)] - {("load", i - 1)}))
                 pair[(cta, ("load", i))].add((1 - cta, release))      # the partner's release
-    return pair
+    return pair, loads, consumer
+
+
+def pair_refill_races(Ts, A, remote_release=True, nstage=NSTAGE):
+    """Loads whose multicast could overwrite a slot the partner still reads: CTA
+    X's load i writes slot i % nstage in both CTAs, so the partner's consumer of
+    load i - nstage must come before it."""
+    pair, loads, consumer = pair_model(Ts, A, nstage, remote_release)
+    races = []
+    for i in range(nstage, len(loads)):
+        for cta in (0, 1):
+            if (1 - cta, consumer[i - nstage]) not in ancestors(pair, (cta, ("load", i))):
+                races.append((cta, loads[i]))
+    return races
 
 
 def test_cluster_pair_has_no_wait_cycle():
     for Ts in CASES:
-        assert acyclic(pair_model(Ts, 2)), Ts
+        assert acyclic(pair_model(Ts, 2)[0]), Ts
+
+
+def test_cluster_pair_never_refills_a_slot_the_partner_reads():
+    for Ts in CASES:
+        assert pair_refill_races(Ts, 2) == [], Ts
+
+
+def test_without_the_partner_release_a_refill_races():
+    assert pair_refill_races([7], 2, remote_release=False)
