@@ -57,7 +57,7 @@ extern "C" {
 typedef enum {
     K6ATTN_OK = 0,
     K6ATTN_ERR_INVALID_ARG = 1, /* null pointer, bad size, indivisible split, aliasing, misalignment */
-    K6ATTN_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (e.g. bf16 with d != 128) */
+    K6ATTN_ERR_UNSUPPORTED = 2, /* valid request the library does not implement (e.g. bf16 with d != 128) */
     K6ATTN_ERR_CUDA = 3,        /* a CUDA runtime call failed; message in k6attn_last_error() */
     K6ATTN_ERR_TIMEOUT = 4,     /* a device-side wait ran out (reported by k6attn_sync) */
     K6ATTN_ERR_WORKSPACE = 5,   /* workspace pointer null or smaller than k6attn_workspace_bytes() */
